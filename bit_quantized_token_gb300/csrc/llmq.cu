@@ -1,0 +1,1133 @@
+// Host runtime and C ABI of the decode step (see include/llmq.h).
+//
+// One model = one weight arena (repacked 4-bit units, bf16 LM-head units),
+// canonical embedding, norm weights, a bf16 KV cache per sequence, a RoPE
+// table and the step's scratch buffers, all allocated in llm_model_create.
+// A batch-1 step is 5 kernels per layer + LM head + logit/argmax reduction,
+// launched with programmatic dependent launch and captured once per sequence
+// as a CUDA graph whose kernels read the token and position from device
+// memory, so the same graph replays for every step.
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cmath>
+#include <cstdio>
+#include <cstring>
+#include <string>
+#include <thread>
+#include <unordered_map>
+#include <vector>
+
+#include "kernels.cuh"
+#include "llmq.h"
+
+using namespace llmq;
+
+namespace {
+
+thread_local std::string g_create_error = "no error";
+
+struct Mat {            // one fused matrix of the weight arena
+  size_t off = 0;       // byte offset of its first unit
+  int rows = 0, cols = 0, n_rt = 0, G = 0;
+  bool bf16 = false;
+  int unit_bytes() const { return bf16 ? kBF16UnitBytes : kQ4UnitBytes; }
+  size_t bytes() const { return (size_t)n_rt * G * unit_bytes(); }
+};
+
+struct GemvPlan {
+  Mat m;
+  Part part;
+  float* part_buf = nullptr;  // partials of row tiles split over CTAs
+  int* counters = nullptr;    // arrival counters of those row tiles
+  int nslot = 0, ring = 0;
+  size_t smem = 0;
+};
+
+// Where a named canonical tensor lives inside a fused matrix.
+struct Placement {
+  int mat;              // index into model->mats
+  int kind;             // 0: rows offset, 1: gate rows (interleaved), 2: up rows (interleaved)
+  int row0;
+};
+
+// Dynamic shared memory of gemv_kernel (layout in the kernel).
+size_t gemv_smem(int ring, int K, int G, int nslot) {
+  return (size_t)ring + 8 * (size_t)K + 4 * (size_t)((G + 3) & ~3) + 4 * kRLoc * kCWarps * 32 + 4 * 64 +
+         4 * kCWarps + 16 + 4 * (kCWarps + 4) + 4 * kCWarps + 16 * (size_t)nslot;
+}
+
+// Canonical nibble of element c in row r.
+inline uint8_t nib(const uint8_t* codes, int64_t cols, int64_t r, int64_t c) {
+  const uint8_t b = codes[r * (cols / 2) + c / 2];
+  return (c & 1) ? (b >> 4) : (b & 15);
+}
+
+template <typename F>
+void parallel_for(int n, F f) {
+  const int nt = std::max(1, std::min<int>(n, (int)std::thread::hardware_concurrency()));
+  std::vector<std::thread> th;
+  for (int t = 0; t < nt; ++t)
+    th.emplace_back([=] {
+      for (int i = (int)((int64_t)n * t / nt); i < (int)((int64_t)n * (t + 1) / nt); ++i) f(i);
+    });
+  for (auto& x : th) x.join();
+}
+
+// Write canonical rows of a 4-bit tensor into 4-bit units (see q4_unit_dot).
+void repack_q4(uint8_t* units, int G, const uint8_t* codes, const uint16_t* scales, const uint16_t* mins,
+               int rows, int cols, int kind, int row0) {
+  parallel_for(rows, [&](int r) {
+    const int fr = kind == 0 ? row0 + r : (r / 16) * 32 + (kind == 2 ? 16 : 0) + (r % 16);
+    const int rt = fr / 32, lane = fr % 32;
+    for (int g = 0; g < G; ++g) {
+      uint8_t* u = units + ((size_t)rt * G + g) * kQ4UnitBytes;
+      for (int h = 0; h < 2; ++h)
+        for (int k = 0; k < 4; ++k)
+          for (int i = 0; i < 4; ++i) {
+            const int e = g * 64 + h * 32 + 8 * k + i;
+            u[(h * 32 + lane) * 16 + 4 * k + i] =
+                (uint8_t)(nib(codes, cols, r, e) | (nib(codes, cols, r, e + 4) << 4));
+          }
+      std::memcpy(u + 1024 + lane * 4, &scales[(size_t)r * G + g], 2);
+      std::memcpy(u + 1024 + lane * 4 + 2, &mins[(size_t)r * G + g], 2);
+    }
+  });
+}
+
+void unpack_q4(const uint8_t* units, int G, uint8_t* codes, uint16_t* scales, uint16_t* mins, int rows, int cols,
+               int kind, int row0) {
+  parallel_for(rows, [&](int r) {
+    const int fr = kind == 0 ? row0 + r : (r / 16) * 32 + (kind == 2 ? 16 : 0) + (r % 16);
+    const int rt = fr / 32, lane = fr % 32;
+    uint8_t* cr = codes + (size_t)r * (cols / 2);
+    for (int g = 0; g < G; ++g) {
+      const uint8_t* u = units + ((size_t)rt * G + g) * kQ4UnitBytes;
+      for (int h = 0; h < 2; ++h)
+        for (int k = 0; k < 4; ++k)
+          for (int i = 0; i < 4; ++i) {
+            const int e = g * 64 + h * 32 + 8 * k + i;
+            const uint8_t b = u[(h * 32 + lane) * 16 + 4 * k + i];
+            const uint8_t lo = b & 15, hi = b >> 4;
+            cr[e / 2] = (e & 1) ? (uint8_t)((cr[e / 2] & 15) | (lo << 4)) : (uint8_t)((cr[e / 2] & 0xF0) | lo);
+            const int e2 = e + 4;
+            cr[e2 / 2] = (e2 & 1) ? (uint8_t)((cr[e2 / 2] & 15) | (hi << 4)) : (uint8_t)((cr[e2 / 2] & 0xF0) | hi);
+          }
+      std::memcpy(&scales[(size_t)r * G + g], u + 1024 + lane * 4, 2);
+      std::memcpy(&mins[(size_t)r * G + g], u + 1024 + lane * 4 + 2, 2);
+    }
+  });
+}
+
+// Dense bf16 [rows][cols] -> bf16 units (see bf16_unit_dot).
+void repack_bf16(uint8_t* units, int G, const uint16_t* data, int rows, int cols) {
+  parallel_for(rows, [&](int r) {
+    const int rt = r / 32, lane = r % 32;
+    for (int g = 0; g < G; ++g) {
+      uint8_t* u = units + ((size_t)rt * G + g) * kBF16UnitBytes;
+      for (int k = 0; k < 8; ++k) std::memcpy(u + (k * 32 + lane) * 16, data + (size_t)r * cols + g * 64 + 8 * k, 16);
+    }
+  });
+}
+
+Part make_part(int n_rt, int G, int n_cta) {
+  Part p;
+  p.U = n_rt * G;
+  p.N = std::max(1, std::min(n_cta, p.U));
+  p.G = G;
+  p.S = 1;
+  for (int rt = 0; rt < n_rt; ++rt) p.S = std::max(p.S, p.n_contrib(rt));
+  return p;
+}
+
+}  // namespace
+
+struct llm_model {
+  llm_config cfg{};
+  int n_sm = 0, q_dim = 0, kv_dim = 0, gq = 0;
+  cudaStream_t stream = nullptr;
+  bool own_stream = false;
+  std::string err = "no error";
+  int poisoned = 0;  // sticky llm_status
+
+  std::vector<Mat> mats;                      // fused matrices in the arena
+  std::unordered_map<std::string, Placement> places;
+  std::unordered_map<std::string, std::pair<int64_t, int64_t>> shapes;
+  uint8_t* d_arena = nullptr;
+  size_t arena_bytes = 0;
+  void* d_embed = nullptr;                    // canonical embedding (gather)
+  bool embed_bf16 = false;
+  float* d_norms = nullptr;
+  std::vector<size_t> off_attn_norm, off_ffn_norm, off_q_norm, off_k_norm;
+  size_t off_final_norm = 0;
+  uint16_t* d_k = nullptr;                    // [B][L][Hkv][cap][hd]
+  uint16_t* d_v = nullptr;
+  float2* d_rope = nullptr;                   // [cap][hd/2]
+
+  // step plans
+  std::vector<GemvPlan> qkv, wo, gu, down;
+  GemvPlan lm;
+  int attn_P = 1;
+
+  // scratch: split-row-tile partials and counters (one set per GEMV kind),
+  // attention split partials, the step's vectors
+  float *d_part = nullptr, *d_attn_part = nullptr;
+  int* d_cnt = nullptr;                       // [5 GEMV kinds][max n_rt] + attention [Hkv] + greedy [1]
+  float *d_qkv = nullptr, *d_obuf = nullptr, *d_abuf = nullptr, *d_xbuf = nullptr, *d_hbuf = nullptr,
+        *d_logits = nullptr, *d_cand_v = nullptr;
+  int* d_cand_i = nullptr;
+  int* d_attn_cnt = nullptr;
+  int* d_greedy_cnt = nullptr;
+  // per-sequence state
+  int *d_pos = nullptr, *d_tok = nullptr, *d_argmax = nullptr, *d_hist = nullptr, *d_hist_ctr = nullptr,
+      *d_status = nullptr, *d_prompt = nullptr;
+  int* h_stage = nullptr;                     // pinned staging
+  std::vector<int> len;
+  std::vector<cudaGraphExec_t> graphs;
+  int kernels_per_step = 0;
+  size_t device_bytes = 0;
+  std::vector<void*> allocs;
+};
+
+namespace {
+
+int set_err(llm_model* m, int code, const std::string& msg) {
+  if (m) m->err = msg;
+  else g_create_error = msg;
+  return code;
+}
+
+int cuda_fail(llm_model* m, cudaError_t e, const char* what) {
+  std::string msg = std::string(what) + ": " + cudaGetErrorString(e);
+  if (m) {
+    m->poisoned = LLM_ERR_CUDA;
+    m->err = msg;
+  } else {
+    g_create_error = msg;
+  }
+  return LLM_ERR_CUDA;
+}
+
+#define CK(call, what)                                  \
+  do {                                                  \
+    cudaError_t e_ = (call);                            \
+    if (e_ != cudaSuccess) return cuda_fail(m, e_, what); \
+  } while (0)
+
+template <typename T>
+cudaError_t dalloc(llm_model* m, T** p, size_t bytes) {
+  void* q = nullptr;
+  cudaError_t e = cudaMalloc(&q, std::max<size_t>(bytes, 16));
+  if (e != cudaSuccess) return e;
+  m->allocs.push_back(q);
+  m->device_bytes += bytes;
+  *p = static_cast<T*>(q);
+  return cudaSuccess;
+}
+
+bool is_device_ptr(const void* p) {
+  cudaPointerAttributes a{};
+  if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+    cudaGetLastError();
+    return false;
+  }
+  return a.type == cudaMemoryTypeDevice || a.type == cudaMemoryTypeManaged;
+}
+
+template <typename Kern, typename Params>
+cudaError_t launch(Kern kern, dim3 grid, dim3 block, size_t smem, cudaStream_t st, bool pdl, const Params& prm) {
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kern, prm);
+}
+
+GemvPlan plan_gemv(const Mat& mat, int n_sm) {
+  GemvPlan g;
+  g.m = mat;
+  g.part = make_part(mat.n_rt, mat.G, n_sm);
+  const int slot = kChunkUnits * mat.unit_bytes();
+  g.nslot = mat.bf16 ? 3 : 8;
+  g.ring = g.nslot * slot;
+  g.smem = gemv_smem(g.ring, mat.G * 64, mat.G, g.nslot);
+  return g;
+}
+
+GemvParams gemv_params(const llm_model* m, const GemvPlan& g) {
+  GemvParams p{};
+  p.units = m->d_arena + g.m.off;
+  p.n_rt = g.m.n_rt;
+  p.G = g.m.G;
+  p.K = g.m.G * 64;
+  p.unit_bytes = g.m.unit_bytes();
+  p.nslot = g.nslot;
+  p.ring_bytes = g.ring;
+  p.part = g.part;
+  p.rows = g.m.rows;
+  p.part_buf = g.part_buf;
+  p.counters = g.counters;
+  p.eps = m->cfg.norm_eps;
+  p.status = m->d_status;
+  p.vocab = m->cfg.vocab;
+  return p;
+}
+
+cudaError_t launch_gemv(const llm_model* m, const GemvPlan& g, const GemvParams& p, bool pdl) {
+  if (g.m.bf16) return launch(gemv_kernel<true>, dim3(g.part.N), dim3(kGemvThreads), g.smem, m->stream, pdl, p);
+  return launch(gemv_kernel<false>, dim3(g.part.N), dim3(kGemvThreads), g.smem, m->stream, pdl, p);
+}
+
+template <int GQ, int HD>
+cudaError_t launch_attn_t(const llm_model* m, const AttnParams& a, bool pdl) {
+  return launch(attention_kernel<GQ, HD>, dim3(m->attn_P, m->cfg.n_kv_heads), dim3(kAttnThreads), 0, m->stream, pdl,
+                a);
+}
+
+cudaError_t launch_attn(const llm_model* m, const AttnParams& a, bool pdl) {
+  const int hd = m->cfg.head_dim;
+  switch (m->gq * 1000 + hd) {
+    case 1064: return launch_attn_t<1, 64>(m, a, pdl);
+    case 2064: return launch_attn_t<2, 64>(m, a, pdl);
+    case 4064: return launch_attn_t<4, 64>(m, a, pdl);
+    case 8064: return launch_attn_t<8, 64>(m, a, pdl);
+    case 1128: return launch_attn_t<1, 128>(m, a, pdl);
+    case 2128: return launch_attn_t<2, 128>(m, a, pdl);
+    case 4128: return launch_attn_t<4, 128>(m, a, pdl);
+    case 8128: return launch_attn_t<8, 128>(m, a, pdl);
+  }
+  return cudaErrorInvalidValue;
+}
+
+// Optional per-launch timing of an eager step.
+struct Prof {
+  std::vector<cudaEvent_t> ev;
+  std::vector<llm_kernel_time> rec;
+  int64_t kv_len = 0;
+  cudaError_t before(cudaStream_t st) {
+    cudaEvent_t e;
+    cudaError_t r = cudaEventCreate(&e);
+    if (r != cudaSuccess) return r;
+    ev.push_back(e);
+    return cudaEventRecord(e, st);
+  }
+  cudaError_t after(cudaStream_t st, int kind, int layer, int64_t bytes) {
+    cudaError_t r = before(st);
+    rec.push_back({kind, layer, bytes, 0.f});
+    return r;
+  }
+};
+
+// The kernels of one batch-1 step, one launcher each (which: 0 q|k|v GEMV,
+// 1 attention, 2 o GEMV, 3 gate|up GEMV, 4 down GEMV, 5 LM head + greedy choice).
+enum Which { W_QKV = 0, W_ATTN = 1, W_WO = 2, W_GU = 3, W_DOWN = 4, W_LM = 5 };
+
+cudaError_t launch_one(llm_model* m, int seq, int which, int l, bool pdl) {
+  const llm_config& c = m->cfg;
+  const int L = c.n_layers, d = c.dim;
+  switch (which) {
+    case W_QKV: {  // q|k|v = Wqkv * rmsnorm(x_l); x_0 = embedding row (stored by CTA 0)
+      GemvParams p = gemv_params(m, m->qkv[l]);
+      if (l == 0) {
+        p.vec_mode = m->embed_bf16 ? VEC_EMBED_BF16 : VEC_EMBED_F32;
+        p.embed = m->d_embed;
+        p.tok = m->d_tok + seq;
+        p.vstore = m->d_xbuf;
+      } else {
+        p.vec_mode = VEC_PLAIN;
+        p.vin = m->d_xbuf + (size_t)l * d;
+      }
+      p.norm_w = m->d_norms + m->off_attn_norm[l];
+      p.epi = EPI_STORE;
+      p.out = m->d_qkv;
+      return launch_gemv(m, m->qkv[l], p, pdl);
+    }
+    case W_ATTN: {  // attention over the cache (+ q/k norm, RoPE, bf16 append)
+      AttnParams a{};
+      a.qkv = m->d_qkv;
+      a.q_dim = m->q_dim;
+      a.kv_dim = m->kv_dim;
+      a.Hkv = c.n_kv_heads;
+      a.P = m->attn_P;
+      a.rope = m->d_rope;
+      a.rope_neox = c.rope_neox;
+      a.q_norm = c.qk_norm ? m->d_norms + m->off_q_norm[l] : nullptr;
+      a.k_norm = c.qk_norm ? m->d_norms + m->off_k_norm[l] : nullptr;
+      a.eps = c.norm_eps;
+      const size_t kvoff = ((size_t)seq * L + l) * (size_t)c.n_kv_heads * c.max_seq * c.head_dim;
+      a.kc = m->d_k + kvoff;
+      a.vc = m->d_v + kvoff;
+      a.cap = c.max_seq;
+      a.pos = m->d_pos + seq;
+      a.part = m->d_attn_part;
+      a.counter = m->d_attn_cnt;
+      a.out = m->d_obuf;
+      a.status = m->d_status;
+      return launch_attn(m, a, pdl);
+    }
+    case W_WO: {  // h_l = x_l + Wo o
+      GemvParams p = gemv_params(m, m->wo[l]);
+      p.vec_mode = VEC_PLAIN;
+      p.vin = m->d_obuf;
+      p.epi = EPI_RESID;
+      p.resid = m->d_xbuf + (size_t)l * d;
+      p.out = m->d_hbuf + (size_t)l * d;
+      return launch_gemv(m, m->wo[l], p, pdl);
+    }
+    case W_GU: {  // a = silu(Wg rmsnorm(h_l)) * (Wu rmsnorm(h_l))
+      GemvParams p = gemv_params(m, m->gu[l]);
+      p.vec_mode = VEC_PLAIN;
+      p.vin = m->d_hbuf + (size_t)l * d;
+      p.norm_w = m->d_norms + m->off_ffn_norm[l];
+      p.epi = EPI_SWIGLU;
+      p.out = m->d_abuf;
+      return launch_gemv(m, m->gu[l], p, pdl);
+    }
+    case W_DOWN: {  // x_{l+1} = h_l + Wd a
+      GemvParams p = gemv_params(m, m->down[l]);
+      p.vec_mode = VEC_PLAIN;
+      p.vin = m->d_abuf;
+      p.epi = EPI_RESID;
+      p.resid = m->d_hbuf + (size_t)l * d;
+      p.out = m->d_xbuf + (size_t)(l + 1) * d;
+      return launch_gemv(m, m->down[l], p, pdl);
+    }
+    default: {  // logits = W_lm rmsnorm(x_L); greedy choice, token feedback, position += 1
+      GemvParams p = gemv_params(m, m->lm);
+      p.vec_mode = VEC_PLAIN;
+      p.vin = m->d_xbuf + (size_t)L * d;
+      p.norm_w = m->d_norms + m->off_final_norm;
+      p.epi = EPI_LOGITS;
+      p.out = m->d_logits;
+      p.cand_v = m->d_cand_v;
+      p.cand_i = m->d_cand_i;
+      p.gcounter = m->d_greedy_cnt;
+      p.tok_io = m->d_tok + seq;
+      p.argmax_out = m->d_argmax + seq;
+      p.hist = m->d_hist;
+      p.hist_ctr = m->d_hist_ctr;
+      p.hist_cap = c.max_seq;
+      p.pos = m->d_pos + seq;
+      return launch_gemv(m, m->lm, p, pdl);
+    }
+  }
+}
+
+// Algorithmic HBM bytes of one launch: weight units, or K/V rows read.
+int64_t launch_bytes(const llm_model* m, int which, int l, int64_t kv_len) {
+  switch (which) {
+    case W_QKV: return (int64_t)m->qkv[l].m.bytes();
+    case W_ATTN: return (int64_t)2 * m->cfg.n_kv_heads * kv_len * m->cfg.head_dim * 2;
+    case W_WO: return (int64_t)m->wo[l].m.bytes();
+    case W_GU: return (int64_t)m->gu[l].m.bytes();
+    case W_DOWN: return (int64_t)m->down[l].m.bytes();
+    case W_LM: return (int64_t)m->lm.m.bytes();
+  }
+  return 0;
+}
+
+int kind_of(const llm_model* m, int which) {
+  if (which == W_ATTN) return 2;
+  return (which == W_LM && m->lm.m.bf16) ? 1 : 0;
+}
+
+// Enqueue one batch-1 decode step of sequence `seq` on m->stream.
+cudaError_t enqueue_step(llm_model* m, int seq, Prof* prof = nullptr) {
+  const int L = m->cfg.n_layers;
+  const bool pdl = !(m->cfg.flags & LLM_NO_PDL) && !prof;
+  cudaError_t e;
+  auto one = [&](int which, int l, bool use_pdl) -> cudaError_t {
+    if (prof && (e = prof->before(m->stream)) != cudaSuccess) return e;
+    if ((e = launch_one(m, seq, which, l, use_pdl)) != cudaSuccess) return e;
+    if (prof) return prof->after(m->stream, kind_of(m, which), which >= W_LM ? -1 : l,
+                                 launch_bytes(m, which, l, prof->kv_len));
+    return cudaSuccess;
+  };
+  for (int l = 0; l < L; ++l) {
+    // the first kernel of a step follows host-side copies: no programmatic edge
+    if ((e = one(W_QKV, l, pdl && l > 0)) != cudaSuccess) return e;
+    for (int which : {W_ATTN, W_WO, W_GU, W_DOWN})
+      if ((e = one(which, l, pdl)) != cudaSuccess) return e;
+  }
+  return one(W_LM, -1, pdl);
+}
+
+int check_status(llm_model* m) {
+  if (m->poisoned) return m->poisoned;
+  int st = 0;
+  CK(cudaMemcpyAsync(&st, m->d_status, sizeof(int), cudaMemcpyDeviceToHost, m->stream), "status read");
+  CK(cudaStreamSynchronize(m->stream), "stream sync");
+  if (st == 0) return LLM_OK;
+  CK(cudaMemsetAsync(m->d_status, 0, sizeof(int), m->stream), "status clear");
+  if (st & ST_TIMEOUT) {
+    m->poisoned = LLM_ERR_TIMEOUT;
+    return set_err(m, LLM_ERR_TIMEOUT, "a device-side wait exceeded its limit");
+  }
+  if (st & ST_NAN) return set_err(m, LLM_ERR_NAN, "NaN in the logits");
+  if (st & ST_CTX_FULL) return set_err(m, LLM_ERR_CTX_FULL, "position reached max_seq on the device");
+  return set_err(m, LLM_ERR_INVALID_ARG, "token id out of range on the device");
+}
+
+int run_step(llm_model* m, int seq) {
+  const bool graph = !(m->cfg.flags & LLM_NO_GRAPH);
+  if (!graph) {
+    CK(enqueue_step(m, seq), "step launch");
+    return LLM_OK;
+  }
+  if (!m->graphs[seq]) {
+    cudaGraph_t g = nullptr;
+    CK(cudaStreamBeginCapture(m->stream, cudaStreamCaptureModeThreadLocal), "begin capture");
+    cudaError_t e = enqueue_step(m, seq);
+    cudaError_t e2 = cudaStreamEndCapture(m->stream, &g);
+    if (e != cudaSuccess) return cuda_fail(m, e, "step capture");
+    if (e2 != cudaSuccess) return cuda_fail(m, e2, "end capture");
+    cudaGraphExec_t ge = nullptr;
+    e = cudaGraphInstantiate(&ge, g, 0);
+    cudaGraphDestroy(g);
+    if (e != cudaSuccess) return cuda_fail(m, e, "graph instantiate");
+    m->graphs[seq] = ge;
+  }
+  CK(cudaGraphLaunch(m->graphs[seq], m->stream), "graph launch");
+  return LLM_OK;
+}
+
+int check_model(llm_model* m, int seq) {
+  if (!m) return set_err(nullptr, LLM_ERR_INVALID_ARG, "model is NULL");
+  if (m->poisoned) return m->poisoned;
+  if (seq < 0 || seq >= m->cfg.max_batch) return set_err(m, LLM_ERR_INVALID_ARG, "seq out of range");
+  return LLM_OK;
+}
+
+int copy_out(llm_model* m, void* dst, const void* src, size_t bytes, bool* host) {
+  if (!dst) return LLM_OK;
+  if (!is_device_ptr(dst)) *host = true;
+  CK(cudaMemcpyAsync(dst, src, bytes, cudaMemcpyDefault, m->stream), "output copy");
+  return LLM_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* llm_last_error(const llm_model* m) { return m ? m->err.c_str() : g_create_error.c_str(); }
+
+void llm_model_destroy(llm_model* m) {
+  if (!m) return;
+  for (auto g : m->graphs)
+    if (g) cudaGraphExecDestroy(g);
+  for (void* p : m->allocs) cudaFree(p);
+  if (m->h_stage) cudaFreeHost(m->h_stage);
+  if (m->own_stream && m->stream) cudaStreamDestroy(m->stream);
+  delete m;
+}
+
+int llm_model_create(const llm_config* cfg, const llm_tensor* tensors, int32_t n_tensors, void* cuda_stream,
+                     llm_model** out) {
+  llm_model* m = nullptr;
+  if (out) *out = nullptr;
+  if (!cfg || !tensors || !out || n_tensors <= 0)
+    return set_err(nullptr, LLM_ERR_INVALID_ARG, "null config, tensors or out pointer");
+  if (cfg->abi_version != LLMQ_ABI_VERSION) return set_err(nullptr, LLM_ERR_UNSUPPORTED, "abi_version mismatch");
+  const llm_config& c = *cfg;
+  if (c.dim <= 0 || c.n_layers <= 0 || c.n_heads <= 0 || c.n_kv_heads <= 0 || c.ffn_dim <= 0 || c.vocab <= 0 ||
+      c.max_seq <= 0 || c.max_batch <= 0 || !(c.norm_eps > 0.f) || !(c.rope_theta > 0.0))
+    return set_err(nullptr, LLM_ERR_INVALID_ARG, "non-positive dimension, max_seq, max_batch, eps or theta");
+  if (c.head_dim != 64 && c.head_dim != 128)
+    return set_err(nullptr, LLM_ERR_UNSUPPORTED, "head_dim=" + std::to_string(c.head_dim) + " (64 or 128 only)");
+  if (c.n_heads % c.n_kv_heads)
+    return set_err(nullptr, LLM_ERR_UNSUPPORTED, "n_heads not a multiple of n_kv_heads");
+  const int gq = c.n_heads / c.n_kv_heads;
+  if (gq != 1 && gq != 2 && gq != 4 && gq != 8)
+    return set_err(nullptr, LLM_ERR_UNSUPPORTED, "GQA group of " + std::to_string(gq) + " (1, 2, 4 or 8 only)");
+  if (c.dim % 64 || c.ffn_dim % 64)
+    return set_err(nullptr, LLM_ERR_UNSUPPORTED, "dim and ffn_dim must be multiples of the group size 64");
+  if (c.ffn_dim > kMaxK || c.dim > kMaxK || c.n_heads * c.head_dim > kMaxK)
+    return set_err(nullptr, LLM_ERR_UNSUPPORTED, "a GEMV input wider than " + std::to_string(kMaxK));
+  if (c.rope_neox != 0 && c.rope_neox != 1) return set_err(nullptr, LLM_ERR_INVALID_ARG, "rope_neox must be 0 or 1");
+
+  std::unordered_map<std::string, const llm_tensor*> by_name;
+  for (int i = 0; i < n_tensors; ++i)
+    if (tensors[i].name) by_name[tensors[i].name] = &tensors[i];
+  auto find = [&](const std::string& n, int dtype, int64_t rows, int64_t cols, const llm_tensor** t) -> int {
+    auto it = by_name.find(n);
+    if (it == by_name.end()) return set_err(nullptr, LLM_ERR_NOT_FOUND, "missing tensor " + n);
+    const llm_tensor* x = it->second;
+    if (x->dtype != dtype) return set_err(nullptr, LLM_ERR_UNSUPPORTED, "tensor " + n + ": unexpected dtype");
+    if (x->rows != rows || x->cols != cols)
+      return set_err(nullptr, LLM_ERR_INVALID_ARG,
+                     "tensor " + n + ": shape " + std::to_string(x->rows) + "x" + std::to_string(x->cols) +
+                         ", expected " + std::to_string(rows) + "x" + std::to_string(cols));
+    if (dtype == LLM_Q4G64 ? (!x->codes || !x->scales || !x->mins) : !x->data)
+      return set_err(nullptr, LLM_ERR_INVALID_ARG, "tensor " + n + ": null data");
+    *t = x;
+    return LLM_OK;
+  };
+
+  m = new llm_model();
+  m->cfg = c;
+  m->gq = gq;
+  m->q_dim = c.n_heads * c.head_dim;
+  m->kv_dim = c.n_kv_heads * c.head_dim;
+  int rc;
+  auto fail = [&](int code) {
+    if (code != LLM_OK && m) {
+      if (m->err != "no error") g_create_error = m->err;
+      llm_model_destroy(m);
+      m = nullptr;
+    }
+    return code;
+  };
+  int dev = 0;
+  {
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&m->n_sm, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return fail(cuda_fail(nullptr, e, "no CUDA device"));
+  }
+  const int L = c.n_layers, d = c.dim, F = c.ffn_dim, hd = c.head_dim, V = c.vocab;
+
+  // ---- lay out the arena: per layer QKV, WO, GU, DOWN; then the LM head
+  size_t off = 0;
+  auto add_mat = [&](int rows, int cols, bool bf16) {
+    Mat x;
+    x.rows = rows;
+    x.cols = cols;
+    x.n_rt = (rows + 31) / 32;
+    x.G = cols / 64;
+    x.bf16 = bf16;
+    x.off = off;
+    off += (x.bytes() + 255) / 256 * 256;
+    m->mats.push_back(x);
+    return (int)m->mats.size() - 1;
+  };
+  std::vector<int> mi_qkv(L), mi_wo(L), mi_gu(L), mi_down(L);
+  for (int l = 0; l < L; ++l) {
+    const std::string P = "L" + std::to_string(l) + ".";
+    mi_qkv[l] = add_mat(m->q_dim + 2 * m->kv_dim, d, false);
+    m->places[P + "wq"] = {mi_qkv[l], 0, 0};
+    m->places[P + "wk"] = {mi_qkv[l], 0, m->q_dim};
+    m->places[P + "wv"] = {mi_qkv[l], 0, m->q_dim + m->kv_dim};
+    mi_wo[l] = add_mat(d, m->q_dim, false);
+    m->places[P + "wo"] = {mi_wo[l], 0, 0};
+    mi_gu[l] = add_mat(2 * F, d, false);
+    m->places[P + "w_gate"] = {mi_gu[l], 1, 0};
+    m->places[P + "w_up"] = {mi_gu[l], 2, 0};
+    mi_down[l] = add_mat(d, F, false);
+    m->places[P + "w_down"] = {mi_down[l], 0, 0};
+    m->shapes[P + "wq"] = {m->q_dim, d};
+    m->shapes[P + "wk"] = {m->kv_dim, d};
+    m->shapes[P + "wv"] = {m->kv_dim, d};
+    m->shapes[P + "wo"] = {d, m->q_dim};
+    m->shapes[P + "w_gate"] = {F, d};
+    m->shapes[P + "w_up"] = {F, d};
+    m->shapes[P + "w_down"] = {d, F};
+  }
+  const int mi_lm = add_mat(V, d, c.tied_embedding != 0);
+  if (!c.tied_embedding) {
+    m->places["lm_head"] = {mi_lm, 0, 0};
+    m->shapes["lm_head"] = {V, d};
+  }
+  m->arena_bytes = off;
+
+  // ---- validate inputs and repack on the host
+  std::vector<uint8_t> arena(off, 0);
+  for (const auto& kv : m->places) {
+    const llm_tensor* t = nullptr;
+    const auto shp = m->shapes[kv.first];
+    if ((rc = find(kv.first, LLM_Q4G64, shp.first, shp.second, &t)) != LLM_OK) return fail(rc);
+    const Mat& x = m->mats[kv.second.mat];
+    repack_q4(arena.data() + x.off, x.G, static_cast<const uint8_t*>(t->codes), static_cast<const uint16_t*>(t->scales),
+              static_cast<const uint16_t*>(t->mins), (int)t->rows, (int)t->cols, kv.second.kind, kv.second.row0);
+  }
+  const llm_tensor* emb = nullptr;
+  m->embed_bf16 = c.tied_embedding != 0;
+  if ((rc = find("embed", m->embed_bf16 ? LLM_BF16 : LLM_F32, V, d, &emb)) != LLM_OK) {
+    if (rc == LLM_ERR_UNSUPPORTED && c.tied_embedding) g_create_error = "tied embedding must be LLM_BF16";
+    return fail(rc);
+  }
+  if (c.tied_embedding) {
+    const Mat& x = m->mats[mi_lm];
+    repack_bf16(arena.data() + x.off, x.G, static_cast<const uint16_t*>(emb->data), V, d);
+  }
+  // norm weights
+  std::vector<float> norms;
+  auto add_norm = [&](const std::string& n, int len, size_t* where) -> int {
+    const llm_tensor* t = nullptr;
+    int r = find(n, LLM_F32, 1, len, &t);
+    if (r != LLM_OK) return r;
+    *where = norms.size();
+    const float* src = static_cast<const float*>(t->data);
+    norms.insert(norms.end(), src, src + len);
+    while (norms.size() % 4) norms.push_back(0.f);
+    return LLM_OK;
+  };
+  m->off_attn_norm.resize(L);
+  m->off_ffn_norm.resize(L);
+  m->off_q_norm.resize(L);
+  m->off_k_norm.resize(L);
+  for (int l = 0; l < L; ++l) {
+    const std::string P = "L" + std::to_string(l) + ".";
+    if ((rc = add_norm(P + "attn_norm", d, &m->off_attn_norm[l])) != LLM_OK) return fail(rc);
+    if ((rc = add_norm(P + "ffn_norm", d, &m->off_ffn_norm[l])) != LLM_OK) return fail(rc);
+    if (c.qk_norm) {
+      if ((rc = add_norm(P + "q_norm", hd, &m->off_q_norm[l])) != LLM_OK) return fail(rc);
+      if ((rc = add_norm(P + "k_norm", hd, &m->off_k_norm[l])) != LLM_OK) return fail(rc);
+    }
+  }
+  if ((rc = add_norm("final_norm", d, &m->off_final_norm)) != LLM_OK) return fail(rc);
+
+  // ---- device allocations (all of them, once)
+  if (cuda_stream) {
+    m->stream = static_cast<cudaStream_t>(cuda_stream);
+  } else {
+    cudaError_t e = cudaStreamCreateWithFlags(&m->stream, cudaStreamNonBlocking);
+    if (e != cudaSuccess) return fail(cuda_fail(nullptr, e, "stream create"));
+    m->own_stream = true;
+  }
+  auto A = [&](auto** p, size_t bytes, const char* what) -> int {
+    cudaError_t e = dalloc(m, p, bytes);
+    if (e == cudaErrorMemoryAllocation) {
+      cudaGetLastError();
+      return set_err(m, LLM_ERR_OOM, std::string("device allocation failed: ") + what);
+    }
+    if (e != cudaSuccess) return cuda_fail(m, e, what);
+    return LLM_OK;
+  };
+#define AL(ptr, bytes, what) \
+  if ((rc = A(&(ptr), (bytes), (what))) != LLM_OK) return fail(rc)
+  AL(m->d_arena, m->arena_bytes, "weights");
+  const size_t emb_bytes = (size_t)V * d * (m->embed_bf16 ? 2 : 4);
+  AL(m->d_embed, emb_bytes, "embedding");
+  AL(m->d_norms, norms.size() * 4, "norms");
+  const size_t kv_elems = (size_t)c.max_batch * L * c.n_kv_heads * c.max_seq * hd;
+  AL(m->d_k, kv_elems * 2, "K cache");
+  AL(m->d_v, kv_elems * 2, "V cache");
+  AL(m->d_rope, (size_t)c.max_seq * (hd / 2) * sizeof(float2), "rope table");
+
+  for (int l = 0; l < L; ++l) {
+    m->qkv.push_back(plan_gemv(m->mats[mi_qkv[l]], m->n_sm));
+    m->wo.push_back(plan_gemv(m->mats[mi_wo[l]], m->n_sm));
+    m->gu.push_back(plan_gemv(m->mats[mi_gu[l]], m->n_sm));
+    m->down.push_back(plan_gemv(m->mats[mi_down[l]], m->n_sm));
+  }
+  m->lm = plan_gemv(m->mats[mi_lm], m->n_sm);
+  // split-row-tile partials: one region per GEMV kind (QKV, WO, GU, DOWN, LM)
+  auto part_floats = [](const GemvPlan& g) { return (size_t)g.m.n_rt * g.part.S * kTileRows; };
+  size_t pf[5] = {0, 0, 0, 0, part_floats(m->lm)};
+  int nrt[5] = {0, 0, 0, 0, m->lm.m.n_rt};
+  for (int l = 0; l < L; ++l) {
+    pf[0] = std::max(pf[0], part_floats(m->qkv[l]));
+    pf[1] = std::max(pf[1], part_floats(m->wo[l]));
+    pf[2] = std::max(pf[2], part_floats(m->gu[l]));
+    pf[3] = std::max(pf[3], part_floats(m->down[l]));
+    nrt[0] = std::max(nrt[0], m->qkv[l].m.n_rt);
+    nrt[1] = std::max(nrt[1], m->wo[l].m.n_rt);
+    nrt[2] = std::max(nrt[2], m->gu[l].m.n_rt);
+    nrt[3] = std::max(nrt[3], m->down[l].m.n_rt);
+  }
+  const size_t part_total = pf[0] + pf[1] + pf[2] + pf[3] + pf[4];
+  const size_t cnt_total = (size_t)nrt[0] + nrt[1] + nrt[2] + nrt[3] + nrt[4] + c.n_kv_heads + 1;
+  AL(m->d_part, part_total * 4, "GEMV partials");
+  AL(m->d_cnt, cnt_total * 4, "counters");
+  {
+    float* pp = m->d_part;
+    int* cc = m->d_cnt;
+    std::vector<GemvPlan>* kinds[4] = {&m->qkv, &m->wo, &m->gu, &m->down};
+    for (int k = 0; k < 4; ++k) {
+      for (auto& g : *kinds[k]) {
+        g.part_buf = pp;
+        g.counters = cc;
+      }
+      pp += pf[k];
+      cc += nrt[k];
+    }
+    m->lm.part_buf = pp;
+    m->lm.counters = cc;
+    cc += nrt[4];
+    m->d_attn_cnt = cc;
+    m->d_greedy_cnt = cc + c.n_kv_heads;
+  }
+  m->attn_P = std::max(1, m->n_sm / c.n_kv_heads);
+  AL(m->d_attn_part, (size_t)c.n_kv_heads * m->attn_P * gq * (hd + 2) * 4, "attention partials");
+  AL(m->d_qkv, (size_t)(m->q_dim + 2 * m->kv_dim) * 4, "q|k|v");
+  AL(m->d_obuf, (size_t)m->q_dim * 4, "attention output");
+  AL(m->d_abuf, (size_t)F * 4, "SwiGLU output");
+  AL(m->d_xbuf, (size_t)(L + 1) * d * 4, "residual stream");
+  AL(m->d_hbuf, (size_t)L * d * 4, "post-attention residual");
+  AL(m->d_logits, (size_t)V * 4, "logits");
+  AL(m->d_cand_v, (size_t)m->lm.part.N * 4, "greedy candidates");
+  AL(m->d_cand_i, (size_t)m->lm.part.N * 4, "greedy candidates");
+  AL(m->d_pos, (size_t)c.max_batch * 4, "positions");
+  AL(m->d_tok, (size_t)c.max_batch * 4, "tokens");
+  AL(m->d_argmax, (size_t)c.max_batch * 4, "argmax");
+  AL(m->d_hist, (size_t)c.max_seq * 4, "history");
+  AL(m->d_hist_ctr, 4, "history counter");
+  AL(m->d_status, 4, "status");
+  AL(m->d_prompt, (size_t)c.max_seq * 4, "prompt");
+#undef AL
+  {
+    cudaError_t e = cudaMallocHost(&m->h_stage, 64 * sizeof(int));
+    if (e != cudaSuccess) return fail(cuda_fail(m, e, "pinned staging"));
+  }
+
+  // ---- uploads
+  auto up = [&](void* dst, const void* src, size_t bytes, const char* what) -> int {
+    cudaError_t e = cudaMemcpy(dst, src, bytes, cudaMemcpyHostToDevice);
+    return e == cudaSuccess ? LLM_OK : cuda_fail(m, e, what);
+  };
+  if ((rc = up(m->d_arena, arena.data(), arena.size(), "weight upload")) != LLM_OK) return fail(rc);
+  std::vector<uint8_t>().swap(arena);
+  if ((rc = up(m->d_embed, emb->data, emb_bytes, "embedding upload")) != LLM_OK) return fail(rc);
+  if ((rc = up(m->d_norms, norms.data(), norms.size() * 4, "norm upload")) != LLM_OK) return fail(rc);
+  {
+    // cos/sin of pos * base^(-2i/hd), evaluated in double, stored as fp32
+    std::vector<float2> rope((size_t)c.max_seq * (hd / 2));
+    for (int pos = 0; pos < c.max_seq; ++pos)
+      for (int i = 0; i < hd / 2; ++i) {
+        const double ang = (double)pos * std::pow(c.rope_theta, -2.0 * i / hd);
+        rope[(size_t)pos * (hd / 2) + i] = make_float2((float)std::cos(ang), (float)std::sin(ang));
+      }
+    if ((rc = up(m->d_rope, rope.data(), rope.size() * sizeof(float2), "rope upload")) != LLM_OK) return fail(rc);
+  }
+  {
+    cudaError_t e = cudaMemset(m->d_cnt, 0, cnt_total * 4);
+    for (int* z : {m->d_pos, m->d_tok, m->d_argmax})
+      if (e == cudaSuccess) e = cudaMemset(z, 0, 4 * (size_t)c.max_batch);
+    if (e == cudaSuccess) e = cudaMemset(m->d_hist_ctr, 0, 4);
+    if (e == cudaSuccess) e = cudaMemset(m->d_status, 0, 4);
+    if (e == cudaSuccess) e = cudaMemset(m->d_k, 0, kv_elems * 2);
+    if (e == cudaSuccess) e = cudaMemset(m->d_v, 0, kv_elems * 2);
+    size_t smax = m->lm.smem;
+    for (int l = 0; l < L; ++l)
+      smax = std::max({smax, m->qkv[l].smem, m->wo[l].smem, m->gu[l].smem, m->down[l].smem});
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(gemv_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smax);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(gemv_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smax);
+    if (e == cudaSuccess) e = cudaDeviceSynchronize();
+    if (e != cudaSuccess) return fail(cuda_fail(m, e, "initialisation"));
+  }
+  m->len.assign(c.max_batch, 0);
+  m->graphs.assign(c.max_batch, nullptr);
+  m->kernels_per_step = 5 * L + 1;
+  *out = m;
+  return LLM_OK;
+}
+
+int llm_decode_step(llm_model* m, int32_t seq, int32_t token, float* logits_out, int32_t* argmax_out) {
+  int rc = check_model(m, seq);
+  if (rc) return rc;
+  if (token < 0 || token >= m->cfg.vocab) return set_err(m, LLM_ERR_INVALID_ARG, "token out of range");
+  if (m->len[seq] + 1 > m->cfg.max_seq) return set_err(m, LLM_ERR_CTX_FULL, "sequence is at max_seq");
+  // pageable source: staged at call time, so back-to-back asynchronous calls cannot race
+  const int32_t tok_host = token;
+  CK(cudaMemcpyAsync(m->d_tok + seq, &tok_host, 4, cudaMemcpyHostToDevice, m->stream), "token upload");
+  if ((rc = run_step(m, seq)) != LLM_OK) return rc;
+  m->len[seq] += 1;
+  bool host = false;
+  if ((rc = copy_out(m, logits_out, m->d_logits, (size_t)m->cfg.vocab * 4, &host)) != LLM_OK) return rc;
+  if ((rc = copy_out(m, argmax_out, m->d_argmax + seq, 4, &host)) != LLM_OK) return rc;
+  if (host) return check_status(m);
+  return LLM_OK;
+}
+
+int llm_prefill(llm_model* m, int32_t seq, const int32_t* tokens, int32_t n, float* logits_out, int32_t* argmax_out) {
+  int rc = check_model(m, seq);
+  if (rc) return rc;
+  if (!tokens || n <= 0) return set_err(m, LLM_ERR_INVALID_ARG, "empty prompt");
+  if (m->len[seq] + n > m->cfg.max_seq) return set_err(m, LLM_ERR_CTX_FULL, "prompt would exceed max_seq");
+  std::vector<int32_t> host_toks(n);
+  CK(cudaMemcpy(host_toks.data(), tokens, (size_t)n * 4, cudaMemcpyDefault), "prompt read");
+  for (int i = 0; i < n; ++i)
+    if (host_toks[i] < 0 || host_toks[i] >= m->cfg.vocab)
+      return set_err(m, LLM_ERR_INVALID_ARG, "prompt token out of range");
+  CK(cudaMemcpyAsync(m->d_prompt, host_toks.data(), (size_t)n * 4, cudaMemcpyHostToDevice, m->stream), "prompt upload");
+  for (int i = 0; i < n; ++i) {
+    CK(cudaMemcpyAsync(m->d_tok + seq, m->d_prompt + i, 4, cudaMemcpyDeviceToDevice, m->stream), "token copy");
+    if ((rc = run_step(m, seq)) != LLM_OK) return rc;
+  }
+  m->len[seq] += n;
+  bool host = false;
+  if ((rc = copy_out(m, logits_out, m->d_logits, (size_t)m->cfg.vocab * 4, &host)) != LLM_OK) return rc;
+  if ((rc = copy_out(m, argmax_out, m->d_argmax + seq, 4, &host)) != LLM_OK) return rc;
+  CK(cudaStreamSynchronize(m->stream), "prefill sync");  // host_toks outlives the upload
+  return check_status(m);
+}
+
+int llm_decode_greedy(llm_model* m, int32_t seq, int32_t first_token, int32_t n_steps, int32_t* tokens_out) {
+  int rc = check_model(m, seq);
+  if (rc) return rc;
+  if (n_steps <= 0 || !tokens_out) return set_err(m, LLM_ERR_INVALID_ARG, "n_steps <= 0 or null tokens_out");
+  if (first_token < 0 || first_token >= m->cfg.vocab) return set_err(m, LLM_ERR_INVALID_ARG, "token out of range");
+  if (m->len[seq] + n_steps > m->cfg.max_seq) return set_err(m, LLM_ERR_CTX_FULL, "steps would exceed max_seq");
+  const int32_t tok_host = first_token;  // pageable: staged at call time
+  CK(cudaMemcpyAsync(m->d_tok + seq, &tok_host, 4, cudaMemcpyHostToDevice, m->stream), "token upload");
+  CK(cudaMemsetAsync(m->d_hist_ctr, 0, 4, m->stream), "history reset");
+  for (int i = 0; i < n_steps; ++i)
+    if ((rc = run_step(m, seq)) != LLM_OK) return rc;
+  m->len[seq] += n_steps;
+  bool host = false;
+  if ((rc = copy_out(m, tokens_out, m->d_hist, (size_t)n_steps * 4, &host)) != LLM_OK) return rc;
+  if (host) return check_status(m);
+  return LLM_OK;
+}
+
+int llm_decode_step_batch(llm_model* m, const int32_t* tokens, int32_t n_seq, float* logits_out, int32_t* argmax_out) {
+  (void)tokens; (void)n_seq; (void)logits_out; (void)argmax_out;
+  if (!m) return set_err(nullptr, LLM_ERR_INVALID_ARG, "model is NULL");
+  return set_err(m, LLM_ERR_UNSUPPORTED, "batched decode step is not built yet");
+}
+
+int llm_kv_reset(llm_model* m, int32_t seq) {
+  if (!m) return set_err(nullptr, LLM_ERR_INVALID_ARG, "model is NULL");
+  if (m->poisoned) return m->poisoned;
+  if (seq < -1 || seq >= m->cfg.max_batch) return set_err(m, LLM_ERR_INVALID_ARG, "seq out of range");
+  for (int s = 0; s < m->cfg.max_batch; ++s)
+    if (seq == -1 || s == seq) {
+      m->len[s] = 0;
+      CK(cudaMemsetAsync(m->d_pos + s, 0, 4, m->stream), "position reset");
+    }
+  return LLM_OK;
+}
+
+static int kv_copy(llm_model* m, int32_t seq, int32_t layer, int32_t pos0, int32_t n, const uint16_t* src_k,
+                   const uint16_t* src_v, uint16_t* dst_k, uint16_t* dst_v, bool write) {
+  int rc = check_model(m, seq);
+  if (rc) return rc;
+  const llm_config& c = m->cfg;
+  if (layer < 0 || layer >= c.n_layers || pos0 < 0 || n <= 0) return set_err(m, LLM_ERR_INVALID_ARG, "bad layer/pos/n");
+  if (pos0 + n > c.max_seq) return set_err(m, LLM_ERR_CTX_FULL, "positions beyond max_seq");
+  const int hd = c.head_dim, H = c.n_kv_heads;
+  const size_t base = (((size_t)seq * c.n_layers + layer) * H) * c.max_seq * hd;
+  for (int g = 0; g < H; ++g) {
+    const size_t cache_off = base + ((size_t)g * c.max_seq + pos0) * hd;
+    for (int which = 0; which < 2; ++which) {
+      uint16_t* cache = (which ? m->d_v : m->d_k) + cache_off;
+      if (write) {
+        const uint16_t* s = (which ? src_v : src_k);
+        if (!s) return set_err(m, LLM_ERR_INVALID_ARG, "null key/value pointer");
+        CK(cudaMemcpy2DAsync(cache, hd * 2, s + (size_t)g * hd, (size_t)H * hd * 2, hd * 2, n, cudaMemcpyDefault,
+                             m->stream), "kv write");
+      } else {
+        uint16_t* dd = (which ? dst_v : dst_k);
+        if (!dd) return set_err(m, LLM_ERR_INVALID_ARG, "null key/value pointer");
+        CK(cudaMemcpy2DAsync(dd + (size_t)g * hd, (size_t)H * hd * 2, cache, hd * 2, hd * 2, n, cudaMemcpyDefault,
+                             m->stream), "kv read");
+      }
+    }
+  }
+  if (write) {
+    m->len[seq] = std::max(m->len[seq], pos0 + n);
+    m->h_stage[1] = m->len[seq];
+    CK(cudaMemcpyAsync(m->d_pos + seq, m->h_stage + 1, 4, cudaMemcpyHostToDevice, m->stream), "position set");
+  }
+  CK(cudaStreamSynchronize(m->stream), "kv sync");
+  return LLM_OK;
+}
+
+int llm_kv_write(llm_model* m, int32_t seq, int32_t layer, int32_t pos0, int32_t n, const uint16_t* k,
+                 const uint16_t* v) {
+  return kv_copy(m, seq, layer, pos0, n, k, v, nullptr, nullptr, true);
+}
+
+int llm_kv_read(llm_model* m, int32_t seq, int32_t layer, int32_t pos0, int32_t n, uint16_t* k, uint16_t* v) {
+  return kv_copy(m, seq, layer, pos0, n, nullptr, nullptr, k, v, false);
+}
+
+int llm_kv_len(const llm_model* m, int32_t seq) {
+  if (!m) return LLM_ERR_INVALID_ARG;
+  if (seq < 0 || seq >= m->cfg.max_batch) return LLM_ERR_INVALID_ARG;
+  return m->len[seq];
+}
+
+int llm_debug_hidden(llm_model* m, float* out) {
+  int rc = check_model(m, 0);
+  if (rc) return rc;
+  if (!out) return set_err(m, LLM_ERR_INVALID_ARG, "null output");
+  CK(cudaMemcpyAsync(out, m->d_xbuf, (size_t)(m->cfg.n_layers + 1) * m->cfg.dim * 4, cudaMemcpyDefault, m->stream),
+     "hidden copy");
+  CK(cudaStreamSynchronize(m->stream), "hidden sync");
+  return LLM_OK;
+}
+
+int llm_debug_unpack(llm_model* m, const char* name, uint8_t* codes, uint16_t* scales, uint16_t* mins) {
+  int rc = check_model(m, 0);
+  if (rc) return rc;
+  if (!name || !codes || !scales || !mins) return set_err(m, LLM_ERR_INVALID_ARG, "null argument");
+  auto it = m->places.find(name);
+  if (it == m->places.end()) return set_err(m, LLM_ERR_NOT_FOUND, std::string("no 4-bit tensor named ") + name);
+  const Mat& x = m->mats[it->second.mat];
+  const auto shp = m->shapes[name];
+  std::vector<uint8_t> units(x.bytes());
+  CK(cudaMemcpy(units.data(), m->d_arena + x.off, x.bytes(), cudaMemcpyDeviceToHost), "unpack copy");
+  std::memset(codes, 0, (size_t)shp.first * shp.second / 2);
+  unpack_q4(units.data(), x.G, codes, scales, mins, (int)shp.first, (int)shp.second, it->second.kind, it->second.row0);
+  return LLM_OK;
+}
+
+int llm_model_stats(const llm_model* m, llm_stats* out) {
+  if (!m || !out) return LLM_ERR_INVALID_ARG;
+  out->device_bytes = (int64_t)m->device_bytes;
+  int64_t w = 0;
+  for (const auto& x : m->mats) w += (int64_t)x.bytes();
+  out->weight_stream_bytes = w;
+  out->kv_bytes_per_pos = (int64_t)2 * m->cfg.n_layers * m->cfg.n_kv_heads * m->cfg.head_dim * 2;
+  out->kernels_per_step = m->kernels_per_step;
+  out->n_sm = m->n_sm;
+  return LLM_OK;
+}
+
+int llm_profile_step(llm_model* m, int32_t seq, int32_t token, llm_kernel_time* out, int32_t max_out) {
+  int rc = check_model(m, seq);
+  if (rc) return rc;
+  if (token < 0 || token >= m->cfg.vocab) return set_err(m, LLM_ERR_INVALID_ARG, "token out of range");
+  if (m->len[seq] + 1 > m->cfg.max_seq) return set_err(m, LLM_ERR_CTX_FULL, "sequence is at max_seq");
+  if (!out || max_out < 0) return set_err(m, LLM_ERR_INVALID_ARG, "null output");
+  const int32_t tok_host = token;
+  CK(cudaMemcpyAsync(m->d_tok + seq, &tok_host, 4, cudaMemcpyHostToDevice, m->stream), "token upload");
+  Prof prof;
+  prof.kv_len = m->len[seq] + 1;
+  cudaError_t e = enqueue_step(m, seq, &prof);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(m->stream);
+  for (size_t i = 0; e == cudaSuccess && i < prof.rec.size(); ++i)
+    e = cudaEventElapsedTime(&prof.rec[i].ms, prof.ev[2 * i], prof.ev[2 * i + 1]);
+  for (auto ev : prof.ev) cudaEventDestroy(ev);
+  if (e != cudaSuccess) return cuda_fail(m, e, "profile step");
+  m->len[seq] += 1;
+  const int n = (int)prof.rec.size();
+  for (int i = 0; i < n && i < max_out; ++i) out[i] = prof.rec[i];
+  rc = check_status(m);
+  return rc ? rc : n;
+}
+
+int llm_time_kernel(llm_model* m, int32_t seq, int32_t which, int32_t layer, int32_t n, float* ms,
+                    int64_t* bytes) {
+  int rc = check_model(m, seq);
+  if (rc) return rc;
+  const int L = m->cfg.n_layers;
+  if (which < 0 || which > 6 || n <= 0 || !ms || !bytes) return set_err(m, LLM_ERR_INVALID_ARG, "bad kernel/n");
+  if (layer < -1 || layer >= L) return set_err(m, LLM_ERR_INVALID_ARG, "bad layer");
+  if (m->len[seq] < 1) return set_err(m, LLM_ERR_INVALID_ARG, "run a step of the sequence first");
+  // attention re-reads position len-1 (and re-appends that slot with the values already there)
+  m->h_stage[2] = m->len[seq] - 1;
+  CK(cudaMemcpyAsync(m->d_pos + seq, m->h_stage + 2, 4, cudaMemcpyHostToDevice, m->stream), "position set");
+  // launch list: one kernel kind over the layers (or one layer), or every 4-bit GEMV of a step
+  std::vector<std::pair<int, int>> seqn;
+  if (which == 6) {
+    for (int l = 0; l < L; ++l)
+      for (int w : {W_QKV, W_WO, W_GU, W_DOWN}) seqn.push_back({w, l});
+    seqn.push_back({W_LM, 0});
+  } else if (which == W_LM) {
+    seqn.push_back({W_LM, 0});
+  } else {
+    for (int l = (layer < 0 ? 0 : layer); l < (layer < 0 ? L : layer + 1); ++l) seqn.push_back({which, l});
+  }
+  int64_t total_bytes = 0;
+  for (auto& x : seqn) total_bytes += launch_bytes(m, x.first, x.second, m->len[seq]);
+  cudaEvent_t e0, e1;
+  CK(cudaEventCreate(&e0), "event");
+  CK(cudaEventCreate(&e1), "event");
+  cudaError_t e = launch_one(m, seq, seqn[0].first, seqn[0].second, false);  // warm, no programmatic edge
+  if (e == cudaSuccess) e = cudaEventRecord(e0, m->stream);
+  for (int i = 0; e == cudaSuccess && i < n; ++i)
+    for (size_t j = 0; e == cudaSuccess && j < seqn.size(); ++j)
+      e = launch_one(m, seq, seqn[j].first, seqn[j].second, !(m->cfg.flags & LLM_NO_PDL));
+  if (e == cudaSuccess) e = cudaEventRecord(e1, m->stream);
+  if (e == cudaSuccess) e = cudaEventSynchronize(e1);
+  float t = 0.f;
+  if (e == cudaSuccess) e = cudaEventElapsedTime(&t, e0, e1);
+  cudaEventDestroy(e0);
+  cudaEventDestroy(e1);
+  if (e != cudaSuccess) return cuda_fail(m, e, "kernel timing");
+  m->h_stage[2] = m->len[seq];
+  CK(cudaMemcpyAsync(m->d_pos + seq, m->h_stage + 2, 4, cudaMemcpyHostToDevice, m->stream), "position restore");
+  *ms = t / (float)(n * seqn.size());
+  *bytes = total_bytes / (int64_t)seqn.size();
+  return check_status(m);
+}
+
+int llm_sync(llm_model* m) {
+  if (!m) return set_err(nullptr, LLM_ERR_INVALID_ARG, "model is NULL");
+  return check_status(m);
+}
+
+int llm_op_matvec(const llm_tensor* w, const float* x, float* y) {
+  if (!w || !x || !y) return set_err(nullptr, LLM_ERR_INVALID_ARG, "null argument");
+  const bool bf16 = w->dtype == LLM_BF16;
+  if (!bf16 && w->dtype != LLM_Q4G64) return set_err(nullptr, LLM_ERR_UNSUPPORTED, "dtype must be Q4G64 or BF16");
+  if (w->rows <= 0 || w->cols <= 0 || w->cols % 64 || w->cols > kMaxK || w->rows > (1 << 24))
+    return set_err(nullptr, LLM_ERR_UNSUPPORTED, "rows > 0 and cols a multiple of 64 up to 8192 required");
+  int n_sm = 0, dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) return cuda_fail(nullptr, e, "no CUDA device");
+  Mat mat;
+  mat.rows = (int)w->rows;
+  mat.cols = (int)w->cols;
+  mat.n_rt = (mat.rows + 31) / 32;
+  mat.G = mat.cols / 64;
+  mat.bf16 = bf16;
+  std::vector<uint8_t> units(mat.bytes(), 0);
+  if (bf16)
+    repack_bf16(units.data(), mat.G, static_cast<const uint16_t*>(w->data), mat.rows, mat.cols);
+  else
+    repack_q4(units.data(), mat.G, static_cast<const uint8_t*>(w->codes), static_cast<const uint16_t*>(w->scales),
+              static_cast<const uint16_t*>(w->mins), mat.rows, mat.cols, 0, 0);
+  GemvPlan g = plan_gemv(mat, n_sm);
+  uint8_t* d_units = nullptr;
+  float *d_x = nullptr, *d_y = nullptr, *d_part = nullptr;
+  int *d_status = nullptr, *d_cnt = nullptr;
+  const size_t part_bytes = (size_t)mat.n_rt * g.part.S * kTileRows * 4;
+  e = cudaMalloc(&d_units, units.size());
+  if (e == cudaSuccess) e = cudaMalloc(&d_x, (size_t)mat.cols * 4);
+  if (e == cudaSuccess) e = cudaMalloc(&d_y, (size_t)mat.rows * 4);
+  if (e == cudaSuccess) e = cudaMalloc(&d_part, part_bytes);
+  if (e == cudaSuccess) e = cudaMalloc(&d_cnt, (size_t)mat.n_rt * 4);
+  if (e == cudaSuccess) e = cudaMalloc(&d_status, 4);
+  if (e == cudaSuccess) e = cudaMemcpy(d_units, units.data(), units.size(), cudaMemcpyHostToDevice);
+  if (e == cudaSuccess) e = cudaMemcpy(d_x, x, (size_t)mat.cols * 4, cudaMemcpyDefault);
+  if (e == cudaSuccess) e = cudaMemset(d_status, 0, 4);
+  if (e == cudaSuccess) e = cudaMemset(d_cnt, 0, (size_t)mat.n_rt * 4);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(bf16 ? gemv_kernel<true> : gemv_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)g.smem);
+  int st = 0;
+  if (e == cudaSuccess) {
+    GemvParams p{};
+    p.units = d_units;
+    p.n_rt = mat.n_rt;
+    p.G = mat.G;
+    p.K = mat.G * 64;
+    p.rows = mat.rows;
+    p.unit_bytes = mat.unit_bytes();
+    p.nslot = g.nslot;
+    p.ring_bytes = g.ring;
+    p.part = g.part;
+    p.vec_mode = VEC_PLAIN;
+    p.vin = d_x;
+    p.epi = EPI_STORE;
+    p.out = d_y;
+    p.part_buf = d_part;
+    p.counters = d_cnt;
+    p.status = d_status;
+    e = launch(bf16 ? gemv_kernel<true> : gemv_kernel<false>, dim3(g.part.N), dim3(kGemvThreads), g.smem, 0, false, p);
+    if (e == cudaSuccess) e = cudaMemcpy(y, d_y, (size_t)mat.rows * 4, cudaMemcpyDefault);
+    if (e == cudaSuccess) e = cudaMemcpy(&st, d_status, 4, cudaMemcpyDeviceToHost);
+  }
+  cudaFree(d_units);
+  cudaFree(d_x);
+  cudaFree(d_y);
+  cudaFree(d_part);
+  cudaFree(d_cnt);
+  cudaFree(d_status);
+  if (e != cudaSuccess) return cuda_fail(nullptr, e, "matvec");
+  if (st & ST_TIMEOUT) return set_err(nullptr, LLM_ERR_TIMEOUT, "a device-side wait exceeded its limit");
+  return LLM_OK;
+}
+
+}  // extern "C"

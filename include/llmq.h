@@ -1,0 +1,211 @@
+/* llmq — GB300-native per-token decode step of a Llama/Qwen-style decoder with
+ * group-64 4-bit weights (W4A16), behind a plain C ABI.
+ *
+ * The operation is the decode step the aot-llm page ("p10node/aot-llm") draws
+ * in its sequence diagram and "static pipeline": embedding -> [RMSNorm ->
+ * q/k/v matvec -> RoPE -> attention over the KV cache -> o matvec + residual
+ * -> RMSNorm -> gate/up -> SwiGLU -> down + residual] x L -> RMSNorm -> logits
+ * -> greedy choice. Weights are "packed group-64 W4A16" (llmopt page); the KV
+ * cache is bf16 appended from f32 (zynfer page, stage M4). The shape of the
+ * API follows aot-llm's C library section (open a model, evaluate tokens, read
+ * n_vocab logits, reset a context) and the pytensor-ml issue's "immutable
+ * model, mutable context" and "fail at load with the missing capability named".
+ *
+ * Conventions for every entry point:
+ *   - returns LLM_OK (0) or a negative llm_status; llm_last_error() then holds
+ *     a one-line reason. LLM_ERR_CUDA and LLM_ERR_TIMEOUT poison the model
+ *     (every later call returns the same error); all other errors leave it
+ *     usable.
+ *   - a model is not thread-safe: the caller serialises calls on one model.
+ *   - output pointers marked "host or device" may point to either; the call
+ *     is synchronous when any output is in host memory.
+ *   - all device memory is owned by the library and allocated once, in
+ *     llm_model_create; no call in the token loop allocates.
+ */
+#ifndef LLMQ_H
+#define LLMQ_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define LLMQ_ABI_VERSION 1
+
+typedef enum {
+  LLM_OK = 0,
+  LLM_ERR_INVALID_ARG = -1,   /* null pointer, out-of-range index, bad size */
+  LLM_ERR_UNSUPPORTED = -2,   /* config the kernels do not cover; message names it */
+  LLM_ERR_OOM = -3,           /* device allocation failed at create */
+  LLM_ERR_CTX_FULL = -4,      /* position would reach max_seq */
+  LLM_ERR_CUDA = -5,          /* CUDA runtime error (poisons the model) */
+  LLM_ERR_TIMEOUT = -6,       /* a device-side wait hit its limit (poisons the model) */
+  LLM_ERR_NAN = -7,           /* the logit reduction saw a NaN */
+  LLM_ERR_NOT_FOUND = -8      /* tensor name unknown */
+} llm_status;
+
+typedef enum { LLM_F32 = 0, LLM_BF16 = 1, LLM_F16 = 2, LLM_Q4G64 = 3 } llm_dtype;
+
+/* llm_config.flags */
+#define LLM_NO_GRAPH 1u       /* launch the step's kernels one by one (debugging) */
+#define LLM_NO_PDL   2u       /* no programmatic dependent launch between kernels */
+
+typedef struct {
+  int32_t abi_version;        /* must equal LLMQ_ABI_VERSION */
+  int32_t dim, n_layers, n_heads, n_kv_heads, head_dim, ffn_dim, vocab;
+  float   norm_eps;           /* RMSNorm epsilon */
+  int32_t rope_neox;          /* 0: rotate pairs (2i, 2i+1); 1: pairs (i, i + head_dim/2) */
+  double  rope_theta;         /* RoPE base: theta_i = base^(-2i/head_dim) */
+  int32_t qk_norm;            /* 1: per-head RMSNorm of q and k before RoPE (Qwen3) */
+  int32_t tied_embedding;     /* 1: LM head is the bf16 embedding table */
+  int32_t max_seq;            /* KV capacity per sequence (positions) */
+  int32_t max_batch;          /* number of sequences (independent caches) */
+  uint32_t flags;             /* LLM_NO_GRAPH | LLM_NO_PDL */
+} llm_config;
+
+/* One input tensor in the canonical layout, host memory, caller-owned, only
+ * read during llm_model_create (the caller may free it afterwards).
+ *   LLM_Q4G64 linear [rows=out][cols=in], cols % 64 == 0:
+ *       codes  uint8 [rows][cols/2], element 2j in the low nibble of byte j,
+ *                    element 2j+1 in the high nibble;
+ *       scales fp16  [rows][cols/64];  mins fp16 [rows][cols/64];
+ *       weight w[r][c] = scale[r][c/64] * q + min[r][c/64].
+ *   LLM_F32 / LLM_BF16 dense [rows][cols] in `data` (norm weights: rows = 1).
+ * Names: "embed" (f32, or bf16 when tied) [vocab][dim]; "final_norm";
+ * per layer l: "L{l}.attn_norm", "L{l}.ffn_norm", "L{l}.q_norm", "L{l}.k_norm"
+ * (qk_norm only, [head_dim]); q4 "L{l}.wq" [n_heads*head_dim][dim],
+ * "L{l}.wk", "L{l}.wv" [n_kv_heads*head_dim][dim], "L{l}.wo"
+ * [dim][n_heads*head_dim], "L{l}.w_gate", "L{l}.w_up" [ffn_dim][dim],
+ * "L{l}.w_down" [dim][ffn_dim]; "lm_head" q4 [vocab][dim] when untied. */
+typedef struct {
+  const char* name;
+  int32_t dtype;              /* llm_dtype */
+  int64_t rows, cols;
+  const void* codes;          /* LLM_Q4G64 */
+  const void* scales;
+  const void* mins;
+  const void* data;           /* LLM_F32 / LLM_BF16 */
+} llm_tensor;
+
+typedef struct llm_model llm_model;
+
+typedef struct {
+  int64_t device_bytes;       /* all device memory owned by the model */
+  int64_t weight_stream_bytes;/* repacked weight bytes read per decode step */
+  int64_t kv_bytes_per_pos;   /* bf16 K+V bytes per cached position, all layers */
+  int32_t kernels_per_step;   /* kernel nodes in one batch-1 step */
+  int32_t n_sm;               /* SMs of the device the model lives on */
+} llm_stats;
+
+/* Validate the config, repack the 4-bit weights into the GPU tile layout, copy
+ * everything to the device, size all buffers and capture the step graph.
+ * cuda_stream: cudaStream_t to run on, or NULL for a stream the model owns.
+ * Errors: INVALID_ARG, UNSUPPORTED (head_dim not 64/128, cols % 64, heads not
+ * divisible, missing tensor...), NOT_FOUND, OOM, CUDA. On error *out = NULL. */
+int llm_model_create(const llm_config* cfg, const llm_tensor* tensors, int32_t n_tensors,
+                     void* cuda_stream, llm_model** out);
+
+/* Free every device allocation of the model. NULL is accepted. */
+void llm_model_destroy(llm_model* m);
+
+/* Append n tokens (host array) to sequence seq at positions len..len+n-1 and
+ * return the last position's fp32 logits [vocab] and greedy token. Runs n
+ * decode steps. logits_out / argmax_out: host or device, may be NULL.
+ * Errors: INVALID_ARG, CTX_FULL (len + n > max_seq), NAN, CUDA, TIMEOUT. */
+int llm_prefill(llm_model* m, int32_t seq, const int32_t* tokens, int32_t n,
+                float* logits_out, int32_t* argmax_out);
+
+/* One decode step of sequence seq for `token` at position len; len += 1.
+ * logits_out [vocab] fp32 and argmax_out (lowest index wins ties): host or
+ * device, may be NULL. Errors as llm_prefill. */
+int llm_decode_step(llm_model* m, int32_t seq, int32_t token, float* logits_out,
+                    int32_t* argmax_out);
+
+/* n_steps greedy steps starting from first_token; each step's argmax feeds the
+ * next step on the device (no host round trip per step). tokens_out
+ * [n_steps] (host or device) receives the token chosen at each step. */
+int llm_decode_greedy(llm_model* m, int32_t seq, int32_t first_token, int32_t n_steps,
+                      int32_t* tokens_out);
+
+/* One decode step for sequences 0..n_seq-1 at once (n_seq == max_batch), each
+ * at its own position. tokens [n_seq] (host or device); logits_out
+ * [n_seq][vocab], argmax_out [n_seq]: host or device, may be NULL. */
+int llm_decode_step_batch(llm_model* m, const int32_t* tokens, int32_t n_seq,
+                          float* logits_out, int32_t* argmax_out);
+
+/* Forget the cache of sequence seq (-1: all); its length becomes 0. */
+int llm_kv_reset(llm_model* m, int32_t seq);
+
+/* Copy bf16 keys/values [n][n_kv_heads][head_dim] (host or device) into
+ * positions pos0..pos0+n-1 of one layer of sequence seq; keys are stored as
+ * given (already rotated). The sequence length becomes max(len, pos0 + n).
+ * Errors: INVALID_ARG, CTX_FULL. */
+int llm_kv_write(llm_model* m, int32_t seq, int32_t layer, int32_t pos0, int32_t n,
+                 const uint16_t* k_bf16, const uint16_t* v_bf16);
+
+/* Read back bf16 keys/values [n][n_kv_heads][head_dim] (host or device). */
+int llm_kv_read(llm_model* m, int32_t seq, int32_t layer, int32_t pos0, int32_t n,
+                uint16_t* k_bf16, uint16_t* v_bf16);
+
+/* Current cache length of sequence seq, or a negative llm_status. */
+int llm_kv_len(const llm_model* m, int32_t seq);
+
+/* Residual stream after the embedding and after every layer of the last
+ * batch-1 step: out [(n_layers+1)][dim] fp32, host or device. */
+int llm_debug_hidden(llm_model* m, float* out);
+
+/* Undo the repack of one 4-bit tensor: write its canonical codes [rows][cols/2],
+ * scales and mins [rows][cols/64] (host) from the device copy. */
+int llm_debug_unpack(llm_model* m, const char* name, uint8_t* codes, uint16_t* scales,
+                     uint16_t* mins);
+
+/* Sizes and counts of the model (host struct). */
+int llm_model_stats(const llm_model* m, llm_stats* out);
+
+/* One launch of a decode step, as timed by llm_profile_step. */
+typedef struct {
+  int32_t kind;               /* 0 4-bit GEMV, 1 bf16 GEMV, 2 attention, 3 logits/argmax */
+  int32_t layer;              /* -1 for the LM head and the argmax */
+  int64_t bytes;              /* algorithmic HBM bytes: weight units, or K/V rows read */
+  float   ms;                 /* CUDA-event duration on the model's stream */
+} llm_kernel_time;
+
+/* Run one decode step of `token` like llm_decode_step, but eagerly and
+ * without programmatic dependent launch, with a CUDA event pair around every
+ * kernel. Writes up to max_out records (launch order) and returns the number
+ * of launches, or a negative llm_status. Meant for measurement, not the token
+ * loop (it creates and destroys events). */
+int llm_profile_step(llm_model* m, int32_t seq, int32_t token, llm_kernel_time* out, int32_t max_out);
+
+/* Time back-to-back launches of the batch-1 step's kernels of sequence seq
+ * (programmatic dependent launch between them, CUDA events on the model's
+ * stream) on the buffers the last step left. which = 0 q|k|v GEMV, 1
+ * attention, 2 o GEMV, 3 gate|up GEMV, 4 down GEMV: that kernel for `layer`,
+ * or for every layer in turn when layer = -1 (so that a weight set larger than
+ * L2 is streamed); 5 the LM-head GEMV; 6 every 4-bit/bf16 GEMV of one step in
+ * step order. The list is launched n times. Attention launches re-append the
+ * last position with the values already there. Writes the mean milliseconds
+ * per launch and the mean algorithmic bytes per launch. Needs at least one
+ * completed step of seq. */
+int llm_time_kernel(llm_model* m, int32_t seq, int32_t which, int32_t layer, int32_t n, float* ms,
+                    int64_t* bytes);
+
+/* Wait for all queued work of the model and report device-side errors. */
+int llm_sync(llm_model* m);
+
+/* Last error text of the model (m may be NULL: the last create error of this
+ * thread). Never NULL; owned by the library. */
+const char* llm_last_error(const llm_model* m);
+
+/* Kernel-level check: y = W x through the same repack and dequant-GEMV kernel
+ * the decode step uses (plain store epilogue). w: one LLM_Q4G64 or LLM_BF16
+ * tensor (host, cols a multiple of 64 up to 8192); x [cols], y [rows] fp32
+ * host arrays. Allocates and frees its
+ * own device memory; not for the token loop. */
+int llm_op_matvec(const llm_tensor* w, const float* x, float* y);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* LLMQ_H */

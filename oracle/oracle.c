@@ -293,6 +293,7 @@ int32_t orc_step(const orc_model* m, orc_cache* cache, int32_t tok, double* logi
     /* the query attends to cached positions 0..pos, itself included */
     int32_t n_att = pos + 1;
     if (g_mut == ORC_MUT_CACHE_FRONTIER && pos > 0) n_att = pos;
+#pragma omp parallel for schedule(static)
     for (int32_t h = 0; h < Hq; ++h) {
       int32_t g = kv_head_of(c, h);
       int64_t base = ((int64_t)l * Hkv + g) * cache->cap * hd;

@@ -1,0 +1,272 @@
+"""GPU parity: the CUDA path through the C ABI against the CPU oracle.
+
+Bars (element by element, on the same seeded inputs):
+  * 4-bit code unpacking and KV-cache indexing: bit-exact;
+  * per-layer hidden states: relative L2 <= 2e-3;
+  * logits: max|d| <= 5e-3 * max|logit| at every compared step;
+  * greedy tokens identical for the whole run on the three batch-1 workloads.
+Kernel-level GEMV checks use a tighter bar derived from fp32 accumulation
+(max|d| <= 1e-5 * max|y|, relative L2 <= 2e-6).
+"""
+import numpy as np
+import pytest
+import torch
+
+import bit_quantized_token_gb300 as bq
+import oracle
+import synth
+
+pytestmark = pytest.mark.gpu
+
+HIDDEN_RL2 = 2e-3
+LOGIT_REL = 5e-3
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    assert torch.cuda.is_available()
+    bq.build()
+    oracle.build()
+
+
+def rel_l2(a, b):
+    return float(np.linalg.norm(np.asarray(a, np.float64) - b) / np.linalg.norm(b))
+
+
+# ---------------------------------------------------------------- kernel level
+
+@pytest.mark.parametrize("rows,cols", [(3, 64), (5, 128), (7, 5632), (33, 256), (2560, 2048), (2048, 5632),
+                                       (1000, 1024), (96, 3072)])
+def test_q4_matvec_matches_oracle(rows, cols):
+    rng = np.random.default_rng(rows + cols)
+    t = synth._q4(rng, rows, cols)
+    x = rng.standard_normal(cols).astype(np.float32)
+    y = bq.matvec(t, x)
+    ref = oracle.matvec(t, x.astype(np.float64))
+    assert np.abs(y - ref).max() <= 1e-5 * np.abs(ref).max()
+    assert rel_l2(y, ref) <= 2e-6
+
+
+@pytest.mark.parametrize("rows,cols", [(32, 64), (1000, 1024), (4747, 1024)])
+def test_bf16_matvec_matches_dense(rows, cols):
+    rng = np.random.default_rng(rows)
+    e = synth.bf16_bits_from_f32(rng.normal(0, 0.02, (rows, cols)).astype(np.float32))
+    x = rng.standard_normal(cols).astype(np.float32)
+    y = bq.matvec(dict(kind="bf16", data=e, rows=rows, cols=cols), x)
+    dense = (e.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    ref = dense @ x.astype(np.float64)
+    assert np.abs(y - ref).max() <= 1e-5 * np.abs(ref).max()
+
+
+# ---------------------------------------------------------------- bit-exact layout
+
+def _mini(idx, **kw):
+    return synth.workload(idx, **kw)
+
+
+@pytest.mark.parametrize("cfg", [synth.workload(0), synth.workload(2, n_layers=2, vocab=4096)],
+                         ids=["tiny", "qwen-shape-2-layers"])
+def test_unpack_is_bit_exact(cfg):
+    w = synth.make_weights(cfg)
+    with bq.Model(cfg, w, max_seq=32) as m:
+        for name, t in w.items():
+            if t["kind"] != "q4":
+                continue
+            codes, scales, mins = m.unpack(name, t["rows"], t["cols"])
+            assert np.array_equal(codes, t["codes"]), name
+            assert np.array_equal(scales, t["scales"].view(np.uint16)), name
+            assert np.array_equal(mins, t["mins"].view(np.uint16)), name
+
+
+def test_kv_write_read_roundtrip_and_append_slot():
+    cfg = synth.workload(0)
+    w = synth.make_weights(cfg)
+    L, H, hd, cap = cfg["n_layers"], cfg["n_kv_heads"], cfg["head_dim"], 24
+    with bq.Model(cfg, w, max_seq=cap, max_batch=2) as m:
+        # position-coded fill of every slot of sequence 1
+        code = lambda l, p: ((np.arange(H * hd, dtype=np.uint16) + 37 * p + 1000 * l) & 0x3FFF).reshape(1, H, hd)
+        for l in range(L):
+            k = np.concatenate([code(l, p) for p in range(cap)])
+            m.kv_write(1, l, 0, k, k ^ 0x4000)
+        for l in range(L):
+            k, v = m.kv_read(1, l, 0, cap)
+            assert np.array_equal(k, np.concatenate([code(l, p) for p in range(cap)]))
+            assert np.array_equal(v, k ^ 0x4000)
+        # make positions 0..4 the real cache, then append one token at position 5
+        m.kv_reset(1)
+        prompt = synth.make_prompt(cfg)[:5]
+        ref_model = oracle.OracleModel(cfg, w)
+        ref_cache = ref_model.new_cache(cap)
+        for t in prompt:
+            ref_model.step(ref_cache, int(t))
+        for l in range(L):
+            m.kv_write(1, l, 0, np.transpose(ref_cache.k[l, :, :5], (1, 0, 2)).copy(),
+                       np.transpose(ref_cache.v[l, :, :5], (1, 0, 2)).copy())
+        assert m.kv_len(1) == 5
+        before = [m.kv_read(1, l, 0, cap) for l in range(L)]
+        m.decode_step(1, 11)
+        ref_model.step(ref_cache, 11)
+        assert m.kv_len(1) == 6
+        for l in range(L):
+            k, v = m.kv_read(1, l, 0, cap)
+            # only slot 5 changed, in every layer and head
+            assert np.array_equal(k[:5], before[l][0][:5]) and np.array_equal(k[6:], before[l][0][6:])
+            assert np.array_equal(v[:5], before[l][1][:5]) and np.array_equal(v[6:], before[l][1][6:])
+            # the appended slot holds this token's bf16 K/V (oracle value within one bf16 ulp)
+            for got, ref in ((k[5], ref_cache.k[l, :, 5]), (v[5], ref_cache.v[l, :, 5])):
+                gf = (got.astype(np.uint32) << 16).view(np.float32)
+                rf = (ref.astype(np.uint32) << 16).view(np.float32)
+                assert np.all(np.abs(gf - rf) <= np.abs(rf) * 2 ** -7 + 1e-30)
+        # sequence 0 was never touched
+        assert m.kv_len(0) == 0
+
+
+# ---------------------------------------------------------------- end to end
+
+def gpu_run(m, cfg, prompt, n_steps, seq=0, hidden=False):
+    """prefill(prompt) -> t0, then n_steps decode_step calls feeding back argmax."""
+    V = cfg["vocab"]
+    logits = np.empty((n_steps + 1, V), np.float32)
+    am = np.zeros(1, np.int32)
+    hid = []
+    m.prefill(seq, prompt, logits[0], am)
+    toks = [int(am[0])]
+    if hidden:
+        hid.append(m.hidden())
+    for i in range(n_steps):
+        m.decode_step(seq, toks[-1], logits[i + 1], am)
+        toks.append(int(am[0]))
+        if hidden:
+            hid.append(m.hidden())
+    return np.array(toks), logits, (np.array(hid) if hidden else None)
+
+
+def check_against_oracle(cfg, toks, logits, hid, ref, greedy=True):
+    if greedy:
+        srt = np.sort(ref["logits"], axis=1)
+        margins = srt[:, -1] - srt[:, -2]
+        mism = np.nonzero(toks != ref["tokens"])[0]
+        assert mism.size == 0, (f"greedy token mismatch at steps {mism[:5]}, oracle margin there "
+                                f"{margins[mism[:5]]}, gpu tokens {toks[mism[:5]]} vs {ref['tokens'][mism[:5]]}")
+    err = np.abs(logits - ref["logits"]).max(axis=1) / np.abs(ref["logits"]).max(axis=1)
+    assert err.max() <= LOGIT_REL, f"logit error {err.max():.3e} at step {err.argmax()}"
+    if hid is not None:
+        for s in range(hid.shape[0]):
+            for l in range(hid.shape[1]):
+                r = rel_l2(hid[s, l], ref["hidden"][s, l])
+                assert r <= HIDDEN_RL2, f"hidden rel L2 {r:.3e} at step {s} layer {l}"
+    return err.max()
+
+
+@pytest.mark.parametrize("flags", [0, bq.LLM_NO_GRAPH, bq.LLM_NO_PDL, bq.LLM_NO_GRAPH | bq.LLM_NO_PDL],
+                         ids=["graph+pdl", "eager+pdl", "graph", "eager"])
+def test_tiny_llama_greedy_matches_oracle(flags):
+    cfg = synth.workload(0)
+    w = synth.make_weights(cfg)
+    prompt = synth.make_prompt(cfg)
+    n = cfg["decode_steps"]
+    ref = oracle.greedy_run(oracle.OracleModel(cfg, w), prompt, n, hidden=True)
+    with bq.Model(cfg, w, max_seq=64, max_batch=2, flags=flags) as m:
+        toks, logits, hid = gpu_run(m, cfg, prompt, n, seq=1, hidden=True)
+        check_against_oracle(cfg, toks, logits, hid, ref)
+        # the device-fed greedy loop gives the same tokens
+        m.kv_reset(1)
+        am = np.zeros(1, np.int32)
+        m.prefill(1, prompt, None, am)
+        assert int(am[0]) == ref["tokens"][0]
+        assert np.array_equal(m.decode_greedy(1, int(am[0]), n), ref["tokens"][1:])
+
+
+def test_bit_reproducible():
+    cfg = synth.workload(0)
+    w = synth.make_weights(cfg)
+    prompt = synth.make_prompt(cfg)
+    outs = []
+    for _ in range(2):
+        with bq.Model(cfg, w, max_seq=64) as m:
+            outs.append(gpu_run(m, cfg, prompt, 6)[1])
+    assert np.array_equal(outs[0], outs[1])
+
+
+def test_qwen_shape_two_layers_full_vocab():
+    # tied bf16 LM head over the full 151936-token vocabulary, q/k norm, NEOX
+    cfg = synth.workload(2, n_layers=2)
+    w = synth.make_weights(cfg)
+    prompt = synth.make_prompt(cfg)
+    ref = oracle.greedy_run(oracle.OracleModel(cfg, w), prompt, 20, hidden=True)
+    with bq.Model(cfg, w, max_seq=64) as m:
+        toks, logits, hid = gpu_run(m, cfg, prompt, 20, hidden=True)
+    check_against_oracle(cfg, toks, logits, hid, ref)
+
+
+@pytest.mark.parametrize("idx", [1, 2], ids=["tinyllama-1.1b", "qwen3-0.6b"])
+def test_full_size_greedy_matches_oracle(idx):
+    cfg = synth.workload(idx)
+    w = synth.make_weights(cfg)
+    prompt = synth.make_prompt(cfg)
+    n = cfg["decode_steps"]
+    ref = oracle.greedy_run(oracle.OracleModel(cfg, w), prompt, n, hidden=True)
+    with bq.Model(cfg, w, max_seq=len(prompt) + n + 1) as m:
+        toks, logits, hid = gpu_run(m, cfg, prompt, n, hidden=True)
+    check_against_oracle(cfg, toks, logits, hid, ref)
+
+
+def test_long_context_teacher_forced():
+    # 4096 pre-filled positions of N(0,1) bf16 K/V, then 64 steps fed with the
+    # oracle's greedy tokens; logits compared at every step
+    cfg = synth.workload(3)
+    w = synth.make_weights(cfg)
+    n_pre, n = cfg["prefill_kv"], cfg["decode_steps"]
+    cap = n_pre + n + 1
+    om = oracle.OracleModel(cfg, w)
+    cache = om.new_cache(cap)
+    with bq.Model(cfg, w, max_seq=cap) as m:
+        for l in range(cfg["n_layers"]):
+            k, v = synth.make_prefilled_kv(cfg, l, 0, n_pre)
+            cache.fill(l, k, v)
+            m.kv_write(0, l, 0, k, v)
+        cache.set_len(n_pre)
+        tok = int(synth.make_first_tokens(cfg, 1)[0])
+        logits = np.empty(cfg["vocab"], np.float32)
+        worst = 0.0
+        for i in range(n):
+            ref, ref_h = om.step(cache, tok, hidden=True)
+            m.decode_step(0, tok, logits)
+            err = np.abs(logits - ref).max() / np.abs(ref).max()
+            worst = max(worst, err)
+            assert err <= LOGIT_REL, f"step {i}: logit error {err:.3e}"
+            hid = m.hidden()
+            for l in range(cfg["n_layers"] + 1):
+                assert rel_l2(hid[l], ref_h[l]) <= HIDDEN_RL2
+            tok = oracle.argmax_f32(ref)
+        assert m.kv_len(0) == n_pre + n
+
+
+# ---------------------------------------------------------------- errors
+
+def test_error_paths_leave_model_usable():
+    cfg = synth.workload(0)
+    w = synth.make_weights(cfg)
+    with bq.Model(cfg, w, max_seq=4) as m:
+        with pytest.raises(bq.LlmError) as e:
+            m.decode_step(0, cfg["vocab"])
+        assert e.value.code == -1
+        with pytest.raises(bq.LlmError) as e:
+            m.prefill(0, [1, 2, 3, 4, 5])
+        assert e.value.code == -4
+        m.prefill(0, [1, 2, 3])
+        m.decode_step(0, 4)
+        with pytest.raises(bq.LlmError) as e:
+            m.decode_step(0, 5)
+        assert e.value.code == -4
+        m.kv_reset(0)
+        m.decode_step(0, 5)
+    bad = dict(cfg, head_dim=96)
+    with pytest.raises(bq.LlmError) as e:
+        bq.Model(bad, w, max_seq=8)
+    assert e.value.code == -2 and "head_dim" in str(e.value)
+    w2 = dict(w)
+    del w2["L1.wo"]
+    with pytest.raises(bq.LlmError) as e:
+        bq.Model(cfg, w2, max_seq=8)
+    assert e.value.code == -8 and "L1.wo" in str(e.value)
