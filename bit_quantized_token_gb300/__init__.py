@@ -30,7 +30,7 @@ STATUS = {0: "OK", -1: "INVALID_ARG", -2: "UNSUPPORTED", -3: "OOM", -4: "CTX_FUL
 EXPORTS = ["llm_model_create", "llm_model_destroy", "llm_prefill", "llm_decode_step", "llm_decode_greedy",
            "llm_decode_step_batch", "llm_kv_reset", "llm_kv_write", "llm_kv_read", "llm_kv_len",
            "llm_debug_hidden", "llm_debug_unpack", "llm_model_stats", "llm_profile_step", "llm_time_kernel", "llm_sync",
-           "llm_last_error", "llm_op_matvec"]
+           "llm_last_error", "llm_op_matvec", "llm_matvec_noalloc"]
 
 
 def nvcc_command(out: str = LIB_PATH) -> list[str]:
@@ -111,6 +111,7 @@ def lib() -> C.CDLL:
             "llm_sync": (i32, [P]),
             "llm_last_error": (C.c_char_p, [P]),
             "llm_op_matvec": (i32, [C.POINTER(Tensor), P, P]),
+            "llm_matvec_noalloc": (i32, [P, C.c_char_p, P, P, P]),
         }
         for name, (res, args) in sig.items():
             f = getattr(L, name)
@@ -284,3 +285,12 @@ def matvec(t: dict, x) -> np.ndarray:
     y = np.empty(int(t["rows"]), np.float32)
     _check(lib().llm_op_matvec(table, x.ctypes.data, y.ctypes.data))
     return y
+
+
+def matvec_noalloc(model: Model, name: str, x, y, stream: int | None = None) -> None:
+    """y = W x with a weight matrix resident in `model`; x, y are device buffers.
+
+    Allocates no device memory (scratch is a static device array inside the
+    library); see llm_matvec_noalloc in include/llmq.h.
+    """
+    _check(lib().llm_matvec_noalloc(model.h, name.encode(), _ptr(x), _ptr(y), stream), model.h)

@@ -13,6 +13,7 @@
 #include <cmath>
 #include <cstdio>
 #include <cstring>
+#include <mutex>
 #include <string>
 #include <thread>
 #include <unordered_map>
@@ -144,6 +145,7 @@ Part make_part(int n_rt, int G, int n_cta) {
 
 struct llm_model {
   llm_config cfg{};
+  int device = 0;
   int n_sm = 0, q_dim = 0, kv_dim = 0, gq = 0;
   cudaStream_t stream = nullptr;
   bool own_stream = false;
@@ -588,6 +590,7 @@ int llm_model_create(const llm_config* cfg, const llm_tensor* tensors, int32_t n
     cudaError_t e = cudaGetDevice(&dev);
     if (e == cudaSuccess) e = cudaDeviceGetAttribute(&m->n_sm, cudaDevAttrMultiProcessorCount, dev);
     if (e != cudaSuccess) return fail(cuda_fail(nullptr, e, "no CUDA device"));
+    m->device = dev;
   }
   const int L = c.n_layers, d = c.dim, F = c.ffn_dim, hd = c.head_dim, V = c.vocab;
 
@@ -1131,3 +1134,106 @@ int llm_op_matvec(const llm_tensor* w, const float* x, float* y) {
 }
 
 }  // extern "C"
+
+// ---- matvec without device allocation ---------------------------------------
+// Scratch of llm_matvec_noalloc: split-row-tile partial sums, arrival
+// counters and a status word, in one file-scope device array. Every GPU that
+// loads this library holds it (4.2 MiB) until the process exits.
+namespace {
+constexpr size_t kNoAllocPartFloats = size_t(1) << 20;  // 4 MiB of partial sums
+constexpr int kNoAllocCounters = 32768;                 // row tiles (32 rows each)
+constexpr size_t kNoAllocBytes = kNoAllocPartFloats * 4 + (size_t)kNoAllocCounters * 4 + 256;
+constexpr int kMaxDevices = 64;
+std::mutex g_noalloc_mu;
+void* g_noalloc_ptr[kMaxDevices] = {};
+}  // namespace
+
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocBytes];
+
+extern "C" int llm_matvec_noalloc(const llm_model* m, const char* name, const float* x, float* y,
+                                  void* cuda_stream) {
+  if (!m || !name || !x || !y) return set_err(nullptr, LLM_ERR_INVALID_ARG, "null argument");
+  llm_model* mm = const_cast<llm_model*>(m);
+  if (m->poisoned) return m->poisoned;
+  int dev = -1;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(mm, e, "cudaGetDevice");
+  if (dev != m->device || dev >= kMaxDevices)
+    return set_err(mm, LLM_ERR_INVALID_ARG, "the model's device must be the current device");
+  if (!is_device_ptr(x) || !is_device_ptr(y)) return set_err(mm, LLM_ERR_INVALID_ARG, "x and y must be device memory");
+  // the weight rows: a 4-bit tensor stored as a contiguous row range, or the tied bf16 LM head
+  const Mat* mat = nullptr;
+  int row0 = 0, rows = 0;
+  const std::string nm(name);
+  if (nm == "embed" && m->cfg.tied_embedding) {
+    mat = &m->lm.m;
+    rows = m->cfg.vocab;
+  } else {
+    auto it = m->places.find(nm);
+    if (it == m->places.end() || it->second.kind != 0)
+      return set_err(mm, LLM_ERR_NOT_FOUND, "no weight matrix " + nm + " stored as a contiguous row range");
+    mat = &m->mats[it->second.mat];
+    row0 = it->second.row0;
+    rows = (int)m->shapes.at(nm).first;
+  }
+  Mat sub = *mat;
+  sub.off = mat->off + (size_t)(row0 / 32) * mat->G * mat->unit_bytes();
+  sub.rows = rows;
+  sub.n_rt = (rows + 31) / 32;
+  const GemvPlan g = plan_gemv(sub, m->n_sm);
+  const size_t part_floats = (size_t)sub.n_rt * g.part.S * kTileRows;
+  if (part_floats > kNoAllocPartFloats || sub.n_rt > kNoAllocCounters)
+    return set_err(mm, LLM_ERR_UNSUPPORTED,
+                   nm + " needs " + std::to_string(part_floats * 4 + sub.n_rt * 4) + " bytes of scratch; the static "
+                   "scratch holds " + std::to_string(kNoAllocPartFloats * 4) + " bytes of partials and " +
+                   std::to_string(kNoAllocCounters) + " row-tile counters");
+  // one-time set-up on this device: the device address of the static array
+  void* base = nullptr;
+  {
+    std::lock_guard<std::mutex> lk(g_noalloc_mu);
+    if (!g_noalloc_ptr[dev]) {
+      e = cudaGetSymbolAddress(&g_noalloc_ptr[dev], g_noalloc_scratch);
+      if (e != cudaSuccess) {
+        g_noalloc_ptr[dev] = nullptr;
+        return cuda_fail(mm, e, "cudaGetSymbolAddress of the static scratch");
+      }
+    }
+    base = g_noalloc_ptr[dev];
+  }
+  float* part = static_cast<float*>(base);
+  int* counters = reinterpret_cast<int*>(static_cast<unsigned char*>(base) + kNoAllocPartFloats * 4);
+  int* status = counters + kNoAllocCounters;
+  cudaStream_t st = static_cast<cudaStream_t>(cuda_stream);
+  // the array keeps the previous call's contents: counters and status must start at zero
+  e = cudaMemsetAsync(counters, 0, (size_t)sub.n_rt * 4, st);
+  if (e == cudaSuccess) e = cudaMemsetAsync(status, 0, 4, st);
+  if (e != cudaSuccess) return cuda_fail(mm, e, "scratch clear");
+  GemvParams p{};
+  p.units = m->d_arena + sub.off;
+  p.n_rt = sub.n_rt;
+  p.G = sub.G;
+  p.K = sub.G * 64;
+  p.rows = rows;
+  p.unit_bytes = sub.unit_bytes();
+  p.nslot = g.nslot;
+  p.ring_bytes = g.ring;
+  p.part = g.part;
+  p.vec_mode = VEC_PLAIN;
+  p.vin = x;
+  p.epi = EPI_STORE;
+  p.out = y;
+  p.part_buf = part;
+  p.counters = counters;
+  p.status = status;
+  e = sub.bf16 ? launch(gemv_kernel<true>, dim3(g.part.N), dim3(kGemvThreads), g.smem, st, false, p)
+               : launch(gemv_kernel<false>, dim3(g.part.N), dim3(kGemvThreads), g.smem, st, false, p);
+  int h_status = 0;
+  if (e == cudaSuccess) e = cudaMemcpyAsync(&h_status, status, 4, cudaMemcpyDeviceToHost, st);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+  if (e != cudaSuccess) return cuda_fail(mm, e, "matvec launch");
+  if (h_status & ST_TIMEOUT) {
+    mm->poisoned = LLM_ERR_TIMEOUT;
+    return set_err(mm, LLM_ERR_TIMEOUT, "a device-side wait exceeded its limit");
+  }
+  return LLM_OK;
+}

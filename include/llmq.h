@@ -205,6 +205,28 @@ const char* llm_last_error(const llm_model* m);
  * own device memory; not for the token loop. */
 int llm_op_matvec(const llm_tensor* w, const float* x, float* y);
 
+/* y = W x with one weight matrix already resident in model m, without any
+ * device allocation. No page has a counterpart: it exists for callers that
+ * cannot call cudaMalloc at this point -- a process whose device memory was
+ * handed to its own pool at start-up (a new cudaMalloc would fail or bypass
+ * the pool's accounting), or a latency-critical loop where cudaMalloc/cudaFree
+ * would stall (cudaFree synchronises the device). The caller passes x [cols]
+ * and y [rows] as fp32 device buffers (y must not overlap x) on the model's
+ * device, which must be the current device; `name` is a 4-bit tensor stored
+ * as a contiguous row range ("L{l}.wq", "L{l}.wk", "L{l}.wv", "L{l}.wo",
+ * "L{l}.w_down", "lm_head") or "embed" for a tied bf16 LM head.
+ * Scratch (split-row-tile partial sums, arrival counters, a status word) lives
+ * in one file-scope device array of 4 MiB + 128 KiB + 256 B that every GPU
+ * loading the library keeps until exit; a matrix needing more partial-sum or
+ * counter space is rejected with LLM_ERR_UNSUPPORTED naming both sizes. The
+ * first call on a device looks up the array's device address
+ * (cudaGetSymbolAddress): make that first call before any stream capture.
+ * Every call shares the array and clears its counters and status on
+ * `cuda_stream` (NULL: the legacy default stream) before the kernel: calls
+ * whose work overlaps on the GPU race on it, so serialise them. The call
+ * returns after y is written. */
+int llm_matvec_noalloc(const llm_model* m, const char* name, const float* x, float* y, void* cuda_stream);
+
 #ifdef __cplusplus
 }
 #endif
