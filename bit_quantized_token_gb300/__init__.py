@@ -22,7 +22,7 @@ SOURCES = [os.path.join(_HERE, "csrc", f) for f in ("llmq.cu", "kernels.cuh", "c
 
 ABI_VERSION = 1
 LLM_F32, LLM_BF16, LLM_F16, LLM_Q4G64 = 0, 1, 2, 3
-LLM_NO_GRAPH, LLM_NO_PDL = 1, 2
+LLM_NO_GRAPH, LLM_NO_PDL, LLM_MULTI_KERNEL = 1, 2, 4
 STATUS = {0: "OK", -1: "INVALID_ARG", -2: "UNSUPPORTED", -3: "OOM", -4: "CTX_FULL", -5: "CUDA",
           -6: "TIMEOUT", -7: "NAN", -8: "NOT_FOUND"}
 

@@ -10,7 +10,8 @@ namespace llmq {
 constexpr int kGroup = 64;           // 4-bit group size along the input dimension
 constexpr int kTileRows = 32;        // rows per unit: lane l of a warp owns row l
 constexpr int kQ4UnitBytes = 1152;   // 32 rows x 64 codes (1024 B) + 32 x half2(scale, min)
-constexpr int kBF16UnitBytes = 4096; // 32 rows x 64 bf16
+constexpr int kBF16UnitBytes = 1024; // 32 rows x 16 bf16
+constexpr int kBF16UnitCols = 16;
 constexpr int kCWarps = 8;           // consumer warps per GEMV CTA
 constexpr int kChunkUnits = kCWarps; // units per ring slot: one per consumer warp
 constexpr int kGemvThreads = (kCWarps + 1) * 32;  // + one producer warp
@@ -119,15 +120,23 @@ __device__ __forceinline__ void sub2(float& d0, float& d1, float a0, float a1, f
 // CTA c owns units [U*c/N, U*(c+1)/N). A row tile rt (units rt*G .. rt*G+G-1)
 // has S partial-sum slots; the CTAs that touch it fill slots 0, 1, ... in CTA
 // order and the remaining slots stay zero (buffers are zeroed once at create).
+// U * N < 2^32 always holds (U < 2^24 units, N <= 256 CTAs), so 32-bit
+// unsigned arithmetic is exact.
 struct Part {
   int U, N, G, S;  // units, CTAs, units per row tile, slots per row tile
-  __host__ __device__ int begin(int c) const { return static_cast<int>((int64_t)U * c / N); }
-  __host__ __device__ int cta_of(int u) const { return static_cast<int>(((int64_t)(u + 1) * N - 1) / U); }
+  __host__ __device__ int begin(int c) const { return static_cast<int>((unsigned)U * (unsigned)c / (unsigned)N); }
+  __host__ __device__ int cta_of(int u) const {
+    return static_cast<int>(((unsigned)(u + 1) * (unsigned)N - 1u) / (unsigned)U);
+  }
   __host__ __device__ int first_cta(int rt) const { return cta_of(rt * G); }
   __host__ __device__ int n_contrib(int rt) const { return cta_of(rt * G + G - 1) - cta_of(rt * G) + 1; }
 };
 
 __device__ __forceinline__ float silu(float z) { return z / (1.0f + expf(-z)); }
+// Same function with the hardware exponential and division (relative error
+// a few 1e-7 over the activation range); __fdividef gives the right limit 0
+// when exp(-z) overflows.
+__device__ __forceinline__ float silu_fast(float z) { return __fdividef(z, 1.0f + __expf(-z)); }
 
 __device__ __forceinline__ float bf16_bits_to_f32(uint16_t b) {
   return __uint_as_float(static_cast<uint32_t>(b) << 16);

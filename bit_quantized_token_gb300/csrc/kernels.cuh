@@ -77,21 +77,25 @@ __device__ __forceinline__ float q4_unit_dot(const uint8_t* __restrict__ ub, con
   return fmaf(s.x, d, s.y * xsum);
 }
 
-// bf16 unit layout (4096 B, 32 rows x 64 inputs): 8 x 32 x 16 B, index
+// bf16 unit layout (1024 B, 32 rows x 16 inputs): 2 x 32 x 16 B, index
 // (k*32 + lane): row `lane`, inputs 8k .. 8k+7.
 __device__ __forceinline__ float bf16_unit_dot(const uint8_t* __restrict__ ub, const float* __restrict__ xg,
                                                int lane) {
+  const uint4 c0 = *reinterpret_cast<const uint4*>(ub + lane * 16);
+  const uint4 c1 = *reinterpret_cast<const uint4*>(ub + 512 + lane * 16);
+  const float4 x0 = *reinterpret_cast<const float4*>(xg);
+  const float4 x1 = *reinterpret_cast<const float4*>(xg + 4);
+  const float4 x2 = *reinterpret_cast<const float4*>(xg + 8);
+  const float4 x3 = *reinterpret_cast<const float4*>(xg + 12);
   float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
-#pragma unroll
-  for (int k = 0; k < 8; ++k) {
-    const uint4 c = *reinterpret_cast<const uint4*>(ub + (k * 32 + lane) * 16);
-    const float4 xa = *reinterpret_cast<const float4*>(xg + 8 * k);
-    const float4 xb = *reinterpret_cast<const float4*>(xg + 8 * k + 4);
-    fma2(a0, a1, __uint_as_float(c.x << 16), __uint_as_float(c.x & 0xFFFF0000u), xa.x, xa.y);
-    fma2(a2, a3, __uint_as_float(c.y << 16), __uint_as_float(c.y & 0xFFFF0000u), xa.z, xa.w);
-    fma2(a0, a1, __uint_as_float(c.z << 16), __uint_as_float(c.z & 0xFFFF0000u), xb.x, xb.y);
-    fma2(a2, a3, __uint_as_float(c.w << 16), __uint_as_float(c.w & 0xFFFF0000u), xb.z, xb.w);
-  }
+  fma2(a0, a1, __uint_as_float(c0.x << 16), __uint_as_float(c0.x & 0xFFFF0000u), x0.x, x0.y);
+  fma2(a2, a3, __uint_as_float(c0.y << 16), __uint_as_float(c0.y & 0xFFFF0000u), x0.z, x0.w);
+  fma2(a0, a1, __uint_as_float(c0.z << 16), __uint_as_float(c0.z & 0xFFFF0000u), x1.x, x1.y);
+  fma2(a2, a3, __uint_as_float(c0.w << 16), __uint_as_float(c0.w & 0xFFFF0000u), x1.z, x1.w);
+  fma2(a0, a1, __uint_as_float(c1.x << 16), __uint_as_float(c1.x & 0xFFFF0000u), x2.x, x2.y);
+  fma2(a2, a3, __uint_as_float(c1.y << 16), __uint_as_float(c1.y & 0xFFFF0000u), x2.z, x2.w);
+  fma2(a0, a1, __uint_as_float(c1.z << 16), __uint_as_float(c1.z & 0xFFFF0000u), x3.x, x3.y);
+  fma2(a2, a3, __uint_as_float(c1.w << 16), __uint_as_float(c1.w & 0xFFFF0000u), x3.z, x3.w);
   return (a0 + a1) + (a2 + a3);
 }
 
@@ -111,7 +115,7 @@ enum Epi : int {
 
 struct GemvParams {
   const uint8_t* units;  // weight unit stream [n_rt][G] units
-  int n_rt, G, K, rows;  // row tiles, groups per row, K = 64*G, real rows (<= 32*n_rt)
+  int n_rt, G, K, rows;  // row tiles, units per row, K inputs, real rows (<= 32*n_rt)
   int unit_bytes, nslot, ring_bytes;
   Part part;             // partition of the units over the CTAs
   // input
@@ -351,7 +355,7 @@ __global__ void __launch_bounds__(kGemvThreads, 2) gemv_kernel(const GemvParams 
           cur_rt = rt;
         }
         const uint8_t* ub = ring + (s * kChunkUnits + warp) * UB;
-        if (BF16) acc += bf16_unit_dot(ub, xh + g * 64, lane);
+        if (BF16) acc += bf16_unit_dot(ub, xh + g * kBF16UnitCols, lane);
         else acc += q4_unit_dot(ub, xh + g * 64, xs[g], lane);
       }
       __syncwarp();
@@ -510,40 +514,42 @@ struct AttnParams {
 
 constexpr int kMinPosPerSplit = 64;
 
-template <int GQ, int HD>
-__global__ void __launch_bounds__(kAttnThreads) attention_kernel(const AttnParams p) {
-  constexpr int NW = kAttnThreads / 32;
-  constexpr int DPL = HD / 32;  // dims per lane in the V accumulation
-  __shared__ __align__(16) float qs[GQ][HD];          // scaled query (log2 domain)
-  __shared__ __align__(16) float kv_cur[2][HD];       // current k (rotated), v, as bf16 values
-  __shared__ __align__(16) float wpart[NW][GQ][HD + 2];
-  __shared__ int is_last;
+// Number of splits of the cache of length `len` (at most P).
+__device__ __forceinline__ int attn_splits(int len, int P) {
+  return min(P, max(1, (len + kMinPosPerSplit - 1) / kMinPosPerSplit));
+}
 
-  pdl_trigger();
-  pdl_wait();
-  const int g = blockIdx.y, split = blockIdx.x;
+// Shared memory of one attention work item.
+template <int GQ, int HD, int NW>
+struct AttnSmem {
+  float qs[GQ][HD];          // scaled query (log2 domain)
+  float kv_cur[2][HD];       // current k (rotated) and v, as bf16 values
+  float wpart[NW][GQ][HD + 2];
+  int is_last;
+};
+
+// One (kv head g, split) item of flash-decoding attention, run by NW warps
+// that synchronise with Sync::sync(). Reads q|k|v through `load(row)`.
+template <int GQ, int HD, int NW, class Sync, class Load>
+__device__ void attention_item(const AttnParams& p, int g, int split, int P_eff, int pos, AttnSmem<GQ, HD, NW>& sm,
+                               Load load) {
+  constexpr int NT = NW * 32;
+  constexpr int DPL = HD / 32;  // dims per lane in the V accumulation
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int pos = *p.pos;
-  if (pos < 0 || pos >= p.cap) {
-    if (tid == 0 && split == 0 && g == 0) atomicOr(p.status, ST_CTX_FULL);
-    return;
-  }
   const int len = pos + 1;
-  const int P_eff = min(p.P, max(1, (len + kMinPosPerSplit - 1) / kMinPosPerSplit));
-  if (split >= P_eff) return;
   const int t0 = (int)((int64_t)len * split / P_eff), t1 = (int)((int64_t)len * (split + 1) / P_eff);
 
   // ---- q (GQ heads), k and v of this kv head
-  for (int i = tid; i < GQ * HD; i += kAttnThreads) qs[i / HD][i % HD] = __ldcg(p.qkv + (g * GQ) * HD + i);
-  for (int i = tid; i < 2 * HD; i += kAttnThreads) {
+  for (int i = tid; i < GQ * HD; i += NT) sm.qs[i / HD][i % HD] = load((g * GQ) * HD + i);
+  for (int i = tid; i < 2 * HD; i += NT) {
     const int row = (i < HD) ? (p.q_dim + g * HD + i) : (p.q_dim + p.kv_dim + g * HD + (i - HD));
-    kv_cur[i / HD][i % HD] = __ldcg(p.qkv + row);
+    sm.kv_cur[i / HD][i % HD] = load(row);
   }
-  __syncthreads();
+  Sync::sync();
   // ---- per-head RMSNorm of q and k (Qwen3): one warp per head
   if (p.q_norm) {
     for (int h = warp; h <= GQ; h += NW) {
-      float* v = (h < GQ) ? qs[h] : kv_cur[0];
+      float* v = (h < GQ) ? sm.qs[h] : sm.kv_cur[0];
       const float* w = (h < GQ) ? p.q_norm : p.k_norm;
       float ss = 0.f;
       for (int d = lane; d < HD; d += 32) ss += v[d] * v[d];
@@ -553,14 +559,14 @@ __global__ void __launch_bounds__(kAttnThreads) attention_kernel(const AttnParam
       __syncwarp();
       for (int d = lane; d < HD; d += 32) v[d] = v[d] * inv * w[d];
     }
-    __syncthreads();
+    Sync::sync();
   }
   // ---- RoPE at `pos`: pairs (2i, 2i+1) or (i, i + HD/2)
   {
     const float2* cs = p.rope + (size_t)pos * (HD / 2);
-    for (int j = tid; j < (GQ + 1) * (HD / 2); j += kAttnThreads) {
+    for (int j = tid; j < (GQ + 1) * (HD / 2); j += NT) {
       const int h = j / (HD / 2), i = j % (HD / 2);
-      float* v = (h < GQ) ? qs[h] : kv_cur[0];
+      float* v = (h < GQ) ? sm.qs[h] : sm.kv_cur[0];
       const int a = p.rope_neox ? i : 2 * i, b = p.rope_neox ? i + HD / 2 : 2 * i + 1;
       const float2 r = cs[i];
       const float x0 = v[a], x1 = v[b];
@@ -568,19 +574,19 @@ __global__ void __launch_bounds__(kAttnThreads) attention_kernel(const AttnParam
       v[b] = x0 * r.y + x1 * r.x;
     }
   }
-  __syncthreads();
+  Sync::sync();
   // ---- round k, v to bf16; the split owning `pos` appends them to the cache
   const float qscale = 1.4426950408889634f / sqrtf((float)HD);  // log2(e)/sqrt(hd)
-  for (int i = tid; i < 2 * HD; i += kAttnThreads) {
-    const __nv_bfloat16 b = __float2bfloat16_rn(kv_cur[i / HD][i % HD]);
-    kv_cur[i / HD][i % HD] = __bfloat162float(b);
+  for (int i = tid; i < 2 * HD; i += NT) {
+    const __nv_bfloat16 b = __float2bfloat16_rn(sm.kv_cur[i / HD][i % HD]);
+    sm.kv_cur[i / HD][i % HD] = __bfloat162float(b);
     if (split == P_eff - 1) {
       uint16_t* dst = (i < HD ? p.kc : p.vc) + ((size_t)g * p.cap + pos) * HD + (i % HD);
       *dst = __bfloat16_as_ushort(b);
     }
   }
-  for (int i = tid; i < GQ * HD; i += kAttnThreads) qs[i / HD][i % HD] *= qscale;
-  __syncthreads();
+  for (int i = tid; i < GQ * HD; i += NT) sm.qs[i / HD][i % HD] *= qscale;
+  Sync::sync();
 
   // ---- online softmax over this split's positions, 32 per warp iteration
   float m[GQ], l[GQ], acc[GQ][DPL];
@@ -593,6 +599,49 @@ __global__ void __launch_bounds__(kAttnThreads) attention_kernel(const AttnParam
   }
   const uint16_t* kbase = p.kc + (size_t)g * p.cap * HD;
   const uint16_t* vbase = p.vc + (size_t)g * p.cap * HD;
+  if (t1 - t0 <= NW * 8) {
+    // short split: warp w takes positions t0+w, t0+w+NW, ...; lane l holds
+    // dims l+32e of q, k, v; a score is a butterfly sum over the warp
+    float qr[GQ][DPL];
+#pragma unroll
+    for (int h = 0; h < GQ; ++h)
+#pragma unroll
+      for (int e = 0; e < DPL; ++e) qr[h][e] = sm.qs[h][lane + 32 * e];
+    for (int t = t0 + warp; t < t1; t += NW) {
+      float kf[DPL], vf[DPL];
+#pragma unroll
+      for (int e = 0; e < DPL; ++e) {
+        if (t == pos) {
+          kf[e] = sm.kv_cur[0][lane + 32 * e];
+          vf[e] = sm.kv_cur[1][lane + 32 * e];
+        } else {
+          kf[e] = bf16_bits_to_f32(__ldg(kbase + (size_t)t * HD + lane + 32 * e));
+          vf[e] = bf16_bits_to_f32(__ldg(vbase + (size_t)t * HD + lane + 32 * e));
+        }
+      }
+      float sc[GQ];
+#pragma unroll
+      for (int h = 0; h < GQ; ++h) {
+        sc[h] = 0.f;
+#pragma unroll
+        for (int e = 0; e < DPL; ++e) sc[h] = fmaf(qr[h][e], kf[e], sc[h]);
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1)
+#pragma unroll
+        for (int h = 0; h < GQ; ++h) sc[h] += __shfl_xor_sync(0xffffffffu, sc[h], o);
+#pragma unroll
+      for (int h = 0; h < GQ; ++h) {
+        const float mn = fmaxf(m[h], sc[h]);
+        const float corr = exp2f(m[h] - mn);
+        const float pj = exp2f(sc[h] - mn);
+        l[h] = l[h] * corr + pj;
+        m[h] = mn;
+#pragma unroll
+        for (int e = 0; e < DPL; ++e) acc[h][e] = fmaf(pj, vf[e], acc[h][e] * corr);
+      }
+    }
+  } else
   for (int tb = t0 + warp * 32; tb < t1; tb += NW * 32) {
     const int t = tb + lane;
     const bool valid = t < t1;
@@ -603,14 +652,14 @@ __global__ void __launch_bounds__(kAttnThreads) attention_kernel(const AttnParam
       if (t == pos) {
 #pragma unroll 4
         for (int d = 0; d < HD; ++d) {
-          const float kd = kv_cur[0][d];
+          const float kd = sm.kv_cur[0][d];
 #pragma unroll
-          for (int h = 0; h < GQ; ++h) s[h] = fmaf(qs[h][d], kd, s[h]);
+          for (int h = 0; h < GQ; ++h) s[h] = fmaf(sm.qs[h][d], kd, s[h]);
         }
       } else {
-        // issue the whole row's loads before using any of them
+        // issue a row's loads before using any of them
         const uint4* kr = reinterpret_cast<const uint4*>(kbase + (size_t)t * HD);
-        constexpr int KB = HD / 8 > 8 ? 8 : HD / 8;
+        constexpr int KB = (GQ >= 8 ? 4 : 8) < HD / 8 ? (GQ >= 8 ? 4 : 8) : HD / 8;
 #pragma unroll
         for (int c0 = 0; c0 < HD / 8; c0 += KB) {
           uint4 u[KB];
@@ -624,8 +673,8 @@ __global__ void __launch_bounds__(kAttnThreads) attention_kernel(const AttnParam
                                  __uint_as_float(u[c8].w << 16), __uint_as_float(u[c8].w & 0xFFFF0000u)};
 #pragma unroll
             for (int h = 0; h < GQ; ++h) {
-              const float4 qa = *reinterpret_cast<const float4*>(&qs[h][(c0 + c8) * 8]);
-              const float4 qb = *reinterpret_cast<const float4*>(&qs[h][(c0 + c8) * 8 + 4]);
+              const float4 qa = *reinterpret_cast<const float4*>(&sm.qs[h][(c0 + c8) * 8]);
+              const float4 qb = *reinterpret_cast<const float4*>(&sm.qs[h][(c0 + c8) * 8 + 4]);
               s[h] = fmaf(qa.x, kf[0], s[h]);
               s[h] = fmaf(qa.y, kf[1], s[h]);
               s[h] = fmaf(qa.z, kf[2], s[h]);
@@ -666,7 +715,7 @@ __global__ void __launch_bounds__(kAttnThreads) attention_kernel(const AttnParam
 #pragma unroll
         for (int e = 0; e < DPL; ++e) {
           if (j0 + jj >= nv) vv[jj][e] = 0.f;
-          else if (tj == pos) vv[jj][e] = kv_cur[1][lane + 32 * e];
+          else if (tj == pos) vv[jj][e] = sm.kv_cur[1][lane + 32 * e];
           else vv[jj][e] = bf16_bits_to_f32(__ldg(vbase + (size_t)tj * HD + lane + 32 * e));
         }
       }
@@ -681,27 +730,27 @@ __global__ void __launch_bounds__(kAttnThreads) attention_kernel(const AttnParam
       }
     }
   }
-  // ---- combine the warps of this CTA
+  // ---- combine the warps of this item
 #pragma unroll
   for (int h = 0; h < GQ; ++h) {
 #pragma unroll
-    for (int e = 0; e < DPL; ++e) wpart[warp][h][lane + 32 * e] = acc[h][e];
+    for (int e = 0; e < DPL; ++e) sm.wpart[warp][h][lane + 32 * e] = acc[h][e];
     if (lane == 0) {
-      wpart[warp][h][HD] = m[h];
-      wpart[warp][h][HD + 1] = l[h];
+      sm.wpart[warp][h][HD] = m[h];
+      sm.wpart[warp][h][HD + 1] = l[h];
     }
   }
-  __syncthreads();
+  Sync::sync();
   float* gpart = p.part + (((size_t)g * p.P + split) * GQ) * (HD + 2);
-  for (int i = tid; i < GQ * HD; i += kAttnThreads) {
+  for (int i = tid; i < GQ * HD; i += NT) {
     const int h = i / HD, d = i % HD;
     float M = -INFINITY;
-    for (int w = 0; w < NW; ++w) M = fmaxf(M, wpart[w][h][HD]);
+    for (int w = 0; w < NW; ++w) M = fmaxf(M, sm.wpart[w][h][HD]);
     float L = 0.f, O = 0.f;
     for (int w = 0; w < NW; ++w) {
-      const float f = (wpart[w][h][HD] == -INFINITY) ? 0.f : exp2f(wpart[w][h][HD] - M);
-      L += wpart[w][h][HD + 1] * f;
-      O += wpart[w][h][d] * f;
+      const float f = (sm.wpart[w][h][HD] == -INFINITY) ? 0.f : exp2f(sm.wpart[w][h][HD] - M);
+      L += sm.wpart[w][h][HD + 1] * f;
+      O += sm.wpart[w][h][d] * f;
     }
     if (P_eff == 1) {
       p.out[(g * GQ + h) * HD + d] = O / L;
@@ -713,29 +762,55 @@ __global__ void __launch_bounds__(kAttnThreads) attention_kernel(const AttnParam
       }
     }
   }
-  if (P_eff == 1) return;
+  if (P_eff == 1) {
+    Sync::sync();  // wpart is reused by the next item
+    return;
+  }
   // ---- last split of this kv head combines all splits (no waiting)
   __threadfence();
-  __syncthreads();
-  if (tid == 0) is_last = (atomicAdd(&p.counter[g], 1) == P_eff - 1);
-  __syncthreads();
-  if (!is_last) return;
-  __threadfence();
-  const float* hp = p.part + ((size_t)g * p.P * GQ) * (HD + 2);
-  for (int i = tid; i < GQ * HD; i += kAttnThreads) {
-    const int h = i / HD, d = i % HD;
-    float M = -INFINITY;
-    for (int sp = 0; sp < P_eff; ++sp) M = fmaxf(M, __ldcg(hp + ((size_t)sp * GQ + h) * (HD + 2) + HD));
-    float L = 0.f, O = 0.f;
-    for (int sp = 0; sp < P_eff; ++sp) {
-      const float* q = hp + ((size_t)sp * GQ + h) * (HD + 2);
-      const float f = exp2f(__ldcg(q + HD) - M);
-      L += __ldcg(q + HD + 1) * f;
-      O += __ldcg(q + d) * f;
+  Sync::sync();
+  if (tid == 0) sm.is_last = (atomicAdd(&p.counter[g], 1) == P_eff - 1);
+  Sync::sync();
+  if (sm.is_last) {
+    __threadfence();
+    const float* hp = p.part + ((size_t)g * p.P * GQ) * (HD + 2);
+    for (int i = tid; i < GQ * HD; i += NT) {
+      const int h = i / HD, d = i % HD;
+      float M = -INFINITY;
+      for (int sp = 0; sp < P_eff; ++sp) M = fmaxf(M, __ldcg(hp + ((size_t)sp * GQ + h) * (HD + 2) + HD));
+      float L = 0.f, O = 0.f;
+      for (int sp = 0; sp < P_eff; ++sp) {
+        const float* q = hp + ((size_t)sp * GQ + h) * (HD + 2);
+        const float f = exp2f(__ldcg(q + HD) - M);
+        L += __ldcg(q + HD + 1) * f;
+        O += __ldcg(q + d) * f;
+      }
+      p.out[(g * GQ + h) * HD + d] = O / L;
     }
-    p.out[(g * GQ + h) * HD + d] = O / L;
+    if (tid == 0) p.counter[g] = 0;
   }
-  if (tid == 0) p.counter[g] = 0;
+  Sync::sync();
+}
+
+struct CtaSync {
+  __device__ static void sync() { __syncthreads(); }
+};
+
+template <int GQ, int HD>
+__global__ void __launch_bounds__(kAttnThreads) attention_kernel(const AttnParams p) {
+  constexpr int NW = kAttnThreads / 32;
+  __shared__ __align__(16) AttnSmem<GQ, HD, NW> sm;
+  pdl_trigger();
+  pdl_wait();
+  const int g = blockIdx.y, split = blockIdx.x;
+  const int pos = *p.pos;
+  if (pos < 0 || pos >= p.cap) {
+    if (threadIdx.x == 0 && split == 0 && g == 0) atomicOr(p.status, ST_CTX_FULL);
+    return;
+  }
+  const int P_eff = attn_splits(pos + 1, p.P);
+  if (split >= P_eff) return;
+  attention_item<GQ, HD, NW, CtaSync>(p, g, split, P_eff, pos, sm, [&](int row) { return __ldcg(p.qkv + row); });
 }
 
 }  // namespace llmq

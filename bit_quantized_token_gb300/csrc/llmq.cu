@@ -20,6 +20,7 @@
 #include <vector>
 
 #include "kernels.cuh"
+#include "step.cuh"
 #include "llmq.h"
 
 using namespace llmq;
@@ -120,13 +121,14 @@ void unpack_q4(const uint8_t* units, int G, uint8_t* codes, uint16_t* scales, ui
   });
 }
 
-// Dense bf16 [rows][cols] -> bf16 units (see bf16_unit_dot).
+// Dense bf16 [rows][cols] -> bf16 units of 16 inputs (see bf16_unit_dot).
 void repack_bf16(uint8_t* units, int G, const uint16_t* data, int rows, int cols) {
   parallel_for(rows, [&](int r) {
     const int rt = r / 32, lane = r % 32;
     for (int g = 0; g < G; ++g) {
       uint8_t* u = units + ((size_t)rt * G + g) * kBF16UnitBytes;
-      for (int k = 0; k < 8; ++k) std::memcpy(u + (k * 32 + lane) * 16, data + (size_t)r * cols + g * 64 + 8 * k, 16);
+      for (int k = 0; k < 2; ++k)
+        std::memcpy(u + (k * 32 + lane) * 16, data + (size_t)r * cols + g * kBF16UnitCols + 8 * k, 16);
     }
   });
 }
@@ -180,6 +182,13 @@ struct llm_model {
   int* d_cand_i = nullptr;
   int* d_attn_cnt = nullptr;
   int* d_greedy_cnt = nullptr;
+  // persistent step kernel
+  bool use_step = false;
+  bool step_eager = false;
+  Phase* d_phases = nullptr;
+  int n_phases = 0;
+  int* d_step_sync = nullptr;                 // [2]: arrivals, abort
+  size_t step_smem = 0;
   // per-sequence state
   int *d_pos = nullptr, *d_tok = nullptr, *d_argmax = nullptr, *d_hist = nullptr, *d_hist_ctr = nullptr,
       *d_status = nullptr, *d_prompt = nullptr;
@@ -256,9 +265,9 @@ GemvPlan plan_gemv(const Mat& mat, int n_sm) {
   g.m = mat;
   g.part = make_part(mat.n_rt, mat.G, n_sm);
   const int slot = kChunkUnits * mat.unit_bytes();
-  g.nslot = mat.bf16 ? 3 : 8;
+  g.nslot = 8;
   g.ring = g.nslot * slot;
-  g.smem = gemv_smem(g.ring, mat.G * 64, mat.G, g.nslot);
+  g.smem = gemv_smem(g.ring, mat.cols, mat.G, g.nslot);
   return g;
 }
 
@@ -267,7 +276,7 @@ GemvParams gemv_params(const llm_model* m, const GemvPlan& g) {
   p.units = m->d_arena + g.m.off;
   p.n_rt = g.m.n_rt;
   p.G = g.m.G;
-  p.K = g.m.G * 64;
+  p.K = g.m.cols;
   p.unit_bytes = g.m.unit_bytes();
   p.nslot = g.nslot;
   p.ring_bytes = g.ring;
@@ -439,8 +448,76 @@ int kind_of(const llm_model* m, int which) {
   return (which == W_LM && m->lm.m.bf16) ? 1 : 0;
 }
 
+// The persistent step kernel for the model's (GQA group, head_dim).
+template <int GQ, int HD>
+cudaError_t launch_step_t(const llm_model* m, const StepParams& sp) {
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3(m->n_sm);
+  cfg.blockDim = dim3(kSThreads);
+  cfg.dynamicSmemBytes = m->step_smem;
+  cfg.stream = m->stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeCooperative;  // all CTAs co-resident: the grid barriers are safe
+  attr[0].val.cooperative = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, step_kernel<GQ, HD>, sp);
+}
+
+bool step_supported(int gq, int hd) { return (gq == 2 && hd == 64) || (gq == 8 && hd == 64) || (gq == 2 && hd == 128); }
+
+template <typename F>
+cudaError_t with_step_kernel(int gq, int hd, F f) {
+  if (gq == 2 && hd == 64) return f(step_kernel<2, 64>, step_smem_bytes<2, 64>());
+  if (gq == 8 && hd == 64) return f(step_kernel<8, 64>, step_smem_bytes<8, 64>());
+  return f(step_kernel<2, 128>, step_smem_bytes<2, 128>());
+}
+
+cudaError_t enqueue_persistent_step(llm_model* m, int seq) {
+  const llm_config& c = m->cfg;
+  StepParams sp{};
+  sp.phases = m->d_phases;
+  sp.n_phases = m->n_phases;
+  sp.sync = m->d_step_sync;
+  sp.status = m->d_status;
+  sp.embed = m->d_embed;
+  sp.tok = m->d_tok + seq;
+  sp.vocab = c.vocab;
+  sp.eps = c.norm_eps;
+  sp.q_dim = m->q_dim;
+  sp.kv_dim = m->kv_dim;
+  sp.Hkv = c.n_kv_heads;
+  sp.P = m->attn_P;
+  sp.cap = c.max_seq;
+  sp.rope_neox = c.rope_neox;
+  sp.rope = m->d_rope;
+  sp.pos = m->d_pos + seq;
+  sp.layer_stride = (size_t)c.n_kv_heads * c.max_seq * c.head_dim;
+  sp.k_base = m->d_k + (size_t)seq * c.n_layers * sp.layer_stride;
+  sp.v_base = m->d_v + (size_t)seq * c.n_layers * sp.layer_stride;
+  sp.attn_part = m->d_attn_part;
+  sp.attn_cnt = m->d_attn_cnt;
+  sp.obuf = m->d_obuf;
+  sp.logits = m->d_logits;
+  sp.cand_v = m->d_cand_v;
+  sp.cand_i = m->d_cand_i;
+  sp.gcounter = m->d_greedy_cnt;
+  sp.tok_io = m->d_tok + seq;
+  sp.argmax_out = m->d_argmax + seq;
+  sp.hist = m->d_hist;
+  sp.hist_ctr = m->d_hist_ctr;
+  sp.hist_cap = c.max_seq;
+  cudaError_t e = cudaMemsetAsync(m->d_step_sync, 0, 2 * sizeof(int), m->stream);
+  if (e != cudaSuccess) return e;
+  const int gq = m->gq, hd = c.head_dim;
+  if (gq == 2 && hd == 64) return launch_step_t<2, 64>(m, sp);
+  if (gq == 8 && hd == 64) return launch_step_t<8, 64>(m, sp);
+  return launch_step_t<2, 128>(m, sp);
+}
+
 // Enqueue one batch-1 decode step of sequence `seq` on m->stream.
 cudaError_t enqueue_step(llm_model* m, int seq, Prof* prof = nullptr) {
+  if (m->use_step && !prof) return enqueue_persistent_step(m, seq);
   const int L = m->cfg.n_layers;
   const bool pdl = !(m->cfg.flags & LLM_NO_PDL) && !prof;
   cudaError_t e;
@@ -482,11 +559,23 @@ int run_step(llm_model* m, int seq) {
     CK(enqueue_step(m, seq), "step launch");
     return LLM_OK;
   }
+  if (m->step_eager) {  // the persistent step is two operations: launch them directly
+    CK(enqueue_step(m, seq), "step launch");
+    return LLM_OK;
+  }
   if (!m->graphs[seq]) {
     cudaGraph_t g = nullptr;
     CK(cudaStreamBeginCapture(m->stream, cudaStreamCaptureModeThreadLocal), "begin capture");
     cudaError_t e = enqueue_step(m, seq);
     cudaError_t e2 = cudaStreamEndCapture(m->stream, &g);
+    if (m->use_step && (e != cudaSuccess || e2 != cudaSuccess)) {
+      // a cooperative launch that this driver does not capture: run the step eagerly
+      cudaGetLastError();
+      if (g) cudaGraphDestroy(g);
+      m->step_eager = true;
+      CK(enqueue_step(m, seq), "step launch");
+      return LLM_OK;
+    }
     if (e != cudaSuccess) return cuda_fail(m, e, "step capture");
     if (e2 != cudaSuccess) return cuda_fail(m, e2, "end capture");
     cudaGraphExec_t ge = nullptr;
@@ -601,7 +690,7 @@ int llm_model_create(const llm_config* cfg, const llm_tensor* tensors, int32_t n
     x.rows = rows;
     x.cols = cols;
     x.n_rt = (rows + 31) / 32;
-    x.G = cols / 64;
+    x.G = cols / (bf16 ? kBF16UnitCols : 64);
     x.bf16 = bf16;
     x.off = off;
     off += (x.bytes() + 255) / 256 * 256;
@@ -763,8 +852,99 @@ int llm_model_create(const llm_config* cfg, const llm_tensor* tensors, int32_t n
   AL(m->d_xbuf, (size_t)(L + 1) * d * 4, "residual stream");
   AL(m->d_hbuf, (size_t)L * d * 4, "post-attention residual");
   AL(m->d_logits, (size_t)V * 4, "logits");
-  AL(m->d_cand_v, (size_t)m->lm.part.N * 4, "greedy candidates");
-  AL(m->d_cand_i, (size_t)m->lm.part.N * 4, "greedy candidates");
+  AL(m->d_cand_v, (size_t)std::max(m->lm.part.N, m->n_sm) * 4, "greedy candidates");
+  AL(m->d_cand_i, (size_t)std::max(m->lm.part.N, m->n_sm) * 4, "greedy candidates");
+  // ---- the persistent step: phase table (one for every sequence)
+  m->use_step = !(c.flags & LLM_MULTI_KERNEL) && step_supported(gq, hd);
+  if (m->use_step) {
+    with_step_kernel(gq, hd, [&](auto kern, size_t smem) {
+      m->step_smem = smem;
+      int per_sm = 0;
+      cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+      if (e == cudaSuccess) e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kSThreads, smem);
+      if (e != cudaSuccess || per_sm < 1) {
+        cudaGetLastError();
+        m->use_step = false;  // fall back to the per-kernel step
+      }
+      return cudaSuccess;
+    });
+  }
+  std::vector<Phase> phases;
+  {
+    auto gemv_phase = [&](const GemvPlan& g, float* out_part) {
+      Phase ph{};
+      ph.type = PH_GEMV;
+      ph.units = m->d_arena + g.m.off;
+      ph.n_rt = g.m.n_rt;
+      ph.G = g.m.G;
+      ph.K = g.m.cols;
+      ph.bf16 = g.m.bf16;
+      ph.unit_bytes = g.m.unit_bytes();
+      ph.part = g.part;
+      ph.out_part = out_part;
+      return ph;
+    };
+    for (int l = 0; l < L; ++l) {
+      Phase q = gemv_phase(m->qkv[l], m->qkv[l].part_buf);
+      q.layer = l;
+      if (l == 0) {
+        q.in_mode = m->embed_bf16 ? IN_EMBED_BF16 : IN_EMBED_F32;
+      } else {
+        q.in_mode = IN_RESID;
+        q.in_base = m->d_hbuf + (size_t)(l - 1) * d;
+        q.in_part = m->down[l - 1].part_buf;
+        q.in_S = m->down[l - 1].part.S;
+      }
+      q.in_store = m->d_xbuf + (size_t)l * d;
+      q.norm_w = m->d_norms + m->off_attn_norm[l];
+      phases.push_back(q);
+      Phase a{};
+      a.type = PH_ATTN;
+      a.layer = l;
+      a.qkv_part = m->qkv[l].part_buf;
+      a.qkv_S = m->qkv[l].part.S;
+      a.q_norm = c.qk_norm ? m->d_norms + m->off_q_norm[l] : nullptr;
+      a.k_norm = c.qk_norm ? m->d_norms + m->off_k_norm[l] : nullptr;
+      phases.push_back(a);
+      Phase o = gemv_phase(m->wo[l], m->wo[l].part_buf);
+      o.layer = l;
+      o.in_mode = IN_PLAIN;
+      o.in_base = m->d_obuf;
+      phases.push_back(o);
+      Phase gu = gemv_phase(m->gu[l], m->gu[l].part_buf);
+      gu.layer = l;
+      gu.in_mode = IN_RESID;
+      gu.in_base = m->d_xbuf + (size_t)l * d;
+      gu.in_part = m->wo[l].part_buf;
+      gu.in_S = m->wo[l].part.S;
+      gu.in_store = m->d_hbuf + (size_t)l * d;
+      gu.norm_w = m->d_norms + m->off_ffn_norm[l];
+      phases.push_back(gu);
+      Phase dn = gemv_phase(m->down[l], m->down[l].part_buf);
+      dn.layer = l;
+      dn.in_mode = IN_SWIGLU;
+      dn.in_part = m->gu[l].part_buf;
+      dn.in_S = m->gu[l].part.S;
+      phases.push_back(dn);
+    }
+    Phase lmp = gemv_phase(m->lm, m->lm.part_buf);
+    lmp.in_mode = IN_RESID;
+    lmp.in_base = m->d_hbuf + (size_t)(L - 1) * d;
+    lmp.in_part = m->down[L - 1].part_buf;
+    lmp.in_S = m->down[L - 1].part.S;
+    lmp.in_store = m->d_xbuf + (size_t)L * d;
+    lmp.norm_w = m->d_norms + m->off_final_norm;
+    phases.push_back(lmp);
+    Phase lg{};
+    lg.type = PH_LOGITS;
+    lg.lm_part = m->lm.part_buf;
+    lg.lm_S = m->lm.part.S;
+    lg.vocab = V;
+    phases.push_back(lg);
+  }
+  m->n_phases = (int)phases.size();
+  AL(m->d_phases, phases.size() * sizeof(Phase), "phase table");
+  AL(m->d_step_sync, 2 * sizeof(int), "step barrier");
   AL(m->d_pos, (size_t)c.max_batch * 4, "positions");
   AL(m->d_tok, (size_t)c.max_batch * 4, "tokens");
   AL(m->d_argmax, (size_t)c.max_batch * 4, "argmax");
@@ -787,6 +967,7 @@ int llm_model_create(const llm_config* cfg, const llm_tensor* tensors, int32_t n
   std::vector<uint8_t>().swap(arena);
   if ((rc = up(m->d_embed, emb->data, emb_bytes, "embedding upload")) != LLM_OK) return fail(rc);
   if ((rc = up(m->d_norms, norms.data(), norms.size() * 4, "norm upload")) != LLM_OK) return fail(rc);
+  if ((rc = up(m->d_phases, phases.data(), phases.size() * sizeof(Phase), "phase upload")) != LLM_OK) return fail(rc);
   {
     // cos/sin of pos * base^(-2i/hd), evaluated in double, stored as fp32
     std::vector<float2> rope((size_t)c.max_seq * (hd / 2));
@@ -817,7 +998,7 @@ int llm_model_create(const llm_config* cfg, const llm_tensor* tensors, int32_t n
   }
   m->len.assign(c.max_batch, 0);
   m->graphs.assign(c.max_batch, nullptr);
-  m->kernels_per_step = 5 * L + 1;
+  m->kernels_per_step = m->use_step ? 1 : 5 * L + 1;
   *out = m;
   return LLM_OK;
 }
@@ -1073,7 +1254,7 @@ int llm_op_matvec(const llm_tensor* w, const float* x, float* y) {
   mat.rows = (int)w->rows;
   mat.cols = (int)w->cols;
   mat.n_rt = (mat.rows + 31) / 32;
-  mat.G = mat.cols / 64;
+  mat.G = mat.cols / (bf16 ? kBF16UnitCols : 64);
   mat.bf16 = bf16;
   std::vector<uint8_t> units(mat.bytes(), 0);
   if (bf16)
@@ -1105,7 +1286,7 @@ int llm_op_matvec(const llm_tensor* w, const float* x, float* y) {
     p.units = d_units;
     p.n_rt = mat.n_rt;
     p.G = mat.G;
-    p.K = mat.G * 64;
+    p.K = mat.cols;
     p.rows = mat.rows;
     p.unit_bytes = mat.unit_bytes();
     p.nslot = g.nslot;
@@ -1212,7 +1393,7 @@ extern "C" int llm_matvec_noalloc(const llm_model* m, const char* name, const fl
   p.units = m->d_arena + sub.off;
   p.n_rt = sub.n_rt;
   p.G = sub.G;
-  p.K = sub.G * 64;
+  p.K = sub.cols;
   p.rows = rows;
   p.unit_bytes = sub.unit_bytes();
   p.nslot = g.nslot;

@@ -50,6 +50,7 @@ typedef enum { LLM_F32 = 0, LLM_BF16 = 1, LLM_F16 = 2, LLM_Q4G64 = 3 } llm_dtype
 /* llm_config.flags */
 #define LLM_NO_GRAPH 1u       /* launch the step's kernels one by one (debugging) */
 #define LLM_NO_PDL   2u       /* no programmatic dependent launch between kernels */
+#define LLM_MULTI_KERNEL 4u   /* one kernel per phase instead of the persistent step kernel */
 
 typedef struct {
   int32_t abi_version;        /* must equal LLMQ_ABI_VERSION */
@@ -61,7 +62,7 @@ typedef struct {
   int32_t tied_embedding;     /* 1: LM head is the bf16 embedding table */
   int32_t max_seq;            /* KV capacity per sequence (positions) */
   int32_t max_batch;          /* number of sequences (independent caches) */
-  uint32_t flags;             /* LLM_NO_GRAPH | LLM_NO_PDL */
+  uint32_t flags;             /* LLM_NO_GRAPH | LLM_NO_PDL | LLM_MULTI_KERNEL */
 } llm_config;
 
 /* One input tensor in the canonical layout, host memory, caller-owned, only

@@ -158,8 +158,10 @@ def check_against_oracle(cfg, toks, logits, hid, ref, greedy=True):
     return err.max()
 
 
-@pytest.mark.parametrize("flags", [0, bq.LLM_NO_GRAPH, bq.LLM_NO_PDL, bq.LLM_NO_GRAPH | bq.LLM_NO_PDL],
-                         ids=["graph+pdl", "eager+pdl", "graph", "eager"])
+@pytest.mark.parametrize("flags", [0, bq.LLM_NO_GRAPH, bq.LLM_MULTI_KERNEL, bq.LLM_MULTI_KERNEL | bq.LLM_NO_GRAPH,
+                                   bq.LLM_MULTI_KERNEL | bq.LLM_NO_PDL],
+                         ids=["persistent", "persistent-eager", "multi-kernel-graph+pdl", "multi-kernel-eager+pdl",
+                              "multi-kernel-graph"])
 def test_tiny_llama_greedy_matches_oracle(flags):
     cfg = synth.workload(0)
     w = synth.make_weights(cfg)
@@ -206,9 +208,10 @@ def test_full_size_greedy_matches_oracle(idx):
     prompt = synth.make_prompt(cfg)
     n = cfg["decode_steps"]
     ref = oracle.greedy_run(oracle.OracleModel(cfg, w), prompt, n, hidden=True)
-    with bq.Model(cfg, w, max_seq=len(prompt) + n + 1) as m:
-        toks, logits, hid = gpu_run(m, cfg, prompt, n, hidden=True)
-    check_against_oracle(cfg, toks, logits, hid, ref)
+    for flags in (0, bq.LLM_MULTI_KERNEL):
+        with bq.Model(cfg, w, max_seq=len(prompt) + n + 1, flags=flags) as m:
+            toks, logits, hid = gpu_run(m, cfg, prompt, n, hidden=True)
+        check_against_oracle(cfg, toks, logits, hid, ref)
 
 
 def test_long_context_teacher_forced():
