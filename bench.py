@@ -54,6 +54,24 @@ def peaks():
     return 6800.0, "fallback"
 
 
+def src_sha():
+    """Hash of the kernel sources: an ncu traffic figure is only used for the code it was taken on."""
+    import hashlib
+    h = hashlib.sha256()
+    for f in ("common.cuh", "kernels.cuh", "step.cuh", "llmq.cu"):
+        h.update(open(os.path.join(ROOT, "bit_quantized_token_gb300", "csrc", f), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic(key):
+    """DRAM bytes per launch from profiles/traffic.json, or None if absent or stale."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    t = json.load(open(p)).get(key)
+    return t["traffic_bytes"] if t and t.get("src_sha") == src_sha() else None
+
+
 def workload_desc(cfg):
     return (f"{cfg['name']}: dim {cfg['dim']}, {cfg['n_layers']} layers, {cfg['n_heads']}/{cfg['n_kv_heads']} heads, "
             f"head_dim {cfg['head_dim']}, ffn {cfg['ffn_dim']}, vocab {cfg['vocab']}, group-64 4-bit weights "
@@ -247,7 +265,8 @@ def main():
         # one persistent kernel per step: its launch duration is the step time
         roofline = {"kernel": "step_kernel (persistent decode step, one launch per token)", "bound": "hbm",
                     "achieved": bytes_tok / (ms / a.steps / 1000.0) / 1e9, "peak": peak, "unit": "GB/s",
-                    "frac": bytes_tok / (ms / a.steps / 1000.0) / 1e9 / peak, "traffic": None,
+                    "frac": bytes_tok / (ms / a.steps / 1000.0) / 1e9 / peak,
+                    "traffic": ncu_traffic(f"step_kernel {cfg['name']}"),
                     "peak_kind": peak_kind, "bytes_per_launch": bytes_tok, "ms_per_launch": ms / a.steps}
     else:
         roofline = {"kernel": "gemv_kernel (4-bit dequant-GEMV stream of one step, back to back)", "bound": "hbm",
