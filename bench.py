@@ -171,6 +171,89 @@ def run_reference(a, cfg, w, prompt, rank, world):
     print(json.dumps(line), flush=True)
 
 
+def run_batched(a, cfg, w, rank, world, local, dist):
+    """One decode step of every sequence of the batch per step (ragged pre-filled caches)."""
+    import torch
+
+    import bit_quantized_token_gb300 as bq
+
+    B = cfg["batch"]
+    lens = synth.make_kv_lengths(cfg, B)
+    n_e2e = 8
+    max_seq = int(lens.max()) + a.warmup + a.steps + n_e2e + 8
+    stream = torch.cuda.Stream()
+    m = bq.Model(cfg, w, max_seq=max_seq, max_batch=B, stream=stream.cuda_stream)
+    st = m.stats()
+    for b in range(B):
+        for l in range(cfg["n_layers"]):
+            m.kv_write(b, l, 0, *synth.make_prefilled_kv(cfg, l, b, int(lens[b])))
+    m.decode_step_batch(synth.make_first_tokens(cfg, B))
+    for _ in range(a.warmup - 1):
+        m.decode_step_batch(None)
+    m.sync()
+    pos0 = lens + a.warmup
+    clocks = ClockSampler(local)
+    time.sleep(0.5)
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(a.steps):
+        m.decode_step_batch(None)  # greedy tokens fed back on the device
+    e1.record(stream)
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    ms = e0.elapsed_time(e1)
+    clk = clocks.stop()
+    m.sync()
+    if dist:
+        t = torch.tensor([ms], dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    tok_s = world * B * a.steps / (ms / 1000.0)
+    per_pos = synth.kv_bytes_per_pos(cfg)
+    kv_step = float(np.mean([sum((int(pos0[b]) + i + 1) * per_pos for b in range(B)) for i in range(a.steps)]))
+    bytes_step = st["weight_stream_bytes"] + kv_step
+    peak, peak_kind = peaks()
+    gbs = bytes_step / (ms / a.steps / 1000.0) / 1e9
+    # end to end: host tokens in, host greedy tokens out, every step
+    am = np.zeros(B, np.int32)
+    toks = synth.make_first_tokens(cfg, B)
+    t0 = time.perf_counter()
+    for _ in range(n_e2e):
+        m.decode_step_batch(toks, None, am)
+        toks = am.copy()
+    e2e_s = time.perf_counter() - t0
+    line = {
+        "metric": METRIC, "value": tok_s, "unit": "tok/s", "n_gpus": world, "steps": a.steps, "warmup": a.warmup,
+        "ms_per_step": ms / a.steps, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f32", "data": "synthetic",
+        "config": {"workload": workload_desc(cfg), "batch": B, "kv_lengths": [int(lens.min()), int(lens.max())],
+                   "kv_lengths_mean": float(lens.mean()), "l2": "inputs larger than L2: ~5.4 GB streamed per step",
+                   "timed": "llm_decode_step_batch(NULL tokens): CUDA-graph replays, greedy tokens fed back on the device"},
+        "hbm": {"bytes_per_step": bytes_step, "weight_bytes": st["weight_stream_bytes"], "kv_bytes_per_step": kv_step,
+                "achieved_gbs": gbs, "frac_of_peak": gbs / peak, "peak_gbs": peak, "peak_kind": peak_kind},
+        "roofline": {"kernel": "batched step (bgemv_kernel + battention_kernel graph; attention reads ~90% of the bytes)",
+                     "bound": "hbm", "achieved": gbs, "peak": peak, "unit": "GB/s", "frac": gbs / peak,
+                     "traffic": None, "peak_kind": peak_kind},
+        "e2e": {"value": world * B * n_e2e / e2e_s, "unit": "tok/s", "h2d_bytes_per_step": 4 * B,
+                "d2h_bytes_per_step": 4 * B, "steps": n_e2e,
+                "call": "llm_decode_step_batch(host tokens -> host greedy tokens)"},
+        "gpu_launches": (5 * cfg["n_layers"] + 2) * a.steps,
+        "clocks": clk,
+    }
+    if rank == 0 and world == 1 and not a.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(cfg, w, synth.make_prompt(cfg, n=1), a.cpu_seconds)
+    m.close()
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if dist:
+        dist.barrier()
+        dist.destroy_process_group()
+
+
 def main():
     a = args_()
     rank = int(os.environ.get("RANK", "0"))
@@ -197,6 +280,9 @@ def main():
     torch.cuda.set_device(local)
     bq.build()
     assert a.warmup >= 3, "at least 3 warm-up steps"
+    if cfg.get("batch", 1) > 1:
+        run_batched(a, cfg, w, rank, world, local, dist)
+        return
     n_e2e, n_kt = 32, 3
     n_pre = max(0, cfg.get("prefill_kv", 0))
     max_seq = n_pre + len(prompt) + a.warmup + a.steps + n_e2e + 8

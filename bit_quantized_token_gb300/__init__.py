@@ -210,11 +210,12 @@ class Model:
         _check(lib().llm_decode_greedy(self.h, seq, int(first_token), int(n_steps), _ptr(out)), self.h)
         return out
 
-    def decode_step_batch(self, tokens, logits=None, argmax=None) -> None:
-        n = int(tokens.shape[0]) if hasattr(tokens, "shape") else len(tokens)
+    def decode_step_batch(self, tokens=None, logits=None, argmax=None) -> None:
+        """One step of every sequence; tokens None = continue from the device-side greedy tokens."""
         if isinstance(tokens, (list, tuple)):
             tokens = np.ascontiguousarray(tokens, np.int32)
-        _check(lib().llm_decode_step_batch(self.h, _ptr(tokens), n, _ptr(logits), _ptr(argmax)), self.h)
+        _check(lib().llm_decode_step_batch(self.h, _ptr(tokens), self.max_batch, _ptr(logits), _ptr(argmax)),
+               self.h)
 
     # ---- cache -------------------------------------------------------------
     def kv_reset(self, seq: int = -1) -> None:

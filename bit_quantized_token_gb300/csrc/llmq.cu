@@ -21,6 +21,7 @@
 
 #include "kernels.cuh"
 #include "step.cuh"
+#include "batch.cuh"
 #include "llmq.h"
 
 using namespace llmq;
@@ -45,6 +46,32 @@ struct GemvPlan {
   int nslot = 0, ring = 0;
   size_t smem = 0;
 };
+
+// One batched GEMV (M tokens): row tiles per CTA, units per chunk, K splits.
+struct BPlan {
+  Mat m;
+  int rtb = 1, kc = 4, ks = 1, n_blocks = 0;
+  size_t smem = 0;
+};
+
+BPlan plan_bgemv(const Mat& mat, int n_sm) {
+  BPlan p;
+  p.m = mat;
+  const int epu = mat.bf16 ? kBF16UnitCols : 64;
+  for (int r : {8, 4, 2})
+    if (mat.n_rt % r == 0 && mat.n_rt / r >= n_sm) {
+      p.rtb = r;
+      break;
+    }
+  // at least 256 inputs per chunk (the warp sums reuse that staging area) and
+  // one unit per warp per chunk
+  p.kc = std::max(256 / epu, kBWarps / p.rtb);
+  p.n_blocks = mat.n_rt / p.rtb;
+  const int max_ks = std::max(1, mat.G / p.kc);
+  p.ks = std::min(max_ks, std::max(1, (2 * n_sm + p.n_blocks - 1) / p.n_blocks));
+  p.smem = bgemv_stage_bytes(p.rtb, p.kc, mat.unit_bytes(), epu);
+  return p;
+}
 
 // Where a named canonical tensor lives inside a fused matrix.
 struct Placement {
@@ -182,6 +209,14 @@ struct llm_model {
   int* d_cand_i = nullptr;
   int* d_attn_cnt = nullptr;
   int* d_greedy_cnt = nullptr;
+  // batched step (max_batch > 1)
+  std::vector<BPlan> bqkv, bwo, bgu, bdown;
+  BPlan blm;
+  float *d_bx = nullptr, *d_bh = nullptr, *d_bqkv = nullptr, *d_bo = nullptr, *d_ba = nullptr,
+        *d_blogits = nullptr, *d_bpart = nullptr, *d_battn_part = nullptr, *d_bcand_v = nullptr;
+  int *d_bcand_i = nullptr, *d_bcnt = nullptr, *d_battn_cnt = nullptr, *d_bgreedy_cnt = nullptr;
+  cudaGraphExec_t bgraph = nullptr;
+  size_t bsmem_max = 0;
   // persistent step kernel
   bool use_step = false;
   bool step_eager = false;
@@ -515,6 +550,140 @@ cudaError_t enqueue_persistent_step(llm_model* m, int seq) {
   return launch_step_t<2, 128>(m, sp);
 }
 
+template <int GQ, int HD>
+cudaError_t launch_battn_t(const llm_model* m, const BAttnParams& b, bool pdl) {
+  return launch(battention_kernel<GQ, HD>, dim3(m->attn_P, m->cfg.n_kv_heads, m->cfg.max_batch), dim3(kAttnThreads), 0,
+                m->stream, pdl, b);
+}
+
+cudaError_t launch_battn(const llm_model* m, const BAttnParams& b, bool pdl) {
+  switch (m->gq * 1000 + m->cfg.head_dim) {
+    case 1064: return launch_battn_t<1, 64>(m, b, pdl);
+    case 2064: return launch_battn_t<2, 64>(m, b, pdl);
+    case 4064: return launch_battn_t<4, 64>(m, b, pdl);
+    case 8064: return launch_battn_t<8, 64>(m, b, pdl);
+    case 1128: return launch_battn_t<1, 128>(m, b, pdl);
+    case 2128: return launch_battn_t<2, 128>(m, b, pdl);
+    case 4128: return launch_battn_t<4, 128>(m, b, pdl);
+    case 8128: return launch_battn_t<8, 128>(m, b, pdl);
+  }
+  return cudaErrorInvalidValue;
+}
+
+BGemvParams bgemv_params(const llm_model* m, const BPlan& b) {
+  BGemvParams p{};
+  p.units = m->d_arena + b.m.off;
+  p.n_rt = b.m.n_rt;
+  p.G = b.m.G;
+  p.K = b.m.cols;
+  p.rows = b.m.rows;
+  p.bf16 = b.m.bf16;
+  p.unit_bytes = b.m.unit_bytes();
+  p.epu = b.m.bf16 ? kBF16UnitCols : 64;
+  p.M = m->cfg.max_batch;
+  p.rtb = b.rtb;
+  p.kc = b.kc;
+  p.ks = b.ks;
+  p.eps = m->cfg.norm_eps;
+  p.part = m->d_bpart;
+  p.counters = m->d_bcnt;
+  p.status = m->d_status;
+  return p;
+}
+
+cudaError_t launch_bgemv(const llm_model* m, const BPlan& b, const BGemvParams& p, bool pdl) {
+  const dim3 grid(b.n_blocks * b.ks);
+  if (b.m.bf16) return launch(bgemv_kernel<true>, grid, dim3(kBThreads), b.smem, m->stream, pdl, p);
+  return launch(bgemv_kernel<false>, grid, dim3(kBThreads), b.smem, m->stream, pdl, p);
+}
+
+// Enqueue one decode step of every sequence (0..max_batch-1) on m->stream.
+cudaError_t enqueue_batch_step(llm_model* m) {
+  const llm_config& c = m->cfg;
+  const int L = c.n_layers, d = c.dim, B = c.max_batch, F = c.ffn_dim;
+  const bool pdl = !(c.flags & LLM_NO_PDL);
+  cudaError_t e;
+  BEmbedParams ep{};
+  ep.embed = m->d_embed;
+  ep.bf16 = m->embed_bf16;
+  ep.dim = d;
+  ep.vocab = c.vocab;
+  ep.M = B;
+  ep.tok = m->d_tok;
+  ep.x = m->d_bx;
+  ep.status = m->d_status;
+  if ((e = launch(bembed_kernel, dim3(B), dim3(256), 0, m->stream, false, ep)) != cudaSuccess) return e;
+  const size_t kv_layer = (size_t)c.n_kv_heads * c.max_seq * c.head_dim;
+  const int qkv_cols = m->q_dim + 2 * m->kv_dim;
+  for (int l = 0; l < L; ++l) {
+    BGemvParams p = bgemv_params(m, m->bqkv[l]);
+    p.x = m->d_bx;
+    p.norm_w = m->d_norms + m->off_attn_norm[l];
+    p.epi = EPI_STORE;
+    p.out = m->d_bqkv;
+    p.out_cols = qkv_cols;
+    if ((e = launch_bgemv(m, m->bqkv[l], p, pdl)) != cudaSuccess) return e;
+    BAttnParams bp{};
+    bp.a.q_dim = m->q_dim;
+    bp.a.kv_dim = m->kv_dim;
+    bp.a.Hkv = c.n_kv_heads;
+    bp.a.P = m->attn_P;
+    bp.a.rope = m->d_rope;
+    bp.a.rope_neox = c.rope_neox;
+    bp.a.q_norm = c.qk_norm ? m->d_norms + m->off_q_norm[l] : nullptr;
+    bp.a.k_norm = c.qk_norm ? m->d_norms + m->off_k_norm[l] : nullptr;
+    bp.a.eps = c.norm_eps;
+    bp.a.kc = m->d_k + (size_t)l * kv_layer;
+    bp.a.vc = m->d_v + (size_t)l * kv_layer;
+    bp.a.cap = c.max_seq;
+    bp.a.part = m->d_battn_part;
+    bp.a.counter = m->d_battn_cnt;
+    bp.a.out = m->d_bo;
+    bp.a.status = m->d_status;
+    bp.qkv = m->d_bqkv;
+    bp.qkv_cols = qkv_cols;
+    bp.o_cols = m->q_dim;
+    bp.pos = m->d_pos;
+    bp.seq_kv_stride = (size_t)L * kv_layer;
+    bp.part_stride = (size_t)c.n_kv_heads * m->attn_P * m->gq * (c.head_dim + 2);
+    if ((e = launch_battn(m, bp, pdl)) != cudaSuccess) return e;
+    p = bgemv_params(m, m->bwo[l]);  // h = x + Wo o
+    p.x = m->d_bo;
+    p.epi = EPI_RESID;
+    p.resid = m->d_bx;
+    p.out = m->d_bh;
+    p.out_cols = d;
+    if ((e = launch_bgemv(m, m->bwo[l], p, pdl)) != cudaSuccess) return e;
+    p = bgemv_params(m, m->bgu[l]);  // a = silu(Wg rmsnorm(h)) * (Wu rmsnorm(h))
+    p.x = m->d_bh;
+    p.norm_w = m->d_norms + m->off_ffn_norm[l];
+    p.epi = EPI_SWIGLU;
+    p.out = m->d_ba;
+    p.out_cols = F;
+    if ((e = launch_bgemv(m, m->bgu[l], p, pdl)) != cudaSuccess) return e;
+    p = bgemv_params(m, m->bdown[l]);  // x = h + Wd a
+    p.x = m->d_ba;
+    p.epi = EPI_RESID;
+    p.resid = m->d_bh;
+    p.out = m->d_bx;
+    p.out_cols = d;
+    if ((e = launch_bgemv(m, m->bdown[l], p, pdl)) != cudaSuccess) return e;
+  }
+  BGemvParams p = bgemv_params(m, m->blm);  // logits, greedy choice per sequence, positions += 1
+  p.x = m->d_bx;
+  p.norm_w = m->d_norms + m->off_final_norm;
+  p.epi = EPI_LOGITS;
+  p.out = m->d_blogits;
+  p.out_cols = c.vocab;
+  p.cand_v = m->d_bcand_v;
+  p.cand_i = m->d_bcand_i;
+  p.gcounter = m->d_bgreedy_cnt;
+  p.tok_io = m->d_tok;
+  p.argmax_out = m->d_argmax;
+  p.pos = m->d_pos;
+  return launch_bgemv(m, m->blm, p, pdl);
+}
+
 // Enqueue one batch-1 decode step of sequence `seq` on m->stream.
 cudaError_t enqueue_step(llm_model* m, int seq, Prof* prof = nullptr) {
   if (m->use_step && !prof) return enqueue_persistent_step(m, seq);
@@ -612,6 +781,7 @@ void llm_model_destroy(llm_model* m) {
   if (!m) return;
   for (auto g : m->graphs)
     if (g) cudaGraphExecDestroy(g);
+  if (m->bgraph) cudaGraphExecDestroy(m->bgraph);
   for (void* p : m->allocs) cudaFree(p);
   if (m->h_stage) cudaFreeHost(m->h_stage);
   if (m->own_stream && m->stream) cudaStreamDestroy(m->stream);
@@ -641,6 +811,8 @@ int llm_model_create(const llm_config* cfg, const llm_tensor* tensors, int32_t n
   if (c.ffn_dim > kMaxK || c.dim > kMaxK || c.n_heads * c.head_dim > kMaxK)
     return set_err(nullptr, LLM_ERR_UNSUPPORTED, "a GEMV input wider than " + std::to_string(kMaxK));
   if (c.rope_neox != 0 && c.rope_neox != 1) return set_err(nullptr, LLM_ERR_INVALID_ARG, "rope_neox must be 0 or 1");
+  if (c.max_batch > kBM)
+    return set_err(nullptr, LLM_ERR_UNSUPPORTED, "max_batch=" + std::to_string(c.max_batch) + " (32 sequences at most)");
 
   std::unordered_map<std::string, const llm_tensor*> by_name;
   for (int i = 0; i < n_tensors; ++i)
@@ -945,6 +1117,41 @@ int llm_model_create(const llm_config* cfg, const llm_tensor* tensors, int32_t n
   m->n_phases = (int)phases.size();
   AL(m->d_phases, phases.size() * sizeof(Phase), "phase table");
   AL(m->d_step_sync, 2 * sizeof(int), "step barrier");
+  // ---- the batched step (one token for every sequence)
+  size_t bcnt_total = 0;
+  if (c.max_batch > 1) {
+    const int B = c.max_batch;
+    size_t part_floats = 0;
+    int max_blocks = 1;
+    for (int l = 0; l < L; ++l) {
+      m->bqkv.push_back(plan_bgemv(m->mats[mi_qkv[l]], m->n_sm));
+      m->bwo.push_back(plan_bgemv(m->mats[mi_wo[l]], m->n_sm));
+      m->bgu.push_back(plan_bgemv(m->mats[mi_gu[l]], m->n_sm));
+      m->bdown.push_back(plan_bgemv(m->mats[mi_down[l]], m->n_sm));
+    }
+    m->blm = plan_bgemv(m->mats[mi_lm], m->n_sm);
+    std::vector<BPlan*> all = {&m->blm};
+    for (int l = 0; l < L; ++l) all.insert(all.end(), {&m->bqkv[l], &m->bwo[l], &m->bgu[l], &m->bdown[l]});
+    for (BPlan* b : all) {
+      if (b->ks > 1) part_floats = std::max(part_floats, (size_t)b->ks * kBM * b->m.n_rt * 32);
+      max_blocks = std::max(max_blocks, b->n_blocks);
+      m->bsmem_max = std::max(m->bsmem_max, b->smem);
+    }
+    bcnt_total = (size_t)max_blocks + (size_t)B * c.n_kv_heads + 1;
+    AL(m->d_bx, (size_t)B * d * 4, "batched residual");
+    AL(m->d_bh, (size_t)B * d * 4, "batched residual");
+    AL(m->d_bqkv, (size_t)B * (m->q_dim + 2 * m->kv_dim) * 4, "batched q|k|v");
+    AL(m->d_bo, (size_t)B * m->q_dim * 4, "batched attention output");
+    AL(m->d_ba, (size_t)B * F * 4, "batched SwiGLU output");
+    AL(m->d_blogits, (size_t)B * V * 4, "batched logits");
+    AL(m->d_bpart, std::max<size_t>(part_floats, 1) * 4, "batched partials");
+    AL(m->d_battn_part, (size_t)B * c.n_kv_heads * m->attn_P * gq * (hd + 2) * 4, "batched attention partials");
+    AL(m->d_bcand_v, (size_t)kBM * m->blm.n_blocks * 4, "batched greedy candidates");
+    AL(m->d_bcand_i, (size_t)kBM * m->blm.n_blocks * 4, "batched greedy candidates");
+    AL(m->d_bcnt, bcnt_total * 4, "batched counters");
+    m->d_battn_cnt = m->d_bcnt + max_blocks;
+    m->d_bgreedy_cnt = m->d_battn_cnt + (size_t)B * c.n_kv_heads;
+  }
   AL(m->d_pos, (size_t)c.max_batch * 4, "positions");
   AL(m->d_tok, (size_t)c.max_batch * 4, "tokens");
   AL(m->d_argmax, (size_t)c.max_batch * 4, "argmax");
@@ -984,6 +1191,11 @@ int llm_model_create(const llm_config* cfg, const llm_tensor* tensors, int32_t n
       if (e == cudaSuccess) e = cudaMemset(z, 0, 4 * (size_t)c.max_batch);
     if (e == cudaSuccess) e = cudaMemset(m->d_hist_ctr, 0, 4);
     if (e == cudaSuccess) e = cudaMemset(m->d_status, 0, 4);
+    if (e == cudaSuccess && m->d_bcnt) e = cudaMemset(m->d_bcnt, 0, bcnt_total * 4);
+    if (e == cudaSuccess && m->bsmem_max)
+      e = cudaFuncSetAttribute(bgemv_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)m->bsmem_max);
+    if (e == cudaSuccess && m->bsmem_max)
+      e = cudaFuncSetAttribute(bgemv_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)m->bsmem_max);
     if (e == cudaSuccess) e = cudaMemset(m->d_k, 0, kv_elems * 2);
     if (e == cudaSuccess) e = cudaMemset(m->d_v, 0, kv_elems * 2);
     size_t smax = m->lm.smem;
@@ -1062,9 +1274,44 @@ int llm_decode_greedy(llm_model* m, int32_t seq, int32_t first_token, int32_t n_
 }
 
 int llm_decode_step_batch(llm_model* m, const int32_t* tokens, int32_t n_seq, float* logits_out, int32_t* argmax_out) {
-  (void)tokens; (void)n_seq; (void)logits_out; (void)argmax_out;
-  if (!m) return set_err(nullptr, LLM_ERR_INVALID_ARG, "model is NULL");
-  return set_err(m, LLM_ERR_UNSUPPORTED, "batched decode step is not built yet");
+  int rc = check_model(m, 0);
+  if (rc) return rc;
+  const llm_config& c = m->cfg;
+  if (c.max_batch < 2) return set_err(m, LLM_ERR_UNSUPPORTED, "the model was created with max_batch < 2");
+  if (n_seq != c.max_batch) return set_err(m, LLM_ERR_INVALID_ARG, "n_seq must equal max_batch");
+  for (int b = 0; b < n_seq; ++b)
+    if (m->len[b] + 1 > c.max_seq) return set_err(m, LLM_ERR_CTX_FULL, "a sequence is at max_seq");
+  std::vector<int32_t> host_toks;
+  if (tokens) {  // else: each sequence continues from its previous greedy token, on the device
+    host_toks.resize(n_seq);
+    CK(cudaMemcpy(host_toks.data(), tokens, (size_t)n_seq * 4, cudaMemcpyDefault), "token read");
+    for (int b = 0; b < n_seq; ++b)
+      if (host_toks[b] < 0 || host_toks[b] >= c.vocab) return set_err(m, LLM_ERR_INVALID_ARG, "token out of range");
+    CK(cudaMemcpyAsync(m->d_tok, host_toks.data(), (size_t)n_seq * 4, cudaMemcpyHostToDevice, m->stream),
+       "token upload");
+  }
+  if (c.flags & LLM_NO_GRAPH) {
+    CK(enqueue_batch_step(m), "batched step launch");
+  } else {
+    if (!m->bgraph) {
+      cudaGraph_t g = nullptr;
+      CK(cudaStreamBeginCapture(m->stream, cudaStreamCaptureModeThreadLocal), "begin capture");
+      cudaError_t e = enqueue_batch_step(m);
+      cudaError_t e2 = cudaStreamEndCapture(m->stream, &g);
+      if (e != cudaSuccess) return cuda_fail(m, e, "batched step capture");
+      if (e2 != cudaSuccess) return cuda_fail(m, e2, "end capture");
+      e = cudaGraphInstantiate(&m->bgraph, g, 0);
+      cudaGraphDestroy(g);
+      if (e != cudaSuccess) return cuda_fail(m, e, "graph instantiate");
+    }
+    CK(cudaGraphLaunch(m->bgraph, m->stream), "graph launch");
+  }
+  for (int b = 0; b < n_seq; ++b) m->len[b] += 1;
+  bool host = false;
+  if ((rc = copy_out(m, logits_out, m->d_blogits, (size_t)n_seq * c.vocab * 4, &host)) != LLM_OK) return rc;
+  if ((rc = copy_out(m, argmax_out, m->d_argmax, (size_t)n_seq * 4, &host)) != LLM_OK) return rc;
+  if (host || tokens) return check_status(m);  // (pageable uploads are staged at call time)
+  return LLM_OK;
 }
 
 int llm_kv_reset(llm_model* m, int32_t seq) {

@@ -129,9 +129,15 @@ int llm_decode_step(llm_model* m, int32_t seq, int32_t token, float* logits_out,
 int llm_decode_greedy(llm_model* m, int32_t seq, int32_t first_token, int32_t n_steps,
                       int32_t* tokens_out);
 
-/* One decode step for sequences 0..n_seq-1 at once (n_seq == max_batch), each
- * at its own position. tokens [n_seq] (host or device); logits_out
- * [n_seq][vocab], argmax_out [n_seq]: host or device, may be NULL. */
+/* One decode step for sequences 0..n_seq-1 at once (n_seq == max_batch >= 2,
+ * at most 32), each at its own position (its cache may come from
+ * llm_kv_write or llm_prefill). The 4-bit matvecs become skinny GEMMs (fp32
+ * register tiles, each weight dequantised once for every sequence); attention
+ * runs over every sequence's own cache length. tokens [n_seq] (host or
+ * device), or NULL to continue every sequence from its previous greedy token
+ * on the device; logits_out [n_seq][vocab] and argmax_out [n_seq]: host or
+ * device, may be NULL. Synchronous when tokens or an output are host memory.
+ * Errors: UNSUPPORTED (max_batch < 2), INVALID_ARG, CTX_FULL, NAN, CUDA. */
 int llm_decode_step_batch(llm_model* m, const int32_t* tokens, int32_t n_seq,
                           float* logits_out, int32_t* argmax_out);
 

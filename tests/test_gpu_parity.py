@@ -273,3 +273,60 @@ def test_error_paths_leave_model_usable():
     with pytest.raises(bq.LlmError) as e:
         bq.Model(cfg, w2, max_seq=8)
     assert e.value.code == -8 and "L1.wo" in str(e.value)
+
+
+# ---------------------------------------------------------------- batched decode
+
+def _batched_vs_oracle(cfg, lens, n_steps, seed_tokens):
+    """Ragged pre-filled caches, teacher-forced batched steps, logits compared per sequence."""
+    B = len(lens)
+    w = synth.make_weights(cfg)
+    om = oracle.OracleModel(cfg, w)
+    cap = int(max(lens)) + n_steps + 1
+    caches = []
+    with bq.Model(cfg, w, max_seq=cap, max_batch=B) as m:
+        for b in range(B):
+            c = om.new_cache(int(lens[b]) + n_steps + 1)
+            for l in range(cfg["n_layers"]):
+                k, v = synth.make_prefilled_kv(cfg, l, b, int(lens[b]))
+                c.fill(l, k, v)
+                m.kv_write(b, l, 0, k, v)
+            c.set_len(int(lens[b]))
+            caches.append(c)
+        toks = np.array(seed_tokens, np.int32)
+        logits = np.empty((B, cfg["vocab"]), np.float32)
+        am = np.zeros(B, np.int32)
+        worst = 0.0
+        for s in range(n_steps):
+            m.decode_step_batch(toks, logits, am)
+            nxt = np.empty(B, np.int32)
+            for b in range(B):
+                ref = om.step(caches[b], int(toks[b]))
+                err = np.abs(logits[b] - ref).max() / np.abs(ref).max()
+                worst = max(worst, err)
+                assert err <= LOGIT_REL, f"step {s} seq {b}: logit error {err:.3e}"
+                assert int(am[b]) == int(np.argmax(logits[b])), "greedy choice of the kernel's own logits"
+                nxt[b] = oracle.argmax_f32(ref)
+            toks = nxt
+        for b in range(B):
+            assert m.kv_len(b) == int(lens[b]) + n_steps
+    return worst
+
+
+def test_batched_tiny_matches_oracle():
+    cfg = synth.workload(0)
+    lens = [3, 17, 1, 40]
+    _batched_vs_oracle(cfg, lens, 6, synth.make_first_tokens(cfg, 4))
+
+
+def test_batched_qwen_shape_ragged_two_layers():
+    # 32 sequences, cache lengths uniform in [512, 2048], full 151936-token vocabulary
+    cfg = synth.workload(4, n_layers=2)
+    lens = synth.make_kv_lengths(cfg, 32)
+    _batched_vs_oracle(cfg, lens, 3, synth.make_first_tokens(cfg, 32))
+
+
+def test_batched_workload_full_size():
+    cfg = synth.workload(4)
+    lens = synth.make_kv_lengths(cfg, 32)
+    _batched_vs_oracle(cfg, lens, 2, synth.make_first_tokens(cfg, 32))
