@@ -43,6 +43,8 @@ def args_():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--layers", type=int, default=0,
+                    help="run only the first N layers of the workload (small profiling cases; not a bench line)")
     return ap.parse_args()
 
 
@@ -73,7 +75,9 @@ def ncu_traffic(key):
 
 
 def workload_desc(cfg):
-    return (f"{cfg['name']}: dim {cfg['dim']}, {cfg['n_layers']} layers, {cfg['n_heads']}/{cfg['n_kv_heads']} heads, "
+    full = synth.workload(cfg["index"])["n_layers"] if "index" in cfg else cfg["n_layers"]
+    layers = f"{cfg['n_layers']} layers" if cfg["n_layers"] == full else f"first {cfg['n_layers']} of {full} layers"
+    return (f"{cfg['name']}: dim {cfg['dim']}, {layers}, {cfg['n_heads']}/{cfg['n_kv_heads']} heads, "
             f"head_dim {cfg['head_dim']}, ffn {cfg['ffn_dim']}, vocab {cfg['vocab']}, group-64 4-bit weights "
             f"(fp16 scale/min), fp32 activations, bf16 KV" + (", tied bf16 LM head" if cfg["tied"] else ""))
 
@@ -263,7 +267,7 @@ def main():
     if world > 1:
         import torch.distributed as dist
         dist.init_process_group("gloo")  # barrier only: the replicas exchange no data
-    cfg = synth.workload(a.workload)
+    cfg = synth.workload(a.workload, **({"n_layers": a.layers} if a.layers else {}))
     w = synth.make_weights(cfg)
     prompt = synth.make_prompt(cfg)
     if a.impl == "reference":

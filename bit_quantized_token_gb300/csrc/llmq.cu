@@ -160,13 +160,23 @@ void repack_bf16(uint8_t* units, int G, const uint16_t* data, int rows, int cols
   });
 }
 
+// Stream-K partition of n_rt row tiles x G units over at most n_cta CTAs.
+// The slot count S (CTAs that touch one row tile) is padded to 1, 2 or 4 so
+// that the consumers of the partials add a tile's slots inside one warp; the
+// CTA count shrinks until no tile has more than 4 contributors.
 Part make_part(int n_rt, int G, int n_cta) {
   Part p;
   p.U = n_rt * G;
-  p.N = std::max(1, std::min(n_cta, p.U));
   p.G = G;
-  p.S = 1;
-  for (int rt = 0; rt < n_rt; ++rt) p.S = std::max(p.S, p.n_contrib(rt));
+  for (int n = std::max(1, std::min(n_cta, p.U));; --n) {
+    p.N = n;
+    int s = 1;
+    for (int rt = 0; rt < n_rt; ++rt) s = std::max(s, p.n_contrib(rt));
+    if (s <= 4 || n == 1) {
+      p.S = s <= 1 ? 1 : (s <= 2 ? 2 : 4);
+      break;
+    }
+  }
   return p;
 }
 
@@ -530,7 +540,9 @@ cudaError_t enqueue_persistent_step(llm_model* m, int seq) {
   sp.layer_stride = (size_t)c.n_kv_heads * c.max_seq * c.head_dim;
   sp.k_base = m->d_k + (size_t)seq * c.n_layers * sp.layer_stride;
   sp.v_base = m->d_v + (size_t)seq * c.n_layers * sp.layer_stride;
-  sp.attn_part = m->d_attn_part;
+  // the split partials of the step kernel share the multi-kernel path's buffer
+  sp.attn_o = m->d_attn_part;
+  sp.attn_ml = m->d_attn_part + (size_t)c.n_kv_heads * m->attn_P * m->gq * c.head_dim;
   sp.attn_cnt = m->d_attn_cnt;
   sp.obuf = m->d_obuf;
   sp.logits = m->d_logits;
@@ -1080,8 +1092,7 @@ int llm_model_create(const llm_config* cfg, const llm_tensor* tensors, int32_t n
       phases.push_back(a);
       Phase o = gemv_phase(m->wo[l], m->wo[l].part_buf);
       o.layer = l;
-      o.in_mode = IN_PLAIN;
-      o.in_base = m->d_obuf;
+      o.in_mode = IN_ATTN;
       phases.push_back(o);
       Phase gu = gemv_phase(m->gu[l], m->gu[l].part_buf);
       gu.layer = l;

@@ -10,10 +10,19 @@
 // shared-memory ring, so the weights of the next phases are already arriving
 // while the current phase finishes and the barrier resolves.
 //
-// Split-K across CTAs leaves one partial sum per CTA that touches a row tile;
-// the next phase adds the slots in CTA order while it builds its input vector
-// (residual add, SwiGLU, RMSNorm are fused there), so no phase needs a fix-up
-// of its own and no float atomics are used.
+// Split-K across CTAs leaves one partial sum per CTA that touches a row tile
+// (S = 1, 2 or 4 slots per tile, unused slots zero); the next phase adds the
+// slots while it builds its input vector (residual add, SwiGLU, RMSNorm are
+// fused there), so no phase needs a fix-up of its own and no float atomics
+// are used. Every input build issues all of its loads before it uses any of
+// them: one L2 round trip per phase.
+//
+// Attention is flash-decoding over (kv head, split) items. An item stages its
+// K/V rows in shared memory with bulk copies, runs one warp per (q head, block
+// of 32 positions) and leaves an unnormalised partial (o, max, sum) per split;
+// with few splits the o-projection's input build merges them, so the merge
+// costs no round trip of its own. With many splits (long caches) the last
+// split of a kv head merges them instead.
 #pragma once
 #include "kernels.cuh"
 
@@ -21,15 +30,26 @@ namespace llmq {
 
 // 15 consumer warps + 1 producer warp = 4 warps per scheduler, 128 registers each
 constexpr int kSWarps = 15;                      // consumer warps
-constexpr int kSThreads = (kSWarps + 1) * 32;    // + one producer warp
+constexpr int kSCThreads = kSWarps * 32;         // consumer threads
+constexpr int kSThreads = kSCThreads + 32;       // + one producer warp
 constexpr int kSChunk = kSWarps;                 // units per ring slot: one per consumer warp
 constexpr int kSSlot = kSChunk * kQ4UnitBytes;   // 17280 B (bf16 chunks use 15360 B)
 constexpr int kSNSlot = 8;
 constexpr int kSRing = kSNSlot * kSSlot;         // 138240 B
 constexpr int kSRLoc = 6;                        // row tiles a reduction window may touch
+constexpr int kSMaxV = (kMaxK / 4 + kSCThreads - 1) / kSCThreads;  // float4s of a K-vector per thread
+constexpr int kSDefer = 4;                       // splits the o-projection's input build merges
+constexpr int kSAttnPP = 128;                    // cache positions staged per attention pass
+
+// Cache positions per attention split (more only when the split count is capped).
+__host__ __device__ constexpr int step_split_len(int hd) { return hd == 64 ? 64 : 128; }
+__host__ __device__ inline int step_splits(int len, int P, int hd) {
+  const int s = (len + step_split_len(hd) - 1) / step_split_len(hd);
+  return s < 1 ? 1 : (s < P ? s : P);
+}
 
 enum PhaseType : int { PH_GEMV = 0, PH_ATTN = 1, PH_LOGITS = 2 };
-enum InMode : int { IN_EMBED_F32 = 0, IN_EMBED_BF16 = 1, IN_PLAIN = 2, IN_RESID = 3, IN_SWIGLU = 4 };
+enum InMode : int { IN_EMBED_F32 = 0, IN_EMBED_BF16 = 1, IN_PLAIN = 2, IN_RESID = 3, IN_SWIGLU = 4, IN_ATTN = 5 };
 
 struct Phase {
   int type;
@@ -42,7 +62,7 @@ struct Phase {
   int in_mode;
   const float* in_base;   // IN_PLAIN: the vector; IN_RESID: the residual base
   const float* in_part;   // IN_RESID / IN_SWIGLU: partials of the previous GEMV
-  int in_S;
+  int in_S;               // 1, 2 or 4
   float* in_store;        // CTA 0 stores the built (pre-norm) vector here, or null
   const float* norm_w;    // RMSNorm weight, or null
   // ---- ATTN
@@ -71,9 +91,10 @@ struct StepParams {
   uint16_t* k_base;       // layer 0 of this sequence's cache: [L][Hkv][cap][hd]
   uint16_t* v_base;
   size_t layer_stride;    // elements per layer of the cache
-  float* attn_part;
-  int* attn_cnt;
-  float* obuf;
+  float* attn_o;          // [Hkv][P][GQ][hd] unnormalised split outputs
+  float* attn_ml;         // [Hkv][P][GQ][2] (max, sum) of the splits
+  int* attn_cnt;          // [Hkv], zero between launches (merge by the last split)
+  float* obuf;            // [q_dim] merged output when the last split merges
   // greedy choice
   float* logits;
   float* cand_v;
@@ -87,14 +108,94 @@ struct StepParams {
 };
 
 struct ConsumerSync {
-  __device__ static void sync() { asm volatile("bar.sync 1, %0;" ::"n"(kSWarps * 32) : "memory"); }
+  __device__ static void sync() { asm volatile("bar.sync 1, %0;" ::"n"(kSCThreads) : "memory"); }
 };
+
+// Consumer barrier that also ANDs a flag over the consumer threads.
+__device__ __forceinline__ bool consumer_and(bool v) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\tbar.red.and.pred q, 1, %2, p;\n\tselp.u32 %0, 1, 0, q;\n\t}"
+      : "=r"(r)
+      : "r"((uint32_t)v), "n"(kSCThreads)
+      : "memory");
+  return r != 0;
+}
 
 __device__ __forceinline__ int ld_acquire(const int* p) {
   int v;
   asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
   return v;
 }
+
+// Loads issued as predicated instructions, so a run of them goes out back to
+// back; the result is zero when !pred. The "memory" clobber keeps them after
+// the barrier that precedes them.
+__device__ __forceinline__ float4 ldcg4_if(const float* ptr, bool pred) {
+  float4 v;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.u32 p, %5, 0;\n\t"
+      "mov.b32 %0, 0;\n\tmov.b32 %1, 0;\n\tmov.b32 %2, 0;\n\tmov.b32 %3, 0;\n\t"
+      "@p ld.global.cg.v4.f32 {%0, %1, %2, %3}, [%4];\n\t}"
+      : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+      : "l"(ptr), "r"((uint32_t)pred)
+      : "memory");
+  return v;
+}
+__device__ __forceinline__ float2 ldcg2_if(const float* ptr, bool pred) {
+  float2 v;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.u32 p, %3, 0;\n\t"
+      "mov.b32 %0, 0;\n\tmov.b32 %1, 0;\n\t"
+      "@p ld.global.cg.v2.f32 {%0, %1}, [%2];\n\t}"
+      : "=f"(v.x), "=f"(v.y)
+      : "l"(ptr), "r"((uint32_t)pred)
+      : "memory");
+  return v;
+}
+__device__ __forceinline__ float ldcg1_if(const float* ptr, bool pred) {
+  float v;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.u32 p, %2, 0;\n\t"
+      "mov.b32 %0, 0;\n\t@p ld.global.cg.f32 %0, [%1];\n\t}"
+      : "=f"(v)
+      : "l"(ptr), "r"((uint32_t)pred)
+      : "memory");
+  return v;
+}
+// Same through the read-only path, for data no kernel writes (norm weights).
+__device__ __forceinline__ float4 ldnc4_if(const float* ptr, bool pred) {
+  float4 v;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.u32 p, %5, 0;\n\t"
+      "mov.b32 %0, 0;\n\tmov.b32 %1, 0;\n\tmov.b32 %2, 0;\n\tmov.b32 %3, 0;\n\t"
+      "@p ld.global.nc.v4.f32 {%0, %1, %2, %3}, [%4];\n\t}"
+      : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+      : "l"(ptr), "r"((uint32_t)pred)
+      : "memory");
+  return v;
+}
+
+// Partial arrays are [tile][S][32] floats with S = 1 << lgS. Float4 f covers
+// rows 4*(f & 7) .. +3 of slot (f >> 3) & (S-1) of tile f >> (3 + lgS); as 8S
+// divides 32, the slots of a row quad sit in lanes l, l^8 (, l^16, l^24) of
+// one warp and a butterfly adds them. Every lane ends with the full sum.
+__device__ __forceinline__ float4 slot_sum(float4 a, int lgS) {
+  if (lgS >= 1) {
+    a.x += __shfl_xor_sync(0xffffffffu, a.x, 8);
+    a.y += __shfl_xor_sync(0xffffffffu, a.y, 8);
+    a.z += __shfl_xor_sync(0xffffffffu, a.z, 8);
+    a.w += __shfl_xor_sync(0xffffffffu, a.w, 8);
+  }
+  if (lgS >= 2) {
+    a.x += __shfl_xor_sync(0xffffffffu, a.x, 16);
+    a.y += __shfl_xor_sync(0xffffffffu, a.y, 16);
+    a.z += __shfl_xor_sync(0xffffffffu, a.z, 16);
+    a.w += __shfl_xor_sync(0xffffffffu, a.w, 16);
+  }
+  return a;
+}
+__device__ __forceinline__ int log2_slots(int S) { return S >= 4 ? 2 : S >= 2 ? 1 : 0; }
 
 // Consumer-side grid barrier: wait until `target` arrivals (bounded). Any
 // timeout sets the shared abort flag, which ends every other wait at once.
@@ -130,7 +231,7 @@ __device__ __forceinline__ void grid_arrive(const StepParams& sp) {
   if (threadIdx.x == 0) asm volatile("red.release.gpu.global.add.s32 [%0], 1;" ::"l"(sp.sync) : "memory");
 }
 
-// Bounded ring wait that also gives up when another CTA aborted the step.
+// Bounded mbarrier wait that also gives up when another CTA aborted the step.
 __device__ __forceinline__ bool ring_wait(uint64_t* bar, uint32_t parity, const StepParams& sp) {
   if (mbar_try_wait(bar, parity)) return true;
   const unsigned long long t0 = globaltimer();
@@ -148,16 +249,26 @@ __device__ __forceinline__ bool ring_wait(uint64_t* bar, uint32_t parity, const 
   return true;
 }
 
-// Sum of the S partial slots of 4 consecutive rows r..r+3 (same row tile).
-__device__ __forceinline__ float4 reduce4(const float* __restrict__ part, int S, int r) {
-  const float4* src = reinterpret_cast<const float4*>(part + ((size_t)(r >> 5) * S) * kTileRows + (r & 31));
-  float4 a = __ldcg(src);
-  for (int j = 1; j < S; ++j) {
-    const float4 b = __ldcg(src + j * (kTileRows / 4));
-    a.x += b.x; a.y += b.y; a.z += b.z; a.w += b.w;
-  }
-  return a;
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
+
+// Shared memory of one attention item.
+template <int GQ, int HD>
+struct StepAttnSmem {
+  static constexpr int NB = kSAttnPP / 32;  // blocks of 32 positions per pass
+  uint16_t kt[kSAttnPP][HD];  // staged K rows (bf16), 16-B aligned for the bulk copy
+  uint16_t vt[kSAttnPP][HD];
+  float cur[GQ + 2][HD];      // this step's q heads, k, v of the kv head
+  float qa[GQ][HD / 2];       // scaled q: dims 8c..8c+3 at qa[4c..4c+3], 8c+4..8c+7 at qb
+  float qb[GQ][HD / 2];
+  float p[kSWarps][32];       // probabilities of a warp's current block
+  float tres[GQ * NB][HD + 2];  // per (block, head): o, block max, block sum
+  float acc[GQ][HD];          // running output of the item over its passes
+  float accm[GQ], accl[GQ];
+  float fac[GQ][NB + 1];
+  int is_last;
+};
 
 template <int GQ, int HD>
 struct StepSmem {
@@ -168,7 +279,7 @@ struct StepSmem {
       float red[kSRLoc][kSWarps][32];      // per-warp row-tile sums of a window
       float carry[2][32];
     } g;
-    AttnSmem<GQ, HD, kSWarps> a;
+    StepAttnSmem<GQ, HD> a;
     struct {
       float fbest[kSWarps];
       int ibest[kSWarps];
@@ -181,7 +292,258 @@ struct StepSmem {
   int flag;
   int abort;
   int issued;
+  int a_issued;           // attention bulk stagings issued (consumer thread 0)
 };
+
+// ---------------------------------------------------------------------------
+// One (kv head g, split) attention item, run by the consumer warps.
+// `apar` counts the completed waits on `abar` (identical in every consumer).
+// Returns false when a wait gave up (uniform over the consumers).
+template <int GQ, int HD>
+__device__ bool step_attn_item(const StepParams& sp, const Phase& P, int g, int split, int P_eff, int pos,
+                               StepAttnSmem<GQ, HD>& sa, uint64_t* abar, uint32_t& apar, int* a_issued) {
+  constexpr int NT = kSCThreads;
+  constexpr int DPL = HD / 32;  // V dims per lane
+  constexpr int NC = HD / 8;    // 16-B chunks of a K row
+  static_assert(DPL == 2 || DPL == 4, "head_dim 64 or 128");
+  static_assert((GQ + 1) * (HD / 2) <= NT && GQ < kSWarps, "one RoPE pair per thread, one warp per q/k head");
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int len = pos + 1;
+  const int t0 = (int)((int64_t)len * split / P_eff), t1 = (int)((int64_t)len * (split + 1) / P_eff);
+  uint16_t* kc = sp.k_base + (size_t)P.layer * sp.layer_stride + (size_t)g * sp.cap * HD;
+  uint16_t* vc = sp.v_base + (size_t)P.layer * sp.layer_stride + (size_t)g * sp.cap * HD;
+
+  // thread 0 stages rows tp .. of K and V (the previous users of this shared
+  // memory finished at the barrier before this item)
+  auto stage = [&](int tp) {
+    const uint32_t bytes = (uint32_t)min(kSAttnPP, t1 - tp) * HD * 2;
+    fence_proxy_async_smem();
+    mbar_expect_tx(abar, 2 * bytes);
+    const uint64_t pol = policy_evict_first();
+    bulk_g2s(sa.kt, kc + (size_t)tp * HD, bytes, abar, pol);
+    bulk_g2s(sa.vt, vc + (size_t)tp * HD, bytes, abar, pol);
+    *a_issued += 1;
+  };
+  if (tid == 0) stage(t0);
+
+  // RoPE factors and q/k norm weights do not depend on the step: load them
+  // in the same round trip as the q|k|v gather
+  const int nrope = (GQ + 1) * (HD / 2);
+  float2 rcs = make_float2(1.f, 0.f);
+  if (tid < nrope) rcs = __ldg(sp.rope + (size_t)pos * (HD / 2) + tid % (HD / 2));
+  float wn[DPL];
+#pragma unroll
+  for (int e = 0; e < DPL; ++e)
+    wn[e] = (P.q_norm && warp <= GQ) ? __ldg((warp < GQ ? P.q_norm : P.k_norm) + lane + 32 * e) : 1.f;
+
+  // ---- gather q (GQ heads), k and v of this kv head from the QKV partials
+  {
+    const int lg = log2_slots(P.qkv_S);
+    const int nq = GQ * HD / 32, nk = HD / 32;
+    const int qt0 = g * nq, kt0 = (sp.q_dim + g * HD) / 32, vt0 = (sp.q_dim + sp.kv_dim + g * HD) / 32;
+    const int T4 = (nq + 2 * nk) << (3 + lg);
+    constexpr int RB = ((GQ + 2) * HD / 32 * 4 * 8 + NT - 1) / NT;  // covers S <= 4 in one batch
+    float4 a[RB];
+#pragma unroll
+    for (int j = 0; j < RB; ++j) {
+      const int f = tid + j * NT;
+      const int ti = f >> (3 + lg);
+      const int tile = ti < nq ? qt0 + ti : (ti < nq + nk ? kt0 + ti - nq : vt0 + ti - nq - nk);
+      a[j] = ldcg4_if(P.qkv_part + ((size_t)tile * (8 << lg) + (f & ((8 << lg) - 1))) * 4, f < T4);
+    }
+#pragma unroll
+    for (int j = 0; j < RB; ++j) {
+      const float4 v = slot_sum(a[j], lg);
+      const int f = tid + j * NT;
+      if (f < T4 && ((f >> 3) & ((1 << lg) - 1)) == 0)
+        *reinterpret_cast<float4*>(&sa.cur[0][0] + (f >> (3 + lg)) * 32 + (f & 7) * 4) = v;
+    }
+  }
+  ConsumerSync::sync();
+  // ---- per-head RMSNorm of q and k (Qwen3): warp h < GQ takes q head h, warp GQ takes k
+  if (P.q_norm) {
+    if (warp <= GQ) {
+      float* v = sa.cur[warp];
+      float x[DPL], ss = 0.f;
+#pragma unroll
+      for (int e = 0; e < DPL; ++e) {
+        x[e] = v[lane + 32 * e];
+        ss += x[e] * x[e];
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+      const float inv = 1.0f / sqrtf(ss / (float)HD + sp.eps);
+#pragma unroll
+      for (int e = 0; e < DPL; ++e) v[lane + 32 * e] = x[e] * inv * wn[e];
+    }
+    ConsumerSync::sync();
+  }
+  // ---- RoPE at `pos`: pairs (2i, 2i+1) or (i, i + HD/2), of the q heads and k
+  if (tid < nrope) {
+    const int h = tid / (HD / 2), i = tid % (HD / 2);
+    float* v = sa.cur[h];
+    const int ia = sp.rope_neox ? i : 2 * i, ib = sp.rope_neox ? i + HD / 2 : 2 * i + 1;
+    const float x0 = v[ia], x1 = v[ib];
+    v[ia] = x0 * rcs.x - x1 * rcs.y;
+    v[ib] = x0 * rcs.y + x1 * rcs.x;
+  }
+  ConsumerSync::sync();
+  // ---- round k, v to bf16 (the split owning `pos` appends them); scale q
+  const float qscale = 1.4426950408889634f / sqrtf((float)HD);  // log2(e)/sqrt(hd)
+  for (int i = tid; i < (GQ + 2) * HD; i += NT) {
+    const int r = i / HD, d = i % HD;
+    if (r >= GQ) {
+      const __nv_bfloat16 b = __float2bfloat16_rn(sa.cur[r][d]);
+      sa.cur[r][d] = __bfloat162float(b);
+      if (split == P_eff - 1) (r == GQ ? kc : vc)[(size_t)pos * HD + d] = __bfloat16_as_ushort(b);
+    } else {
+      const float q = sa.cur[r][d] * qscale;
+      const int cq = d >> 3, e = d & 7;
+      if (e < 4) sa.qa[r][4 * cq + e] = q;
+      else sa.qb[r][4 * cq + e - 4] = q;
+    }
+  }
+  for (int i = tid; i < GQ * HD; i += NT) sa.acc[i / HD][i % HD] = 0.f;
+  if (tid < GQ) {
+    sa.accm[tid] = -INFINITY;
+    sa.accl[tid] = 0.f;
+  }
+
+  // ---- passes of at most kSAttnPP positions
+  for (int tp = t0; tp < t1; tp += kSAttnPP) {
+    const int n = min(kSAttnPP, t1 - tp), nb = (n + 31) / 32;
+    const bool got = ring_wait(abar, apar & 1, sp);
+    ++apar;
+    if (!consumer_and(got)) return false;  // also orders the writes above before the reads below
+    if (pos >= tp && pos < tp + n)           // the current position's row is this step's k, v
+      for (int d = tid; d < HD; d += NT) {
+        sa.kt[pos - tp][d] = __bfloat16_as_ushort(__float2bfloat16_rn(sa.cur[GQ][d]));
+        sa.vt[pos - tp][d] = __bfloat16_as_ushort(__float2bfloat16_rn(sa.cur[GQ + 1][d]));
+      }
+    ConsumerSync::sync();
+    // warp task (q head h, block b): lane = position 32b + lane for the
+    // scores; lane = dims DPL*lane.. for the weighted V sum
+    for (int task = warp; task < GQ * nb; task += kSWarps) {
+      const int h = task % GQ, b = task / GQ;
+      const int nv = min(32, n - 32 * b);
+      const bool valid = lane < nv;
+      const uint16_t* kr = sa.kt[32 * b + (valid ? lane : 0)];
+      float s0 = 0.f, s1 = 0.f;
+#pragma unroll
+      for (int c = 0; c < NC; ++c) {
+        const int cc = (c + lane) & (NC - 1);  // rotated: the lanes of a quarter warp hit distinct banks
+        const uint4 kk = *reinterpret_cast<const uint4*>(kr + 8 * cc);
+        const float4 qa = *reinterpret_cast<const float4*>(&sa.qa[h][4 * cc]);
+        const float4 qb = *reinterpret_cast<const float4*>(&sa.qb[h][4 * cc]);
+        s0 = fmaf(qa.x, __uint_as_float(kk.x << 16), s0);
+        s1 = fmaf(qa.y, __uint_as_float(kk.x & 0xFFFF0000u), s1);
+        s0 = fmaf(qa.z, __uint_as_float(kk.y << 16), s0);
+        s1 = fmaf(qa.w, __uint_as_float(kk.y & 0xFFFF0000u), s1);
+        s0 = fmaf(qb.x, __uint_as_float(kk.z << 16), s0);
+        s1 = fmaf(qb.y, __uint_as_float(kk.z & 0xFFFF0000u), s1);
+        s0 = fmaf(qb.z, __uint_as_float(kk.w << 16), s0);
+        s1 = fmaf(qb.w, __uint_as_float(kk.w & 0xFFFF0000u), s1);
+      }
+      const float s = valid ? s0 + s1 : -INFINITY;
+      float mx = s;
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+      const float pj = valid ? exp2f(s - mx) : 0.f;
+      float l = pj;
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) l += __shfl_xor_sync(0xffffffffu, l, o);
+      sa.p[warp][lane] = pj;
+      __syncwarp();
+      float o[DPL];
+#pragma unroll
+      for (int e = 0; e < DPL; ++e) o[e] = 0.f;
+      const uint16_t* vr = &sa.vt[32 * b][DPL * lane];
+#pragma unroll 4
+      for (int j = 0; j < nv; ++j) {
+        const float pv = sa.p[warp][j];
+        if constexpr (DPL == 2) {
+          const uint32_t w = *reinterpret_cast<const uint32_t*>(vr + (size_t)j * HD);
+          o[0] = fmaf(pv, __uint_as_float(w << 16), o[0]);
+          o[1] = fmaf(pv, __uint_as_float(w & 0xFFFF0000u), o[1]);
+        } else {
+          const uint2 w = *reinterpret_cast<const uint2*>(vr + (size_t)j * HD);
+          o[0] = fmaf(pv, __uint_as_float(w.x << 16), o[0]);
+          o[1] = fmaf(pv, __uint_as_float(w.x & 0xFFFF0000u), o[1]);
+          o[2] = fmaf(pv, __uint_as_float(w.y << 16), o[2]);
+          o[3] = fmaf(pv, __uint_as_float(w.y & 0xFFFF0000u), o[3]);
+        }
+      }
+      float* tr = sa.tres[task];
+#pragma unroll
+      for (int e = 0; e < DPL; ++e) tr[DPL * lane + e] = o[e];
+      if (lane == 0) {
+        tr[HD] = mx;
+        tr[HD + 1] = l;
+      }
+      __syncwarp();  // sa.p is rewritten by this warp's next task
+    }
+    ConsumerSync::sync();
+    // the staged rows are no longer read: stage the next pass
+    if (tid == 0 && tp + kSAttnPP < t1) stage(tp + kSAttnPP);
+    // fold the pass into the running output
+    if (tid < GQ) {
+      const int h = tid;
+      float M = sa.accm[h];
+      for (int bb = 0; bb < nb; ++bb) M = fmaxf(M, sa.tres[bb * GQ + h][HD]);
+      const float fa = sa.accm[h] == -INFINITY ? 0.f : exp2f(sa.accm[h] - M);
+      float L = sa.accl[h] * fa;
+      sa.fac[h][0] = fa;
+      for (int bb = 0; bb < nb; ++bb) {
+        const float f = exp2f(sa.tres[bb * GQ + h][HD] - M);
+        sa.fac[h][1 + bb] = f;
+        L += sa.tres[bb * GQ + h][HD + 1] * f;
+      }
+      sa.accm[h] = M;
+      sa.accl[h] = L;
+    }
+    ConsumerSync::sync();
+    for (int i = tid; i < GQ * HD; i += NT) {
+      const int h = i / HD, d = i % HD;
+      float O = sa.acc[h][d] * sa.fac[h][0];
+      for (int bb = 0; bb < nb; ++bb) O += sa.tres[bb * GQ + h][d] * sa.fac[h][1 + bb];
+      sa.acc[h][d] = O;
+    }
+    ConsumerSync::sync();
+  }
+
+  // ---- the split's partial
+  const size_t pbase = ((size_t)g * sp.P + split) * GQ;
+  for (int i = tid; i < GQ * HD; i += NT) sp.attn_o[pbase * HD + i] = sa.acc[i / HD][i % HD];
+  if (tid < GQ) {
+    sp.attn_ml[(pbase + tid) * 2] = sa.accm[tid];
+    sp.attn_ml[(pbase + tid) * 2 + 1] = sa.accl[tid];
+  }
+  if (P_eff <= kSDefer) return true;  // the o-projection's input build merges the splits
+  // many splits: the last one of this kv head merges them into obuf
+  __threadfence();
+  ConsumerSync::sync();
+  if (tid == 0) sa.is_last = (atomicAdd(&sp.attn_cnt[g], 1) == P_eff - 1);
+  ConsumerSync::sync();
+  if (sa.is_last) {
+    __threadfence();
+    const float* ho = sp.attn_o + (size_t)g * sp.P * GQ * HD;
+    const float* hm = sp.attn_ml + (size_t)g * sp.P * GQ * 2;
+    for (int i = tid; i < GQ * HD; i += NT) {
+      const int h = i / HD, d = i % HD;
+      float M = -INFINITY;
+      for (int s = 0; s < P_eff; ++s) M = fmaxf(M, __ldcg(hm + ((size_t)s * GQ + h) * 2));
+      float L = 0.f, O = 0.f;
+      for (int s = 0; s < P_eff; ++s) {
+        const float f = exp2f(__ldcg(hm + ((size_t)s * GQ + h) * 2) - M);
+        L += __ldcg(hm + ((size_t)s * GQ + h) * 2 + 1) * f;
+        O += __ldcg(ho + ((size_t)s * GQ + h) * HD + d) * f;
+      }
+      sp.obuf[(g * GQ + h) * HD + d] = O / L;
+    }
+    if (tid == 0) sp.attn_cnt[g] = 0;
+  }
+  return true;
+}
 
 template <int GQ, int HD>
 __global__ void __launch_bounds__(kSThreads, 1) step_kernel(const StepParams sp) {
@@ -190,6 +552,7 @@ __global__ void __launch_bounds__(kSThreads, 1) step_kernel(const StepParams sp)
   StepSmem<GQ, HD>& sm = *reinterpret_cast<StepSmem<GQ, HD>*>(smem_raw + kSRing);
   uint64_t* full = reinterpret_cast<uint64_t*>(smem_raw + kSRing + ((sizeof(StepSmem<GQ, HD>) + 15) & ~size_t(15)));
   uint64_t* empty = full + kSNSlot;
+  uint64_t* abar = empty + kSNSlot;
 
   const int c = blockIdx.x, N = gridDim.x;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -198,9 +561,11 @@ __global__ void __launch_bounds__(kSThreads, 1) step_kernel(const StepParams sp)
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], kSWarps);
     }
+    mbar_init(abar, 1);
     mbar_fence_init();
     sm.abort = 0;
     sm.issued = 0;
+    sm.a_issued = 0;
   }
   __syncthreads();
 
@@ -229,129 +594,215 @@ __global__ void __launch_bounds__(kSThreads, 1) step_kernel(const StepParams sp)
     }
   } else {
     // ================= consumers
+    constexpr int NT = kSCThreads;
     int gi = 0;
+    uint32_t apar = 0;
+    // the position only changes at the very end of the step (greedy choice)
+    const int spos = *sp.pos;
     // descriptors go to shared memory one phase ahead (the phase table is immutable)
     static_assert(sizeof(Phase) % 4 == 0, "");
     auto fetch_phase = [&](int ph) {
       if (ph < sp.n_phases)
-        for (int i = tid; i < (int)(sizeof(Phase) / 4); i += kSWarps * 32)
+        for (int i = tid; i < (int)(sizeof(Phase) / 4); i += NT)
           reinterpret_cast<int*>(&sm.ph[ph & 1])[i] = __ldg(reinterpret_cast<const int*>(&sp.phases[ph]) + i);
     };
     fetch_phase(0);
     ConsumerSync::sync();
     for (int ph = 0; ph < sp.n_phases; ++ph) {
+      const Phase& P = sm.ph[ph & 1];
+      // norm weights do not depend on the step: in flight while the barrier resolves
+      float4 w4[kSMaxV];
+      {
+        const bool nw = P.type == PH_GEMV && P.norm_w != nullptr;
+#pragma unroll
+        for (int j = 0; j < kSMaxV; ++j) {
+          const int i = tid + j * NT;
+          w4[j] = ldnc4_if(nw ? P.norm_w + 4 * i : nullptr, nw && i < P.K / 4);
+        }
+      }
       if (ph > 0 && !grid_wait(sp, ph * N, &sm.flag)) {
         sm.abort = 1;
         break;
       }
-      const Phase& P = sm.ph[ph & 1];
       fetch_phase(ph + 1);  // read by the next phase, after this phase's closing barriers
       if (P.type == PH_GEMV) {
-        // ---------------- build the input vector (thread t: float4s t, t+512, ...)
-        constexpr int MAXV = (kMaxK / 4 + kSWarps * 32 - 1) / (kSWarps * 32);
+        // ---------------- build the input vector: every load of the build in one round trip
         const int K = P.K, n4 = K / 4;
-        float4 v[MAXV];
-        if (P.in_mode == IN_EMBED_F32 || P.in_mode == IN_EMBED_BF16) {
-          int t = *sp.tok;
-          if (t < 0 || t >= sp.vocab) {
-            if (tid == 0) atomicOr(sp.status, ST_BAD_TOKEN);
-            t = 0;
-          }
+        float4* xh4 = reinterpret_cast<float4*>(sm.u.g.xh);
+        float ss = 0.f;
+        auto put = [&](int i4, float4 v) {  // pre-norm inputs 4*i4 .. 4*i4+3
+          xh4[i4] = v;
+          if (P.in_store && c == 0) reinterpret_cast<float4*>(P.in_store)[i4] = v;
+          ss += (v.x * v.x + v.y * v.y) + (v.z * v.z + v.w * v.w);
+        };
+        if (P.in_mode == IN_RESID) {
+          // x = residual + sum of the previous GEMV's slots (row tiles of 32 inputs)
+          constexpr int RB = 6;
+          const int lg = log2_slots(P.in_S);
+          const int T4 = (K / 32) << (3 + lg);
+          for (int f0 = 0; f0 < T4; f0 += RB * NT) {
+            float4 a[RB], b[RB];
 #pragma unroll
-          for (int j = 0; j < MAXV; ++j) {
-            const int i = tid + j * kSWarps * 32;
-            if (i < n4) {
-              if (P.in_mode == IN_EMBED_F32) {
-                v[j] = __ldg(reinterpret_cast<const float4*>(static_cast<const float*>(sp.embed) + (size_t)t * K) + i);
-              } else {
-                const uint2 u = __ldg(reinterpret_cast<const uint2*>(static_cast<const uint16_t*>(sp.embed) + (size_t)t * K) + i);
-                v[j] = make_float4(__uint_as_float(u.x << 16), __uint_as_float(u.x & 0xFFFF0000u),
-                                   __uint_as_float(u.y << 16), __uint_as_float(u.y & 0xFFFF0000u));
+            for (int j = 0; j < RB; ++j) {
+              const int f = f0 + tid + j * NT;
+              const bool s0 = ((f >> 3) & ((1 << lg) - 1)) == 0;
+              const int r4 = ((f >> (3 + lg)) << 3) + (f & 7);
+              a[j] = ldcg4_if(P.in_part + (size_t)f * 4, f < T4);
+              b[j] = ldcg4_if(P.in_base + (size_t)r4 * 4, f < T4 && s0);
+            }
+#pragma unroll
+            for (int j = 0; j < RB; ++j) {
+              const float4 s = slot_sum(a[j], lg);
+              const int f = f0 + tid + j * NT;
+              if (f < T4 && ((f >> 3) & ((1 << lg) - 1)) == 0)
+                put(((f >> (3 + lg)) << 3) + (f & 7),
+                    make_float4(b[j].x + s.x, b[j].y + s.y, b[j].z + s.z, b[j].w + s.w));
+            }
+          }
+        } else if (P.in_mode == IN_SWIGLU) {
+          // row tile t of the gate|up GEMV: 16 gate rows, then their 16 up rows -> inputs 16t..16t+15
+          constexpr int RB = 12;
+          const int lg = log2_slots(P.in_S);
+          const int T4 = (K / 16) << (3 + lg);
+          for (int f0 = 0; f0 < T4; f0 += RB * NT) {
+            float4 a[RB];
+#pragma unroll
+            for (int j = 0; j < RB; ++j) {
+              const int f = f0 + tid + j * NT;
+              a[j] = ldcg4_if(P.in_part + (size_t)f * 4, f < T4);
+            }
+#pragma unroll
+            for (int j = 0; j < RB; ++j) {
+              const float4 gt = slot_sum(a[j], lg);
+              float4 up;
+              up.x = __shfl_down_sync(0xffffffffu, gt.x, 4);
+              up.y = __shfl_down_sync(0xffffffffu, gt.y, 4);
+              up.z = __shfl_down_sync(0xffffffffu, gt.z, 4);
+              up.w = __shfl_down_sync(0xffffffffu, gt.w, 4);
+              const int f = f0 + tid + j * NT;
+              if (f < T4 && ((f >> 3) & ((1 << lg) - 1)) == 0 && (f & 7) < 4)
+                put(((f >> (3 + lg)) << 2) + (f & 7),
+                    make_float4(silu_fast(gt.x) * up.x, silu_fast(gt.y) * up.y, silu_fast(gt.z) * up.z,
+                                silu_fast(gt.w) * up.w));
+            }
+          }
+        } else if (P.in_mode == IN_ATTN && step_splits(spos + 1, sp.P, HD) <= kSDefer) {
+          // o = merge of the attention splits: sum_s 2^(m_s - M) o_s / sum_s 2^(m_s - M) l_s
+          const int P_eff = step_splits(spos + 1, sp.P, HD);
+          for (int r0 = 0; r0 < n4; r0 += 2 * NT) {
+            float4 o[2][kSDefer];
+            float2 ml[2][kSDefer];
+#pragma unroll
+            for (int q = 0; q < 2; ++q) {
+              const int i4 = r0 + q * NT + tid;
+              const int h = (4 * i4) / HD, d = (4 * i4) % HD, g = h / GQ, hh = h % GQ;
+#pragma unroll
+              for (int s = 0; s < kSDefer; ++s) {
+                const bool pr = i4 < n4 && s < P_eff;
+                const size_t base = ((size_t)g * sp.P + s) * GQ + hh;
+                o[q][s] = ldcg4_if(sp.attn_o + base * HD + d, pr);
+                ml[q][s] = ldcg2_if(sp.attn_ml + base * 2, pr);
+              }
+            }
+#pragma unroll
+            for (int q = 0; q < 2; ++q) {
+              const int i4 = r0 + q * NT + tid;
+              if (i4 < n4) {
+                float M = ml[q][0].x;
+#pragma unroll
+                for (int s = 1; s < kSDefer; ++s)
+                  if (s < P_eff) M = fmaxf(M, ml[q][s].x);
+                float L = 0.f;
+                float4 O = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+                for (int s = 0; s < kSDefer; ++s)
+                  if (s < P_eff) {
+                    const float f = exp2f(ml[q][s].x - M);
+                    L += ml[q][s].y * f;
+                    O.x += o[q][s].x * f;
+                    O.y += o[q][s].y * f;
+                    O.z += o[q][s].z * f;
+                    O.w += o[q][s].w * f;
+                  }
+                const float il = 1.0f / L;
+                put(i4, make_float4(O.x * il, O.y * il, O.z * il, O.w * il));
               }
             }
           }
-        } else if (P.in_mode == IN_PLAIN) {
-#pragma unroll
-          for (int j = 0; j < MAXV; ++j) {
-            const int i = tid + j * kSWarps * 32;
-            if (i < n4) v[j] = __ldcg(reinterpret_cast<const float4*>(P.in_base) + i);
-          }
-        } else if (P.in_mode == IN_RESID) {
-#pragma unroll
-          for (int j = 0; j < MAXV; ++j) {
-            const int i = tid + j * kSWarps * 32;
-            if (i < n4) {
-              const float4 b = __ldcg(reinterpret_cast<const float4*>(P.in_base) + i);
-              const float4 a = reduce4(P.in_part, P.in_S, 4 * i);
-              v[j] = make_float4(b.x + a.x, b.y + a.y, b.z + a.z, b.w + a.w);
+        } else {
+          // embedding row of the token, or a plain vector (the merged attention output)
+          const bool emb = P.in_mode == IN_EMBED_F32 || P.in_mode == IN_EMBED_BF16;
+          int t = 0;
+          if (emb) {
+            t = *sp.tok;
+            if (t < 0 || t >= sp.vocab) {
+              if (tid == 0) atomicOr(sp.status, ST_BAD_TOKEN);
+              t = 0;
             }
           }
-        } else {  // IN_SWIGLU: gate rows 16t.., up rows 16t+16.. of row tile t
+          const float* src = P.in_mode == IN_ATTN ? sp.obuf : P.in_base;
+          float4 v[kSMaxV];
 #pragma unroll
-          for (int j = 0; j < MAXV; ++j) {
-            const int i = tid + j * kSWarps * 32;
-            if (i < n4) {
-              const int e = 4 * i, r = (e >> 4) * 32 + (e & 15);
-              const float4 gt = reduce4(P.in_part, P.in_S, r);
-              const float4 up = reduce4(P.in_part, P.in_S, r + 16);
-              v[j] = make_float4(silu_fast(gt.x) * up.x, silu_fast(gt.y) * up.y, silu_fast(gt.z) * up.z,
-                                 silu_fast(gt.w) * up.w);
+          for (int j = 0; j < kSMaxV; ++j) {
+            const int i = tid + j * NT;
+            if (P.in_mode == IN_EMBED_BF16) {
+              v[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+              if (i < n4) {
+                const uint2 u = __ldg(reinterpret_cast<const uint2*>(static_cast<const uint16_t*>(sp.embed) +
+                                                                      (size_t)t * K) + i);
+                v[j] = make_float4(__uint_as_float(u.x << 16), __uint_as_float(u.x & 0xFFFF0000u),
+                                   __uint_as_float(u.y << 16), __uint_as_float(u.y & 0xFFFF0000u));
+              }
+            } else if (P.in_mode == IN_EMBED_F32) {
+              v[j] = ldnc4_if(static_cast<const float*>(sp.embed) + (size_t)t * K + 4 * i, i < n4);
+            } else {
+              v[j] = ldcg4_if(src + 4 * i, i < n4);
             }
           }
+#pragma unroll
+          for (int j = 0; j < kSMaxV; ++j)
+            if (tid + j * NT < n4) put(tid + j * NT, v[j]);
         }
-        float4 nw4[MAXV];  // norm weights, loaded in the same round trip as the input
-        if (P.norm_w)
-#pragma unroll
-          for (int j = 0; j < MAXV; ++j) {
-            const int i = tid + j * kSWarps * 32;
-            if (i < n4) nw4[j] = __ldg(reinterpret_cast<const float4*>(P.norm_w) + i);
-          }
-        if (P.in_store && c == 0)
-#pragma unroll
-          for (int j = 0; j < MAXV; ++j) {
-            const int i = tid + j * kSWarps * 32;
-            if (i < n4) reinterpret_cast<float4*>(P.in_store)[i] = v[j];
-          }
-        if (P.norm_w) {  // RMSNorm: x / sqrt(mean(x^2) + eps) * w
-          float ss = 0.f;
-#pragma unroll
-          for (int j = 0; j < MAXV; ++j)
-            if (tid + j * kSWarps * 32 < n4)
-              ss += v[j].x * v[j].x + v[j].y * v[j].y + v[j].z * v[j].z + v[j].w * v[j].w;
+        // RMSNorm factor over the whole vector
+        float inv = 1.f;
+        if (P.norm_w) {
 #pragma unroll
           for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
           if (lane == 0) sm.bred[warp] = ss;
-          ConsumerSync::sync();
-          ss = 0.f;
+        }
+        ConsumerSync::sync();  // publishes xh (written in row order by other threads)
+        if (P.norm_w) {
+          float t = 0.f;
 #pragma unroll
-          for (int w = 0; w < kSWarps; ++w) ss += sm.bred[w];
-          const float inv = 1.0f / sqrtf(ss / (float)K + sp.eps);
+          for (int w = 0; w < kSWarps; ++w) t += sm.bred[w];
+          inv = 1.0f / sqrtf(t / (float)K + sp.eps);
+        }
+        // normalise in place (x / rms * w); per-group sums for the 4-bit units
 #pragma unroll
-          for (int j = 0; j < MAXV; ++j) {
-            const int i = tid + j * kSWarps * 32;
-            if (i < n4) {
-              const float4 w4 = nw4[j];
-              v[j] = make_float4(v[j].x * inv * w4.x, v[j].y * inv * w4.y, v[j].z * inv * w4.z, v[j].w * inv * w4.w);
+        for (int j = 0; j < kSMaxV; ++j) {
+          const int i = tid + j * NT;
+          if (j * NT >= n4) break;  // uniform
+          float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
+          if (i < n4) {
+            x = xh4[i];
+            if (P.norm_w) {
+              const float4 w = w4[j];
+              x = make_float4(x.x * inv * w.x, x.y * inv * w.y, x.z * inv * w.z, x.w * inv * w.w);
+              xh4[i] = x;
             }
           }
-        }
-#pragma unroll
-        for (int j = 0; j < MAXV; ++j) {
-          const int i = tid + j * kSWarps * 32;
-          if (j * kSWarps * 32 >= n4) break;  // uniform
-          if (i < n4) reinterpret_cast<float4*>(sm.u.g.xh)[i] = v[j];
-          if (!P.bf16) {  // per-group sums over the 16 threads holding a group
-            float gs = (i < n4) ? (v[j].x + v[j].y) + (v[j].z + v[j].w) : 0.f;
+          if (!P.bf16) {  // the 16 threads holding a group of 64 inputs
+            float gs = (x.x + x.y) + (x.z + x.w);
 #pragma unroll
             for (int o = 8; o > 0; o >>= 1) gs += __shfl_xor_sync(0xffffffffu, gs, o);
             if (i < n4 && (lane & 15) == 0) sm.u.g.xs[i / 16] = gs;
           }
         }
-        for (int i = tid; i < kSRLoc * kSWarps * 32; i += kSWarps * 32) (&sm.u.g.red[0][0][0])[i] = 0.f;
+        for (int i = tid; i < kSRLoc * kSWarps * 32; i += NT) (&sm.u.g.red[0][0][0])[i] = 0.f;
         if (tid < 2) sm.carry_rt[tid] = -1;
         ConsumerSync::sync();
 
-        // ---------------- stream the units; chunk i = units u0+16i .. u0+16i+15
+        // ---------------- stream the units; chunk i = units u0+15i .. u0+15i+14
         const int G = P.G, EPU = P.bf16 ? kBF16UnitCols : 64;
         const int u0 = c < P.part.N ? P.part.begin(c) : 0, u1 = c < P.part.N ? P.part.begin(c + 1) : 0;
         const int n_chunks = (u1 - u0 + kSChunk - 1) / kSChunk;
@@ -418,53 +869,50 @@ __global__ void __launch_bounds__(kSThreads, 1) step_kernel(const StepParams sp)
         if (*(volatile int*)&sm.abort) break;
       } else if (P.type == PH_ATTN) {
         // ---------------- attention items (kv head, split) over the CTAs
-        const int pos = *sp.pos;
+        const int pos = spos;
         if (pos < 0 || pos >= sp.cap) {
           if (tid == 0 && c == 0) atomicOr(sp.status, ST_CTX_FULL);
         } else {
-          const int P_eff = attn_splits(pos + 1, sp.P);
-          AttnParams a{};
-          a.q_dim = sp.q_dim;
-          a.kv_dim = sp.kv_dim;
-          a.Hkv = sp.Hkv;
-          a.P = sp.P;
-          a.rope = sp.rope;
-          a.rope_neox = sp.rope_neox;
-          a.q_norm = P.q_norm;
-          a.k_norm = P.k_norm;
-          a.eps = sp.eps;
-          a.kc = sp.k_base + (size_t)P.layer * sp.layer_stride;
-          a.vc = sp.v_base + (size_t)P.layer * sp.layer_stride;
-          a.cap = sp.cap;
-          a.part = sp.attn_part;
-          a.counter = sp.attn_cnt;
-          a.out = sp.obuf;
-          a.status = sp.status;
-          const float* qp = P.qkv_part;
-          const int qS = P.qkv_S;
-          for (int item = c; item < sp.Hkv * P_eff; item += N)
-            attention_item<GQ, HD, kSWarps, ConsumerSync>(a, item / P_eff, item % P_eff, P_eff, pos, sm.u.a,
-                                                         [&](int row) {
-                                                           const float* src = qp + ((size_t)(row >> 5) * qS) * 32 + (row & 31);
-                                                           float x = __ldcg(src);
-                                                           for (int j = 1; j < qS; ++j) x += __ldcg(src + j * 32);
-                                                           return x;
-                                                         });
+          const int P_eff = step_splits(pos + 1, sp.P, HD);
+          bool ok = true;
+          for (int item = c; item < sp.Hkv * P_eff && ok; item += N) {
+            ok = step_attn_item<GQ, HD>(sp, P, item / P_eff, item % P_eff, P_eff, pos, sm.u.a, abar, apar,
+                                        &sm.a_issued);
+            ConsumerSync::sync();  // shared memory is reused by the next item
+          }
+          if (!ok) {
+            sm.abort = 1;
+            break;
+          }
         }
       } else {
         // ---------------- logits = sum of LM-head partials; greedy choice
         const int V = P.vocab;
         const int r0 = (int)((int64_t)V * c / N), r1 = (int)((int64_t)V * (c + 1) / N);
+        const int lS = P.lm_S;
         float bv = -INFINITY;
         int bi = 0x7fffffff;
         bool nan = false;
-        for (int r = r0 + tid; r < r1; r += kSWarps * 32) {
-          const float* src = P.lm_part + ((size_t)(r >> 5) * P.lm_S) * 32 + (r & 31);
-          float y = __ldcg(src);
-          for (int j = 1; j < P.lm_S; ++j) y += __ldcg(src + j * 32);
-          sp.logits[r] = y;
-          if (y != y) nan = true;
-          else if (better(y, r, bv, bi)) { bv = y; bi = r; }
+        constexpr int RR = 4;  // rows per thread per round
+        for (int rb = r0; rb < r1; rb += RR * NT) {
+          float y[RR][4];
+#pragma unroll
+          for (int j = 0; j < RR; ++j) {
+            const int r = rb + tid + j * NT;
+            const float* src = P.lm_part + ((size_t)(r >> 5) * lS) * 32 + (r & 31);
+#pragma unroll
+            for (int s = 0; s < 4; ++s) y[j][s] = ldcg1_if(src + s * 32, r < r1 && s < lS);
+          }
+#pragma unroll
+          for (int j = 0; j < RR; ++j) {
+            const int r = rb + tid + j * NT;
+            if (r < r1) {
+              const float v = (y[j][0] + y[j][1]) + (y[j][2] + y[j][3]);
+              sp.logits[r] = v;
+              if (v != v) nan = true;
+              else if (better(v, r, bv, bi)) { bv = v; bi = r; }
+            }
+          }
         }
         if (nan) atomicOr(sp.status, ST_NAN);
 #pragma unroll
@@ -491,7 +939,7 @@ __global__ void __launch_bounds__(kSThreads, 1) step_kernel(const StepParams sp)
           __threadfence();
           bv = -INFINITY;
           bi = 0x7fffffff;
-          for (int k = tid; k < N; k += kSWarps * 32) {
+          for (int k = tid; k < N; k += NT) {
             const float v2 = __ldcg(sp.cand_v + k);
             const int i2 = __ldcg(sp.cand_i + k);
             if (better(v2, i2, bv, bi)) { bv = v2; bi = i2; }
@@ -524,6 +972,12 @@ __global__ void __launch_bounds__(kSThreads, 1) step_kernel(const StepParams sp)
       }
       if (ph + 1 < sp.n_phases) grid_arrive(sp);  // its CTA barrier also retires this phase's reads of sm.ph
     }
+    // a bulk staging of the attention may still be landing after an abort
+    if (tid == 0 && sm.a_issued > 0) {
+      const unsigned long long t0 = globaltimer();
+      while (!mbar_try_wait(abar, (sm.a_issued - 1) & 1) && globaltimer() - t0 < kWaitLimitNs) {
+      }
+    }
   }
   __syncthreads();
   // After an abort, wait (bounded) for copies still landing in the ring.
@@ -539,7 +993,7 @@ __global__ void __launch_bounds__(kSThreads, 1) step_kernel(const StepParams sp)
 
 template <int GQ, int HD>
 constexpr size_t step_smem_bytes() {
-  return kSRing + ((sizeof(StepSmem<GQ, HD>) + 15) & ~size_t(15)) + 2 * kSNSlot * sizeof(uint64_t);
+  return kSRing + ((sizeof(StepSmem<GQ, HD>) + 15) & ~size_t(15)) + (2 * kSNSlot + 1) * sizeof(uint64_t);
 }
 
 }  // namespace llmq
