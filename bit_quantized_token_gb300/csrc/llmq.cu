@@ -1039,7 +1039,7 @@ int llm_model_create(const llm_config* cfg, const llm_tensor* tensors, int32_t n
   AL(m->d_cand_v, (size_t)std::max(m->lm.part.N, m->n_sm) * 4, "greedy candidates");
   AL(m->d_cand_i, (size_t)std::max(m->lm.part.N, m->n_sm) * 4, "greedy candidates");
   // ---- the persistent step: phase table (one for every sequence)
-  m->use_step = !(c.flags & LLM_MULTI_KERNEL) && step_supported(gq, hd);
+  m->use_step = !(c.flags & LLM_MULTI_KERNEL) && step_supported(gq, hd) && d <= kSMaxDim;
   if (m->use_step) {
     with_step_kernel(gq, hd, [&](auto kern, size_t smem) {
       m->step_smem = smem;

@@ -40,6 +40,7 @@ constexpr int kSRLoc = 6;                        // row tiles a reduction window
 constexpr int kSMaxV = (kMaxK / 4 + kSCThreads - 1) / kSCThreads;  // float4s of a K-vector per thread
 constexpr int kSDefer = 4;                       // splits the o-projection's input build merges
 constexpr int kSAttnPP = 128;                    // cache positions staged per attention pass
+constexpr int kSMaxDim = 4096;                   // widest residual stream (kept in shared memory)
 
 // Cache positions per attention split (more only when the split count is capped).
 __host__ __device__ constexpr int step_split_len(int hd) { return hd == 64 ? 64 : 128; }
@@ -286,6 +287,7 @@ struct StepSmem {
       int last;
     } l;
   } u;
+  __align__(16) float xres[kSMaxDim];  // this CTA's copy of the residual stream (pre-norm)
   Phase ph[2];            // descriptors of the current and the next phase
   float bred[kSWarps];
   int carry_rt[2];
@@ -620,43 +622,59 @@ __global__ void __launch_bounds__(kSThreads, 1) step_kernel(const StepParams sp)
           w4[j] = ldnc4_if(nw ? P.norm_w + 4 * i : nullptr, nw && i < P.K / 4);
         }
       }
+      // the unit range of this CTA (divisions: done while the barrier resolves)
+      int u0 = 0, u1 = 0, n_chunks = 0, wch = 1, k_rt = 0, k_g = 0, rt0 = 0;
+      if (P.type == PH_GEMV && c < P.part.N) {
+        u0 = P.part.begin(c);
+        u1 = P.part.begin(c + 1);
+        rt0 = u0 / P.G;
+        n_chunks = (u1 - u0 + kSChunk - 1) / kSChunk;
+        wch = max(1, ((kSRLoc - 2) * P.G + 1) / kSChunk);
+        k_rt = (u0 + warp) / P.G;
+        k_g = (u0 + warp) - k_rt * P.G;
+      }
+      // the next descriptor goes to the buffer the previous phase used: its
+      // round trip overlaps the barrier wait
+      fetch_phase(ph + 1);
       if (ph > 0 && !grid_wait(sp, ph * N, &sm.flag)) {
         sm.abort = 1;
         break;
       }
-      fetch_phase(ph + 1);  // read by the next phase, after this phase's closing barriers
       if (P.type == PH_GEMV) {
         // ---------------- build the input vector: every load of the build in one round trip
         const int K = P.K, n4 = K / 4;
         float4* xh4 = reinterpret_cast<float4*>(sm.u.g.xh);
         float ss = 0.f;
+        float4* xr4 = reinterpret_cast<float4*>(sm.xres);
         auto put = [&](int i4, float4 v) {  // pre-norm inputs 4*i4 .. 4*i4+3
           xh4[i4] = v;
           if (P.in_store && c == 0) reinterpret_cast<float4*>(P.in_store)[i4] = v;
           ss += (v.x * v.x + v.y * v.y) + (v.z * v.z + v.w * v.w);
         };
         if (P.in_mode == IN_RESID) {
-          // x = residual + sum of the previous GEMV's slots (row tiles of 32 inputs)
-          constexpr int RB = 6;
+          // x = residual (this CTA's resident copy) + sum of the previous
+          // GEMV's slots (row tiles of 32 inputs); x becomes the new residual
+          constexpr int RB = 8;
           const int lg = log2_slots(P.in_S);
           const int T4 = (K / 32) << (3 + lg);
           for (int f0 = 0; f0 < T4; f0 += RB * NT) {
-            float4 a[RB], b[RB];
+            float4 a[RB];
 #pragma unroll
             for (int j = 0; j < RB; ++j) {
               const int f = f0 + tid + j * NT;
-              const bool s0 = ((f >> 3) & ((1 << lg) - 1)) == 0;
-              const int r4 = ((f >> (3 + lg)) << 3) + (f & 7);
               a[j] = ldcg4_if(P.in_part + (size_t)f * 4, f < T4);
-              b[j] = ldcg4_if(P.in_base + (size_t)r4 * 4, f < T4 && s0);
             }
 #pragma unroll
             for (int j = 0; j < RB; ++j) {
               const float4 s = slot_sum(a[j], lg);
               const int f = f0 + tid + j * NT;
-              if (f < T4 && ((f >> 3) & ((1 << lg) - 1)) == 0)
-                put(((f >> (3 + lg)) << 3) + (f & 7),
-                    make_float4(b[j].x + s.x, b[j].y + s.y, b[j].z + s.z, b[j].w + s.w));
+              if (f < T4 && ((f >> 3) & ((1 << lg) - 1)) == 0) {
+                const int r4 = ((f >> (3 + lg)) << 3) + (f & 7);
+                const float4 b = xr4[r4];
+                const float4 x = make_float4(b.x + s.x, b.y + s.y, b.z + s.z, b.w + s.w);
+                xr4[r4] = x;
+                put(r4, x);
+              }
             }
           }
         } else if (P.in_mode == IN_SWIGLU) {
@@ -761,7 +779,10 @@ __global__ void __launch_bounds__(kSThreads, 1) step_kernel(const StepParams sp)
           }
 #pragma unroll
           for (int j = 0; j < kSMaxV; ++j)
-            if (tid + j * NT < n4) put(tid + j * NT, v[j]);
+            if (tid + j * NT < n4) {
+              if (emb) xr4[tid + j * NT] = v[j];  // the residual stream starts at the embedding
+              put(tid + j * NT, v[j]);
+            }
         }
         // RMSNorm factor over the whole vector
         float inv = 1.f;
@@ -804,11 +825,7 @@ __global__ void __launch_bounds__(kSThreads, 1) step_kernel(const StepParams sp)
 
         // ---------------- stream the units; chunk i = units u0+15i .. u0+15i+14
         const int G = P.G, EPU = P.bf16 ? kBF16UnitCols : 64;
-        const int u0 = c < P.part.N ? P.part.begin(c) : 0, u1 = c < P.part.N ? P.part.begin(c + 1) : 0;
-        const int n_chunks = (u1 - u0 + kSChunk - 1) / kSChunk;
-        const int wch = max(1, ((kSRLoc - 2) * G + 1) / kSChunk);
-        int win_first = 0, win_idx = 0, win_rt0 = u0 / G, cur_rt = -1;
-        int k_rt = (u0 + warp) / G, k_g = (u0 + warp) - k_rt * G;
+        int win_first = 0, win_idx = 0, win_rt0 = rt0, cur_rt = -1;
         float acc = 0.f;
         bool ok = true;
         for (int i = 0; i < n_chunks; ++i, ++gi) {
