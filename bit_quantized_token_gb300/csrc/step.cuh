@@ -17,14 +17,17 @@
 // are used. Every input build issues all of its loads before it uses any of
 // them: one L2 round trip per phase.
 //
-// Attention is flash-decoding over (kv head, split) items. An item stages its
-// K/V rows in shared memory with bulk copies, runs one warp per (q head, block
-// of 32 positions) and leaves an unnormalised partial (o, max, sum) per split;
+// Attention is flash-decoding over (kv head, split) items. An item loads its
+// K/V rows into padded shared-memory tiles in the same round trip as its q|k|v
+// gather; each warp then scores all GQ heads against 16 positions on the
+// tensor cores (attn_mma.cuh) and the item leaves an unnormalised partial
+// (o, max, sum) per split;
 // with few splits the o-projection's input build merges them, so the merge
 // costs no round trip of its own. With many splits (long caches) the last
 // split of a kv head merges them instead.
 #pragma once
 #include "kernels.cuh"
+#include "attn_mma.cuh"
 
 namespace llmq {
 
@@ -39,13 +42,14 @@ constexpr int kSRing = kSNSlot * kSSlot;         // 138240 B
 constexpr int kSRLoc = 6;                        // row tiles a reduction window may touch
 constexpr int kSMaxV = (kMaxK / 4 + kSCThreads - 1) / kSCThreads;  // float4s of a K-vector per thread
 constexpr int kSDefer = 4;                       // splits the o-projection's input build merges
-constexpr int kSAttnPP = 128;                    // cache positions staged per attention pass
 constexpr int kSMaxDim = 4096;                   // widest residual stream (kept in shared memory)
 
-// Cache positions per attention split (more only when the split count is capped).
-__host__ __device__ constexpr int step_split_len(int hd) { return hd == 64 ? 64 : 128; }
+// Cache positions staged per attention pass (the K/V tiles fill about 36 KB
+// resp. 52 KB of shared memory); a split is one pass unless the split count
+// is capped.
+__host__ __device__ constexpr int step_attn_pp(int hd) { return hd == 64 ? 128 : 96; }
 __host__ __device__ inline int step_splits(int len, int P, int hd) {
-  const int s = (len + step_split_len(hd) - 1) / step_split_len(hd);
+  const int s = (len + step_attn_pp(hd) - 1) / step_attn_pp(hd);
   return s < 1 ? 1 : (s < P ? s : P);
 }
 
@@ -250,24 +254,19 @@ __device__ __forceinline__ bool ring_wait(uint64_t* bar, uint32_t parity, const 
   return true;
 }
 
-__device__ __forceinline__ void fence_proxy_async_smem() {
-  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-}
-
 // Shared memory of one attention item.
 template <int GQ, int HD>
 struct StepAttnSmem {
-  static constexpr int NB = kSAttnPP / 32;  // blocks of 32 positions per pass
-  uint16_t kt[kSAttnPP][HD];  // staged K rows (bf16), 16-B aligned for the bulk copy
-  uint16_t vt[kSAttnPP][HD];
-  float cur[GQ + 2][HD];      // this step's q heads, k, v of the kv head
-  float qa[GQ][HD / 2];       // scaled q: dims 8c..8c+3 at qa[4c..4c+3], 8c+4..8c+7 at qb
-  float qb[GQ][HD / 2];
-  float p[kSWarps][32];       // probabilities of a warp's current block
-  float tres[GQ * NB][HD + 2];  // per (block, head): o, block max, block sum
+  static constexpr int PP = step_attn_pp(HD);  // positions per pass
+  static constexpr int RS = HD + 8;             // padded row (halves): conflict-free ldmatrix
+  static constexpr int NBW = PP / 16;           // warps with a 16-position block
+  uint16_t kt[PP][RS];        // staged K rows (fp16)
+  uint16_t vt[PP][RS];
+  float cur[GQ + 2][HD];      // this step's q heads (scaled after RoPE), k, v of the kv head
+  float tres[NBW][GQ][HD + 2];  // per block warp and head: o, max, sum
   float acc[GQ][HD];          // running output of the item over its passes
   float accm[GQ], accl[GQ];
-  float fac[GQ][NB + 1];
+  float fac[GQ][NBW + 1];
   int is_last;
 };
 
@@ -294,42 +293,53 @@ struct StepSmem {
   int flag;
   int abort;
   int issued;
-  int a_issued;           // attention bulk stagings issued (consumer thread 0)
 };
 
 // ---------------------------------------------------------------------------
 // One (kv head g, split) attention item, run by the consumer warps.
-// `apar` counts the completed waits on `abar` (identical in every consumer).
-// Returns false when a wait gave up (uniform over the consumers).
 template <int GQ, int HD>
-__device__ bool step_attn_item(const StepParams& sp, const Phase& P, int g, int split, int P_eff, int pos,
-                               StepAttnSmem<GQ, HD>& sa, uint64_t* abar, uint32_t& apar, int* a_issued) {
-  constexpr int NT = kSCThreads;
-  constexpr int DPL = HD / 32;  // V dims per lane
-  constexpr int NC = HD / 8;    // 16-B chunks of a K row
-  static_assert(DPL == 2 || DPL == 4, "head_dim 64 or 128");
-  static_assert((GQ + 1) * (HD / 2) <= NT && GQ < kSWarps, "one RoPE pair per thread, one warp per q/k head");
+__device__ void step_attn_item(const StepParams& sp, const Phase& P, int g, int split, int P_eff, int pos,
+                               StepAttnSmem<GQ, HD>& sa) {
+  using SA = StepAttnSmem<GQ, HD>;
+  constexpr int NT = kSCThreads, PP = SA::PP, RS = SA::RS, CH = HD / 8;
+  constexpr int TB = (2 * PP * CH + NT - 1) / NT;  // 16-B tile loads per thread
+  static_assert((GQ + 1) * (HD / 2) + HD <= NT && GQ <= 8 && SA::NBW <= kSWarps,
+                "one RoPE pair or v element per thread, GQ <= 8");
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int len = pos + 1;
   const int t0 = (int)((int64_t)len * split / P_eff), t1 = (int)((int64_t)len * (split + 1) / P_eff);
   uint16_t* kc = sp.k_base + (size_t)P.layer * sp.layer_stride + (size_t)g * sp.cap * HD;
   uint16_t* vc = sp.v_base + (size_t)P.layer * sp.layer_stride + (size_t)g * sp.cap * HD;
 
-  // thread 0 stages rows tp .. of K and V (the previous users of this shared
-  // memory finished at the barrier before this item)
-  auto stage = [&](int tp) {
-    const uint32_t bytes = (uint32_t)min(kSAttnPP, t1 - tp) * HD * 2;
-    fence_proxy_async_smem();
-    mbar_expect_tx(abar, 2 * bytes);
-    const uint64_t pol = policy_evict_first();
-    bulk_g2s(sa.kt, kc + (size_t)tp * HD, bytes, abar, pol);
-    bulk_g2s(sa.vt, vc + (size_t)tp * HD, bytes, abar, pol);
-    *a_issued += 1;
+  // K/V rows tp .. tp+n-1 -> registers (zero beyond the split); stored into
+  // the padded tiles once the previous readers are done
+  uint4 tl[TB];
+  auto load_tile = [&](int tp) {
+    const int n = min(PP, t1 - tp);
+#pragma unroll
+    for (int j = 0; j < TB; ++j) {
+      const int idx = tid + j * NT, kv = idx / (PP * CH), rem = idx - kv * (PP * CH), row = rem / CH, ch = rem - row * CH;
+      const float4 v = ldcg4_if(reinterpret_cast<const float*>((kv ? vc : kc) + (size_t)(tp + row) * HD + 8 * ch),
+                                kv < 2 && row < n);
+      tl[j] = make_uint4(__float_as_uint(v.x), __float_as_uint(v.y), __float_as_uint(v.z), __float_as_uint(v.w));
+    }
   };
-  if (tid == 0) stage(t0);
+  auto store_tile = [&](int tp) {
+    const int rows = ((min(PP, t1 - tp) + 15) / 16) * 16;
+#pragma unroll
+    for (int j = 0; j < TB; ++j) {
+      const int idx = tid + j * NT, kv = idx / (PP * CH), rem = idx - kv * (PP * CH), row = rem / CH, ch = rem - row * CH;
+      if (kv < 2 && row < rows)
+        *reinterpret_cast<uint4*>(&(kv ? sa.vt : sa.kt)[row][8 * ch]) =
+            make_uint4(bf16x2_to_f16x2(tl[j].x), bf16x2_to_f16x2(tl[j].y), bf16x2_to_f16x2(tl[j].z),
+                       bf16x2_to_f16x2(tl[j].w));
+    }
+  };
+  load_tile(t0);
 
   // RoPE factors and q/k norm weights do not depend on the step: load them
-  // in the same round trip as the q|k|v gather
+  // in the same round trip as the q|k|v gather and the first tile
+  constexpr int DPL = HD / 32;
   const int nrope = (GQ + 1) * (HD / 2);
   float2 rcs = make_float2(1.f, 0.f);
   if (tid < nrope) rcs = __ldg(sp.rope + (size_t)pos * (HD / 2) + tid % (HD / 2));
@@ -361,6 +371,7 @@ __device__ bool step_attn_item(const StepParams& sp, const Phase& P, int g, int 
         *reinterpret_cast<float4*>(&sa.cur[0][0] + (f >> (3 + lg)) * 32 + (f & 7) * 4) = v;
     }
   }
+  store_tile(t0);
   ConsumerSync::sync();
   // ---- per-head RMSNorm of q and k (Qwen3): warp h < GQ takes q head h, warp GQ takes k
   if (P.q_norm) {
@@ -380,125 +391,94 @@ __device__ bool step_attn_item(const StepParams& sp, const Phase& P, int g, int 
     }
     ConsumerSync::sync();
   }
-  // ---- RoPE at `pos`: pairs (2i, 2i+1) or (i, i + HD/2), of the q heads and k
+  // ---- RoPE at `pos` (pairs (2i, 2i+1) or (i, i + HD/2)) of the q heads and
+  // k; q is then scaled by log2(e)/sqrt(hd), k and v are rounded to bf16
+  // (the split owning `pos` appends them and puts them into its tile)
+  const float qscale = 1.4426950408889634f / sqrtf((float)HD);
+  const bool owner = split == P_eff - 1 && pos - t0 < PP;
+  auto keep = [&](int r, int d, float x) {  // final value of cur[r][d], r >= GQ
+    const __nv_bfloat16 b = __float2bfloat16_rn(x);
+    const float xr = __bfloat162float(b);
+    sa.cur[r][d] = xr;
+    if (split == P_eff - 1) {
+      (r == GQ ? kc : vc)[(size_t)pos * HD + d] = __bfloat16_as_ushort(b);
+      if (owner) (r == GQ ? sa.kt : sa.vt)[pos - t0][d] = __half_as_ushort(__float2half_rn(xr));
+    }
+  };
   if (tid < nrope) {
     const int h = tid / (HD / 2), i = tid % (HD / 2);
     float* v = sa.cur[h];
     const int ia = sp.rope_neox ? i : 2 * i, ib = sp.rope_neox ? i + HD / 2 : 2 * i + 1;
     const float x0 = v[ia], x1 = v[ib];
-    v[ia] = x0 * rcs.x - x1 * rcs.y;
-    v[ib] = x0 * rcs.y + x1 * rcs.x;
-  }
-  ConsumerSync::sync();
-  // ---- round k, v to bf16 (the split owning `pos` appends them); scale q
-  const float qscale = 1.4426950408889634f / sqrtf((float)HD);  // log2(e)/sqrt(hd)
-  for (int i = tid; i < (GQ + 2) * HD; i += NT) {
-    const int r = i / HD, d = i % HD;
-    if (r >= GQ) {
-      const __nv_bfloat16 b = __float2bfloat16_rn(sa.cur[r][d]);
-      sa.cur[r][d] = __bfloat162float(b);
-      if (split == P_eff - 1) (r == GQ ? kc : vc)[(size_t)pos * HD + d] = __bfloat16_as_ushort(b);
+    const float y0 = x0 * rcs.x - x1 * rcs.y, y1 = x0 * rcs.y + x1 * rcs.x;
+    if (h < GQ) {
+      v[ia] = y0 * qscale;
+      v[ib] = y1 * qscale;
     } else {
-      const float q = sa.cur[r][d] * qscale;
-      const int cq = d >> 3, e = d & 7;
-      if (e < 4) sa.qa[r][4 * cq + e] = q;
-      else sa.qb[r][4 * cq + e - 4] = q;
+      keep(GQ, ia, y0);
+      keep(GQ, ib, y1);
     }
+  } else if (tid < nrope + HD) {
+    keep(GQ + 1, tid - nrope, sa.cur[GQ + 1][tid - nrope]);
   }
   for (int i = tid; i < GQ * HD; i += NT) sa.acc[i / HD][i % HD] = 0.f;
   if (tid < GQ) {
     sa.accm[tid] = -INFINITY;
     sa.accl[tid] = 0.f;
   }
+  ConsumerSync::sync();
 
-  // ---- passes of at most kSAttnPP positions
-  for (int tp = t0; tp < t1; tp += kSAttnPP) {
-    const int n = min(kSAttnPP, t1 - tp), nb = (n + 31) / 32;
-    const bool got = ring_wait(abar, apar & 1, sp);
-    ++apar;
-    if (!consumer_and(got)) return false;  // also orders the writes above before the reads below
-    if (pos >= tp && pos < tp + n)           // the current position's row is this step's k, v
-      for (int d = tid; d < HD; d += NT) {
-        sa.kt[pos - tp][d] = __bfloat16_as_ushort(__float2bfloat16_rn(sa.cur[GQ][d]));
-        sa.vt[pos - tp][d] = __bfloat16_as_ushort(__float2bfloat16_rn(sa.cur[GQ + 1][d]));
-      }
+  // ---- passes of at most PP positions: warp w takes positions 16w .. 16w+15
+  for (int tp = t0; tp < t1; tp += PP) {
+    const int n = min(PP, t1 - tp), nb = (n + 15) / 16;
+    if (tp != t0) {
+      load_tile(tp);
+      store_tile(tp);
+      if (pos >= tp && pos < tp + n)
+        for (int d = tid; d < HD; d += NT) {
+          sa.kt[pos - tp][d] = __half_as_ushort(__float2half_rn(sa.cur[GQ][d]));
+          sa.vt[pos - tp][d] = __half_as_ushort(__float2half_rn(sa.cur[GQ + 1][d]));
+        }
+      ConsumerSync::sync();
+    }
+    if (warp < nb)
+      attn_block16<GQ, HD, RS>(&sa.cur[0][0], &sa.kt[0][0], &sa.vt[0][0], 16 * warp, n - 16 * warp, lane,
+                               &sa.tres[warp][0][0], HD + 2);
     ConsumerSync::sync();
-    // warp task (q head h, block b): lane = position 32b + lane for the
-    // scores; lane = dims DPL*lane.. for the weighted V sum
-    for (int task = warp; task < GQ * nb; task += kSWarps) {
-      const int h = task % GQ, b = task / GQ;
-      const int nv = min(32, n - 32 * b);
-      const bool valid = lane < nv;
-      const uint16_t* kr = sa.kt[32 * b + (valid ? lane : 0)];
-      float s0 = 0.f, s1 = 0.f;
-#pragma unroll
-      for (int c = 0; c < NC; ++c) {
-        const int cc = (c + lane) & (NC - 1);  // rotated: the lanes of a quarter warp hit distinct banks
-        const uint4 kk = *reinterpret_cast<const uint4*>(kr + 8 * cc);
-        const float4 qa = *reinterpret_cast<const float4*>(&sa.qa[h][4 * cc]);
-        const float4 qb = *reinterpret_cast<const float4*>(&sa.qb[h][4 * cc]);
-        s0 = fmaf(qa.x, __uint_as_float(kk.x << 16), s0);
-        s1 = fmaf(qa.y, __uint_as_float(kk.x & 0xFFFF0000u), s1);
-        s0 = fmaf(qa.z, __uint_as_float(kk.y << 16), s0);
-        s1 = fmaf(qa.w, __uint_as_float(kk.y & 0xFFFF0000u), s1);
-        s0 = fmaf(qb.x, __uint_as_float(kk.z << 16), s0);
-        s1 = fmaf(qb.y, __uint_as_float(kk.z & 0xFFFF0000u), s1);
-        s0 = fmaf(qb.z, __uint_as_float(kk.w << 16), s0);
-        s1 = fmaf(qb.w, __uint_as_float(kk.w & 0xFFFF0000u), s1);
-      }
-      const float s = valid ? s0 + s1 : -INFINITY;
-      float mx = s;
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-      const float pj = valid ? exp2f(s - mx) : 0.f;
-      float l = pj;
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) l += __shfl_xor_sync(0xffffffffu, l, o);
-      sa.p[warp][lane] = pj;
-      __syncwarp();
-      float o[DPL];
-#pragma unroll
-      for (int e = 0; e < DPL; ++e) o[e] = 0.f;
-      const uint16_t* vr = &sa.vt[32 * b][DPL * lane];
-#pragma unroll 4
-      for (int j = 0; j < nv; ++j) {
-        const float pv = sa.p[warp][j];
-        if constexpr (DPL == 2) {
-          const uint32_t w = *reinterpret_cast<const uint32_t*>(vr + (size_t)j * HD);
-          o[0] = fmaf(pv, __uint_as_float(w << 16), o[0]);
-          o[1] = fmaf(pv, __uint_as_float(w & 0xFFFF0000u), o[1]);
-        } else {
-          const uint2 w = *reinterpret_cast<const uint2*>(vr + (size_t)j * HD);
-          o[0] = fmaf(pv, __uint_as_float(w.x << 16), o[0]);
-          o[1] = fmaf(pv, __uint_as_float(w.x & 0xFFFF0000u), o[1]);
-          o[2] = fmaf(pv, __uint_as_float(w.y << 16), o[2]);
-          o[3] = fmaf(pv, __uint_as_float(w.y & 0xFFFF0000u), o[3]);
+    const size_t pbase = ((size_t)g * sp.P + split) * GQ;
+    if (tp + PP >= t1) {
+      // last pass: merge its warps with the running output into the split's partial
+      for (int i = tid; i < GQ * HD; i += NT) {
+        const int h = i / HD, d = i % HD;
+        float M = sa.accm[h];
+        for (int w = 0; w < nb; ++w) M = fmaxf(M, sa.tres[w][h][HD]);
+        const float fa = sa.accm[h] == -INFINITY ? 0.f : exp2f(sa.accm[h] - M);
+        float O = sa.acc[h][d] * fa, L = sa.accl[h] * fa;
+        for (int w = 0; w < nb; ++w) {
+          const float f = exp2f(sa.tres[w][h][HD] - M);
+          O += sa.tres[w][h][d] * f;
+          L += sa.tres[w][h][HD + 1] * f;
+        }
+        sp.attn_o[pbase * HD + i] = O;
+        if (d == 0) {
+          sp.attn_ml[(pbase + h) * 2] = M;
+          sp.attn_ml[(pbase + h) * 2 + 1] = L;
         }
       }
-      float* tr = sa.tres[task];
-#pragma unroll
-      for (int e = 0; e < DPL; ++e) tr[DPL * lane + e] = o[e];
-      if (lane == 0) {
-        tr[HD] = mx;
-        tr[HD + 1] = l;
-      }
-      __syncwarp();  // sa.p is rewritten by this warp's next task
+      break;
     }
-    ConsumerSync::sync();
-    // the staged rows are no longer read: stage the next pass
-    if (tid == 0 && tp + kSAttnPP < t1) stage(tp + kSAttnPP);
     // fold the pass into the running output
     if (tid < GQ) {
       const int h = tid;
       float M = sa.accm[h];
-      for (int bb = 0; bb < nb; ++bb) M = fmaxf(M, sa.tres[bb * GQ + h][HD]);
+      for (int w = 0; w < nb; ++w) M = fmaxf(M, sa.tres[w][h][HD]);
       const float fa = sa.accm[h] == -INFINITY ? 0.f : exp2f(sa.accm[h] - M);
       float L = sa.accl[h] * fa;
       sa.fac[h][0] = fa;
-      for (int bb = 0; bb < nb; ++bb) {
-        const float f = exp2f(sa.tres[bb * GQ + h][HD] - M);
-        sa.fac[h][1 + bb] = f;
-        L += sa.tres[bb * GQ + h][HD + 1] * f;
+      for (int w = 0; w < nb; ++w) {
+        const float f = exp2f(sa.tres[w][h][HD] - M);
+        sa.fac[h][1 + w] = f;
+        L += sa.tres[w][h][HD + 1] * f;
       }
       sa.accm[h] = M;
       sa.accl[h] = L;
@@ -507,20 +487,14 @@ __device__ bool step_attn_item(const StepParams& sp, const Phase& P, int g, int 
     for (int i = tid; i < GQ * HD; i += NT) {
       const int h = i / HD, d = i % HD;
       float O = sa.acc[h][d] * sa.fac[h][0];
-      for (int bb = 0; bb < nb; ++bb) O += sa.tres[bb * GQ + h][d] * sa.fac[h][1 + bb];
+      for (int w = 0; w < nb; ++w) O += sa.tres[w][h][d] * sa.fac[h][1 + w];
       sa.acc[h][d] = O;
     }
     ConsumerSync::sync();
   }
 
-  // ---- the split's partial
-  const size_t pbase = ((size_t)g * sp.P + split) * GQ;
-  for (int i = tid; i < GQ * HD; i += NT) sp.attn_o[pbase * HD + i] = sa.acc[i / HD][i % HD];
-  if (tid < GQ) {
-    sp.attn_ml[(pbase + tid) * 2] = sa.accm[tid];
-    sp.attn_ml[(pbase + tid) * 2 + 1] = sa.accl[tid];
-  }
-  if (P_eff <= kSDefer) return true;  // the o-projection's input build merges the splits
+  // ---- the split's partial is written (last pass above)
+  if (P_eff <= kSDefer) return;  // the o-projection's input build merges the splits
   // many splits: the last one of this kv head merges them into obuf
   __threadfence();
   ConsumerSync::sync();
@@ -544,7 +518,6 @@ __device__ bool step_attn_item(const StepParams& sp, const Phase& P, int g, int 
     }
     if (tid == 0) sp.attn_cnt[g] = 0;
   }
-  return true;
 }
 
 template <int GQ, int HD>
@@ -554,7 +527,6 @@ __global__ void __launch_bounds__(kSThreads, 1) step_kernel(const StepParams sp)
   StepSmem<GQ, HD>& sm = *reinterpret_cast<StepSmem<GQ, HD>*>(smem_raw + kSRing);
   uint64_t* full = reinterpret_cast<uint64_t*>(smem_raw + kSRing + ((sizeof(StepSmem<GQ, HD>) + 15) & ~size_t(15)));
   uint64_t* empty = full + kSNSlot;
-  uint64_t* abar = empty + kSNSlot;
 
   const int c = blockIdx.x, N = gridDim.x;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -563,11 +535,9 @@ __global__ void __launch_bounds__(kSThreads, 1) step_kernel(const StepParams sp)
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], kSWarps);
     }
-    mbar_init(abar, 1);
     mbar_fence_init();
     sm.abort = 0;
     sm.issued = 0;
-    sm.a_issued = 0;
   }
   __syncthreads();
 
@@ -598,7 +568,6 @@ __global__ void __launch_bounds__(kSThreads, 1) step_kernel(const StepParams sp)
     // ================= consumers
     constexpr int NT = kSCThreads;
     int gi = 0;
-    uint32_t apar = 0;
     // the position only changes at the very end of the step (greedy choice)
     const int spos = *sp.pos;
     // descriptors go to shared memory one phase ahead (the phase table is immutable)
@@ -891,15 +860,9 @@ __global__ void __launch_bounds__(kSThreads, 1) step_kernel(const StepParams sp)
           if (tid == 0 && c == 0) atomicOr(sp.status, ST_CTX_FULL);
         } else {
           const int P_eff = step_splits(pos + 1, sp.P, HD);
-          bool ok = true;
-          for (int item = c; item < sp.Hkv * P_eff && ok; item += N) {
-            ok = step_attn_item<GQ, HD>(sp, P, item / P_eff, item % P_eff, P_eff, pos, sm.u.a, abar, apar,
-                                        &sm.a_issued);
+          for (int item = c; item < sp.Hkv * P_eff; item += N) {
+            step_attn_item<GQ, HD>(sp, P, item / P_eff, item % P_eff, P_eff, pos, sm.u.a);
             ConsumerSync::sync();  // shared memory is reused by the next item
-          }
-          if (!ok) {
-            sm.abort = 1;
-            break;
           }
         }
       } else {
@@ -989,12 +952,6 @@ __global__ void __launch_bounds__(kSThreads, 1) step_kernel(const StepParams sp)
       }
       if (ph + 1 < sp.n_phases) grid_arrive(sp);  // its CTA barrier also retires this phase's reads of sm.ph
     }
-    // a bulk staging of the attention may still be landing after an abort
-    if (tid == 0 && sm.a_issued > 0) {
-      const unsigned long long t0 = globaltimer();
-      while (!mbar_try_wait(abar, (sm.a_issued - 1) & 1) && globaltimer() - t0 < kWaitLimitNs) {
-      }
-    }
   }
   __syncthreads();
   // After an abort, wait (bounded) for copies still landing in the ring.
@@ -1010,7 +967,7 @@ __global__ void __launch_bounds__(kSThreads, 1) step_kernel(const StepParams sp)
 
 template <int GQ, int HD>
 constexpr size_t step_smem_bytes() {
-  return kSRing + ((sizeof(StepSmem<GQ, HD>) + 15) & ~size_t(15)) + (2 * kSNSlot + 1) * sizeof(uint64_t);
+  return kSRing + ((sizeof(StepSmem<GQ, HD>) + 15) & ~size_t(15)) + 2 * kSNSlot * sizeof(uint64_t);
 }
 
 }  // namespace llmq
