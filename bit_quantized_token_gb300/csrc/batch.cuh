@@ -3,21 +3,30 @@
 // The 4-bit matvec of the batch-1 step becomes a skinny GEMM Y[M][rows] =
 // X[M][K] W^T. bgemv_kernel: a CTA owns RT_B row tiles (32 rows each) and a
 // contiguous range of K units; chunk by chunk it stages the weight units with
-// 1-D bulk copies and the normalised input tile, transposed to [k][token], in
-// shared memory. Each lane owns a 4-row x 8-token register tile, so every
-// weight is dequantised once and used for 8 tokens, every input value for 4
-// rows. Arithmetic stays fp32 (exact dequantisation, fp32 accumulation, as in
-// the batch-1 path). When K is split over several CTAs the last CTA of a row
-// block to arrive adds the partials in CTA order and runs the epilogue
-// (store, residual, SwiGLU, or logits with the per-sequence greedy choice).
+// 1-D bulk copies and the normalised inputs in shared memory.
+//   * 4-bit units run on the tensor cores (mma.sync m16n8k16, fp16, fp32
+//     accumulation): the 4-bit codes become exact fp16 integers, the inputs
+//     are split into fp16 high parts and remainders (64 columns: 32 tokens x
+//     2, a 22-bit-mantissa input), and each group's fp16 scale and min are
+//     applied to the fp32 MMA result: y = s * sum_k q_k x_k + m * sum_k x_k.
+//     Warp w owns 16 rows of one row tile (with several warps per 16 rows
+//     when the block has fewer row tiles, each taking every wp-th unit).
+//   * bf16 units (the tied LM head): the same with bf16 operands; the weight
+//     fragments are single ldmatrix loads and the inputs are split into bf16
+//     high parts and remainders (16-bit mantissa).
+// When K is split over several CTAs the last CTA of a row block to arrive
+// adds the partials in CTA order and runs the epilogue (store, residual,
+// SwiGLU, or logits with the per-sequence greedy choice).
 #pragma once
 #include "kernels.cuh"
+#include "attn_mma.cuh"
 
 namespace llmq {
 
 constexpr int kBWarps = 8;
 constexpr int kBThreads = kBWarps * 32;
 constexpr int kBM = 32;  // tokens per step (sequences), padded to 32
+constexpr int kQKC = 4;  // 4-bit units per chunk (256 inputs) of the tensor-core path
 
 struct BGemvParams {
   const uint8_t* units;    // [n_rt][G] units
@@ -25,15 +34,19 @@ struct BGemvParams {
   int M;                   // live tokens (<= 32)
   int rtb, kc;             // row tiles per CTA, units per chunk (per row tile)
   int ks;                  // K splits (CTAs per row block)
-  // input: X [M][K] fp32 (+ optional RMSNorm per token)
+  // input: X [M][K] fp32 (+ optional RMSNorm per token, whose sums of squares
+  // come as ss_n partials per token: ss_in[b * 32 + m])
   const float* x;
   const float* norm_w;
+  const float* ss_in;
+  int ss_n;
   float eps;
   // output
   int epi;                 // EPI_STORE / EPI_RESID / EPI_SWIGLU / EPI_LOGITS
   float* out;              // [M][out_cols]
   int out_cols;
   const float* resid;      // [M][rows] (EPI_RESID)
+  float* ss_out;           // EPI_RESID: [n_blocks][32] sums of squares of the written rows
   float* part;             // [ks][M][rows] partials
   int* counters;           // [n_rt / rtb] arrival counters (zero between launches)
   // EPI_LOGITS: per-token best over the row blocks, then the greedy choice
@@ -46,248 +59,346 @@ struct BGemvParams {
   int* status;
 };
 
-// Dynamic shared memory of one CTA: per stage RT_B*kc units + [kc*epu][32] inputs.
+// Dynamic shared memory of one CTA: two buffers of RT_B*kc units (256 inputs per row tile),
+// the staged inputs [64][256+8] halves and the 4-bit per-group input sums
+// [4][32]; after the last chunk the per-warp results [8][32][20] fp32.
 __host__ __device__ inline size_t bgemv_stage_bytes(int rtb, int kc, int unit_bytes, int epu) {
-  return (size_t)rtb * kc * unit_bytes + (size_t)kc * epu * kBM * 4;
+  const size_t w = (size_t)2 * rtb * kc * unit_bytes;  // two alternating weight buffers
+  const size_t x = (size_t)2 * kBM * (256 + 8) * 2 + (size_t)(256 / 64) * kBM * 4;
+  const size_t red = (size_t)kBWarps * kBM * 20 * 4;
+  return (w + x) > red ? (w + x) : red;
+}
+
+// Two 4-bit codes of a unit word -> fp16 pair (exact integers 0..15): the
+// nibbles sit at bit `sh` and `sh + 8` of w; placed under the exponent of
+// 1024 (0x6400) they read 1024 + q, and subtracting 1024 is exact.
+__device__ __forceinline__ uint32_t q4_pair_f16(uint32_t w, int sh) {
+  uint32_t v = __byte_perm(w >> sh, 0u, 0x4140u);  // [byte0, 0, byte1, 0]
+  v = (v & 0x000F000Fu) | 0x64006400u;
+  __half2 h = *reinterpret_cast<const __half2*>(&v);
+  h = __hsub2(h, __float2half2_rn(1024.f));
+  return *reinterpret_cast<const uint32_t*>(&h);
 }
 
 template <bool BF16>
-__global__ void __launch_bounds__(kBThreads) bgemv_kernel(const BGemvParams p) {
+__global__ void __launch_bounds__(kBThreads, 2) bgemv_kernel(const BGemvParams p) {
   extern __shared__ __align__(128) uint8_t smem[];
   __shared__ float s_inv[kBM];
-  __shared__ uint64_t s_bar;
+  __shared__ uint64_t s_bar[2];
   __shared__ int s_last;
   __shared__ float s_bv[kBWarps][kBM];
-  __shared__ int s_bi[kBWarps][kBM];
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int n_blocks = p.n_rt / p.rtb;
   const int blk = blockIdx.x / p.ks, ksi = blockIdx.x % p.ks;
   const int g0 = (int)((int64_t)p.G * ksi / p.ks), g1 = (int)((int64_t)p.G * (ksi + 1) / p.ks);
   const int rt0 = blk * p.rtb;
+  constexpr int KW = 256;          // inputs per chunk
+  constexpr int XS = KW + 8;       // staged input row (halves): conflict-free ldmatrix rows
+  constexpr int EPU = BF16 ? kBF16UnitCols : 64;
   uint8_t* wbuf = smem;
-  float* xbuf = reinterpret_cast<float*>(smem + (size_t)p.rtb * p.kc * p.unit_bytes);  // [kc*epu][32]
-  float* red = xbuf;  // reused after the last chunk: [kBWarps][32 lanes][32]
+  // inputs of the chunk: xh[token][k] (fp16 or bf16) high parts, xh[32 + token][k] the remainders
+  uint16_t* xh = reinterpret_cast<uint16_t*>(smem + (size_t)2 * p.rtb * p.kc * p.unit_bytes);
+  float* xsm = reinterpret_cast<float*>(xh + (size_t)2 * kBM * XS);  // 4-bit: [group][token] input sums
 
+  // the weight units of every row tile of the block (one bulk copy per row
+  // tile); weights do not depend on the previous kernel: the first chunk is
+  // requested before waiting on it
+  const size_t wchunk = (size_t)p.rtb * p.kc * p.unit_bytes;  // one weight buffer (two, alternating)
+  auto stage_weights = [&](int ga) {
+    const int nk = min(p.kc, g1 - ga), b = ((ga - g0) / p.kc) & 1;
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // earlier reads of this buffer
+    mbar_expect_tx(&s_bar[b], p.rtb * nk * p.unit_bytes);
+    for (int r = 0; r < p.rtb; ++r)
+      bulk_g2s(wbuf + b * wchunk + (size_t)r * p.kc * p.unit_bytes,
+               p.units + ((size_t)(rt0 + r) * p.G + ga) * p.unit_bytes, nk * p.unit_bytes, &s_bar[b],
+               policy_evict_first());
+  };
   if (tid == 0) {
-    mbar_init(&s_bar, 1);
+    mbar_init(&s_bar[0], 1);
+    mbar_init(&s_bar[1], 1);
     mbar_fence_init();
+    stage_weights(g0);
+    if (g0 + p.kc < g1) stage_weights(g0 + p.kc);
   }
   __syncthreads();
   pdl_trigger();
   pdl_wait();
 
-  // ---- RMSNorm factor per token (the whole row of X), 8 threads per token
-  if (p.norm_w) {
-    const int m = tid >> 3, sub = tid & 7;
-    float ss = 0.f;
-    if (m < p.M) {
-      const float4* xr = reinterpret_cast<const float4*>(p.x + (size_t)m * p.K);
-      for (int i = sub; i < p.K / 4; i += 8) {
-        const float4 v = __ldcg(xr + i);
-        ss += v.x * v.x + v.y * v.y + v.z * v.z + v.w * v.w;
-      }
-    }
+  // the first chunk's inputs are requested in the same round trip as the
+  // RMSNorm statistics (they are normalised once those are known)
+  constexpr int NL = kBM * (KW / 4) / kBThreads;  // float4 per thread (k fastest: coalesced reads)
+  static_assert(kBThreads % (KW / 4) == 0, "a thread stages one input column (k4) for NL tokens");
+  float4 xv[NL], wv;
+  auto load_inputs = [&](int ga) {
+    const int kw = min(p.kc, g1 - ga) * EPU, kbase = ga * EPU, k4 = tid % (KW / 4);
 #pragma unroll
-    for (int o = 4; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
-    if (sub == 0) s_inv[m] = 1.0f / sqrtf(ss / (float)p.K + p.eps);
+    for (int it = 0; it < NL; ++it) {
+      const int m = (tid + it * kBThreads) / (KW / 4);
+      xv[it] = ldcg4_if(p.x + (size_t)m * p.K + kbase + 4 * k4, m < p.M && k4 < kw / 4);
+    }
+    wv = ldnc4_if(p.norm_w ? p.norm_w + kbase + 4 * k4 : nullptr, p.norm_w != nullptr && k4 < kw / 4);
+  };
+  load_inputs(g0);
+
+  // ---- RMSNorm factor per token from the producer's partial sums of squares
+  // (thread: token tid % 32, partials tid/32, +8, ...; added in a fixed order)
+  if (p.norm_w) {
+    const int m = tid & 31, sub = tid >> 5;
+    float v[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) v[j] = ldcg1_if(p.ss_in + (size_t)(sub + 8 * j) * kBM + m, sub + 8 * j < p.ss_n);
+    float ss = ((v[0] + v[1]) + (v[2] + v[3])) + ((v[4] + v[5]) + (v[6] + v[7]));
+    for (int b = sub + 64; b < p.ss_n; b += 8) ss += __ldcg(p.ss_in + (size_t)b * kBM + m);  // > 64 partials
+    s_bv[sub][m] = ss;
+    __syncthreads();
+    if (tid < kBM) {
+      float t = 0.f;
+#pragma unroll
+      for (int w = 0; w < kBWarps; ++w) t += s_bv[w][tid];
+      s_inv[tid] = 1.0f / sqrtf(t / (float)p.K + p.eps);
+    }
   }
   __syncthreads();
 
-  // lane tile: rows 4*rg .. 4*rg+3 of the warp's row tile, tokens 8*tg .. 8*tg+7
-  const int rg = lane >> 2, tg = lane & 3;
-  const int rt_loc = warp % p.rtb, wsub = warp / p.rtb, wstride = kBWarps / p.rtb;
-  float acc[4][8];
+  // warp -> 16 rows (row tile rt_q, half 16*(pair&1)) x every wp-th unit of the chunk;
+  // lane (g, t) holds rows R0 = 16*(pair&1) + g, R0 + 8 and tokens 8nt + 2t + e
+  const int wp = kBWarps / (2 * p.rtb), pair = warp / wp, usub = warp % wp;
+  const int rt_q = pair >> 1, mt = pair & 1, R0 = 16 * mt + (lane >> 2), t = lane & 3;
+  const int r8 = lane & 7, mi = lane >> 3;
+  const int sh = 16 * (t & 1) + 4 * (t >> 1);  // 4-bit: bit of input 2t within its code word
+  float qacc[4][2][2];
 #pragma unroll
-  for (int i = 0; i < 4; ++i)
-#pragma unroll
-    for (int j = 0; j < 8; ++j) acc[i][j] = 0.f;
+  for (int i = 0; i < 4; ++i) qacc[i][0][0] = qacc[i][0][1] = qacc[i][1][0] = qacc[i][1][1] = 0.f;
 
-  uint32_t phase = 0;
   bool ok = true;
-  for (int ga = g0; ga < g1 && ok; ga += p.kc) {
+  for (int ga = g0, ci = 0; ga < g1 && ok; ga += p.kc, ++ci) {
     const int nk = min(p.kc, g1 - ga);
-    // stage the weight units of every row tile of the block (one bulk copy per row tile)
-    if (tid == 0) {
-      mbar_expect_tx(&s_bar, p.rtb * nk * p.unit_bytes);
-      for (int r = 0; r < p.rtb; ++r)
-        bulk_g2s(wbuf + (size_t)r * p.kc * p.unit_bytes, p.units + ((size_t)(rt0 + r) * p.G + ga) * p.unit_bytes,
-                 nk * p.unit_bytes, &s_bar, policy_evict_first());
-    }
-    // stage the (normalised) inputs transposed: xbuf[k][token]
-    const int kw = nk * p.epu, kbase = ga * p.epu;
-    for (int i = tid; i < kBM * (kw / 4); i += kBThreads) {
-      const int m = i % kBM, k4 = i / kBM;  // token fastest: conflict-free transposed stores
-      float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-      if (m < p.M) {
-        v = __ldcg(reinterpret_cast<const float4*>(p.x + (size_t)m * p.K + kbase) + k4);
+    const uint8_t* wb = wbuf + (ci & 1) * wchunk;
+    {
+      // stage the (normalised) inputs of the chunk, loaded during the previous chunk
+#pragma unroll
+      for (int it = 0; it < NL; ++it) {
+        const int i = tid + it * kBThreads, m = i / (KW / 4), k4 = i % (KW / 4);
+        float4 v = xv[it];
         if (p.norm_w) {
-          const float4 w = __ldg(reinterpret_cast<const float4*>(p.norm_w + kbase) + k4);
-          const float inv = s_inv[m];
+          const float4 w = wv;
+          const float inv = m < p.M ? s_inv[m] : 0.f;
           v = make_float4(v.x * inv * w.x, v.y * inv * w.y, v.z * inv * w.z, v.w * inv * w.w);
         }
-      }
-      xbuf[(4 * k4 + 0) * kBM + m] = v.x;
-      xbuf[(4 * k4 + 1) * kBM + m] = v.y;
-      xbuf[(4 * k4 + 2) * kBM + m] = v.z;
-      xbuf[(4 * k4 + 3) * kBM + m] = v.w;
-    }
-    __syncthreads();
-    ok = __syncthreads_and(mbar_wait(&s_bar, phase, p.status));  // uniform across the CTA
-    phase ^= 1;
-    // ---- units of this warp: row tile rt_loc, units wsub, wsub + wstride, ...
-    if (ok) {
-      for (int u = wsub; u < nk; u += wstride) {
-        const uint8_t* ub = wbuf + ((size_t)rt_loc * p.kc + u) * p.unit_bytes;
-        const float* xu = xbuf + (size_t)u * p.epu * kBM + tg * 8;
-        if (!BF16) {
-          float s_[4], m_[4];
-#pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            const float2 sm2 = __half22float2(*reinterpret_cast<const __half2*>(ub + 1024 + (4 * rg + i) * 4));
-            s_[i] = sm2.x;
-            m_[i] = sm2.y;
-          }
-#pragma unroll
-          for (int wd = 0; wd < 8; ++wd) {  // word wd: inputs 32h+8k' + {0..3} (lo) and + {4..7} (hi)
-            const int h = wd >> 2, kq = wd & 3;
-            float wv[4][8];
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-              const uint32_t v = *reinterpret_cast<const uint32_t*>(ub + (h * 32 + 4 * rg + i) * 16 + 4 * kq);
-#pragma unroll
-              for (int b = 0; b < 4; ++b) {
-                const uint32_t a = __byte_perm(v, 0x4B000000u, 0x7650 + b);
-                const float A = __uint_as_float(a), B = __uint_as_float(a & 0xFFFFFFF0u);
-                wv[i][b] = fmaf(s_[i], A - B, m_[i]);                               // low nibble
-                wv[i][4 + b] = fmaf(s_[i], (B - 8388608.0f) * 0.0625f, m_[i]);     // high nibble
-              }
-            }
-#pragma unroll
-            for (int e = 0; e < 8; ++e) {
-              const float* xk = xu + (h * 32 + kq * 8 + e) * kBM;
-              const float4 xa = *reinterpret_cast<const float4*>(xk);
-              const float4 xb = *reinterpret_cast<const float4*>(xk + 4);
-#pragma unroll
-              for (int i = 0; i < 4; ++i) {
-                fma2(acc[i][0], acc[i][1], wv[i][e], wv[i][e], xa.x, xa.y);
-                fma2(acc[i][2], acc[i][3], wv[i][e], wv[i][e], xa.z, xa.w);
-                fma2(acc[i][4], acc[i][5], wv[i][e], wv[i][e], xb.x, xb.y);
-                fma2(acc[i][6], acc[i][7], wv[i][e], wv[i][e], xb.z, xb.w);
-              }
-            }
-          }
+        uint2 hv, lv;
+        if constexpr (!BF16) {
+          const float hx = __half2float(__float2half_rn(v.x)), hy = __half2float(__float2half_rn(v.y));
+          const float hz = __half2float(__float2half_rn(v.z)), hw = __half2float(__float2half_rn(v.w));
+          hv = make_uint2(pack_f16x2(hx, hy), pack_f16x2(hz, hw));
+          lv = make_uint2(pack_f16x2(v.x - hx, v.y - hy), pack_f16x2(v.z - hz, v.w - hw));
         } else {
+          const float hx = __bfloat162float(__float2bfloat16_rn(v.x)), hy = __bfloat162float(__float2bfloat16_rn(v.y));
+          const float hz = __bfloat162float(__float2bfloat16_rn(v.z)), hw = __bfloat162float(__float2bfloat16_rn(v.w));
+          hv = make_uint2(pack_bf16x2(hx, hy), pack_bf16x2(hz, hw));
+          lv = make_uint2(pack_bf16x2(v.x - hx, v.y - hy), pack_bf16x2(v.z - hz, v.w - hw));
+        }
+        *reinterpret_cast<uint2*>(xh + (size_t)m * XS + 4 * k4) = hv;
+        *reinterpret_cast<uint2*>(xh + (size_t)(kBM + m) * XS + 4 * k4) = lv;
+        if constexpr (!BF16) {  // sum of each group of 64 inputs (16 consecutive lanes) per token
+          float gs = (v.x + v.y) + (v.z + v.w);
 #pragma unroll
-          for (int kk = 0; kk < 2; ++kk) {  // inputs 8kk .. 8kk+7
-            float wv[4][8];
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-              const uint4 c = *reinterpret_cast<const uint4*>(ub + (kk * 32 + 4 * rg + i) * 16);
-              const uint32_t cw[4] = {c.x, c.y, c.z, c.w};
-#pragma unroll
-              for (int b = 0; b < 4; ++b) {
-                wv[i][2 * b] = __uint_as_float(cw[b] << 16);
-                wv[i][2 * b + 1] = __uint_as_float(cw[b] & 0xFFFF0000u);
-              }
-            }
-#pragma unroll
-            for (int e = 0; e < 8; ++e) {
-              const float* xk = xu + (kk * 8 + e) * kBM;
-              const float4 xa = *reinterpret_cast<const float4*>(xk);
-              const float4 xb = *reinterpret_cast<const float4*>(xk + 4);
-#pragma unroll
-              for (int i = 0; i < 4; ++i) {
-                fma2(acc[i][0], acc[i][1], wv[i][e], wv[i][e], xa.x, xa.y);
-                fma2(acc[i][2], acc[i][3], wv[i][e], wv[i][e], xa.z, xa.w);
-                fma2(acc[i][4], acc[i][5], wv[i][e], wv[i][e], xb.x, xb.y);
-                fma2(acc[i][6], acc[i][7], wv[i][e], wv[i][e], xb.z, xb.w);
-              }
-            }
-          }
+          for (int o = 8; o > 0; o >>= 1) gs += __shfl_xor_sync(0xffffffffu, gs, o);
+          if ((k4 & 15) == 0) xsm[(k4 >> 4) * kBM + m] = gs;
         }
       }
     }
-    __syncthreads();  // the buffers are restaged by the next chunk
+    if (ga + p.kc < g1) load_inputs(ga + p.kc);  // in flight while this chunk computes
+    __syncthreads();
+    ok = __syncthreads_and(mbar_wait(&s_bar[ci & 1], (ci >> 1) & 1, p.status));  // uniform across the CTA
+    if (ok) {
+      for (int u = usub; u < nk; u += wp) {
+        float d[8][4];
+#pragma unroll
+        for (int nt = 0; nt < 8; ++nt) d[nt][0] = d[nt][1] = d[nt][2] = d[nt][3] = 0.f;
+        if constexpr (!BF16) {
+          const uint8_t* ub = wb + ((size_t)rt_q * p.kc + u) * p.unit_bytes;
+          // rows R0 and R0 + 8: 16 B of codes per input half (inputs 0-31, 32-63)
+          const uint4 c00 = *reinterpret_cast<const uint4*>(ub + R0 * 16);
+          const uint4 c01 = *reinterpret_cast<const uint4*>(ub + (32 + R0) * 16);
+          const uint4 c10 = *reinterpret_cast<const uint4*>(ub + (R0 + 8) * 16);
+          const uint4 c11 = *reinterpret_cast<const uint4*>(ub + (32 + R0 + 8) * 16);
+          const float2 sm0 = __half22float2(*reinterpret_cast<const __half2*>(ub + 1024 + 4 * R0));
+          const float2 sm1 = __half22float2(*reinterpret_cast<const __half2*>(ub + 1024 + 4 * (R0 + 8)));
+#pragma unroll
+          for (int ks = 0; ks < 4; ++ks) {
+            // inputs 16ks + 2t(+1) and +8 sit in words 2(ks%2) and 2(ks%2)+1 of input half ks/2
+            const uint4 w0 = ks < 2 ? c00 : c01, w1 = ks < 2 ? c10 : c11;
+            const uint32_t w0a = (ks & 1) ? w0.z : w0.x, w0b = (ks & 1) ? w0.w : w0.y;
+            const uint32_t w1a = (ks & 1) ? w1.z : w1.x, w1b = (ks & 1) ? w1.w : w1.y;
+            const uint32_t a[4] = {q4_pair_f16(w0a, sh), q4_pair_f16(w1a, sh), q4_pair_f16(w0b, sh),
+                                   q4_pair_f16(w1b, sh)};
+#pragma unroll
+            for (int nt = 0; nt < 8; nt += 2) {
+              uint32_t b[4];
+              ldsm_x4(b, xh + (size_t)(8 * (nt + (mi >> 1)) + r8) * XS + u * 64 + 16 * ks + 8 * (mi & 1));
+              mma_f16_16816(d[nt], a, b[0], b[1]);
+              mma_f16_16816(d[nt + 1], a, b[2], b[3]);
+            }
+          }
+          // y += s * (high + remainder columns) + m * sum(x)
+#pragma unroll
+          for (int nt = 0; nt < 4; ++nt)
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+              const float X = xsm[u * kBM + 8 * nt + 2 * t + e];
+              qacc[nt][e][0] = fmaf(sm0.x, d[nt][e] + d[nt + 4][e], fmaf(sm0.y, X, qacc[nt][e][0]));
+              qacc[nt][e][1] = fmaf(sm1.x, d[nt][2 + e] + d[nt + 4][2 + e], fmaf(sm1.y, X, qacc[nt][e][1]));
+            }
+        } else {
+          // bf16 unit [k half][row][8 k]: the A fragment of rows 16mt.. is one ldmatrix
+          const uint8_t* ub = wb + ((size_t)rt_q * p.kc + u) * p.unit_bytes;
+          uint32_t a[4];
+          ldsm_x4(a, ub + ((mi >> 1) * 32 + 16 * mt + 8 * (mi & 1) + r8) * 16);
+#pragma unroll
+          for (int nt = 0; nt < 8; nt += 2) {
+            uint32_t b[4];
+            ldsm_x4(b, xh + (size_t)(8 * (nt + (mi >> 1)) + r8) * XS + u * 16 + 8 * (mi & 1));
+            mma_bf16_16816(d[nt], a, b[0], b[1]);
+            mma_bf16_16816(d[nt + 1], a, b[2], b[3]);
+          }
+#pragma unroll
+          for (int nt = 0; nt < 4; ++nt)
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+              qacc[nt][e][0] += d[nt][e] + d[nt + 4][e];
+              qacc[nt][e][1] += d[nt][2 + e] + d[nt + 4][2 + e];
+            }
+        }
+      }
+    }
+    __syncthreads();  // the buffers are restaged by the next chunks
+    if (tid == 0 && ok && ga + 2 * p.kc < g1) stage_weights(ga + 2 * p.kc);  // into this chunk's buffer
   }
   if (!ok) return;  // every wait is bounded; the status word carries the timeout
 
-  // ---- each warp's tile -> shared memory (the input staging is no longer needed)
+  // ---- each warp's results -> shared memory [warp][32 tokens][QS] (16 rows,
+  // padded: both the fragment stores and the row-contiguous reads below are
+  // free of bank conflicts); the staging is no longer needed
+  constexpr int QS = 20;
+  float* qred = reinterpret_cast<float*>(smem);
+  {
+    const int rr = lane >> 2;
 #pragma unroll
-  for (int i = 0; i < 4; ++i)
+    for (int nt = 0; nt < 4; ++nt)
 #pragma unroll
-    for (int j = 0; j < 8; ++j) red[(warp * 32 + lane) * 32 + i * 8 + j] = acc[i][j];
+      for (int e = 0; e < 2; ++e) {
+        qred[(warp * kBM + 8 * nt + 2 * t + e) * QS + rr] = qacc[nt][e][0];
+        qred[(warp * kBM + 8 * nt + 2 * t + e) * QS + rr + 8] = qacc[nt][e][1];
+      }
+  }
   __syncthreads();
-
-  // element (r, m) of the block (r < rtb*32 rows, m < 32 tokens) sits in lane
-  // (r%32)/4*4 + m/8, slot (r%4)*8 + m%8 of every warp w with w % rtb == r/32
-  auto cta_sum = [&](int r, int m) {
-    const int rl = r >> 5, rr = r & 31;
-    const int ln = (rr >> 2) * 4 + (m >> 3), slot = (rr & 3) * 8 + (m & 7);
-    float s = 0.f;
-    for (int w = rl; w < kBWarps; w += p.rtb) s += red[(w * 32 + ln) * 32 + slot];
-    return s;
+  // Sum of this CTA for element (r, m) of the block (r < rtb*32 rows, m < 32
+  // tokens): rows 16h .. 16h+15 of row tile rl are the wp warps of pair 2rl + h.
+  auto cta_sum = [&](int r, int mm) {
+    const int pr = r >> 4, rr = r & 15;
+    float v = 0.f;
+    for (int w = pr * wp; w < pr * wp + wp; ++w) v += qred[(w * kBM + mm) * QS + rr];
+    return v;
   };
-  const int rows_blk = p.rtb * 32, row0 = rt0 * 32, rows_pad = p.n_rt * 32;
-  const int m = tid & 31, rstep = kBThreads / 32;  // thread: token m, rows tid/32, +8, ...
-  bool last = true;
+  // Epilogue: warp w takes tokens w, w+8, w+16, w+24; lane = row within a row
+  // tile, so every global access below is one contiguous 128-B line.
+  const int row0 = rt0 * 32, rows_pad = p.n_rt * 32;
   if (p.ks > 1) {
-    for (int r = tid >> 5; r < rows_blk; r += rstep)
-      p.part[((size_t)ksi * kBM + m) * rows_pad + row0 + r] = cta_sum(r, m);
+    for (int rl = 0; rl < p.rtb; ++rl)
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const int mm = warp + 8 * k;
+        p.part[((size_t)ksi * kBM + mm) * rows_pad + row0 + rl * 32 + lane] = cta_sum(rl * 32 + lane, mm);
+      }
     __threadfence();
     __syncthreads();
     if (tid == 0) s_last = atomicAdd(&p.counters[blk], 1) == p.ks - 1;
     __syncthreads();
-    last = s_last;
-    if (!last) return;
+    if (!s_last) return;
     __threadfence();
   }
-  // final value of (r, m): this CTA's sum, or the K-split partials in CTA order
-  auto value = [&](int r, int mm) {
-    if (p.ks == 1) return cta_sum(r, mm);
-    float s = 0.f;
-    for (int j = 0; j < p.ks; ++j) s += __ldcg(p.part + ((size_t)j * kBM + mm) * rows_pad + row0 + r);
-    return s;
-  };
-  float bv = -INFINITY;
-  int bi = 0x7fffffff;
+  constexpr int KSMAX = 16;
+  float ssq[4] = {0.f, 0.f, 0.f, 0.f};  // EPI_RESID: sums of squares per token of the warp
+  float bv[4];
+  int bi[4];
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    bv[k] = -INFINITY;
+    bi[k] = 0x7fffffff;
+  }
   bool nan = false;
-  if (m < p.M) {
-    for (int r = tid >> 5; r < rows_blk; r += rstep) {
-      const int row = row0 + r;
-      if (p.epi == EPI_SWIGLU) {  // row tile t: 16 gate rows, then their 16 up rows
-        if ((r & 31) < 16) {
-          const float g = value(r, m), u = value(r + 16, m);
-          p.out[(size_t)m * p.out_cols + (row >> 5) * 16 + (row & 15)] = silu(g) * u;
+  for (int rl = 0; rl < p.rtb; ++rl) {
+    const int r = rl * 32 + lane, row = row0 + r;
+    float y[4];
+    if (p.ks == 1) {
+#pragma unroll
+      for (int k = 0; k < 4; ++k) y[k] = cta_sum(r, warp + 8 * k);
+    } else {  // the K-split partials, added in CTA order; two tokens' loads in flight together
+#pragma unroll
+      for (int k0 = 0; k0 < 4; k0 += 2) {
+        float pv[2][KSMAX];
+#pragma unroll
+        for (int k = 0; k < 2; ++k)
+#pragma unroll
+          for (int j = 0; j < KSMAX; ++j)
+            pv[k][j] = ldcg1_if(p.part + ((size_t)j * kBM + warp + 8 * (k0 + k)) * rows_pad + row, j < p.ks);
+#pragma unroll
+        for (int k = 0; k < 2; ++k) {
+          float sum = 0.f;
+#pragma unroll
+          for (int j = 0; j < KSMAX; ++j) sum += pv[k][j];
+          y[k0 + k] = sum;
         }
+      }
+    }
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const int mm = warp + 8 * k;
+      if (p.epi == EPI_SWIGLU) {  // lanes 0-15: gate rows; their up rows are lanes 16-31
+        const float up = __shfl_down_sync(0xffffffffu, y[k], 16);
+        if (mm < p.M && lane < 16) p.out[(size_t)mm * p.out_cols + (row >> 5) * 16 + lane] = silu(y[k]) * up;
         continue;
       }
-      if (row >= p.rows) continue;
-      const float y = value(r, m);
+      if (mm >= p.M || row >= p.rows) continue;
       if (p.epi == EPI_RESID) {
-        p.out[(size_t)m * p.out_cols + row] = __ldcg(p.resid + (size_t)m * p.out_cols + row) + y;
+        const float xn = __ldcg(p.resid + (size_t)mm * p.out_cols + row) + y[k];
+        p.out[(size_t)mm * p.out_cols + row] = xn;
+        ssq[k] += xn * xn;
       } else {
-        p.out[(size_t)m * p.out_cols + row] = y;
+        p.out[(size_t)mm * p.out_cols + row] = y[k];
         if (p.epi == EPI_LOGITS) {
-          if (y != y) nan = true;
-          else if (better(y, row, bv, bi)) { bv = y; bi = row; }
+          if (y[k] != y[k]) nan = true;
+          else if (better(y[k], row, bv[k], bi[k])) { bv[k] = y[k]; bi[k] = row; }
         }
       }
     }
   }
   if (p.ks > 1 && tid == 0) p.counters[blk] = 0;
+  if (p.epi == EPI_RESID && p.ss_out) {  // per-token partial over this block's rows
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      float v = ssq[k];
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+      if (lane == 0) p.ss_out[(size_t)blk * kBM + warp + 8 * k] = v;
+    }
+    return;
+  }
   if (p.epi != EPI_LOGITS) return;
   // ---- greedy choice per sequence: best of this block, then over all blocks
   if (nan) atomicOr(p.status, ST_NAN);
-  s_bv[warp][m] = bv;
-  s_bi[warp][m] = bi;
-  __syncthreads();
-  if (tid < kBM) {
-    float b2 = s_bv[0][tid];
-    int i2 = s_bi[0][tid];
-    for (int w = 1; w < kBWarps; ++w)
-      if (better(s_bv[w][tid], s_bi[w][tid], b2, i2)) { b2 = s_bv[w][tid]; i2 = s_bi[w][tid]; }
-    p.cand_v[(size_t)tid * n_blocks + blk] = b2;
-    p.cand_i[(size_t)tid * n_blocks + blk] = i2;
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const float ov = __shfl_xor_sync(0xffffffffu, bv[k], o);
+      const int oi = __shfl_xor_sync(0xffffffffu, bi[k], o);
+      if (better(ov, oi, bv[k], bi[k])) { bv[k] = ov; bi[k] = oi; }
+    }
+    if (lane == 0) {
+      p.cand_v[(size_t)(warp + 8 * k) * n_blocks + blk] = bv[k];
+      p.cand_i[(size_t)(warp + 8 * k) * n_blocks + blk] = bi[k];
+    }
   }
   __threadfence();
   __syncthreads();
@@ -326,6 +437,7 @@ struct BEmbedParams {
   int bf16, dim, vocab, M;
   const int* tok;
   float* x;
+  float* ss_out;  // [32]: sum of squares of each token's row
   int* status;
 };
 
@@ -338,9 +450,24 @@ __global__ void __launch_bounds__(256) bembed_kernel(const BEmbedParams p) {
     if (threadIdx.x == 0) atomicOr(p.status, ST_BAD_TOKEN);
     t = 0;
   }
-  for (int i = threadIdx.x; i < p.dim; i += 256)
-    p.x[(size_t)m * p.dim + i] = p.bf16 ? bf16_bits_to_f32(static_cast<const uint16_t*>(p.embed)[(size_t)t * p.dim + i])
-                                        : static_cast<const float*>(p.embed)[(size_t)t * p.dim + i];
+  float ss = 0.f;
+  for (int i = threadIdx.x; i < p.dim; i += 256) {
+    const float v = p.bf16 ? bf16_bits_to_f32(static_cast<const uint16_t*>(p.embed)[(size_t)t * p.dim + i])
+                           : static_cast<const float*>(p.embed)[(size_t)t * p.dim + i];
+    p.x[(size_t)m * p.dim + i] = v;
+    ss += v * v;
+  }
+  // sum of squares of the row (the first RMSNorm): warps, then warp sums in order
+  __shared__ float s_w[8];
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+  if ((threadIdx.x & 31) == 0) s_w[threadIdx.x >> 5] = ss;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    float t = 0.f;
+    for (int w = 0; w < 8; ++w) t += s_w[w];
+    p.ss_out[m] = t;
+  }
 }
 
 // Flash-decoding attention of every sequence of the batch: grid (split, kv head, sequence).
@@ -353,28 +480,255 @@ struct BAttnParams {
   size_t part_stride;     // attention partial floats per sequence
 };
 
+__device__ __forceinline__ void cp_async16(void* dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+
+constexpr int kBAttnThreads = 256;
+constexpr int kBAttnPP = 128;  // cache positions per pass
+
+// Shared memory of one batched attention item (sequence, kv head, split).
 template <int GQ, int HD>
-__global__ void __launch_bounds__(kAttnThreads) battention_kernel(const BAttnParams bp) {
-  constexpr int NW = kAttnThreads / 32;
-  __shared__ __align__(16) AttnSmem<GQ, HD, NW> sm;
+struct BAttnSmem {
+  static constexpr int PP = kBAttnPP, RS = HD + 8, NBW = PP / 16;
+  uint16_t kt[PP][RS];            // K rows of the pass (fp16, padded rows)
+  uint16_t vt[PP][RS];
+  float cur[GQ + 2][HD];          // q heads (scaled), k, v of this step
+  float tres[NBW][GQ][HD + 2];    // per 16-position block and head: o, max, sum
+  float acc[GQ][HD];
+  float accm[GQ], accl[GQ], fac[GQ][NBW + 1];
+  int is_last;
+};
+
+// Flash-decoding attention of every sequence of the batch on the tensor
+// cores: grid (split, kv head, sequence), 8 warps; warp w scores all GQ heads
+// against positions 16w .. 16w+15 of the pass (attn_mma.cuh). The last split
+// of a (sequence, kv head) to finish merges the splits into the output row.
+template <int GQ, int HD>
+__global__ void __launch_bounds__(kBAttnThreads) battn_mma_kernel(const BAttnParams bp) {
+  using SA = BAttnSmem<GQ, HD>;
+  constexpr int NT = kBAttnThreads, PP = SA::PP, RS = SA::RS, CH = HD / 8, DPL = HD / 32;
+  static_assert(GQ <= 8 && SA::NBW == NT / 32, "layout");
+  extern __shared__ __align__(16) uint8_t smraw[];
+  SA& sa = *reinterpret_cast<SA*>(smraw);
   pdl_trigger();
   pdl_wait();
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int g = blockIdx.y, split = blockIdx.x, b = blockIdx.z;
-  AttnParams p = bp.a;
+  const AttnParams& a = bp.a;
   const int pos = bp.pos[b];
-  if (pos < 0 || pos >= p.cap) {
-    if (threadIdx.x == 0 && split == 0 && g == 0) atomicOr(p.status, ST_CTX_FULL);
+  if (pos < 0 || pos >= a.cap) {
+    if (tid == 0 && split == 0 && g == 0) atomicOr(a.status, ST_CTX_FULL);
     return;
   }
-  const int P_eff = attn_splits(pos + 1, p.P);
+  const int len = pos + 1;
+  constexpr int PMAX = 24;  // splits a (sequence, kv head) merges at most (longer splits take several passes)
+  const int P_eff = min(min(a.P, PMAX), (len + PP - 1) / PP);
   if (split >= P_eff) return;
-  p.kc += (size_t)b * bp.seq_kv_stride;
-  p.vc += (size_t)b * bp.seq_kv_stride;
-  p.part += (size_t)b * bp.part_stride;
-  p.counter += (size_t)b * p.Hkv;
-  p.out += (size_t)b * bp.o_cols;
-  const float* q = bp.qkv + (size_t)b * bp.qkv_cols;
-  attention_item<GQ, HD, NW, CtaSync>(p, g, split, P_eff, pos, sm, [&](int row) { return __ldcg(q + row); });
+  const int t0 = (int)((int64_t)len * split / P_eff), t1 = (int)((int64_t)len * (split + 1) / P_eff);
+  uint16_t* kc = a.kc + (size_t)b * bp.seq_kv_stride + (size_t)g * a.cap * HD;
+  uint16_t* vc = a.vc + (size_t)b * bp.seq_kv_stride + (size_t)g * a.cap * HD;
+  const float* qkv = bp.qkv + (size_t)b * bp.qkv_cols;
+
+  // rows tp .. tp+n-1 of K and V -> tiles (async copies; zero rows up to the
+  // next multiple of 16), then bf16 -> fp16 in place by the same threads
+  static_assert((CH & (CH - 1)) == 0, "16-B chunks per row: a power of two");
+  constexpr int LCH = CH == 8 ? 3 : 4;
+  auto stage = [&](int tp) {
+    const int n = min(PP, t1 - tp), rows = ((n + 15) / 16) * 16;
+#pragma unroll
+    for (int kv = 0; kv < 2; ++kv) {
+      uint16_t(*tile)[RS] = kv ? sa.vt : sa.kt;
+      const uint16_t* src = (kv ? vc : kc) + (size_t)tp * HD;
+      for (int idx = tid; idx < rows * CH; idx += NT) {
+        const int row = idx >> LCH, ch = idx & (CH - 1);
+        if (row < n) cp_async16(&tile[row][8 * ch], src + (size_t)row * HD + 8 * ch);
+        else *reinterpret_cast<uint4*>(&tile[row][8 * ch]) = make_uint4(0u, 0u, 0u, 0u);
+      }
+    }
+  };
+  auto convert = [&](int tp) {
+    const int n = min(PP, t1 - tp), rows = ((n + 15) / 16) * 16;
+    cp_async_wait_all();
+#pragma unroll
+    for (int kv = 0; kv < 2; ++kv) {
+      uint16_t(*tile)[RS] = kv ? sa.vt : sa.kt;
+      for (int idx = tid; idx < rows * CH; idx += NT) {
+        uint4* q = reinterpret_cast<uint4*>(&tile[idx >> LCH][8 * (idx & (CH - 1))]);
+        const uint4 w = *q;
+        *q = make_uint4(bf16x2_to_f16x2(w.x), bf16x2_to_f16x2(w.y), bf16x2_to_f16x2(w.z), bf16x2_to_f16x2(w.w));
+      }
+    }
+  };
+  stage(t0);
+  // q heads, k, v of this kv head; RoPE factors and q/k norm weights
+  for (int i = tid; i < (GQ + 2) * HD; i += NT) {
+    const int r = i / HD, d = i % HD;
+    const int row = r < GQ ? (g * GQ + r) * HD + d : (r == GQ ? a.q_dim + g * HD + d : a.q_dim + a.kv_dim + g * HD + d);
+    sa.cur[r][d] = __ldcg(qkv + row);
+  }
+  const int nrope = (GQ + 1) * (HD / 2);
+  // q/k norm weights: warp w takes head w (and w + 8; head GQ is k)
+  float wn[2][DPL];
+#pragma unroll
+  for (int k2 = 0; k2 < 2; ++k2)
+#pragma unroll
+    for (int e = 0; e < DPL; ++e) {
+      const int h = warp + 8 * k2;
+      wn[k2][e] = (a.q_norm && h <= GQ) ? __ldg((h < GQ ? a.q_norm : a.k_norm) + lane + 32 * e) : 1.f;
+    }
+  convert(t0);
+  __syncthreads();
+  if (a.q_norm) {  // per-head RMSNorm of the q heads and k
+#pragma unroll
+    for (int k2 = 0; k2 < 2; ++k2) {
+      const int h = warp + 8 * k2;
+      if (h <= GQ) {
+        float* v = sa.cur[h];
+        float x[DPL], ss = 0.f;
+#pragma unroll
+        for (int e = 0; e < DPL; ++e) {
+          x[e] = v[lane + 32 * e];
+          ss += x[e] * x[e];
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+        const float inv = 1.0f / sqrtf(ss / (float)HD + a.eps);
+#pragma unroll
+        for (int e = 0; e < DPL; ++e) v[lane + 32 * e] = x[e] * inv * wn[k2][e];
+      }
+    }
+    __syncthreads();
+  }
+  // RoPE of q and k; q scaled by log2(e)/sqrt(hd); k, v rounded to bf16 (the
+  // split owning `pos` appends them and puts them into its tile)
+  const float qscale = 1.4426950408889634f / sqrtf((float)HD);
+  const bool owner = split == P_eff - 1 && pos - t0 < PP;
+  auto keep = [&](int r, int d, float x) {
+    const __nv_bfloat16 h = __float2bfloat16_rn(x);
+    const float xr = __bfloat162float(h);
+    sa.cur[r][d] = xr;
+    if (split == P_eff - 1) {
+      (r == GQ ? kc : vc)[(size_t)pos * HD + d] = __bfloat16_as_ushort(h);
+      if (owner) (r == GQ ? sa.kt : sa.vt)[pos - t0][d] = __half_as_ushort(__float2half_rn(xr));
+    }
+  };
+  for (int j = tid; j < nrope + HD; j += NT) {  // RoPE pairs of the q heads and k, then v elements
+    if (j < nrope) {
+      const int h = j / (HD / 2), i = j % (HD / 2);
+      const float2 rcs = __ldg(a.rope + (size_t)pos * (HD / 2) + i);
+      float* v = sa.cur[h];
+      const int ia = a.rope_neox ? i : 2 * i, ib = a.rope_neox ? i + HD / 2 : 2 * i + 1;
+      const float x0 = v[ia], x1 = v[ib];
+      const float y0 = x0 * rcs.x - x1 * rcs.y, y1 = x0 * rcs.y + x1 * rcs.x;
+      if (h < GQ) {
+        v[ia] = y0 * qscale;
+        v[ib] = y1 * qscale;
+      } else {
+        keep(GQ, ia, y0);
+        keep(GQ, ib, y1);
+      }
+    } else {
+      keep(GQ + 1, j - nrope, sa.cur[GQ + 1][j - nrope]);
+    }
+  }
+  for (int i = tid; i < GQ * HD; i += NT) sa.acc[i / HD][i % HD] = 0.f;
+  if (tid < GQ) {
+    sa.accm[tid] = -INFINITY;
+    sa.accl[tid] = 0.f;
+  }
+  __syncthreads();
+
+  float* gpart = a.part + (size_t)b * bp.part_stride + (((size_t)g * a.P + split) * GQ) * (HD + 2);
+  for (int tp = t0; tp < t1; tp += PP) {
+    const int n = min(PP, t1 - tp), nb = (n + 15) / 16;
+    if (tp != t0) {
+      stage(tp);
+      convert(tp);
+      __syncthreads();
+      if (pos >= tp && pos < tp + n)
+        for (int d = tid; d < HD; d += NT) {
+          sa.kt[pos - tp][d] = __half_as_ushort(__float2half_rn(sa.cur[GQ][d]));
+          sa.vt[pos - tp][d] = __half_as_ushort(__float2half_rn(sa.cur[GQ + 1][d]));
+        }
+      __syncthreads();
+    }
+    if (warp < nb)
+      attn_block16<GQ, HD, RS>(&sa.cur[0][0], &sa.kt[0][0], &sa.vt[0][0], 16 * warp, n - 16 * warp, lane,
+                               &sa.tres[warp][0][0], HD + 2);
+    __syncthreads();
+    const bool last_pass = tp + PP >= t1;
+    // merge the pass's blocks with the running output (into the split's partial on the last pass)
+    for (int i = tid; i < GQ * HD; i += NT) {
+      const int h = i / HD, d = i % HD;
+      float M = sa.accm[h];
+      for (int w = 0; w < nb; ++w) M = fmaxf(M, sa.tres[w][h][HD]);
+      const float fa = sa.accm[h] == -INFINITY ? 0.f : exp2f(sa.accm[h] - M);
+      float O = sa.acc[h][d] * fa, L = sa.accl[h] * fa;
+      for (int w = 0; w < nb; ++w) {
+        const float f = exp2f(sa.tres[w][h][HD] - M);
+        O += sa.tres[w][h][d] * f;
+        L += sa.tres[w][h][HD + 1] * f;
+      }
+      if (last_pass) {
+        gpart[h * (HD + 2) + d] = O;
+        if (d == 0) {
+          gpart[h * (HD + 2) + HD] = M;
+          gpart[h * (HD + 2) + HD + 1] = L;
+        }
+      } else {
+        sa.acc[h][d] = O;
+        if (d == 0) sa.fac[h][0] = M, sa.fac[h][1] = L;  // new running max / sum, published below
+      }
+    }
+    __syncthreads();
+    if (!last_pass && tid < GQ) {
+      sa.accm[tid] = sa.fac[tid][0];
+      sa.accl[tid] = sa.fac[tid][1];
+    }
+    __syncthreads();
+  }
+  // ---- the last split of this (sequence, kv head) merges the splits (no waiting)
+  int* counter = a.counter + (size_t)b * a.Hkv + g;
+  __threadfence();
+  __syncthreads();
+  if (tid == 0) sa.is_last = (atomicAdd(counter, 1) == P_eff - 1);
+  __syncthreads();
+  if (!sa.is_last) return;
+  __threadfence();
+  // the last split: (max, sum) of every split and head to shared memory while
+  // each thread loads its output element of every split (one round trip)
+  const float* hp = a.part + (size_t)b * bp.part_stride + ((size_t)g * a.P * GQ) * (HD + 2);
+  float* out = a.out + (size_t)b * bp.o_cols;
+  float* ml = &sa.tres[0][0][0];  // [P_eff][GQ][2] (the block results are no longer needed)
+  static_assert(sizeof(sa.tres) >= PMAX * GQ * 2 * sizeof(float), "merge scratch");
+  for (int i = tid; i < P_eff * GQ * 2; i += NT) {
+    const int sidx = i / (2 * GQ), h = (i / 2) % GQ, e = i & 1;
+    ml[i] = __ldcg(hp + ((size_t)sidx * GQ + h) * (HD + 2) + HD + e);
+  }
+  for (int i0 = 0; i0 < GQ * HD; i0 += NT) {
+    const int i = i0 + tid, h = i / HD, d = i % HD;
+    float ov[PMAX];
+#pragma unroll
+    for (int s2 = 0; s2 < PMAX; ++s2)
+      ov[s2] = ldcg1_if(hp + ((size_t)s2 * GQ + (i < GQ * HD ? h : 0)) * (HD + 2) + d, s2 < P_eff && i < GQ * HD);
+    __syncthreads();
+    if (i < GQ * HD) {
+      float M = -INFINITY;
+      for (int s2 = 0; s2 < P_eff; ++s2) M = fmaxf(M, ml[(s2 * GQ + h) * 2]);
+      float L = 0.f, O = 0.f;
+#pragma unroll
+      for (int s2 = 0; s2 < PMAX; ++s2)
+        if (s2 < P_eff) {
+          const float f = exp2f(ml[(s2 * GQ + h) * 2] - M);
+          L += ml[(s2 * GQ + h) * 2 + 1] * f;
+          O += ov[s2] * f;
+        }
+      out[(g * GQ + h) * HD + d] = O / L;
+    }
+  }
+  if (tid == 0) *counter = 0;
 }
 
 }  // namespace llmq

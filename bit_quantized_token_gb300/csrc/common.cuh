@@ -100,6 +100,54 @@ __device__ __forceinline__ uint64_t policy_evict_first() {
   return p;
 }
 
+// Loads issued as predicated instructions, so a run of them goes out back to
+// back; the result is zero when !pred. The "memory" clobber keeps them after
+// the barrier that precedes them.
+__device__ __forceinline__ float4 ldcg4_if(const float* ptr, bool pred) {
+  float4 v;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.u32 p, %5, 0;\n\t"
+      "mov.b32 %0, 0;\n\tmov.b32 %1, 0;\n\tmov.b32 %2, 0;\n\tmov.b32 %3, 0;\n\t"
+      "@p ld.global.cg.v4.f32 {%0, %1, %2, %3}, [%4];\n\t}"
+      : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+      : "l"(ptr), "r"((uint32_t)pred)
+      : "memory");
+  return v;
+}
+__device__ __forceinline__ float2 ldcg2_if(const float* ptr, bool pred) {
+  float2 v;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.u32 p, %3, 0;\n\t"
+      "mov.b32 %0, 0;\n\tmov.b32 %1, 0;\n\t"
+      "@p ld.global.cg.v2.f32 {%0, %1}, [%2];\n\t}"
+      : "=f"(v.x), "=f"(v.y)
+      : "l"(ptr), "r"((uint32_t)pred)
+      : "memory");
+  return v;
+}
+__device__ __forceinline__ float ldcg1_if(const float* ptr, bool pred) {
+  float v;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.u32 p, %2, 0;\n\t"
+      "mov.b32 %0, 0;\n\t@p ld.global.cg.f32 %0, [%1];\n\t}"
+      : "=f"(v)
+      : "l"(ptr), "r"((uint32_t)pred)
+      : "memory");
+  return v;
+}
+// Same through the read-only path, for data no kernel writes (norm weights).
+__device__ __forceinline__ float4 ldnc4_if(const float* ptr, bool pred) {
+  float4 v;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.u32 p, %5, 0;\n\t"
+      "mov.b32 %0, 0;\n\tmov.b32 %1, 0;\n\tmov.b32 %2, 0;\n\tmov.b32 %3, 0;\n\t"
+      "@p ld.global.nc.v4.f32 {%0, %1, %2, %3}, [%4];\n\t}"
+      : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+      : "l"(ptr), "r"((uint32_t)pred)
+      : "memory");
+  return v;
+}
+
 // ---- paired fp32 arithmetic (sm_100+ f32x2) --------------------------------
 // Operands are packed into 64-bit registers inside the asm block so that the
 // register allocator pairs them without extra moves.

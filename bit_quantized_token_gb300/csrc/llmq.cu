@@ -55,20 +55,26 @@ struct BPlan {
 };
 
 BPlan plan_bgemv(const Mat& mat, int n_sm) {
+  // 256 inputs per chunk (4 four-bit units or 16 bf16 units per row tile);
+  // 1, 2 or 4 row tiles per CTA (8 warps = 16-row halves x unit subsets);
+  // enough CTAs to fill the GPU twice through the K splits (at most 16, the
+  // epilogue's limit)
   BPlan p;
   p.m = mat;
   const int epu = mat.bf16 ? kBF16UnitCols : 64;
-  for (int r : {8, 4, 2})
-    if (mat.n_rt % r == 0 && mat.n_rt / r >= n_sm) {
+  p.kc = 256 / epu;
+  // more row tiles per CTA only while the row blocks alone fill the GPU; else
+  // one row tile per CTA and just enough K splits to fill it once (split-K
+  // costs a partial round trip and a merge)
+  const int max_ks = std::max(1, (mat.G + p.kc - 1) / p.kc);
+  p.rtb = 1;
+  for (int r : {4, 2})  // bf16 units: at most 2 row tiles (two CTAs of double-buffered 16 KB units per SM)
+    if (mat.n_rt % r == 0 && mat.n_rt / r >= n_sm && (!mat.bf16 || r <= 2)) {
       p.rtb = r;
       break;
     }
-  // at least 256 inputs per chunk (the warp sums reuse that staging area) and
-  // one unit per warp per chunk
-  p.kc = std::max(256 / epu, kBWarps / p.rtb);
   p.n_blocks = mat.n_rt / p.rtb;
-  const int max_ks = std::max(1, mat.G / p.kc);
-  p.ks = std::min(max_ks, std::max(1, (2 * n_sm + p.n_blocks - 1) / p.n_blocks));
+  p.ks = std::min({max_ks, 16, std::max(1, (n_sm + p.n_blocks - 1) / p.n_blocks)});
   p.smem = bgemv_stage_bytes(p.rtb, p.kc, mat.unit_bytes(), epu);
   return p;
 }
@@ -222,6 +228,7 @@ struct llm_model {
   // batched step (max_batch > 1)
   std::vector<BPlan> bqkv, bwo, bgu, bdown;
   BPlan blm;
+  float *d_bss_x = nullptr, *d_bss_h = nullptr;  // batched: per-(row block, token) sums of squares
   float *d_bx = nullptr, *d_bh = nullptr, *d_bqkv = nullptr, *d_bo = nullptr, *d_ba = nullptr,
         *d_blogits = nullptr, *d_bpart = nullptr, *d_battn_part = nullptr, *d_bcand_v = nullptr;
   int *d_bcand_i = nullptr, *d_bcnt = nullptr, *d_battn_cnt = nullptr, *d_bgreedy_cnt = nullptr;
@@ -564,8 +571,26 @@ cudaError_t enqueue_persistent_step(llm_model* m, int seq) {
 
 template <int GQ, int HD>
 cudaError_t launch_battn_t(const llm_model* m, const BAttnParams& b, bool pdl) {
-  return launch(battention_kernel<GQ, HD>, dim3(m->attn_P, m->cfg.n_kv_heads, m->cfg.max_batch), dim3(kAttnThreads), 0,
-                m->stream, pdl, b);
+  return launch(battn_mma_kernel<GQ, HD>, dim3(m->attn_P, m->cfg.n_kv_heads, m->cfg.max_batch), dim3(kBAttnThreads),
+                sizeof(BAttnSmem<GQ, HD>), m->stream, pdl, b);
+}
+template <int GQ, int HD>
+cudaError_t battn_smem_attr() {
+  return cudaFuncSetAttribute(battn_mma_kernel<GQ, HD>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              (int)sizeof(BAttnSmem<GQ, HD>));
+}
+cudaError_t battn_set_smem(int gq, int hd) {
+  switch (gq * 1000 + hd) {
+    case 1064: return battn_smem_attr<1, 64>();
+    case 2064: return battn_smem_attr<2, 64>();
+    case 4064: return battn_smem_attr<4, 64>();
+    case 8064: return battn_smem_attr<8, 64>();
+    case 1128: return battn_smem_attr<1, 128>();
+    case 2128: return battn_smem_attr<2, 128>();
+    case 4128: return battn_smem_attr<4, 128>();
+    case 8128: return battn_smem_attr<8, 128>();
+  }
+  return cudaErrorInvalidValue;
 }
 
 cudaError_t launch_battn(const llm_model* m, const BAttnParams& b, bool pdl) {
@@ -623,6 +648,7 @@ cudaError_t enqueue_batch_step(llm_model* m) {
   ep.M = B;
   ep.tok = m->d_tok;
   ep.x = m->d_bx;
+  ep.ss_out = m->d_bss_x;
   ep.status = m->d_status;
   if ((e = launch(bembed_kernel, dim3(B), dim3(256), 0, m->stream, false, ep)) != cudaSuccess) return e;
   const size_t kv_layer = (size_t)c.n_kv_heads * c.max_seq * c.head_dim;
@@ -631,6 +657,8 @@ cudaError_t enqueue_batch_step(llm_model* m) {
     BGemvParams p = bgemv_params(m, m->bqkv[l]);
     p.x = m->d_bx;
     p.norm_w = m->d_norms + m->off_attn_norm[l];
+    p.ss_in = m->d_bss_x;
+    p.ss_n = l == 0 ? 1 : m->bdown[l - 1].n_blocks;
     p.epi = EPI_STORE;
     p.out = m->d_bqkv;
     p.out_cols = qkv_cols;
@@ -663,12 +691,15 @@ cudaError_t enqueue_batch_step(llm_model* m) {
     p.x = m->d_bo;
     p.epi = EPI_RESID;
     p.resid = m->d_bx;
+    p.ss_out = m->d_bss_h;
     p.out = m->d_bh;
     p.out_cols = d;
     if ((e = launch_bgemv(m, m->bwo[l], p, pdl)) != cudaSuccess) return e;
     p = bgemv_params(m, m->bgu[l]);  // a = silu(Wg rmsnorm(h)) * (Wu rmsnorm(h))
     p.x = m->d_bh;
     p.norm_w = m->d_norms + m->off_ffn_norm[l];
+    p.ss_in = m->d_bss_h;
+    p.ss_n = m->bwo[l].n_blocks;
     p.epi = EPI_SWIGLU;
     p.out = m->d_ba;
     p.out_cols = F;
@@ -677,6 +708,7 @@ cudaError_t enqueue_batch_step(llm_model* m) {
     p.x = m->d_ba;
     p.epi = EPI_RESID;
     p.resid = m->d_bh;
+    p.ss_out = m->d_bss_x;
     p.out = m->d_bx;
     p.out_cols = d;
     if ((e = launch_bgemv(m, m->bdown[l], p, pdl)) != cudaSuccess) return e;
@@ -684,6 +716,8 @@ cudaError_t enqueue_batch_step(llm_model* m) {
   BGemvParams p = bgemv_params(m, m->blm);  // logits, greedy choice per sequence, positions += 1
   p.x = m->d_bx;
   p.norm_w = m->d_norms + m->off_final_norm;
+  p.ss_in = m->d_bss_x;
+  p.ss_n = m->bdown[L - 1].n_blocks;
   p.epi = EPI_LOGITS;
   p.out = m->d_blogits;
   p.out_cols = c.vocab;
@@ -1150,6 +1184,8 @@ int llm_model_create(const llm_config* cfg, const llm_tensor* tensors, int32_t n
     }
     bcnt_total = (size_t)max_blocks + (size_t)B * c.n_kv_heads + 1;
     AL(m->d_bx, (size_t)B * d * 4, "batched residual");
+    AL(m->d_bss_x, (size_t)max_blocks * kBM * 4, "batched sums of squares");
+    AL(m->d_bss_h, (size_t)max_blocks * kBM * 4, "batched sums of squares");
     AL(m->d_bh, (size_t)B * d * 4, "batched residual");
     AL(m->d_bqkv, (size_t)B * (m->q_dim + 2 * m->kv_dim) * 4, "batched q|k|v");
     AL(m->d_bo, (size_t)B * m->q_dim * 4, "batched attention output");
@@ -1207,6 +1243,7 @@ int llm_model_create(const llm_config* cfg, const llm_tensor* tensors, int32_t n
       e = cudaFuncSetAttribute(bgemv_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)m->bsmem_max);
     if (e == cudaSuccess && m->bsmem_max)
       e = cudaFuncSetAttribute(bgemv_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)m->bsmem_max);
+    if (e == cudaSuccess && c.max_batch > 1) e = battn_set_smem(gq, hd);
     if (e == cudaSuccess) e = cudaMemset(m->d_k, 0, kv_elems * 2);
     if (e == cudaSuccess) e = cudaMemset(m->d_v, 0, kv_elems * 2);
     size_t smax = m->lm.smem;
