@@ -60,8 +60,10 @@ def src_sha():
     """Hash of the kernel sources: an ncu traffic figure is only used for the code it was taken on."""
     import hashlib
     h = hashlib.sha256()
-    for f in ("common.cuh", "kernels.cuh", "step.cuh", "llmq.cu"):
-        h.update(open(os.path.join(ROOT, "bit_quantized_token_gb300", "csrc", f), "rb").read())
+    d = os.path.join(ROOT, "bit_quantized_token_gb300", "csrc")
+    for f in sorted(os.listdir(d)):
+        if f.endswith((".cu", ".cuh")):
+            h.update(open(os.path.join(d, f), "rb").read())
     return h.hexdigest()[:16]
 
 
@@ -239,7 +241,7 @@ def run_batched(a, cfg, w, rank, world, local, dist):
                    "timed": "llm_decode_step_batch(NULL tokens): CUDA-graph replays, greedy tokens fed back on the device"},
         "hbm": {"bytes_per_step": bytes_step, "weight_bytes": st["weight_stream_bytes"], "kv_bytes_per_step": kv_step,
                 "achieved_gbs": gbs, "frac_of_peak": gbs / peak, "peak_gbs": peak, "peak_kind": peak_kind},
-        "roofline": {"kernel": "batched step (bgemv_kernel + battention_kernel graph; attention reads ~90% of the bytes)",
+        "roofline": {"kernel": "batched step (bgemv_kernel + battn_mma_kernel graph; attention reads ~90% of the bytes)",
                      "bound": "hbm", "achieved": gbs, "peak": peak, "unit": "GB/s", "frac": gbs / peak,
                      "traffic": None, "peak_kind": peak_kind},
         "e2e": {"value": world * B * n_e2e / e2e_s, "unit": "tok/s", "h2d_bytes_per_step": 4 * B,
