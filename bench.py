@@ -289,9 +289,9 @@ def main():
     if cfg.get("batch", 1) > 1:
         run_batched(a, cfg, w, rank, world, local, dist)
         return
-    n_e2e, n_kt = 32, 3
+    n_e2e, n_kt, n_pf = 32, 3, 512
     n_pre = max(0, cfg.get("prefill_kv", 0))
-    max_seq = n_pre + len(prompt) + a.warmup + a.steps + n_e2e + 8
+    max_seq = max(n_pre + len(prompt) + a.warmup + a.steps + n_e2e + 8, n_pf + 8)
     stream = torch.cuda.Stream()  # the library launches on it; events are recorded on it
     m = bq.Model(cfg, w, max_seq=max_seq, stream=stream.cuda_stream)
     st = m.stats()
@@ -353,6 +353,25 @@ def main():
     e2e = {"value": world * n_e2e / e2e_s, "unit": "tok/s", "h2d_bytes_per_step": 4, "d2h_bytes_per_step": 4,
            "steps": n_e2e, "call": "llm_decode_step(host token -> host argmax)"}
 
+    # prompt processing: a 512-token prompt, token by token (n graph steps) and
+    # batched (chunks of 32 through the tensor-core pipeline); wall clock of the call
+    prefill = None
+    if n_pre == 0:
+        pf_prompt = synth.make_prompt(cfg, n=n_pf)
+        rates = {}
+        for name, call in (("batched", m.prefill_batched), ("token_by_token", m.prefill)):
+            m.kv_reset(0)
+            call(0, pf_prompt[:64])  # warm
+            m.kv_reset(0)
+            torch.cuda.synchronize()
+            t0 = time.perf_counter()
+            call(0, pf_prompt, None, am_h)
+            rates[name] = n_pf / (time.perf_counter() - t0)
+        prefill = {"prompt_tokens": n_pf, "batched_tok_s": rates["batched"],
+                   "token_by_token_tok_s": rates["token_by_token"],
+                   "speedup": rates["batched"] / rates["token_by_token"],
+                   "call": "llm_prefill_batched vs llm_prefill (wall clock of the call, host tokens in)"}
+
     if st["kernels_per_step"] == 1:
         # one persistent kernel per step: its launch duration is the step time
         roofline = {"kernel": "step_kernel (persistent decode step, one launch per token)", "bound": "hbm",
@@ -387,6 +406,8 @@ def main():
         "gpu_launches": st["kernels_per_step"] * a.steps,
         "clocks": clk,
     }
+    if prefill:
+        line["prefill"] = prefill
     if rank == 0 and world == 1 and not a.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(cfg, w, prompt, a.cpu_seconds)
     m.close()

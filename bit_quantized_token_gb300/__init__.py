@@ -27,7 +27,8 @@ STATUS = {0: "OK", -1: "INVALID_ARG", -2: "UNSUPPORTED", -3: "OOM", -4: "CTX_FUL
           -6: "TIMEOUT", -7: "NAN", -8: "NOT_FOUND"}
 
 # Every entry point include/llmq.h declares.
-EXPORTS = ["llm_model_create", "llm_model_destroy", "llm_prefill", "llm_decode_step", "llm_decode_greedy",
+EXPORTS = ["llm_model_create", "llm_model_destroy", "llm_prefill", "llm_prefill_batched", "llm_decode_step",
+           "llm_decode_greedy",
            "llm_decode_step_batch", "llm_kv_reset", "llm_kv_write", "llm_kv_read", "llm_kv_len",
            "llm_debug_hidden", "llm_debug_unpack", "llm_model_stats", "llm_profile_step", "llm_time_kernel", "llm_sync",
            "llm_last_error", "llm_op_matvec", "llm_matvec_noalloc"]
@@ -96,6 +97,7 @@ def lib() -> C.CDLL:
             "llm_model_create": (i32, [C.POINTER(Config), C.POINTER(Tensor), i32, P, C.POINTER(P)]),
             "llm_model_destroy": (None, [P]),
             "llm_prefill": (i32, [P, i32, P, i32, P, P]),
+            "llm_prefill_batched": (i32, [P, i32, P, i32, P, P]),
             "llm_decode_step": (i32, [P, i32, i32, P, P]),
             "llm_decode_greedy": (i32, [P, i32, i32, i32, P]),
             "llm_decode_step_batch": (i32, [P, P, i32, P, P]),
@@ -201,6 +203,12 @@ class Model:
     def prefill(self, seq: int, tokens, logits=None, argmax=None) -> None:
         toks = np.ascontiguousarray(tokens, np.int32)
         _check(lib().llm_prefill(self.h, seq, toks.ctypes.data, toks.size, _ptr(logits), _ptr(argmax)), self.h)
+
+    def prefill_batched(self, seq: int, tokens, logits=None, argmax=None) -> None:
+        """llm_prefill's contract, processed in chunks of up to 32 tokens."""
+        toks = np.ascontiguousarray(tokens, np.int32)
+        _check(lib().llm_prefill_batched(self.h, seq, toks.ctypes.data, toks.size, _ptr(logits), _ptr(argmax)),
+               self.h)
 
     def decode_step(self, seq: int, token: int, logits=None, argmax=None) -> None:
         _check(lib().llm_decode_step(self.h, seq, int(token), _ptr(logits), _ptr(argmax)), self.h)

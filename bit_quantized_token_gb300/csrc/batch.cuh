@@ -471,13 +471,18 @@ __global__ void __launch_bounds__(256) bembed_kernel(const BEmbedParams p) {
 }
 
 // Flash-decoding attention of every sequence of the batch: grid (split, kv head, sequence).
+enum BAttnMode : int { BA_APPEND_ATTEND = 0, BA_APPEND = 1, BA_ATTEND = 2 };
+
 struct BAttnParams {
   AttnParams a;           // per-sequence fields are offset below
   const float* qkv;       // [M][q_dim + 2 kv_dim]
   int qkv_cols, o_cols;
-  const int* pos;         // [M]
+  const int* pos;         // [M] position of each row's token
+  const int* seq;         // [M] cache (sequence) of each row, or null: row b uses cache b
+  int mode;               // BA_APPEND_ATTEND; or, for several rows of one sequence (a prompt
+                          // chunk), BA_APPEND for all rows, then BA_ATTEND over the cache
   size_t seq_kv_stride;   // cache elements per sequence
-  size_t part_stride;     // attention partial floats per sequence
+  size_t part_stride;     // attention partial floats per row
 };
 
 __device__ __forceinline__ void cp_async16(void* dst, const void* src) {
@@ -486,7 +491,7 @@ __device__ __forceinline__ void cp_async16(void* dst, const void* src) {
 __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
 
 constexpr int kBAttnThreads = 256;
-constexpr int kBAttnPP = 128;  // cache positions per pass
+constexpr int kBAttnPP = 64;  // cache positions per pass (~42 KB of tiles: 4 CTAs per SM)
 
 // Shared memory of one batched attention item (sequence, kv head, split).
 template <int GQ, int HD>
@@ -502,14 +507,15 @@ struct BAttnSmem {
 };
 
 // Flash-decoding attention of every sequence of the batch on the tensor
-// cores: grid (split, kv head, sequence), 8 warps; warp w scores all GQ heads
-// against positions 16w .. 16w+15 of the pass (attn_mma.cuh). The last split
-// of a (sequence, kv head) to finish merges the splits into the output row.
+// cores: grid (split, kv head, sequence), 8 warps that stage the pass's K/V
+// rows together; warp w < PP/16 scores all GQ heads against positions
+// 16w .. 16w+15 (attn_mma.cuh). The last split of a (sequence, kv head) to
+// finish merges the splits into the output row.
 template <int GQ, int HD>
 __global__ void __launch_bounds__(kBAttnThreads) battn_mma_kernel(const BAttnParams bp) {
   using SA = BAttnSmem<GQ, HD>;
   constexpr int NT = kBAttnThreads, PP = SA::PP, RS = SA::RS, CH = HD / 8, DPL = HD / 32;
-  static_assert(GQ <= 8 && SA::NBW == NT / 32, "layout");
+  static_assert(GQ <= 8 && SA::NBW <= NT / 32, "layout");
   extern __shared__ __align__(16) uint8_t smraw[];
   SA& sa = *reinterpret_cast<SA*>(smraw);
   pdl_trigger();
@@ -527,8 +533,11 @@ __global__ void __launch_bounds__(kBAttnThreads) battn_mma_kernel(const BAttnPar
   const int P_eff = min(min(a.P, PMAX), (len + PP - 1) / PP);
   if (split >= P_eff) return;
   const int t0 = (int)((int64_t)len * split / P_eff), t1 = (int)((int64_t)len * (split + 1) / P_eff);
-  uint16_t* kc = a.kc + (size_t)b * bp.seq_kv_stride + (size_t)g * a.cap * HD;
-  uint16_t* vc = a.vc + (size_t)b * bp.seq_kv_stride + (size_t)g * a.cap * HD;
+  const int sb = bp.seq ? bp.seq[b] : b;  // this row's cache
+  uint16_t* kc = a.kc + (size_t)sb * bp.seq_kv_stride + (size_t)g * a.cap * HD;
+  uint16_t* vc = a.vc + (size_t)sb * bp.seq_kv_stride + (size_t)g * a.cap * HD;
+  const bool attend = bp.mode != BA_APPEND;
+  const bool append = bp.mode == BA_APPEND || (bp.mode == BA_APPEND_ATTEND && split == P_eff - 1);
   const float* qkv = bp.qkv + (size_t)b * bp.qkv_cols;
 
   // rows tp .. tp+n-1 of K and V -> tiles (async copies; zero rows up to the
@@ -561,7 +570,7 @@ __global__ void __launch_bounds__(kBAttnThreads) battn_mma_kernel(const BAttnPar
       }
     }
   };
-  stage(t0);
+  if (attend) stage(t0);
   // q heads, k, v of this kv head; RoPE factors and q/k norm weights
   for (int i = tid; i < (GQ + 2) * HD; i += NT) {
     const int r = i / HD, d = i % HD;
@@ -578,7 +587,7 @@ __global__ void __launch_bounds__(kBAttnThreads) battn_mma_kernel(const BAttnPar
       const int h = warp + 8 * k2;
       wn[k2][e] = (a.q_norm && h <= GQ) ? __ldg((h < GQ ? a.q_norm : a.k_norm) + lane + 32 * e) : 1.f;
     }
-  convert(t0);
+  if (attend) convert(t0);
   __syncthreads();
   if (a.q_norm) {  // per-head RMSNorm of the q heads and k
 #pragma unroll
@@ -604,15 +613,13 @@ __global__ void __launch_bounds__(kBAttnThreads) battn_mma_kernel(const BAttnPar
   // RoPE of q and k; q scaled by log2(e)/sqrt(hd); k, v rounded to bf16 (the
   // split owning `pos` appends them and puts them into its tile)
   const float qscale = 1.4426950408889634f / sqrtf((float)HD);
-  const bool owner = split == P_eff - 1 && pos - t0 < PP;
+  const bool owner = attend && split == P_eff - 1 && pos - t0 < PP;
   auto keep = [&](int r, int d, float x) {
     const __nv_bfloat16 h = __float2bfloat16_rn(x);
     const float xr = __bfloat162float(h);
     sa.cur[r][d] = xr;
-    if (split == P_eff - 1) {
-      (r == GQ ? kc : vc)[(size_t)pos * HD + d] = __bfloat16_as_ushort(h);
-      if (owner) (r == GQ ? sa.kt : sa.vt)[pos - t0][d] = __half_as_ushort(__float2half_rn(xr));
-    }
+    if (append) (r == GQ ? kc : vc)[(size_t)pos * HD + d] = __bfloat16_as_ushort(h);
+    if (owner) (r == GQ ? sa.kt : sa.vt)[pos - t0][d] = __half_as_ushort(__float2half_rn(xr));
   };
   for (int j = tid; j < nrope + HD; j += NT) {  // RoPE pairs of the q heads and k, then v elements
     if (j < nrope) {
@@ -633,6 +640,7 @@ __global__ void __launch_bounds__(kBAttnThreads) battn_mma_kernel(const BAttnPar
       keep(GQ + 1, j - nrope, sa.cur[GQ + 1][j - nrope]);
     }
   }
+  if (!attend) return;  // the rows' k, v are in the cache
   for (int i = tid; i < GQ * HD; i += NT) sa.acc[i / HD][i % HD] = 0.f;
   if (tid < GQ) {
     sa.accm[tid] = -INFINITY;
@@ -658,36 +666,48 @@ __global__ void __launch_bounds__(kBAttnThreads) battn_mma_kernel(const BAttnPar
       attn_block16<GQ, HD, RS>(&sa.cur[0][0], &sa.kt[0][0], &sa.vt[0][0], 16 * warp, n - 16 * warp, lane,
                                &sa.tres[warp][0][0], HD + 2);
     __syncthreads();
+    // fold the pass into the running output. Warp h < GQ finds head h's
+    // factors, lane w < nb for block w: new max, 2^(m_w - M), sum update
+    if (warp < GQ) {
+      const int h = warp;
+      const float am = sa.accm[h], al = sa.accl[h];
+      const float mw = lane < nb ? sa.tres[lane][h][HD] : -INFINITY;
+      const float lw = lane < nb ? sa.tres[lane][h][HD + 1] : 0.f;
+      float M = fmaxf(mw, am);
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+      const float f = lane < nb ? exp2f(mw - M) : 0.f;
+      float L = lw * f;
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) L += __shfl_xor_sync(0xffffffffu, L, o);
+      const float fa = am == -INFINITY ? 0.f : exp2f(am - M);
+      __syncwarp();
+      if (lane < SA::NBW) sa.fac[h][1 + lane] = f;
+      if (lane == 0) {
+        sa.fac[h][0] = fa;
+        sa.accm[h] = M;
+        sa.accl[h] = al * fa + L;
+      }
+    }
+    __syncthreads();
     const bool last_pass = tp + PP >= t1;
-    // merge the pass's blocks with the running output (into the split's partial on the last pass)
     for (int i = tid; i < GQ * HD; i += NT) {
       const int h = i / HD, d = i % HD;
-      float M = sa.accm[h];
-      for (int w = 0; w < nb; ++w) M = fmaxf(M, sa.tres[w][h][HD]);
-      const float fa = sa.accm[h] == -INFINITY ? 0.f : exp2f(sa.accm[h] - M);
-      float O = sa.acc[h][d] * fa, L = sa.accl[h] * fa;
-      for (int w = 0; w < nb; ++w) {
-        const float f = exp2f(sa.tres[w][h][HD] - M);
-        O += sa.tres[w][h][d] * f;
-        L += sa.tres[w][h][HD + 1] * f;
-      }
-      if (last_pass) {
+      float O = sa.acc[h][d] * sa.fac[h][0];
+#pragma unroll
+      for (int w = 0; w < SA::NBW; ++w)
+        if (w < nb) O += sa.tres[w][h][d] * sa.fac[h][1 + w];
+      if (last_pass) {  // the split's partial: o, max, sum
         gpart[h * (HD + 2) + d] = O;
         if (d == 0) {
-          gpart[h * (HD + 2) + HD] = M;
-          gpart[h * (HD + 2) + HD + 1] = L;
+          gpart[h * (HD + 2) + HD] = sa.accm[h];
+          gpart[h * (HD + 2) + HD + 1] = sa.accl[h];
         }
       } else {
         sa.acc[h][d] = O;
-        if (d == 0) sa.fac[h][0] = M, sa.fac[h][1] = L;  // new running max / sum, published below
       }
     }
-    __syncthreads();
-    if (!last_pass && tid < GQ) {
-      sa.accm[tid] = sa.fac[tid][0];
-      sa.accl[tid] = sa.fac[tid][1];
-    }
-    __syncthreads();
+    // the next pass writes its tiles and blocks after the barriers of its staging
   }
   // ---- the last split of this (sequence, kv head) merges the splits (no waiting)
   int* counter = a.counter + (size_t)b * a.Hkv + g;

@@ -236,6 +236,9 @@ struct llm_model {
   size_t bsmem_max = 0;
   // persistent step kernel
   bool use_step = false;
+  int step_R = 1;                             // input ranges of the persistent step's GEMVs
+  int step_fuse_len = 0;                      // cache lengths the step's o-projection builds attend over itself
+  float* d_step_ss = nullptr;                 // [phases][4] per-range sums of squares
   bool step_eager = false;
   Phase* d_phases = nullptr;
   int n_phases = 0;
@@ -244,6 +247,8 @@ struct llm_model {
   // per-sequence state
   int *d_pos = nullptr, *d_tok = nullptr, *d_argmax = nullptr, *d_hist = nullptr, *d_hist_ctr = nullptr,
       *d_status = nullptr, *d_prompt = nullptr;
+  int* d_pf = nullptr;                        // batched prefill: [tok | pos | seq][pf_cap], then [2][kBM] scratch
+  size_t pf_cap = 0;
   int* h_stage = nullptr;                     // pinned staging
   std::vector<int> len;
   std::vector<cudaGraphExec_t> graphs;
@@ -502,7 +507,7 @@ int kind_of(const llm_model* m, int which) {
 
 // The persistent step kernel for the model's (GQA group, head_dim).
 template <int GQ, int HD>
-cudaError_t launch_step_t(const llm_model* m, const StepParams& sp) {
+cudaError_t launch_step_t(const llm_model* m, const StepParams& sp, bool fused) {
   cudaLaunchConfig_t cfg{};
   cfg.gridDim = dim3(m->n_sm);
   cfg.blockDim = dim3(kSThreads);
@@ -513,23 +518,29 @@ cudaError_t launch_step_t(const llm_model* m, const StepParams& sp) {
   attr[0].val.cooperative = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, step_kernel<GQ, HD>, sp);
+  if (fused) return cudaLaunchKernelEx(&cfg, step_kernel<GQ, HD, true>, sp);
+  return cudaLaunchKernelEx(&cfg, step_kernel<GQ, HD, false>, sp);
 }
 
 bool step_supported(int gq, int hd) { return (gq == 2 && hd == 64) || (gq == 8 && hd == 64) || (gq == 2 && hd == 128); }
 
 template <typename F>
-cudaError_t with_step_kernel(int gq, int hd, F f) {
-  if (gq == 2 && hd == 64) return f(step_kernel<2, 64>, step_smem_bytes<2, 64>());
-  if (gq == 8 && hd == 64) return f(step_kernel<8, 64>, step_smem_bytes<8, 64>());
-  return f(step_kernel<2, 128>, step_smem_bytes<2, 128>());
+cudaError_t with_step_kernel(int gq, int hd, bool fused, F f) {
+  if (gq == 2 && hd == 64) return fused ? f(step_kernel<2, 64, true>, step_smem_bytes<2, 64>())
+                                        : f(step_kernel<2, 64, false>, step_smem_bytes<2, 64>());
+  if (gq == 8 && hd == 64) return fused ? f(step_kernel<8, 64, true>, step_smem_bytes<8, 64>())
+                                        : f(step_kernel<8, 64, false>, step_smem_bytes<8, 64>());
+  return fused ? f(step_kernel<2, 128, true>, step_smem_bytes<2, 128>())
+               : f(step_kernel<2, 128, false>, step_smem_bytes<2, 128>());
 }
 
-cudaError_t enqueue_persistent_step(llm_model* m, int seq) {
+cudaError_t enqueue_persistent_step(llm_model* m, int seq, bool fused) {
   const llm_config& c = m->cfg;
   StepParams sp{};
   sp.phases = m->d_phases;
   sp.n_phases = m->n_phases;
+  sp.R = m->step_R;
+  sp.dim = c.dim;
   sp.sync = m->d_step_sync;
   sp.status = m->d_status;
   sp.embed = m->d_embed;
@@ -564,14 +575,14 @@ cudaError_t enqueue_persistent_step(llm_model* m, int seq) {
   cudaError_t e = cudaMemsetAsync(m->d_step_sync, 0, 2 * sizeof(int), m->stream);
   if (e != cudaSuccess) return e;
   const int gq = m->gq, hd = c.head_dim;
-  if (gq == 2 && hd == 64) return launch_step_t<2, 64>(m, sp);
-  if (gq == 8 && hd == 64) return launch_step_t<8, 64>(m, sp);
-  return launch_step_t<2, 128>(m, sp);
+  if (gq == 2 && hd == 64) return launch_step_t<2, 64>(m, sp, fused);
+  if (gq == 8 && hd == 64) return launch_step_t<8, 64>(m, sp, fused);
+  return launch_step_t<2, 128>(m, sp, fused);
 }
 
 template <int GQ, int HD>
-cudaError_t launch_battn_t(const llm_model* m, const BAttnParams& b, bool pdl) {
-  return launch(battn_mma_kernel<GQ, HD>, dim3(m->attn_P, m->cfg.n_kv_heads, m->cfg.max_batch), dim3(kBAttnThreads),
+cudaError_t launch_battn_t(const llm_model* m, const BAttnParams& b, int splits, int rows, bool pdl) {
+  return launch(battn_mma_kernel<GQ, HD>, dim3(splits, m->cfg.n_kv_heads, rows), dim3(kBAttnThreads),
                 sizeof(BAttnSmem<GQ, HD>), m->stream, pdl, b);
 }
 template <int GQ, int HD>
@@ -593,21 +604,21 @@ cudaError_t battn_set_smem(int gq, int hd) {
   return cudaErrorInvalidValue;
 }
 
-cudaError_t launch_battn(const llm_model* m, const BAttnParams& b, bool pdl) {
+cudaError_t launch_battn(const llm_model* m, const BAttnParams& b, int splits, int rows, bool pdl) {
   switch (m->gq * 1000 + m->cfg.head_dim) {
-    case 1064: return launch_battn_t<1, 64>(m, b, pdl);
-    case 2064: return launch_battn_t<2, 64>(m, b, pdl);
-    case 4064: return launch_battn_t<4, 64>(m, b, pdl);
-    case 8064: return launch_battn_t<8, 64>(m, b, pdl);
-    case 1128: return launch_battn_t<1, 128>(m, b, pdl);
-    case 2128: return launch_battn_t<2, 128>(m, b, pdl);
-    case 4128: return launch_battn_t<4, 128>(m, b, pdl);
-    case 8128: return launch_battn_t<8, 128>(m, b, pdl);
+    case 1064: return launch_battn_t<1, 64>(m, b, splits, rows, pdl);
+    case 2064: return launch_battn_t<2, 64>(m, b, splits, rows, pdl);
+    case 4064: return launch_battn_t<4, 64>(m, b, splits, rows, pdl);
+    case 8064: return launch_battn_t<8, 64>(m, b, splits, rows, pdl);
+    case 1128: return launch_battn_t<1, 128>(m, b, splits, rows, pdl);
+    case 2128: return launch_battn_t<2, 128>(m, b, splits, rows, pdl);
+    case 4128: return launch_battn_t<4, 128>(m, b, splits, rows, pdl);
+    case 8128: return launch_battn_t<8, 128>(m, b, splits, rows, pdl);
   }
   return cudaErrorInvalidValue;
 }
 
-BGemvParams bgemv_params(const llm_model* m, const BPlan& b) {
+BGemvParams bgemv_params(const llm_model* m, const BPlan& b, int M) {
   BGemvParams p{};
   p.units = m->d_arena + b.m.off;
   p.n_rt = b.m.n_rt;
@@ -617,7 +628,7 @@ BGemvParams bgemv_params(const llm_model* m, const BPlan& b) {
   p.bf16 = b.m.bf16;
   p.unit_bytes = b.m.unit_bytes();
   p.epu = b.m.bf16 ? kBF16UnitCols : 64;
-  p.M = m->cfg.max_batch;
+  p.M = M;
   p.rtb = b.rtb;
   p.kc = b.kc;
   p.ks = b.ks;
@@ -634,10 +645,35 @@ cudaError_t launch_bgemv(const llm_model* m, const BPlan& b, const BGemvParams& 
   return launch(bgemv_kernel<false>, grid, dim3(kBThreads), b.smem, m->stream, pdl, p);
 }
 
-// Enqueue one decode step of every sequence (0..max_batch-1) on m->stream.
-cudaError_t enqueue_batch_step(llm_model* m) {
+// Rows of one pass of the batched pipeline: one token per row.
+struct BatchedIO {
+  int M;                 // rows (tokens), at most kBM
+  const int* tok;        // [M] device tokens
+  int* pos;              // [M] device positions (the LM head's greedy epilogue advances them)
+  const int* seq;        // [M] cache of each row, or null: row b is sequence b
+  bool chunk;            // rows are consecutive tokens of one sequence (a prompt chunk)
+  bool lm;               // run the LM head with its greedy choice
+  int* tok_io;           // [M] greedy choice fed back as the next token
+  int* argmax_out;       // [M]
+};
+
+BatchedIO decode_io(llm_model* m) {
+  BatchedIO io{};
+  io.M = m->cfg.max_batch;
+  io.tok = m->d_tok;
+  io.pos = m->d_pos;
+  io.lm = true;
+  io.tok_io = m->d_tok;
+  io.argmax_out = m->d_argmax;
+  return io;
+}
+
+// Enqueue one pass of the batched pipeline on m->stream: a decode step of
+// every sequence, or a chunk of a prompt (all rows append their k, v first,
+// then attend causally over the cache).
+cudaError_t enqueue_batched(llm_model* m, const BatchedIO& io) {
   const llm_config& c = m->cfg;
-  const int L = c.n_layers, d = c.dim, B = c.max_batch, F = c.ffn_dim;
+  const int L = c.n_layers, d = c.dim, B = io.M, F = c.ffn_dim;
   const bool pdl = !(c.flags & LLM_NO_PDL);
   cudaError_t e;
   BEmbedParams ep{};
@@ -646,7 +682,7 @@ cudaError_t enqueue_batch_step(llm_model* m) {
   ep.dim = d;
   ep.vocab = c.vocab;
   ep.M = B;
-  ep.tok = m->d_tok;
+  ep.tok = io.tok;
   ep.x = m->d_bx;
   ep.ss_out = m->d_bss_x;
   ep.status = m->d_status;
@@ -654,7 +690,7 @@ cudaError_t enqueue_batch_step(llm_model* m) {
   const size_t kv_layer = (size_t)c.n_kv_heads * c.max_seq * c.head_dim;
   const int qkv_cols = m->q_dim + 2 * m->kv_dim;
   for (int l = 0; l < L; ++l) {
-    BGemvParams p = bgemv_params(m, m->bqkv[l]);
+    BGemvParams p = bgemv_params(m, m->bqkv[l], B);
     p.x = m->d_bx;
     p.norm_w = m->d_norms + m->off_attn_norm[l];
     p.ss_in = m->d_bss_x;
@@ -683,11 +719,19 @@ cudaError_t enqueue_batch_step(llm_model* m) {
     bp.qkv = m->d_bqkv;
     bp.qkv_cols = qkv_cols;
     bp.o_cols = m->q_dim;
-    bp.pos = m->d_pos;
+    bp.pos = io.pos;
+    bp.seq = io.seq;
     bp.seq_kv_stride = (size_t)L * kv_layer;
     bp.part_stride = (size_t)c.n_kv_heads * m->attn_P * m->gq * (c.head_dim + 2);
-    if ((e = launch_battn(m, bp, pdl)) != cudaSuccess) return e;
-    p = bgemv_params(m, m->bwo[l]);  // h = x + Wo o
+    if (io.chunk) {
+      bp.mode = BA_APPEND;
+      if ((e = launch_battn(m, bp, 1, B, pdl)) != cudaSuccess) return e;
+      bp.mode = BA_ATTEND;
+    } else {
+      bp.mode = BA_APPEND_ATTEND;
+    }
+    if ((e = launch_battn(m, bp, m->attn_P, B, pdl)) != cudaSuccess) return e;
+    p = bgemv_params(m, m->bwo[l], B);  // h = x + Wo o
     p.x = m->d_bo;
     p.epi = EPI_RESID;
     p.resid = m->d_bx;
@@ -695,7 +739,7 @@ cudaError_t enqueue_batch_step(llm_model* m) {
     p.out = m->d_bh;
     p.out_cols = d;
     if ((e = launch_bgemv(m, m->bwo[l], p, pdl)) != cudaSuccess) return e;
-    p = bgemv_params(m, m->bgu[l]);  // a = silu(Wg rmsnorm(h)) * (Wu rmsnorm(h))
+    p = bgemv_params(m, m->bgu[l], B);  // a = silu(Wg rmsnorm(h)) * (Wu rmsnorm(h))
     p.x = m->d_bh;
     p.norm_w = m->d_norms + m->off_ffn_norm[l];
     p.ss_in = m->d_bss_h;
@@ -704,7 +748,7 @@ cudaError_t enqueue_batch_step(llm_model* m) {
     p.out = m->d_ba;
     p.out_cols = F;
     if ((e = launch_bgemv(m, m->bgu[l], p, pdl)) != cudaSuccess) return e;
-    p = bgemv_params(m, m->bdown[l]);  // x = h + Wd a
+    p = bgemv_params(m, m->bdown[l], B);  // x = h + Wd a
     p.x = m->d_ba;
     p.epi = EPI_RESID;
     p.resid = m->d_bh;
@@ -713,7 +757,8 @@ cudaError_t enqueue_batch_step(llm_model* m) {
     p.out_cols = d;
     if ((e = launch_bgemv(m, m->bdown[l], p, pdl)) != cudaSuccess) return e;
   }
-  BGemvParams p = bgemv_params(m, m->blm);  // logits, greedy choice per sequence, positions += 1
+  if (!io.lm) return cudaSuccess;
+  BGemvParams p = bgemv_params(m, m->blm, B);  // logits, greedy choice per sequence, positions += 1
   p.x = m->d_bx;
   p.norm_w = m->d_norms + m->off_final_norm;
   p.ss_in = m->d_bss_x;
@@ -724,15 +769,15 @@ cudaError_t enqueue_batch_step(llm_model* m) {
   p.cand_v = m->d_bcand_v;
   p.cand_i = m->d_bcand_i;
   p.gcounter = m->d_bgreedy_cnt;
-  p.tok_io = m->d_tok;
-  p.argmax_out = m->d_argmax;
-  p.pos = m->d_pos;
+  p.tok_io = io.tok_io;
+  p.argmax_out = io.argmax_out;
+  p.pos = io.pos;
   return launch_bgemv(m, m->blm, p, pdl);
 }
 
 // Enqueue one batch-1 decode step of sequence `seq` on m->stream.
-cudaError_t enqueue_step(llm_model* m, int seq, Prof* prof = nullptr) {
-  if (m->use_step && !prof) return enqueue_persistent_step(m, seq);
+cudaError_t enqueue_step(llm_model* m, int seq, Prof* prof = nullptr, bool fused = false) {
+  if (m->use_step && !prof) return enqueue_persistent_step(m, seq, fused);
   const int L = m->cfg.n_layers;
   const bool pdl = !(m->cfg.flags & LLM_NO_PDL) && !prof;
   cudaError_t e;
@@ -768,27 +813,27 @@ int check_status(llm_model* m) {
   return set_err(m, LLM_ERR_INVALID_ARG, "token id out of range on the device");
 }
 
-int run_step(llm_model* m, int seq) {
+// One step of sequence seq for the token at position `pos` (known on the
+// host: it picks the persistent step's variant for that cache length).
+int run_step(llm_model* m, int seq, int pos) {
+  const bool fused = m->use_step && pos + 1 <= m->step_fuse_len;
   const bool graph = !(m->cfg.flags & LLM_NO_GRAPH);
-  if (!graph) {
-    CK(enqueue_step(m, seq), "step launch");
+  if (!graph || m->step_eager) {  // (the persistent step is two operations: launch them directly)
+    CK(enqueue_step(m, seq, nullptr, fused), "step launch");
     return LLM_OK;
   }
-  if (m->step_eager) {  // the persistent step is two operations: launch them directly
-    CK(enqueue_step(m, seq), "step launch");
-    return LLM_OK;
-  }
-  if (!m->graphs[seq]) {
+  cudaGraphExec_t& slot = m->graphs[2 * seq + (fused ? 1 : 0)];
+  if (!slot) {
     cudaGraph_t g = nullptr;
     CK(cudaStreamBeginCapture(m->stream, cudaStreamCaptureModeThreadLocal), "begin capture");
-    cudaError_t e = enqueue_step(m, seq);
+    cudaError_t e = enqueue_step(m, seq, nullptr, fused);
     cudaError_t e2 = cudaStreamEndCapture(m->stream, &g);
     if (m->use_step && (e != cudaSuccess || e2 != cudaSuccess)) {
       // a cooperative launch that this driver does not capture: run the step eagerly
       cudaGetLastError();
       if (g) cudaGraphDestroy(g);
       m->step_eager = true;
-      CK(enqueue_step(m, seq), "step launch");
+      CK(enqueue_step(m, seq, nullptr, fused), "step launch");
       return LLM_OK;
     }
     if (e != cudaSuccess) return cuda_fail(m, e, "step capture");
@@ -797,9 +842,9 @@ int run_step(llm_model* m, int seq) {
     e = cudaGraphInstantiate(&ge, g, 0);
     cudaGraphDestroy(g);
     if (e != cudaSuccess) return cuda_fail(m, e, "graph instantiate");
-    m->graphs[seq] = ge;
+    slot = ge;
   }
-  CK(cudaGraphLaunch(m->graphs[seq], m->stream), "graph launch");
+  CK(cudaGraphLaunch(slot, m->stream), "graph launch");
   return LLM_OK;
 }
 
@@ -1027,7 +1072,27 @@ int llm_model_create(const llm_config* cfg, const llm_tensor* tensors, int32_t n
   }
   m->lm = plan_gemv(m->mats[mi_lm], m->n_sm);
   // split-row-tile partials: one region per GEMV kind (QKV, WO, GU, DOWN, LM)
-  auto part_floats = [](const GemvPlan& g) { return (size_t)g.m.n_rt * g.part.S * kTileRows; };
+  // input ranges of the persistent step: 4 (else 2, else 1) equal ranges of
+  // whole 64-input groups, whole heads of the attention output, and at least
+  // 4 groups per range (a reduction window of the step spans at most 6 row tiles)
+  m->step_R = 1;
+  for (int R : {4, 2}) {
+    auto ok = [&](int K) { return K % (64 * R) == 0 && K / R >= 256; };
+    if (ok(d) && ok(m->q_dim) && ok(F) && (m->q_dim / R) % hd == 0 && m->n_sm >= R) {
+      m->step_R = R;
+      break;
+    }
+  }
+  // Up to 4 passes over the cache, every CTA computes the attention of the kv
+  // head of its o-projection range itself when that range is exactly one kv
+  // head (its CTAs would otherwise run several items one after another);
+  // otherwise, and for longer caches, the attention phase spreads the items.
+  {
+    const int hpr = c.n_kv_heads / m->step_R;
+    m->step_fuse_len = (c.n_kv_heads % m->step_R == 0 && hpr == 1 && gq * hd <= kSFuseOut) ? 4 * step_attn_pp(hd) : 0;
+  }
+  // slots per row tile: the per-kernel path's split count or the step's ranges
+  auto part_floats = [&](const GemvPlan& g) { return (size_t)g.m.n_rt * std::max(g.part.S, m->step_R) * kTileRows; };
   size_t pf[5] = {0, 0, 0, 0, part_floats(m->lm)};
   int nrt[5] = {0, 0, 0, 0, m->lm.m.n_rt};
   for (int l = 0; l < L; ++l) {
@@ -1073,9 +1138,11 @@ int llm_model_create(const llm_config* cfg, const llm_tensor* tensors, int32_t n
   AL(m->d_cand_v, (size_t)std::max(m->lm.part.N, m->n_sm) * 4, "greedy candidates");
   AL(m->d_cand_i, (size_t)std::max(m->lm.part.N, m->n_sm) * 4, "greedy candidates");
   // ---- the persistent step: phase table (one for every sequence)
-  m->use_step = !(c.flags & LLM_MULTI_KERNEL) && step_supported(gq, hd) && d <= kSMaxDim;
-  if (m->use_step) {
-    with_step_kernel(gq, hd, [&](auto kern, size_t smem) {
+  m->use_step = !(c.flags & LLM_MULTI_KERNEL) && step_supported(gq, hd) && d <= kSMaxDim &&
+                std::min({d, m->q_dim, F}) >= 256;
+  for (bool fused : {false, true}) {
+    if (!m->use_step) break;
+    with_step_kernel(gq, hd, fused, [&](auto kern, size_t smem) {
       m->step_smem = smem;
       int per_sm = 0;
       cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
@@ -1098,10 +1165,14 @@ int llm_model_create(const llm_config* cfg, const llm_tensor* tensors, int32_t n
       ph.K = g.m.cols;
       ph.bf16 = g.m.bf16;
       ph.unit_bytes = g.m.unit_bytes();
-      ph.part = g.part;
+      ph.GR = g.m.G / m->step_R;
       ph.out_part = out_part;
       return ph;
     };
+    // per-range sums of squares: 4 floats per phase (entries beyond R stay zero)
+    const int n_ph = 5 * L + 2;
+    AL(m->d_step_ss, (size_t)n_ph * 4 * 4, "step sums of squares");
+    auto ssp = [&](int ph) { return m->d_step_ss + 4 * (size_t)ph; };
     for (int l = 0; l < L; ++l) {
       Phase q = gemv_phase(m->qkv[l], m->qkv[l].part_buf);
       q.layer = l;
@@ -1109,63 +1180,66 @@ int llm_model_create(const llm_config* cfg, const llm_tensor* tensors, int32_t n
         q.in_mode = m->embed_bf16 ? IN_EMBED_BF16 : IN_EMBED_F32;
       } else {
         q.in_mode = IN_RESID;
-        q.in_base = m->d_hbuf + (size_t)(l - 1) * d;
         q.in_part = m->down[l - 1].part_buf;
-        q.in_S = m->down[l - 1].part.S;
       }
       q.in_store = m->d_xbuf + (size_t)l * d;
       q.norm_w = m->d_norms + m->off_attn_norm[l];
+      q.ss_out = ssp(5 * l);
       phases.push_back(q);
       Phase a{};
       a.type = PH_ATTN;
       a.layer = l;
       a.qkv_part = m->qkv[l].part_buf;
-      a.qkv_S = m->qkv[l].part.S;
+      a.ss_in = ssp(5 * l);
       a.q_norm = c.qk_norm ? m->d_norms + m->off_q_norm[l] : nullptr;
       a.k_norm = c.qk_norm ? m->d_norms + m->off_k_norm[l] : nullptr;
       phases.push_back(a);
       Phase o = gemv_phase(m->wo[l], m->wo[l].part_buf);
       o.layer = l;
       o.in_mode = IN_ATTN;
+      // what the attention needs when the o-projection's build computes it
+      o.qkv_part = a.qkv_part;
+      o.ss_in = a.ss_in;
+      o.q_norm = a.q_norm;
+      o.k_norm = a.k_norm;
       phases.push_back(o);
       Phase gu = gemv_phase(m->gu[l], m->gu[l].part_buf);
       gu.layer = l;
       gu.in_mode = IN_RESID;
-      gu.in_base = m->d_xbuf + (size_t)l * d;
       gu.in_part = m->wo[l].part_buf;
-      gu.in_S = m->wo[l].part.S;
       gu.in_store = m->d_hbuf + (size_t)l * d;
       gu.norm_w = m->d_norms + m->off_ffn_norm[l];
+      gu.ss_out = ssp(5 * l + 3);
       phases.push_back(gu);
       Phase dn = gemv_phase(m->down[l], m->down[l].part_buf);
       dn.layer = l;
       dn.in_mode = IN_SWIGLU;
       dn.in_part = m->gu[l].part_buf;
-      dn.in_S = m->gu[l].part.S;
+      dn.ss_in = ssp(5 * l + 3);
       phases.push_back(dn);
     }
     Phase lmp = gemv_phase(m->lm, m->lm.part_buf);
     lmp.in_mode = IN_RESID;
-    lmp.in_base = m->d_hbuf + (size_t)(L - 1) * d;
     lmp.in_part = m->down[L - 1].part_buf;
-    lmp.in_S = m->down[L - 1].part.S;
     lmp.in_store = m->d_xbuf + (size_t)L * d;
     lmp.norm_w = m->d_norms + m->off_final_norm;
+    lmp.ss_out = ssp(5 * L);
     phases.push_back(lmp);
     Phase lg{};
     lg.type = PH_LOGITS;
     lg.lm_part = m->lm.part_buf;
-    lg.lm_S = m->lm.part.S;
+    lg.ss_in = ssp(5 * L);
     lg.vocab = V;
     phases.push_back(lg);
   }
   m->n_phases = (int)phases.size();
   AL(m->d_phases, phases.size() * sizeof(Phase), "phase table");
   AL(m->d_step_sync, 2 * sizeof(int), "step barrier");
-  // ---- the batched step (one token for every sequence)
+  // ---- the batched pipeline (one token for every sequence of a batch, or a
+  // chunk of up to kBM prompt tokens of one sequence)
   size_t bcnt_total = 0;
-  if (c.max_batch > 1) {
-    const int B = c.max_batch;
+  {
+    const int B = std::max(c.max_batch, kBM);  // rows
     size_t part_floats = 0;
     int max_blocks = 1;
     for (int l = 0; l < L; ++l) {
@@ -1206,6 +1280,11 @@ int llm_model_create(const llm_config* cfg, const llm_tensor* tensors, int32_t n
   AL(m->d_hist_ctr, 4, "history counter");
   AL(m->d_status, 4, "status");
   AL(m->d_prompt, (size_t)c.max_seq * 4, "prompt");
+  {
+    const size_t pf = ((size_t)c.max_seq + kBM - 1) / kBM * kBM;  // prompt rows, whole chunks
+    AL(m->d_pf, (3 * pf + 2 * kBM) * 4, "prompt chunk rows");
+    m->pf_cap = pf;
+  }
 #undef AL
   {
     cudaError_t e = cudaMallocHost(&m->h_stage, 64 * sizeof(int));
@@ -1234,6 +1313,7 @@ int llm_model_create(const llm_config* cfg, const llm_tensor* tensors, int32_t n
   }
   {
     cudaError_t e = cudaMemset(m->d_cnt, 0, cnt_total * 4);
+    if (e == cudaSuccess && m->d_step_ss) e = cudaMemset(m->d_step_ss, 0, (size_t)(5 * L + 2) * 16);
     for (int* z : {m->d_pos, m->d_tok, m->d_argmax})
       if (e == cudaSuccess) e = cudaMemset(z, 0, 4 * (size_t)c.max_batch);
     if (e == cudaSuccess) e = cudaMemset(m->d_hist_ctr, 0, 4);
@@ -1243,7 +1323,7 @@ int llm_model_create(const llm_config* cfg, const llm_tensor* tensors, int32_t n
       e = cudaFuncSetAttribute(bgemv_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)m->bsmem_max);
     if (e == cudaSuccess && m->bsmem_max)
       e = cudaFuncSetAttribute(bgemv_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)m->bsmem_max);
-    if (e == cudaSuccess && c.max_batch > 1) e = battn_set_smem(gq, hd);
+    if (e == cudaSuccess) e = battn_set_smem(gq, hd);
     if (e == cudaSuccess) e = cudaMemset(m->d_k, 0, kv_elems * 2);
     if (e == cudaSuccess) e = cudaMemset(m->d_v, 0, kv_elems * 2);
     size_t smax = m->lm.smem;
@@ -1257,7 +1337,7 @@ int llm_model_create(const llm_config* cfg, const llm_tensor* tensors, int32_t n
     if (e != cudaSuccess) return fail(cuda_fail(m, e, "initialisation"));
   }
   m->len.assign(c.max_batch, 0);
-  m->graphs.assign(c.max_batch, nullptr);
+  m->graphs.assign(2 * (size_t)c.max_batch, nullptr);  // per sequence: split, fused variant
   m->kernels_per_step = m->use_step ? 1 : 5 * L + 1;
   *out = m;
   return LLM_OK;
@@ -1271,7 +1351,7 @@ int llm_decode_step(llm_model* m, int32_t seq, int32_t token, float* logits_out,
   // pageable source: staged at call time, so back-to-back asynchronous calls cannot race
   const int32_t tok_host = token;
   CK(cudaMemcpyAsync(m->d_tok + seq, &tok_host, 4, cudaMemcpyHostToDevice, m->stream), "token upload");
-  if ((rc = run_step(m, seq)) != LLM_OK) return rc;
+  if ((rc = run_step(m, seq, m->len[seq])) != LLM_OK) return rc;
   m->len[seq] += 1;
   bool host = false;
   if ((rc = copy_out(m, logits_out, m->d_logits, (size_t)m->cfg.vocab * 4, &host)) != LLM_OK) return rc;
@@ -1293,13 +1373,54 @@ int llm_prefill(llm_model* m, int32_t seq, const int32_t* tokens, int32_t n, flo
   CK(cudaMemcpyAsync(m->d_prompt, host_toks.data(), (size_t)n * 4, cudaMemcpyHostToDevice, m->stream), "prompt upload");
   for (int i = 0; i < n; ++i) {
     CK(cudaMemcpyAsync(m->d_tok + seq, m->d_prompt + i, 4, cudaMemcpyDeviceToDevice, m->stream), "token copy");
-    if ((rc = run_step(m, seq)) != LLM_OK) return rc;
+    if ((rc = run_step(m, seq, m->len[seq] + i)) != LLM_OK) return rc;
   }
   m->len[seq] += n;
   bool host = false;
   if ((rc = copy_out(m, logits_out, m->d_logits, (size_t)m->cfg.vocab * 4, &host)) != LLM_OK) return rc;
   if ((rc = copy_out(m, argmax_out, m->d_argmax + seq, 4, &host)) != LLM_OK) return rc;
   CK(cudaStreamSynchronize(m->stream), "prefill sync");  // host_toks outlives the upload
+  return check_status(m);
+}
+
+int llm_prefill_batched(llm_model* m, int32_t seq, const int32_t* tokens, int32_t n, float* logits_out,
+                        int32_t* argmax_out) {
+  int rc = check_model(m, seq);
+  if (rc) return rc;
+  if (!tokens || n <= 0) return set_err(m, LLM_ERR_INVALID_ARG, "empty prompt");
+  if (m->len[seq] + n > m->cfg.max_seq) return set_err(m, LLM_ERR_CTX_FULL, "prompt would exceed max_seq");
+  std::vector<int32_t> rows(3 * m->pf_cap);  // [tok | pos | seq]
+  CK(cudaMemcpy(rows.data(), tokens, (size_t)n * 4, cudaMemcpyDefault), "prompt read");
+  for (int i = 0; i < n; ++i) {
+    if (rows[i] < 0 || rows[i] >= m->cfg.vocab) return set_err(m, LLM_ERR_INVALID_ARG, "prompt token out of range");
+    rows[m->pf_cap + i] = m->len[seq] + i;
+    rows[2 * m->pf_cap + i] = seq;
+  }
+  CK(cudaMemcpyAsync(m->d_pf, rows.data(), rows.size() * 4, cudaMemcpyHostToDevice, m->stream), "prompt rows upload");
+  int* scratch = m->d_pf + 3 * m->pf_cap;  // [kBM] greedy tokens, [kBM] argmax of the last chunk
+  int last_rows = 0;
+  for (int c0 = 0; c0 < n; c0 += kBM) {
+    BatchedIO io{};
+    io.M = std::min(kBM, n - c0);
+    io.tok = m->d_pf + c0;
+    io.pos = m->d_pf + m->pf_cap + c0;
+    io.seq = m->d_pf + 2 * m->pf_cap + c0;
+    io.chunk = true;
+    io.lm = c0 + io.M == n;  // logits of the prompt's last token only
+    io.tok_io = scratch;
+    io.argmax_out = scratch + kBM;
+    last_rows = io.M;
+    CK(enqueue_batched(m, io), "prompt chunk launch");
+  }
+  m->len[seq] += n;
+  const int32_t next_pos = m->len[seq];  // the decode steps' position counter (pageable: staged at call time)
+  CK(cudaMemcpyAsync(m->d_pos + seq, &next_pos, 4, cudaMemcpyHostToDevice, m->stream), "position update");
+  bool host = false;
+  if ((rc = copy_out(m, logits_out, m->d_blogits + (size_t)(last_rows - 1) * m->cfg.vocab,
+                     (size_t)m->cfg.vocab * 4, &host)) != LLM_OK)
+    return rc;
+  if ((rc = copy_out(m, argmax_out, scratch + kBM + last_rows - 1, 4, &host)) != LLM_OK) return rc;
+  CK(cudaStreamSynchronize(m->stream), "prefill sync");  // `rows` outlives the upload
   return check_status(m);
 }
 
@@ -1313,7 +1434,7 @@ int llm_decode_greedy(llm_model* m, int32_t seq, int32_t first_token, int32_t n_
   CK(cudaMemcpyAsync(m->d_tok + seq, &tok_host, 4, cudaMemcpyHostToDevice, m->stream), "token upload");
   CK(cudaMemsetAsync(m->d_hist_ctr, 0, 4, m->stream), "history reset");
   for (int i = 0; i < n_steps; ++i)
-    if ((rc = run_step(m, seq)) != LLM_OK) return rc;
+    if ((rc = run_step(m, seq, m->len[seq] + i)) != LLM_OK) return rc;
   m->len[seq] += n_steps;
   bool host = false;
   if ((rc = copy_out(m, tokens_out, m->d_hist, (size_t)n_steps * 4, &host)) != LLM_OK) return rc;
@@ -1339,12 +1460,12 @@ int llm_decode_step_batch(llm_model* m, const int32_t* tokens, int32_t n_seq, fl
        "token upload");
   }
   if (c.flags & LLM_NO_GRAPH) {
-    CK(enqueue_batch_step(m), "batched step launch");
+    CK(enqueue_batched(m, decode_io(m)), "batched step launch");
   } else {
     if (!m->bgraph) {
       cudaGraph_t g = nullptr;
       CK(cudaStreamBeginCapture(m->stream, cudaStreamCaptureModeThreadLocal), "begin capture");
-      cudaError_t e = enqueue_batch_step(m);
+      cudaError_t e = enqueue_batched(m, decode_io(m));
       cudaError_t e2 = cudaStreamEndCapture(m->stream, &g);
       if (e != cudaSuccess) return cuda_fail(m, e, "batched step capture");
       if (e2 != cudaSuccess) return cuda_fail(m, e2, "end capture");

@@ -10,12 +10,18 @@
 // shared-memory ring, so the weights of the next phases are already arriving
 // while the current phase finishes and the barrier resolves.
 //
-// Split-K across CTAs leaves one partial sum per CTA that touches a row tile
-// (S = 1, 2 or 4 slots per tile, unused slots zero); the next phase adds the
-// slots while it builds its input vector (residual add, SwiGLU, RMSNorm are
-// fused there), so no phase needs a fix-up of its own and no float atomics
-// are used. Every input build issues all of its loads before it uses any of
-// them: one L2 round trip per phase.
+// Split-K by input ranges: the K inputs of every GEMV are cut into R equal
+// ranges and the CTAs into R equal groups; a CTA of group r computes whole row
+// tiles over range r only, so it gathers just that range of its input vector
+// and every row tile ends with exactly one partial sum per range (R slots).
+// The next phase adds the slots while it builds its input (residual add,
+// SwiGLU, attention-split merge are fused there); no phase needs a fix-up of
+// its own and no float atomics are used. RMSNorm is linear in the GEMV
+// after the per-vector factor 1/rms, so a CTA multiplies its range by the
+// norm weight only and publishes the range's sum of squares; whoever reads
+// the GEMV's output adds the R sums and applies 1/rms there. Every input
+// build issues all of its loads before it uses any of them: one L2 round trip
+// per phase.
 //
 // Attention is flash-decoding over (kv head, split) items. An item loads its
 // K/V rows into padded shared-memory tiles in the same round trip as its q|k|v
@@ -39,10 +45,12 @@ constexpr int kSChunk = kSWarps;                 // units per ring slot: one per
 constexpr int kSSlot = kSChunk * kQ4UnitBytes;   // 17280 B (bf16 chunks use 15360 B)
 constexpr int kSNSlot = 8;
 constexpr int kSRing = kSNSlot * kSSlot;         // 138240 B
-constexpr int kSRLoc = 6;                        // row tiles a reduction window may touch
+constexpr int kSRLoc = 14;                       // row tiles a reduction window may touch
 constexpr int kSMaxV = (kMaxK / 4 + kSCThreads - 1) / kSCThreads;  // float4s of a K-vector per thread
 constexpr int kSDefer = 4;                       // splits the o-projection's input build merges
 constexpr int kSMaxDim = 4096;                   // widest residual stream (kept in shared memory)
+constexpr int kSFuseOut = 1024;                  // attention outputs a CTA computes for its o-projection range
+constexpr int kSMaxW = (kSMaxDim / 4 + kSCThreads - 1) / kSCThreads;  // float4s of a norm weight per thread
 
 // Cache positions staged per attention pass (the K/V tiles fill about 36 KB
 // resp. 52 KB of shared memory); a split is one pass unless the split count
@@ -60,29 +68,49 @@ struct Phase {
   int type;
   int layer;
   // ---- GEMV
-  const uint8_t* units;
+  const uint8_t* units;   // [n_rt][G] units
   int n_rt, G, K, bf16, unit_bytes;
-  Part part;
-  float* out_part;        // [n_rt][part.S][32], unused slots stay zero
+  int GR;                 // groups (units) of a row tile per input range: G / R
+  float* out_part;        // [n_rt][R][32]: slot r = the sum over input range r
   int in_mode;
-  const float* in_base;   // IN_PLAIN: the vector; IN_RESID: the residual base
-  const float* in_part;   // IN_RESID / IN_SWIGLU: partials of the previous GEMV
-  int in_S;               // 1, 2 or 4
-  float* in_store;        // CTA 0 stores the built (pre-norm) vector here, or null
+  const float* in_base;   // IN_PLAIN: the vector
+  const float* in_part;   // IN_RESID / IN_SWIGLU: partials of the previous GEMV ([tile][R][32])
+  float* in_store;        // the first CTA of each range stores its range of the built (pre-norm) vector, or null
   const float* norm_w;    // RMSNorm weight, or null
+  float* ss_out;          // [4]: sum of squares of the pre-norm input over range r (norm phases)
+  const float* ss_in;     // [4]: the sums of the GEMV whose output this phase reads (null: no norm)
   // ---- ATTN
   const float* qkv_part;
-  int qkv_S;
   const float* q_norm;
   const float* k_norm;
   // ---- LOGITS
   const float* lm_part;
-  int lm_S, vocab;
+  int vocab;
 };
+
+// The CTAs [floor(rN/R), floor((r+1)N/R)) serve input range r; CTA c of that
+// group takes the row tiles [n_rt (c-c0) / nr, n_rt (c-c0+1) / nr).
+struct KRange {
+  int r, c0, nr;
+  __host__ __device__ KRange(int c, int N, int R) {
+    r = ((c + 1) * R - 1) / N;
+    c0 = r * N / R;
+    nr = (r + 1) * N / R - c0;
+  }
+  __host__ __device__ int tile(int c, int n_rt) const { return (int)((unsigned)n_rt * (unsigned)(c - c0) / (unsigned)nr); }
+};
+
+// 1/rms of a vector of `dim` elements from the per-range sums of squares
+// (unused entries are zero), added in a fixed order.
+__device__ __forceinline__ float rms_inv(float4 ss, int dim, float eps) {
+  return 1.0f / sqrtf(((ss.x + ss.y) + (ss.z + ss.w)) / (float)dim + eps);
+}
 
 struct StepParams {
   const Phase* phases;
   int n_phases;
+  int R;                  // input ranges of every GEMV (1, 2 or 4); slots per row tile
+  int dim;                // residual width (RMSNorm mean)
   int* sync;              // [0] arrivals (phases x CTAs), [1] abort; zeroed before each launch
   int* status;
   const void* embed;
@@ -238,8 +266,10 @@ struct StepSmem {
       int last;
     } l;
   } u;
-  __align__(16) float xres[kSMaxDim];  // this CTA's copy of the residual stream (pre-norm)
+  __align__(16) float xres[kSMaxDim];  // this CTA's range of the residual stream (pre-norm)
+  float fo[kSFuseOut];                 // attention output of this CTA's o-projection range
   Phase ph[2];            // descriptors of the current and the next phase
+  int rt[2];              // this CTA's row tiles [rt[0], rt[1]) in the current GEMV phase
   float bred[kSWarps];
   int carry_rt[2];
   int flag;
@@ -248,10 +278,14 @@ struct StepSmem {
 };
 
 // ---------------------------------------------------------------------------
-// One (kv head g, split) attention item, run by the consumer warps.
+// One (kv head g, split) attention item, run by the consumer warps. `append`:
+// this item writes the step's k, v into the cache. With `fo` null the item
+// leaves its split's unnormalised partial (o, max, sum) in global memory;
+// otherwise (one split over the whole cache) it writes the normalised output
+// of its GQ heads to fo[h * HD + d] in shared memory.
 template <int GQ, int HD>
 __device__ void step_attn_item(const StepParams& sp, const Phase& P, int g, int split, int P_eff, int pos,
-                               StepAttnSmem<GQ, HD>& sa) {
+                               StepAttnSmem<GQ, HD>& sa, bool append, float* fo) {
   using SA = StepAttnSmem<GQ, HD>;
   constexpr int NT = kSCThreads, PP = SA::PP, RS = SA::RS, CH = HD / 8;
   constexpr int TB = (2 * PP * CH + NT - 1) / NT;  // 16-B tile loads per thread
@@ -264,7 +298,8 @@ __device__ void step_attn_item(const StepParams& sp, const Phase& P, int g, int 
   uint16_t* vc = sp.v_base + (size_t)P.layer * sp.layer_stride + (size_t)g * sp.cap * HD;
 
   // K/V rows tp .. tp+n-1 -> registers (zero beyond the split); stored into
-  // the padded tiles once the previous readers are done
+  // the padded tiles once the previous readers are done. Row `pos` is left to
+  // this step's k, v (another CTA may be appending it to the cache meanwhile).
   uint4 tl[TB];
   auto load_tile = [&](int tp) {
     const int n = min(PP, t1 - tp);
@@ -272,7 +307,7 @@ __device__ void step_attn_item(const StepParams& sp, const Phase& P, int g, int 
     for (int j = 0; j < TB; ++j) {
       const int idx = tid + j * NT, kv = idx / (PP * CH), rem = idx - kv * (PP * CH), row = rem / CH, ch = rem - row * CH;
       const float4 v = ldcg4_if(reinterpret_cast<const float*>((kv ? vc : kc) + (size_t)(tp + row) * HD + 8 * ch),
-                                kv < 2 && row < n);
+                                kv < 2 && row < n && tp + row != pos);
       tl[j] = make_uint4(__float_as_uint(v.x), __float_as_uint(v.y), __float_as_uint(v.z), __float_as_uint(v.w));
     }
   };
@@ -281,7 +316,7 @@ __device__ void step_attn_item(const StepParams& sp, const Phase& P, int g, int 
 #pragma unroll
     for (int j = 0; j < TB; ++j) {
       const int idx = tid + j * NT, kv = idx / (PP * CH), rem = idx - kv * (PP * CH), row = rem / CH, ch = rem - row * CH;
-      if (kv < 2 && row < rows)
+      if (kv < 2 && row < rows && tp + row != pos)
         *reinterpret_cast<uint4*>(&(kv ? sa.vt : sa.kt)[row][8 * ch]) =
             make_uint4(bf16x2_to_f16x2(tl[j].x), bf16x2_to_f16x2(tl[j].y), bf16x2_to_f16x2(tl[j].z),
                        bf16x2_to_f16x2(tl[j].w));
@@ -300,9 +335,11 @@ __device__ void step_attn_item(const StepParams& sp, const Phase& P, int g, int 
   for (int e = 0; e < DPL; ++e)
     wn[e] = (P.q_norm && warp <= GQ) ? __ldg((warp < GQ ? P.q_norm : P.k_norm) + lane + 32 * e) : 1.f;
 
-  // ---- gather q (GQ heads), k and v of this kv head from the QKV partials
+  // ---- gather q (GQ heads), k and v of this kv head from the QKV partials;
+  // the attention norm's 1/rms multiplies their sum
   {
-    const int lg = log2_slots(P.qkv_S);
+    const float4 ssv = ldcg4_if(P.ss_in, true);
+    const int lg = log2_slots(sp.R);
     const int nq = GQ * HD / 32, nk = HD / 32;
     const int qt0 = g * nq, kt0 = (sp.q_dim + g * HD) / 32, vt0 = (sp.q_dim + sp.kv_dim + g * HD) / 32;
     const int T4 = (nq + 2 * nk) << (3 + lg);
@@ -315,12 +352,14 @@ __device__ void step_attn_item(const StepParams& sp, const Phase& P, int g, int 
       const int tile = ti < nq ? qt0 + ti : (ti < nq + nk ? kt0 + ti - nq : vt0 + ti - nq - nk);
       a[j] = ldcg4_if(P.qkv_part + ((size_t)tile * (8 << lg) + (f & ((8 << lg) - 1))) * 4, f < T4);
     }
+    const float inv = rms_inv(ssv, sp.dim, sp.eps);
 #pragma unroll
     for (int j = 0; j < RB; ++j) {
       const float4 v = slot_sum(a[j], lg);
       const int f = tid + j * NT;
       if (f < T4 && ((f >> 3) & ((1 << lg) - 1)) == 0)
-        *reinterpret_cast<float4*>(&sa.cur[0][0] + (f >> (3 + lg)) * 32 + (f & 7) * 4) = v;
+        *reinterpret_cast<float4*>(&sa.cur[0][0] + (f >> (3 + lg)) * 32 + (f & 7) * 4) =
+            make_float4(v.x * inv, v.y * inv, v.z * inv, v.w * inv);
     }
   }
   store_tile(t0);
@@ -347,15 +386,13 @@ __device__ void step_attn_item(const StepParams& sp, const Phase& P, int g, int 
   // k; q is then scaled by log2(e)/sqrt(hd), k and v are rounded to bf16
   // (the split owning `pos` appends them and puts them into its tile)
   const float qscale = 1.4426950408889634f / sqrtf((float)HD);
-  const bool owner = split == P_eff - 1 && pos - t0 < PP;
+  const bool owner = t1 == len && pos - t0 < PP;  // the first pass's tile holds `pos`
   auto keep = [&](int r, int d, float x) {  // final value of cur[r][d], r >= GQ
     const __nv_bfloat16 b = __float2bfloat16_rn(x);
     const float xr = __bfloat162float(b);
     sa.cur[r][d] = xr;
-    if (split == P_eff - 1) {
-      (r == GQ ? kc : vc)[(size_t)pos * HD + d] = __bfloat16_as_ushort(b);
-      if (owner) (r == GQ ? sa.kt : sa.vt)[pos - t0][d] = __half_as_ushort(__float2half_rn(xr));
-    }
+    if (append) (r == GQ ? kc : vc)[(size_t)pos * HD + d] = __bfloat16_as_ushort(b);
+    if (owner) (r == GQ ? sa.kt : sa.vt)[pos - t0][d] = __half_as_ushort(__float2half_rn(xr));
   };
   if (tid < nrope) {
     const int h = tid / (HD / 2), i = tid % (HD / 2);
@@ -397,55 +434,58 @@ __device__ void step_attn_item(const StepParams& sp, const Phase& P, int g, int 
       attn_block16<GQ, HD, RS>(&sa.cur[0][0], &sa.kt[0][0], &sa.vt[0][0], 16 * warp, n - 16 * warp, lane,
                                &sa.tres[warp][0][0], HD + 2);
     ConsumerSync::sync();
-    const size_t pbase = ((size_t)g * sp.P + split) * GQ;
-    if (tp + PP >= t1) {
-      // last pass: merge its warps with the running output into the split's partial
-      for (int i = tid; i < GQ * HD; i += NT) {
-        const int h = i / HD, d = i % HD;
-        float M = sa.accm[h];
-        for (int w = 0; w < nb; ++w) M = fmaxf(M, sa.tres[w][h][HD]);
-        const float fa = sa.accm[h] == -INFINITY ? 0.f : exp2f(sa.accm[h] - M);
-        float O = sa.acc[h][d] * fa, L = sa.accl[h] * fa;
-        for (int w = 0; w < nb; ++w) {
-          const float f = exp2f(sa.tres[w][h][HD] - M);
-          O += sa.tres[w][h][d] * f;
-          L += sa.tres[w][h][HD + 1] * f;
-        }
-        sp.attn_o[pbase * HD + i] = O;
-        if (d == 0) {
-          sp.attn_ml[(pbase + h) * 2] = M;
-          sp.attn_ml[(pbase + h) * 2 + 1] = L;
-        }
+    // fold the pass into the running output. Warp h < GQ finds head h's
+    // factors, lane w < nb for block w: new max, 2^(m_w - M), sum update
+    if (warp < GQ) {
+      const int h = warp;
+      const float am = sa.accm[h], al = sa.accl[h];
+      const float mw = lane < nb ? sa.tres[lane][h][HD] : -INFINITY;
+      const float lw = lane < nb ? sa.tres[lane][h][HD + 1] : 0.f;
+      float M = fmaxf(mw, am);
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+      const float f = lane < nb ? exp2f(mw - M) : 0.f;
+      float L = lw * f;
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) L += __shfl_xor_sync(0xffffffffu, L, o);
+      const float fa = am == -INFINITY ? 0.f : exp2f(am - M);
+      __syncwarp();
+      if (lane < SA::NBW) sa.fac[h][1 + lane] = f;
+      if (lane == 0) {
+        sa.fac[h][0] = fa;
+        sa.accm[h] = M;
+        sa.accl[h] = al * fa + L;
       }
-      break;
-    }
-    // fold the pass into the running output
-    if (tid < GQ) {
-      const int h = tid;
-      float M = sa.accm[h];
-      for (int w = 0; w < nb; ++w) M = fmaxf(M, sa.tres[w][h][HD]);
-      const float fa = sa.accm[h] == -INFINITY ? 0.f : exp2f(sa.accm[h] - M);
-      float L = sa.accl[h] * fa;
-      sa.fac[h][0] = fa;
-      for (int w = 0; w < nb; ++w) {
-        const float f = exp2f(sa.tres[w][h][HD] - M);
-        sa.fac[h][1 + w] = f;
-        L += sa.tres[w][h][HD + 1] * f;
-      }
-      sa.accm[h] = M;
-      sa.accl[h] = L;
     }
     ConsumerSync::sync();
     for (int i = tid; i < GQ * HD; i += NT) {
       const int h = i / HD, d = i % HD;
       float O = sa.acc[h][d] * sa.fac[h][0];
-      for (int w = 0; w < nb; ++w) O += sa.tres[w][h][d] * sa.fac[h][1 + w];
+#pragma unroll
+      for (int w = 0; w < SA::NBW; ++w)
+        if (w < nb) O += sa.tres[w][h][d] * sa.fac[h][1 + w];
       sa.acc[h][d] = O;
     }
-    ConsumerSync::sync();
+    // the next pass writes its tiles and blocks after the barrier of its staging
   }
 
-  // ---- the split's partial is written (last pass above)
+  // ---- the output: every thread reads back the elements it folded
+  if (fo) {
+    for (int i = tid; i < GQ * HD; i += NT) fo[i] = sa.acc[i / HD][i % HD] / sa.accl[i / HD];
+    return;
+  }
+  {
+    const size_t pbase = ((size_t)g * sp.P + split) * GQ;
+    for (int i = tid; i < GQ * HD; i += NT) {
+      const int h = i / HD, d = i % HD;
+      sp.attn_o[pbase * HD + i] = sa.acc[h][d];
+      if (d == 0) {
+        sp.attn_ml[(pbase + h) * 2] = sa.accm[h];
+        sp.attn_ml[(pbase + h) * 2 + 1] = sa.accl[h];
+      }
+    }
+  }
+
   if (P_eff <= kSDefer) return;  // the o-projection's input build merges the splits
   // many splits: the last one of this kv head merges them into obuf
   __threadfence();
@@ -472,7 +512,10 @@ __device__ void step_attn_item(const StepParams& sp, const Phase& P, int g, int 
   }
 }
 
-template <int GQ, int HD>
+// FUSED: the variant for short caches (every CTA computes the attention of
+// its o-projection range in that GEMV's input build; no attention phase). The
+// two variants are separate kernels: either one alone keeps its registers.
+template <int GQ, int HD, bool FUSED>
 __global__ void __launch_bounds__(kSThreads, 1) step_kernel(const StepParams sp) {
   extern __shared__ __align__(128) uint8_t smem_raw[];
   uint8_t* ring = smem_raw;
@@ -493,6 +536,7 @@ __global__ void __launch_bounds__(kSThreads, 1) step_kernel(const StepParams sp)
   }
   __syncthreads();
 
+  const KRange kr(c, N, sp.R);  // this CTA's input range in every GEMV phase
   if (warp == kSWarps) {
     // ================= producer: every GEMV phase's units, in phase order
     if (lane == 0) {
@@ -501,17 +545,25 @@ __global__ void __launch_bounds__(kSThreads, 1) step_kernel(const StepParams sp)
       bool ok = true;
       for (int ph = 0; ph < sp.n_phases && ok; ++ph) {
         const Phase& P = sp.phases[ph];
-        if (P.type != PH_GEMV || c >= P.part.N) continue;  // small GEMVs use the first part.N CTAs
-        const int u0 = P.part.begin(c), u1 = P.part.begin(c + 1);
+        if (P.type != PH_GEMV) continue;
+        // this CTA's units in range order: v = tile * GR + (group - r * GR)
+        const int GR = P.GR, UB = P.unit_bytes;
+        const int u0 = kr.tile(c, P.n_rt) * GR, u1 = kr.tile(c + 1, P.n_rt) * GR;
         for (int ub = u0; ub < u1; ub += kSChunk, ++gi) {
           const int s = gi % kSNSlot;
           if (gi >= kSNSlot && !ring_wait(&empty[s], ((gi / kSNSlot) - 1) & 1, sp)) {
             ok = false;
             break;
           }
-          const int bytes = min(kSChunk, u1 - ub) * P.unit_bytes;
-          mbar_expect_tx(&full[s], bytes);
-          bulk_g2s(ring + s * kSSlot, P.units + (size_t)ub * P.unit_bytes, bytes, &full[s], pol);
+          const int ue = min(u1, ub + kSChunk);
+          mbar_expect_tx(&full[s], (ue - ub) * UB);
+          // one copy per row tile touched: the range's units of a tile are contiguous
+          for (int v = ub; v < ue;) {
+            const int rt = v / GR, gp = v - rt * GR, run = min(ue - v, GR - gp);
+            bulk_g2s(ring + s * kSSlot + (v - ub) * UB, P.units + ((size_t)rt * P.G + kr.r * GR + gp) * UB,
+                     run * UB, &full[s], pol);
+            v += run;
+          }
           sm.issued = gi + 1;
         }
       }
@@ -531,59 +583,72 @@ __global__ void __launch_bounds__(kSThreads, 1) step_kernel(const StepParams sp)
     };
     fetch_phase(0);
     ConsumerSync::sync();
+    // the window sums are zero after a GEMV phase (every window close clears
+    // what it read); attention and logit phases reuse their shared memory
+    bool red_clear = false;
+    // short caches: every CTA computes the attention of its o-projection range
+    // while it builds that GEMV's input, and the attention phase is skipped
+    constexpr bool fuse = FUSED;
+    int bars = 0;  // grid barriers this CTA arrived at
     for (int ph = 0; ph < sp.n_phases; ++ph) {
       const Phase& P = sm.ph[ph & 1];
+      if (P.type == PH_ATTN && fuse) {
+        fetch_phase(ph + 1);
+        ConsumerSync::sync();
+        red_clear = false;  // the o-projection's build reuses that shared memory
+        continue;
+      }
+      const int Kr = P.type == PH_GEMV ? P.K / sp.R : 0;  // inputs of this CTA's range
       // norm weights do not depend on the step: in flight while the barrier resolves
-      float4 w4[kSMaxV];
+      float4 w4[kSMaxW];
       {
         const bool nw = P.type == PH_GEMV && P.norm_w != nullptr;
 #pragma unroll
-        for (int j = 0; j < kSMaxV; ++j) {
+        for (int j = 0; j < kSMaxW; ++j) {
           const int i = tid + j * NT;
-          w4[j] = ldnc4_if(nw ? P.norm_w + 4 * i : nullptr, nw && i < P.K / 4);
+          w4[j] = ldnc4_if(nw ? P.norm_w + kr.r * Kr + 4 * i : nullptr, nw && i < Kr / 4);
         }
       }
-      // the unit range of this CTA (divisions: done while the barrier resolves)
-      int u0 = 0, u1 = 0, n_chunks = 0, wch = 1, k_rt = 0, k_g = 0, rt0 = 0;
-      if (P.type == PH_GEMV && c < P.part.N) {
-        u0 = P.part.begin(c);
-        u1 = P.part.begin(c + 1);
-        rt0 = u0 / P.G;
-        n_chunks = (u1 - u0 + kSChunk - 1) / kSChunk;
-        wch = max(1, ((kSRLoc - 2) * P.G + 1) / kSChunk);
-        k_rt = (u0 + warp) / P.G;
-        k_g = (u0 + warp) - k_rt * P.G;
+      // the units of this CTA in range order, v = tile * GR + group within the
+      // range (divisions: done while the barrier resolves)
+      // (kept in shared memory until the chunk loop: no registers held over the build)
+      if (P.type == PH_GEMV && tid == 0) {
+        sm.rt[0] = kr.tile(c, P.n_rt);
+        sm.rt[1] = kr.tile(c + 1, P.n_rt);
       }
       // the next descriptor goes to the buffer the previous phase used: its
       // round trip overlaps the barrier wait
       fetch_phase(ph + 1);
-      if (ph > 0 && !grid_wait(sp, ph * N, &sm.flag)) {
+      if (ph > 0 && !grid_wait(sp, bars * N, &sm.flag)) {
         sm.abort = 1;
         break;
       }
       if (P.type == PH_GEMV) {
-        // ---------------- build the input vector: every load of the build in one round trip
-        const int K = P.K, n4 = K / 4;
+        // ---------------- build this CTA's range of the input vector (inputs
+        // r*K .. r*K+K-1 of the GEMV): every load of the build in one round trip
+        const int K = Kr, n4 = K / 4;
+        const bool first = c == kr.c0;  // the range's first CTA publishes what all of its CTAs build
         float4* xh4 = reinterpret_cast<float4*>(sm.u.g.xh);
         float ss = 0.f;
         float4* xr4 = reinterpret_cast<float4*>(sm.xres);
-        auto put = [&](int i4, float4 v) {  // pre-norm inputs 4*i4 .. 4*i4+3
+        auto put = [&](int i4, float4 v) {  // pre-norm inputs r*K + 4*i4 .. +3
           xh4[i4] = v;
-          if (P.in_store && c == 0) reinterpret_cast<float4*>(P.in_store)[i4] = v;
+          if (P.in_store && first) reinterpret_cast<float4*>(P.in_store + kr.r * K)[i4] = v;
           ss += (v.x * v.x + v.y * v.y) + (v.z * v.z + v.w * v.w);
         };
         if (P.in_mode == IN_RESID) {
-          // x = residual (this CTA's resident copy) + sum of the previous
-          // GEMV's slots (row tiles of 32 inputs); x becomes the new residual
+          // x = residual (this CTA's resident copy of its range) + sum of the
+          // previous GEMV's slots (row tiles of 32 inputs); x becomes the new residual
           constexpr int RB = 8;
-          const int lg = log2_slots(P.in_S);
+          const int lg = log2_slots(sp.R);
           const int T4 = (K / 32) << (3 + lg);
+          const float* src = P.in_part + (size_t)kr.r * (K / 32) * (32 << lg);
           for (int f0 = 0; f0 < T4; f0 += RB * NT) {
             float4 a[RB];
 #pragma unroll
             for (int j = 0; j < RB; ++j) {
               const int f = f0 + tid + j * NT;
-              a[j] = ldcg4_if(P.in_part + (size_t)f * 4, f < T4);
+              a[j] = ldcg4_if(src + (size_t)f * 4, f < T4);
             }
 #pragma unroll
             for (int j = 0; j < RB; ++j) {
@@ -599,20 +664,25 @@ __global__ void __launch_bounds__(kSThreads, 1) step_kernel(const StepParams sp)
             }
           }
         } else if (P.in_mode == IN_SWIGLU) {
-          // row tile t of the gate|up GEMV: 16 gate rows, then their 16 up rows -> inputs 16t..16t+15
+          // row tile t of the gate|up GEMV: 16 gate rows, then their 16 up rows
+          // -> inputs 16t..16t+15; both carry the FFN norm's 1/rms
           constexpr int RB = 12;
-          const int lg = log2_slots(P.in_S);
+          const int lg = log2_slots(sp.R);
           const int T4 = (K / 16) << (3 + lg);
+          const float* src = P.in_part + (size_t)kr.r * (K / 16) * (32 << lg);
+          const float4 ssv = ldcg4_if(P.ss_in, true);
           for (int f0 = 0; f0 < T4; f0 += RB * NT) {
             float4 a[RB];
 #pragma unroll
             for (int j = 0; j < RB; ++j) {
               const int f = f0 + tid + j * NT;
-              a[j] = ldcg4_if(P.in_part + (size_t)f * 4, f < T4);
+              a[j] = ldcg4_if(src + (size_t)f * 4, f < T4);
             }
+            const float inv = rms_inv(ssv, sp.dim, sp.eps);
 #pragma unroll
             for (int j = 0; j < RB; ++j) {
-              const float4 gt = slot_sum(a[j], lg);
+              float4 gt = slot_sum(a[j], lg);
+              gt = make_float4(gt.x * inv, gt.y * inv, gt.z * inv, gt.w * inv);
               float4 up;
               up.x = __shfl_down_sync(0xffffffffu, gt.x, 4);
               up.y = __shfl_down_sync(0xffffffffu, gt.y, 4);
@@ -625,6 +695,17 @@ __global__ void __launch_bounds__(kSThreads, 1) step_kernel(const StepParams sp)
                                 silu_fast(gt.w) * up.w));
             }
           }
+        } else if (P.in_mode == IN_ATTN && fuse) {
+          // the attention of the range's kv heads over the whole cache, here
+          // (the range's first CTA appends k, v to the cache)
+          const bool pos_ok = spos >= 0 && spos < sp.cap;  // else: the status says so, the step runs on zeros
+          if (!pos_ok && tid == 0 && c == 0) atomicOr(sp.status, ST_CTX_FULL);
+          const int hpr = sp.Hkv / sp.R;
+          for (int j = 0; j < hpr && pos_ok; ++j) {
+            step_attn_item<GQ, HD>(sp, P, kr.r * hpr + j, 0, 1, spos, sm.u.a, first, sm.fo + j * GQ * HD);
+            ConsumerSync::sync();  // the next item and the input vector reuse the shared memory
+          }
+          for (int i = tid; i < K; i += NT) sm.u.g.xh[i] = pos_ok ? sm.fo[i] : 0.f;
         } else if (P.in_mode == IN_ATTN && step_splits(spos + 1, sp.P, HD) <= kSDefer) {
           // o = merge of the attention splits: sum_s 2^(m_s - M) o_s / sum_s 2^(m_s - M) l_s
           const int P_eff = step_splits(spos + 1, sp.P, HD);
@@ -633,8 +714,8 @@ __global__ void __launch_bounds__(kSThreads, 1) step_kernel(const StepParams sp)
             float2 ml[2][kSDefer];
 #pragma unroll
             for (int q = 0; q < 2; ++q) {
-              const int i4 = r0 + q * NT + tid;
-              const int h = (4 * i4) / HD, d = (4 * i4) % HD, g = h / GQ, hh = h % GQ;
+              const int i4 = r0 + q * NT + tid, e = kr.r * K + 4 * i4;  // q_dim element
+              const int h = e / HD, d = e % HD, g = h / GQ, hh = h % GQ;
 #pragma unroll
               for (int s = 0; s < kSDefer; ++s) {
                 const bool pr = i4 < n4 && s < P_eff;
@@ -679,7 +760,7 @@ __global__ void __launch_bounds__(kSThreads, 1) step_kernel(const StepParams sp)
               t = 0;
             }
           }
-          const float* src = P.in_mode == IN_ATTN ? sp.obuf : P.in_base;
+          const float* src = (P.in_mode == IN_ATTN ? sp.obuf : P.in_base) + kr.r * K;
           float4 v[kSMaxV];
 #pragma unroll
           for (int j = 0; j < kSMaxV; ++j) {
@@ -688,12 +769,12 @@ __global__ void __launch_bounds__(kSThreads, 1) step_kernel(const StepParams sp)
               v[j] = make_float4(0.f, 0.f, 0.f, 0.f);
               if (i < n4) {
                 const uint2 u = __ldg(reinterpret_cast<const uint2*>(static_cast<const uint16_t*>(sp.embed) +
-                                                                      (size_t)t * K) + i);
+                                                                      (size_t)t * P.K + kr.r * K) + i);
                 v[j] = make_float4(__uint_as_float(u.x << 16), __uint_as_float(u.x & 0xFFFF0000u),
                                    __uint_as_float(u.y << 16), __uint_as_float(u.y & 0xFFFF0000u));
               }
             } else if (P.in_mode == IN_EMBED_F32) {
-              v[j] = ldnc4_if(static_cast<const float*>(sp.embed) + (size_t)t * K + 4 * i, i < n4);
+              v[j] = ldnc4_if(static_cast<const float*>(sp.embed) + (size_t)t * P.K + kr.r * K + 4 * i, i < n4);
             } else {
               v[j] = ldcg4_if(src + 4 * i, i < n4);
             }
@@ -705,21 +786,20 @@ __global__ void __launch_bounds__(kSThreads, 1) step_kernel(const StepParams sp)
               put(tid + j * NT, v[j]);
             }
         }
-        // RMSNorm factor over the whole vector
-        float inv = 1.f;
+        // the range's sum of squares (the readers of this GEMV apply 1/rms)
         if (P.norm_w) {
 #pragma unroll
           for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
           if (lane == 0) sm.bred[warp] = ss;
         }
         ConsumerSync::sync();  // publishes xh (written in row order by other threads)
-        if (P.norm_w) {
+        if (P.norm_w && first && tid == 0) {
           float t = 0.f;
 #pragma unroll
           for (int w = 0; w < kSWarps; ++w) t += sm.bred[w];
-          inv = 1.0f / sqrtf(t / (float)K + sp.eps);
+          P.ss_out[kr.r] = t;
         }
-        // normalise in place (x / rms * w); per-group sums for the 4-bit units
+        // x * w in place (RMSNorm without its 1/rms); per-group sums for the 4-bit units
 #pragma unroll
         for (int j = 0; j < kSMaxV; ++j) {
           const int i = tid + j * NT;
@@ -727,9 +807,9 @@ __global__ void __launch_bounds__(kSThreads, 1) step_kernel(const StepParams sp)
           float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
           if (i < n4) {
             x = xh4[i];
-            if (P.norm_w) {
+            if (P.norm_w && j < kSMaxW) {  // normed inputs are residual-wide
               const float4 w = w4[j];
-              x = make_float4(x.x * inv * w.x, x.y * inv * w.y, x.z * inv * w.z, x.w * inv * w.w);
+              x = make_float4(x.x * w.x, x.y * w.y, x.z * w.z, x.w * w.w);
               xh4[i] = x;
             }
           }
@@ -740,12 +820,21 @@ __global__ void __launch_bounds__(kSThreads, 1) step_kernel(const StepParams sp)
             if (i < n4 && (lane & 15) == 0) sm.u.g.xs[i / 16] = gs;
           }
         }
-        for (int i = tid; i < kSRLoc * kSWarps * 32; i += NT) (&sm.u.g.red[0][0][0])[i] = 0.f;
+        if (!red_clear)
+          for (int i = tid; i < kSRLoc * kSWarps * 32; i += NT) (&sm.u.g.red[0][0][0])[i] = 0.f;
         if (tid < 2) sm.carry_rt[tid] = -1;
         ConsumerSync::sync();
 
         // ---------------- stream the units; chunk i = units u0+15i .. u0+15i+14
-        const int G = P.G, EPU = P.bf16 ? kBF16UnitCols : 64;
+        const int G = P.GR, EPU = P.bf16 ? kBF16UnitCols : 64;
+        const int rt0 = sm.rt[0], u0 = rt0 * G, u1 = sm.rt[1] * G;
+        const int n_chunks = (u1 - u0 + kSChunk - 1) / kSChunk;
+        const int wch = max(1, ((kSRLoc - 2) * G + 1) / kSChunk);
+        int k_rt = rt0, k_g = warp;  // this warp's first unit: u0 + warp
+        while (k_g >= G) {
+          k_g -= G;
+          ++k_rt;
+        }
         int win_first = 0, win_idx = 0, win_rt0 = rt0, cur_rt = -1;
         float acc = 0.f;
         bool ok = true;
@@ -785,16 +874,16 @@ __global__ void __launch_bounds__(kSThreads, 1) step_kernel(const StepParams sp)
             const int rt_a = wu0 / G, rt_b = (wu1 - 1) / G;
             const int next_rt = (wu1 < u1) ? wu1 / G : -1;
             const int carry_in_rt = sm.carry_rt[(win_idx + 1) & 1];
-            for (int r = rt_a + warp; r <= rt_b; r += kSWarps) {
-              const int li = r - rt_a;
-              float sum = (r == carry_in_rt) ? sm.u.g.carry[(win_idx + 1) & 1][lane] : 0.f;
+            for (int t = rt_a + warp; t <= rt_b; t += kSWarps) {
+              const int li = t - rt_a;
+              float sum = (t == carry_in_rt) ? sm.u.g.carry[(win_idx + 1) & 1][lane] : 0.f;
 #pragma unroll
               for (int w2 = 0; w2 < kSWarps; ++w2) {
                 sum += sm.u.g.red[li][w2][lane];
                 sm.u.g.red[li][w2][lane] = 0.f;
               }
-              if (r == next_rt) sm.u.g.carry[win_idx & 1][lane] = sum;
-              else P.out_part[((size_t)r * P.part.S + (c - P.part.first_cta(r))) * 32 + lane] = sum;
+              if (t == next_rt) sm.u.g.carry[win_idx & 1][lane] = sum;
+              else P.out_part[((size_t)t * sp.R + kr.r) * 32 + lane] = sum;
             }
             if (tid == 0) sm.carry_rt[win_idx & 1] = (next_rt == rt_b) ? rt_b : -1;
             ConsumerSync::sync();
@@ -806,22 +895,27 @@ __global__ void __launch_bounds__(kSThreads, 1) step_kernel(const StepParams sp)
         // every warp passed the last window's closing barrier: the flag is uniform
         if (*(volatile int*)&sm.abort) break;
       } else if (P.type == PH_ATTN) {
-        // ---------------- attention items (kv head, split) over the CTAs
-        const int pos = spos;
-        if (pos < 0 || pos >= sp.cap) {
-          if (tid == 0 && c == 0) atomicOr(sp.status, ST_CTX_FULL);
-        } else {
-          const int P_eff = step_splits(pos + 1, sp.P, HD);
-          for (int item = c; item < sp.Hkv * P_eff; item += N) {
-            step_attn_item<GQ, HD>(sp, P, item / P_eff, item % P_eff, P_eff, pos, sm.u.a);
-            ConsumerSync::sync();  // shared memory is reused by the next item
+        if constexpr (!FUSED) {
+          // ---------------- attention items (kv head, split) over the CTAs
+          const int pos = spos;
+          if (pos < 0 || pos >= sp.cap) {
+            if (tid == 0 && c == 0) atomicOr(sp.status, ST_CTX_FULL);
+          } else {
+            const int P_eff = step_splits(pos + 1, sp.P, HD);
+            for (int item = c; item < sp.Hkv * P_eff; item += N) {
+              step_attn_item<GQ, HD>(sp, P, item / P_eff, item % P_eff, P_eff, pos, sm.u.a,
+                                     item % P_eff == P_eff - 1, nullptr);
+              ConsumerSync::sync();  // shared memory is reused by the next item
+            }
           }
         }
       } else {
-        // ---------------- logits = sum of LM-head partials; greedy choice
+        // ---------------- logits = 1/rms (final norm) x sum of the LM-head
+        // partials; greedy choice
         const int V = P.vocab;
         const int r0 = (int)((int64_t)V * c / N), r1 = (int)((int64_t)V * (c + 1) / N);
-        const int lS = P.lm_S;
+        const int lS = sp.R;
+        const float4 ssv = ldcg4_if(P.ss_in, true);
         float bv = -INFINITY;
         int bi = 0x7fffffff;
         bool nan = false;
@@ -835,11 +929,12 @@ __global__ void __launch_bounds__(kSThreads, 1) step_kernel(const StepParams sp)
 #pragma unroll
             for (int s = 0; s < 4; ++s) y[j][s] = ldcg1_if(src + s * 32, r < r1 && s < lS);
           }
+          const float inv = rms_inv(ssv, sp.dim, sp.eps);
 #pragma unroll
           for (int j = 0; j < RR; ++j) {
             const int r = rb + tid + j * NT;
             if (r < r1) {
-              const float v = (y[j][0] + y[j][1]) + (y[j][2] + y[j][3]);
+              const float v = ((y[j][0] + y[j][1]) + (y[j][2] + y[j][3])) * inv;
               sp.logits[r] = v;
               if (v != v) nan = true;
               else if (better(v, r, bv, bi)) { bv = v; bi = r; }
@@ -902,7 +997,11 @@ __global__ void __launch_bounds__(kSThreads, 1) step_kernel(const StepParams sp)
           }
         }
       }
-      if (ph + 1 < sp.n_phases) grid_arrive(sp);  // its CTA barrier also retires this phase's reads of sm.ph
+      red_clear = P.type == PH_GEMV;
+      if (ph + 1 < sp.n_phases) {
+        grid_arrive(sp);  // its CTA barrier also retires this phase's reads of sm.ph
+        ++bars;
+      }
     }
   }
   __syncthreads();

@@ -117,6 +117,18 @@ void llm_model_destroy(llm_model* m);
 int llm_prefill(llm_model* m, int32_t seq, const int32_t* tokens, int32_t n,
                 float* logits_out, int32_t* argmax_out);
 
+/* The same contract as llm_prefill, computed as batched prompt processing
+ * (aot-llm "Batched prompt processing": each weight row read once per chunk of
+ * tokens; llmopt "prefill-style GEMM"): chunks of up to 32 tokens go through
+ * the batched pipeline (4-bit skinny GEMMs on the tensor cores, fp32
+ * accumulation) with the chunk's rows appending their k, v to the cache first
+ * and then attending causally over it. Equal to token-by-token prefill within
+ * floating-point tolerance (a different summation order); the greedy token is
+ * the argmax of the returned logits. llm_debug_hidden is not updated.
+ * Errors as llm_prefill. */
+int llm_prefill_batched(llm_model* m, int32_t seq, const int32_t* tokens, int32_t n,
+                        float* logits_out, int32_t* argmax_out);
+
 /* One decode step of sequence seq for `token` at position len; len += 1.
  * logits_out [vocab] fp32 and argmax_out (lowest index wins ties): host or
  * device, may be NULL. Errors as llm_prefill. */
