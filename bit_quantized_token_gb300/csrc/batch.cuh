@@ -485,10 +485,6 @@ struct BAttnParams {
   size_t part_stride;     // attention partial floats per row
 };
 
-__device__ __forceinline__ void cp_async16(void* dst, const void* src) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
-}
-__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
 
 constexpr int kBAttnThreads = 256;
 constexpr int kBAttnPP = 64;  // cache positions per pass (~42 KB of tiles: 4 CTAs per SM)

@@ -170,6 +170,13 @@ __device__ __forceinline__ void sub2(float& d0, float& d1, float a0, float a1, f
 // order and the remaining slots stay zero (buffers are zeroed once at create).
 // U * N < 2^32 always holds (U < 2^24 units, N <= 256 CTAs), so 32-bit
 // unsigned arithmetic is exact.
+// 16-byte asynchronous global -> shared copy (both addresses 16-byte aligned);
+// cp_async_wait_all waits for every copy this thread issued.
+__device__ __forceinline__ void cp_async16(void* dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+
 struct Part {
   int U, N, G, S;  // units, CTAs, units per row tile, slots per row tile
   __host__ __device__ int begin(int c) const { return static_cast<int>((unsigned)U * (unsigned)c / (unsigned)N); }

@@ -278,6 +278,30 @@ struct StepSmem {
 };
 
 // ---------------------------------------------------------------------------
+// The first pass's K/V rows t0 .. of an attention item straight into its tiles
+// (raw bf16, asynchronous copies). The cached rows were appended by earlier
+// steps, so this runs before the grid barrier that the item's q|k|v wait for;
+// row `pos` and the zero rows are written by the item. Thread-to-chunk map of
+// step_attn_item's tile loads.
+template <int GQ, int HD>
+__device__ void step_attn_prefetch(const StepParams& sp, int layer, int g, int t0, int t1, int pos,
+                                   StepAttnSmem<GQ, HD>& sa) {
+  using SA = StepAttnSmem<GQ, HD>;
+  constexpr int NT = kSCThreads, PP = SA::PP, CH = HD / 8;
+  constexpr int TB = (2 * PP * CH + NT - 1) / NT;
+  const int tid = threadIdx.x;
+  const uint16_t* kc = sp.k_base + (size_t)layer * sp.layer_stride + (size_t)g * sp.cap * HD;
+  const uint16_t* vc = sp.v_base + (size_t)layer * sp.layer_stride + (size_t)g * sp.cap * HD;
+  const int n = min(PP, t1 - t0);
+#pragma unroll
+  for (int j = 0; j < TB; ++j) {
+    const int idx = tid + j * NT, kv = idx / (PP * CH), rem = idx - kv * (PP * CH), row = rem / CH, ch = rem - row * CH;
+    if (kv < 2 && row < n && t0 + row != pos)
+      cp_async16(&(kv ? sa.vt : sa.kt)[row][8 * ch], (kv ? vc : kc) + (size_t)(t0 + row) * HD + 8 * ch);
+  }
+}
+
+// ---------------------------------------------------------------------------
 // One (kv head g, split) attention item, run by the consumer warps. `append`:
 // this item writes the step's k, v into the cache. With `fo` null the item
 // leaves its split's unnormalised partial (o, max, sum) in global memory;
@@ -285,7 +309,7 @@ struct StepSmem {
 // of its GQ heads to fo[h * HD + d] in shared memory.
 template <int GQ, int HD>
 __device__ void step_attn_item(const StepParams& sp, const Phase& P, int g, int split, int P_eff, int pos,
-                               StepAttnSmem<GQ, HD>& sa, bool append, float* fo) {
+                               StepAttnSmem<GQ, HD>& sa, bool append, float* fo, bool prefetched) {
   using SA = StepAttnSmem<GQ, HD>;
   constexpr int NT = kSCThreads, PP = SA::PP, RS = SA::RS, CH = HD / 8;
   constexpr int TB = (2 * PP * CH + NT - 1) / NT;  // 16-B tile loads per thread
@@ -322,7 +346,7 @@ __device__ void step_attn_item(const StepParams& sp, const Phase& P, int g, int 
                        bf16x2_to_f16x2(tl[j].w));
     }
   };
-  load_tile(t0);
+  if (!prefetched) step_attn_prefetch<GQ, HD>(sp, P.layer, g, t0, t1, pos, sa);
 
   // RoPE factors and q/k norm weights do not depend on the step: load them
   // in the same round trip as the q|k|v gather and the first tile
@@ -362,7 +386,21 @@ __device__ void step_attn_item(const StepParams& sp, const Phase& P, int g, int 
             make_float4(v.x * inv, v.y * inv, v.z * inv, v.w * inv);
     }
   }
-  store_tile(t0);
+  {
+    // the first pass's rows arrive by step_attn_prefetch: bf16 -> fp16 in place
+    // (each thread its own chunks), zero rows up to the next multiple of 16
+    cp_async_wait_all();
+    const int n = min(PP, t1 - t0), rows = ((n + 15) / 16) * 16;
+#pragma unroll
+    for (int j = 0; j < TB; ++j) {
+      const int idx = tid + j * NT, kv = idx / (PP * CH), rem = idx - kv * (PP * CH), row = rem / CH, ch = rem - row * CH;
+      if (kv < 2 && row < rows && t0 + row != pos) {
+        uint4* q = reinterpret_cast<uint4*>(&(kv ? sa.vt : sa.kt)[row][8 * ch]);
+        const uint4 w = row < n ? *q : make_uint4(0u, 0u, 0u, 0u);
+        *q = make_uint4(bf16x2_to_f16x2(w.x), bf16x2_to_f16x2(w.y), bf16x2_to_f16x2(w.z), bf16x2_to_f16x2(w.w));
+      }
+    }
+  }
   ConsumerSync::sync();
   // ---- per-head RMSNorm of q and k (Qwen3): warp h < GQ takes q head h, warp GQ takes k
   if (P.q_norm) {
@@ -619,7 +657,28 @@ __global__ void __launch_bounds__(kSThreads, 1) step_kernel(const StepParams sp)
       // the next descriptor goes to the buffer the previous phase used: its
       // round trip overlaps the barrier wait
       fetch_phase(ph + 1);
+      // attention: the cached K/V rows of this CTA's first item start arriving
+      // while the barrier resolves (the union's previous user finished before
+      // its phase's arrival)
+      bool pf = false;
+      if (spos >= 0 && spos < sp.cap) {
+        if constexpr (FUSED) {
+          if (P.type == PH_GEMV && P.in_mode == IN_ATTN) {
+            step_attn_prefetch<GQ, HD>(sp, P.layer, kr.r * (sp.Hkv / sp.R), 0, spos + 1, spos, sm.u.a);
+            pf = true;
+          }
+        } else if (P.type == PH_ATTN) {
+          const int P_eff = step_splits(spos + 1, sp.P, HD);
+          if (c < sp.Hkv * P_eff) {
+            const int split = c % P_eff, len = spos + 1;
+            const int t0 = (int)((int64_t)len * split / P_eff), t1 = (int)((int64_t)len * (split + 1) / P_eff);
+            step_attn_prefetch<GQ, HD>(sp, P.layer, c / P_eff, t0, t1, spos, sm.u.a);
+            pf = true;
+          }
+        }
+      }
       if (ph > 0 && !grid_wait(sp, bars * N, &sm.flag)) {
+        cp_async_wait_all();  // no copy may land after the CTA leaves
         sm.abort = 1;
         break;
       }
@@ -702,7 +761,8 @@ __global__ void __launch_bounds__(kSThreads, 1) step_kernel(const StepParams sp)
           if (!pos_ok && tid == 0 && c == 0) atomicOr(sp.status, ST_CTX_FULL);
           const int hpr = sp.Hkv / sp.R;
           for (int j = 0; j < hpr && pos_ok; ++j) {
-            step_attn_item<GQ, HD>(sp, P, kr.r * hpr + j, 0, 1, spos, sm.u.a, first, sm.fo + j * GQ * HD);
+            step_attn_item<GQ, HD>(sp, P, kr.r * hpr + j, 0, 1, spos, sm.u.a, first, sm.fo + j * GQ * HD,
+                                   j == 0 && pf);
             ConsumerSync::sync();  // the next item and the input vector reuse the shared memory
           }
           for (int i = tid; i < K; i += NT) sm.u.g.xh[i] = pos_ok ? sm.fo[i] : 0.f;
@@ -904,7 +964,7 @@ __global__ void __launch_bounds__(kSThreads, 1) step_kernel(const StepParams sp)
             const int P_eff = step_splits(pos + 1, sp.P, HD);
             for (int item = c; item < sp.Hkv * P_eff; item += N) {
               step_attn_item<GQ, HD>(sp, P, item / P_eff, item % P_eff, P_eff, pos, sm.u.a,
-                                     item % P_eff == P_eff - 1, nullptr);
+                                     item % P_eff == P_eff - 1, nullptr, item == c && pf);
               ConsumerSync::sync();  // shared memory is reused by the next item
             }
           }
