@@ -164,6 +164,21 @@ def cpu_baseline(cfg, w, prompt, seconds):
                        f"{n_pre + len(prompt) + n - 1}")}
 
 
+def max_over_ranks(ms, dist):
+    """The slowest rank's timed-region length (ms); the replicas' own value without torch.distributed."""
+    if not dist:
+        return ms
+    import torch
+    t = torch.tensor([ms], dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_rate(world, units_per_rank, ms):
+    """Whole-job throughput: every rank's units over the slowest rank's time (weak scaling)."""
+    return world * units_per_rank / (ms / 1000.0)
+
+
 def run_reference(a, cfg, w, prompt, rank, world):
     if rank != 0:
         return
@@ -214,11 +229,8 @@ def run_batched(a, cfg, w, rank, world, local, dist):
     ms = e0.elapsed_time(e1)
     clk = clocks.stop()
     m.sync()
-    if dist:
-        t = torch.tensor([ms], dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
-    tok_s = world * B * a.steps / (ms / 1000.0)
+    ms = max_over_ranks(ms, dist)
+    tok_s = job_rate(world, B * a.steps, ms)
     per_pos = synth.kv_bytes_per_pos(cfg)
     kv_step = float(np.mean([sum((int(pos0[b]) + i + 1) * per_pos for b in range(B)) for i in range(a.steps)]))
     bytes_step = st["weight_stream_bytes"] + kv_step
@@ -324,12 +336,9 @@ def main():
     ms = e0.elapsed_time(e1)
     clk = clocks.stop()
     m.sync()
-    if dist:
-        t = torch.tensor([ms], dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(ms, dist)
     tok = int(toks_dev[-1].item())
-    tok_s = world * a.steps / (ms / 1000.0)
+    tok_s = job_rate(world, a.steps, ms)
     bytes_tok = st["weight_stream_bytes"] + kv_read_bytes(cfg, positions)
     peak, peak_kind = peaks()
 
