@@ -56,14 +56,17 @@ def peaks():
     return 6800.0, "fallback"
 
 
-def src_sha():
-    """Hash of the kernel sources: an ncu traffic figure is only used for the code it was taken on."""
+# the sources a kernel's code comes from (the step kernel is defined in these headers)
+KERNEL_SOURCES = {"step_kernel": ("common.cuh", "kernels.cuh", "attn_mma.cuh", "step.cuh")}
+
+
+def src_sha(kernel="step_kernel"):
+    """Hash of a kernel's sources: an ncu traffic figure is only used for the code it was taken on."""
     import hashlib
     h = hashlib.sha256()
     d = os.path.join(ROOT, "bit_quantized_token_gb300", "csrc")
-    for f in sorted(os.listdir(d)):
-        if f.endswith((".cu", ".cuh")):
-            h.update(open(os.path.join(d, f), "rb").read())
+    for f in KERNEL_SOURCES[kernel]:
+        h.update(open(os.path.join(d, f), "rb").read())
     return h.hexdigest()[:16]
 
 
@@ -73,7 +76,7 @@ def ncu_traffic(key):
     if not os.path.exists(p):
         return None
     t = json.load(open(p)).get(key)
-    return t["traffic_bytes"] if t and t.get("src_sha") == src_sha() else None
+    return t["traffic_bytes"] if t and t.get("src_sha") == src_sha(key.split()[0]) else None
 
 
 def workload_desc(cfg):
@@ -303,7 +306,7 @@ def main():
         return
     n_e2e, n_kt, n_pf = 32, 3, 512
     n_pre = max(0, cfg.get("prefill_kv", 0))
-    max_seq = max(n_pre + len(prompt) + a.warmup + a.steps + n_e2e + 8, n_pf + 8)
+    max_seq = max(n_pre + len(prompt) + 2 * (a.warmup + a.steps) + n_e2e + 8, n_pf + 8)
     stream = torch.cuda.Stream()  # the library launches on it; events are recorded on it
     m = bq.Model(cfg, w, max_seq=max_seq, stream=stream.cuda_stream)
     st = m.stats()
@@ -362,6 +365,22 @@ def main():
     e2e = {"value": world * n_e2e / e2e_s, "unit": "tok/s", "h2d_bytes_per_step": 4, "d2h_bytes_per_step": 4,
            "steps": n_e2e, "call": "llm_decode_step(host token -> host argmax)"}
 
+    # sampled choice (temperature 0.8, top-k 40, top-p 0.95, Philox draw): the
+    # same device-fed loop with the sampling kernel in each step's graph
+    m.set_sampling(0.8, 40, 0.95, 42)
+    toks_s = torch.empty(a.steps, dtype=torch.int32, device="cuda")
+    warm_s = m.decode_greedy(0, int(am_h[0]), a.warmup)
+    torch.cuda.synchronize()
+    e0.record(stream)
+    m.decode_greedy(0, int(warm_s[-1]), a.steps, toks_s)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms_s = e0.elapsed_time(e1)
+    m.set_sampling(0.0)
+    sampled = {"temperature": 0.8, "top_k": 40, "top_p": 0.95, "ms_per_step": ms_s / a.steps,
+               "overhead_us_per_step": (ms_s - ms) / a.steps * 1000.0,
+               "call": "llm_decode_greedy after llm_set_sampling (CUDA events)"}
+
     # prompt processing: a 512-token prompt, token by token (n graph steps) and
     # batched (chunks of 32 through the tensor-core pipeline); wall clock of the call
     prefill = None
@@ -415,6 +434,7 @@ def main():
         "gpu_launches": st["kernels_per_step"] * a.steps,
         "clocks": clk,
     }
+    line["sampling"] = sampled
     if prefill:
         line["prefill"] = prefill
     if rank == 0 and world == 1 and not a.no_cpu_baseline:

@@ -28,7 +28,7 @@ STATUS = {0: "OK", -1: "INVALID_ARG", -2: "UNSUPPORTED", -3: "OOM", -4: "CTX_FUL
 
 # Every entry point include/llmq.h declares.
 EXPORTS = ["llm_model_create", "llm_model_destroy", "llm_prefill", "llm_prefill_batched", "llm_decode_step",
-           "llm_decode_greedy",
+           "llm_decode_greedy", "llm_set_sampling",
            "llm_decode_step_batch", "llm_kv_reset", "llm_kv_write", "llm_kv_read", "llm_kv_len",
            "llm_debug_hidden", "llm_debug_unpack", "llm_model_stats", "llm_profile_step", "llm_time_kernel", "llm_sync",
            "llm_last_error", "llm_op_matvec", "llm_matvec_noalloc"]
@@ -98,6 +98,7 @@ def lib() -> C.CDLL:
             "llm_model_destroy": (None, [P]),
             "llm_prefill": (i32, [P, i32, P, i32, P, P]),
             "llm_prefill_batched": (i32, [P, i32, P, i32, P, P]),
+            "llm_set_sampling": (i32, [P, C.c_float, i32, C.c_float, C.c_uint64]),
             "llm_decode_step": (i32, [P, i32, i32, P, P]),
             "llm_decode_greedy": (i32, [P, i32, i32, i32, P]),
             "llm_decode_step_batch": (i32, [P, P, i32, P, P]),
@@ -209,6 +210,10 @@ class Model:
         toks = np.ascontiguousarray(tokens, np.int32)
         _check(lib().llm_prefill_batched(self.h, seq, toks.ctypes.data, toks.size, _ptr(logits), _ptr(argmax)),
                self.h)
+
+    def set_sampling(self, temperature: float, top_k: int = 40, top_p: float = 0.95, seed: int = 42) -> None:
+        """Sampled next-token choice for the batch-1 calls; temperature 0 = greedy."""
+        _check(lib().llm_set_sampling(self.h, float(temperature), int(top_k), float(top_p), int(seed)), self.h)
 
     def decode_step(self, seq: int, token: int, logits=None, argmax=None) -> None:
         _check(lib().llm_decode_step(self.h, seq, int(token), _ptr(logits), _ptr(argmax)), self.h)

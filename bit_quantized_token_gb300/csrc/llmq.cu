@@ -22,6 +22,7 @@
 #include "kernels.cuh"
 #include "step.cuh"
 #include "batch.cuh"
+#include "sample.cuh"
 #include "llmq.h"
 
 using namespace llmq;
@@ -248,6 +249,8 @@ struct llm_model {
   int *d_pos = nullptr, *d_tok = nullptr, *d_argmax = nullptr, *d_hist = nullptr, *d_hist_ctr = nullptr,
       *d_status = nullptr, *d_prompt = nullptr;
   int* d_pf = nullptr;                        // batched prefill: [tok | pos | seq][pf_cap], then [2][kBM] scratch
+  SampleCfg* d_samp = nullptr;                // sampling options (temperature 0: greedy)
+  bool sampling = false;
   size_t pf_cap = 0;
   int* h_stage = nullptr;                     // pinned staging
   std::vector<int> len;
@@ -776,7 +779,32 @@ cudaError_t enqueue_batched(llm_model* m, const BatchedIO& io) {
 }
 
 // Enqueue one batch-1 decode step of sequence `seq` on m->stream.
+// The sampled choice of sequence seq from `logits` (after the step that wrote them).
+cudaError_t launch_sample(llm_model* m, int seq, const float* logits, const int* pos, int* tok_io, int* choice,
+                          bool hist) {
+  SampleParams sp{};
+  sp.logits = logits;
+  sp.V = m->cfg.vocab;
+  sp.cfg = m->d_samp;
+  sp.seq = seq;
+  sp.pos = pos;
+  sp.tok_io = tok_io;
+  sp.choice_out = choice;
+  sp.hist = hist ? m->d_hist : nullptr;
+  sp.hist_ctr = m->d_hist_ctr;
+  sp.hist_cap = m->cfg.max_seq;
+  return launch(sample_kernel, dim3(1), dim3(kSampleThreads), 0, m->stream, false, sp);
+}
+
+cudaError_t enqueue_step_only(llm_model* m, int seq, Prof* prof, bool fused);
+
 cudaError_t enqueue_step(llm_model* m, int seq, Prof* prof = nullptr, bool fused = false) {
+  cudaError_t e = enqueue_step_only(m, seq, prof, fused);
+  if (e != cudaSuccess || !m->sampling || prof) return e;
+  return launch_sample(m, seq, m->d_logits, m->d_pos + seq, m->d_tok + seq, m->d_argmax + seq, true);
+}
+
+cudaError_t enqueue_step_only(llm_model* m, int seq, Prof* prof, bool fused) {
   if (m->use_step && !prof) return enqueue_persistent_step(m, seq, fused);
   const int L = m->cfg.n_layers;
   const bool pdl = !(m->cfg.flags & LLM_NO_PDL) && !prof;
@@ -1280,6 +1308,7 @@ int llm_model_create(const llm_config* cfg, const llm_tensor* tensors, int32_t n
   AL(m->d_hist_ctr, 4, "history counter");
   AL(m->d_status, 4, "status");
   AL(m->d_prompt, (size_t)c.max_seq * 4, "prompt");
+  AL(m->d_samp, sizeof(SampleCfg), "sampling options");
   {
     const size_t pf = ((size_t)c.max_seq + kBM - 1) / kBM * kBM;  // prompt rows, whole chunks
     AL(m->d_pf, (3 * pf + 2 * kBM) * 4, "prompt chunk rows");
@@ -1314,6 +1343,7 @@ int llm_model_create(const llm_config* cfg, const llm_tensor* tensors, int32_t n
   {
     cudaError_t e = cudaMemset(m->d_cnt, 0, cnt_total * 4);
     if (e == cudaSuccess && m->d_step_ss) e = cudaMemset(m->d_step_ss, 0, (size_t)(5 * L + 2) * 16);
+    if (e == cudaSuccess) e = cudaMemset(m->d_samp, 0, sizeof(SampleCfg));  // temperature 0: greedy
     for (int* z : {m->d_pos, m->d_tok, m->d_argmax})
       if (e == cudaSuccess) e = cudaMemset(z, 0, 4 * (size_t)c.max_batch);
     if (e == cudaSuccess) e = cudaMemset(m->d_hist_ctr, 0, 4);
@@ -1412,6 +1442,10 @@ int llm_prefill_batched(llm_model* m, int32_t seq, const int32_t* tokens, int32_
     last_rows = io.M;
     CK(enqueue_batched(m, io), "prompt chunk launch");
   }
+  if (m->sampling)  // the last row's logits; its position counter was advanced by the greedy epilogue
+    CK(launch_sample(m, seq, m->d_blogits + (size_t)(last_rows - 1) * m->cfg.vocab, m->d_pf + m->pf_cap + n - 1,
+                     nullptr, scratch + kBM + last_rows - 1, false),
+       "sampling launch");
   m->len[seq] += n;
   const int32_t next_pos = m->len[seq];  // the decode steps' position counter (pageable: staged at call time)
   CK(cudaMemcpyAsync(m->d_pos + seq, &next_pos, 4, cudaMemcpyHostToDevice, m->stream), "position update");
@@ -1422,6 +1456,35 @@ int llm_prefill_batched(llm_model* m, int32_t seq, const int32_t* tokens, int32_
   if ((rc = copy_out(m, argmax_out, scratch + kBM + last_rows - 1, 4, &host)) != LLM_OK) return rc;
   CK(cudaStreamSynchronize(m->stream), "prefill sync");  // `rows` outlives the upload
   return check_status(m);
+}
+
+int llm_set_sampling(llm_model* m, float temperature, int32_t top_k, float top_p, uint64_t seed) {
+  int rc = check_model(m, 0);
+  if (rc) return rc;
+  if (!(temperature >= 0.f) || !(temperature < INFINITY))
+    return set_err(m, LLM_ERR_INVALID_ARG, "temperature must be finite and >= 0");
+  if (temperature > 0.f && (top_k < 1 || top_k > kSampleMaxK))
+    return set_err(m, LLM_ERR_INVALID_ARG, "top_k must be in 1..64 when sampling");
+  if (temperature > 0.f && !(top_p > 0.f && top_p <= 1.f))
+    return set_err(m, LLM_ERR_INVALID_ARG, "top_p must be in (0, 1]");
+  SampleCfg h{};
+  h.temperature = temperature;
+  h.top_p = top_p;
+  h.top_k = top_k;
+  h.seed_lo = (uint32_t)(seed & 0xFFFFFFFFull);
+  h.seed_hi = (uint32_t)(seed >> 32);
+  CK(cudaStreamSynchronize(m->stream), "sampling sync");  // no step in flight reads the options
+  CK(cudaMemcpy(m->d_samp, &h, sizeof(h), cudaMemcpyHostToDevice), "sampling upload");
+  const bool on = temperature > 0.f;
+  if (on != m->sampling) {  // the captured steps gain or lose the sampling kernel: capture again
+    for (auto& g : m->graphs)
+      if (g) {
+        cudaGraphExecDestroy(g);
+        g = nullptr;
+      }
+    m->sampling = on;
+  }
+  return LLM_OK;
 }
 
 int llm_decode_greedy(llm_model* m, int32_t seq, int32_t first_token, int32_t n_steps, int32_t* tokens_out) {

@@ -141,6 +141,22 @@ int llm_decode_step(llm_model* m, int32_t seq, int32_t token, float* logits_out,
 int llm_decode_greedy(llm_model* m, int32_t seq, int32_t first_token, int32_t n_steps,
                       int32_t* tokens_out);
 
+/* Sampled instead of greedy next-token choice for the batch-1 calls
+ * (llm_prefill, llm_prefill_batched, llm_decode_step, llm_decode_greedy), from
+ * the options the aot-llm page lists ("Generated binary options": temperature,
+ * 0 = greedy; top-k; top-p; seed). Keep the top_k largest logits (ties: lower
+ * token id), p = softmax((l - l_max) / temperature), keep the shortest prefix
+ * whose cumulative probability reaches top_p, and take the first token whose
+ * cumulative probability exceeds u times the prefix total. The draw u for the
+ * token after position pos of sequence seq is Philox4x32-10 (Salmon et al.,
+ * SC 2011) of counter (pos, seq, 0, 0) and key (seed low, seed high word):
+ * u = (x0 >> 8) / 2^24, reproducible from the seed. The chosen token is what
+ * argmax_out / tokens_out return and what llm_decode_greedy feeds back.
+ * temperature 0 restores the greedy choice. llm_decode_step_batch stays
+ * greedy. Errors: INVALID_ARG (temperature < 0 or not finite; when sampling,
+ * top_k outside 1..64 or top_p outside (0, 1]). */
+int llm_set_sampling(llm_model* m, float temperature, int32_t top_k, float top_p, uint64_t seed);
+
 /* One decode step for sequences 0..n_seq-1 at once (n_seq == max_batch >= 2,
  * at most 32), each at its own position (its cache may come from
  * llm_kv_write or llm_prefill). The 4-bit matvecs become skinny GEMMs (fp32

@@ -14,6 +14,7 @@ import torch
 
 import bit_quantized_token_gb300 as bq
 import oracle
+from oracle import sampling
 import synth
 
 pytestmark = pytest.mark.gpu
@@ -337,6 +338,65 @@ def test_batched_prefill_matches_token_by_token(cfg, n_prompt):
                 assert rl2.max() <= 1e-2, (f"{name} of layer {l}: rel. L2 {rl2.max():.2e} at (pos, head) "
                                            f"{np.unravel_index(rl2.argmax(), rl2.shape)}")
         assert np.array_equal(m.decode_greedy(1, int(am[0]), n), ref["tokens"][1:])
+
+
+# ---------------------------------------------------------------- sampled choice
+
+def _sampled_matches(logits, token, T, k, p, seed, seq, pos):
+    """The oracle's choice from the same fp32 logits and draw; a decision may
+    differ only where its target lies within rounding of a cumulative boundary."""
+    ref, info = sampling.sample(logits, T, k, p, sampling.uniform(seed, seq, pos))
+    if token == ref:
+        return True
+    c, n = info["cum"], info["n"]
+    near = min(abs(c[j] - info["target"]) for j in range(n)) < 1e-5 or abs(c[n - 1] - p) < 1e-5
+    assert near and token in info["ids"][:n], (f"position {pos}: sampled {token}, oracle {ref} "
+                                               f"(target {info['target']:.6f}, cumulative {c[:n]})")
+    return False
+
+
+@pytest.mark.parametrize("idx,flags", [(0, 0), (0, bq.LLM_MULTI_KERNEL), (1, 0)],
+                         ids=["tiny-persistent", "tiny-multi-kernel", "tinyllama-1.1b"])
+def test_sampled_choice_matches_the_oracle(idx, flags):
+    # temperature / top-k / top-p with the Philox draw of (seed, sequence,
+    # position): every chosen token equals the oracle's choice from the GPU's
+    # own logits; the device-fed loop reproduces them from the seed alone
+    cfg = synth.workload(idx)
+    w = synth.make_weights(cfg)
+    prompt = synth.make_prompt(cfg)
+    T, k, p, seed, seq, n = 0.9, 40, 0.95, 20261202, 1, 24
+    with bq.Model(cfg, w, max_seq=len(prompt) + n + 2, max_batch=2, flags=flags) as m:
+        m.set_sampling(T, k, p, seed)
+        logits = np.empty(cfg["vocab"], np.float32)
+        am = np.zeros(1, np.int32)
+        m.prefill(seq, prompt, logits, am)
+        pos = len(prompt) - 1
+        toks = [int(am[0])]
+        exact = [_sampled_matches(logits, toks[-1], T, k, p, seed, seq, pos)]
+        not_greedy = [toks[-1] != int(np.argmax(logits))]
+        for _ in range(n):
+            pos += 1
+            m.decode_step(seq, toks[-1], logits, am)
+            toks.append(int(am[0]))
+            exact.append(_sampled_matches(logits, toks[-1], T, k, p, seed, seq, pos))
+            not_greedy.append(toks[-1] != int(np.argmax(logits)))
+        assert sum(exact) >= len(exact) - 1 and any(not_greedy)
+        # the device-fed loop draws the same tokens from the same seed
+        m.kv_reset(seq)
+        m.prefill(seq, prompt, None, am)
+        assert int(am[0]) == toks[0]
+        assert list(m.decode_greedy(seq, toks[0], n)) == toks[1:]
+        # batched prompt processing samples the same first token
+        m.kv_reset(seq)
+        m.prefill_batched(seq, prompt, logits, am)
+        _sampled_matches(logits, int(am[0]), T, k, p, seed, seq, len(prompt) - 1)
+        # temperature 0: greedy again
+        m.set_sampling(0.0)
+        m.kv_reset(seq)
+        m.prefill(seq, prompt, logits, am)
+        assert int(am[0]) == int(np.argmax(logits))
+        with pytest.raises(bq.LlmError):
+            m.set_sampling(0.5, 0)
 
 
 # ---------------------------------------------------------------- errors
