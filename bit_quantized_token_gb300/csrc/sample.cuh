@@ -12,9 +12,9 @@
 // u = (x0 >> 8) / 2^24, so a run is reproducible from the seed alone.
 //
 // One CTA of 1024 threads: an exact radix select of the k-th largest logit
-// (4 passes of 8-bit histograms over order-preserving keys), the k candidates
-// gathered in token order, ranked, then one thread does the sequential fp32
-// softmax, nucleus and draw.
+// (4 passes of 8-bit histograms over order-preserving keys held in registers),
+// the k candidates gathered in token order, ranked, then one thread does the
+// sequential fp32 softmax, nucleus and draw.
 #pragma once
 #include "common.cuh"
 
@@ -22,6 +22,7 @@ namespace llmq {
 
 constexpr int kSampleMaxK = 64;
 constexpr int kSampleThreads = 1024;
+constexpr int kSampleKPT = 32;  // logits a thread keeps per batch (a batch: 32768 logits)
 
 struct SampleCfg {      // the options, in device memory (read by the captured graphs)
   float temperature;    // <= 0: greedy, the kernel keeps the step's choice
@@ -108,15 +109,42 @@ __global__ void __launch_bounds__(kSampleThreads) sample_kernel(const SamplePara
   const int tid = threadIdx.x, V = p.V;
   const int k = min(max(cfg.top_k, 1), min(kSampleMaxK, V));
 
-  // ---- the k-th largest key, 8 bits a pass from the top
+  // ---- the k-th largest key, 8 bits a pass from the top. A thread keeps the
+  // keys of a contiguous chunk in registers (one batch of NT * KPT logits;
+  // larger vocabularies are walked batch by batch) and adds runs of equal
+  // bins to the histogram at once: the logits share their top bytes.
+  constexpr int KPT = kSampleKPT;
+  const int span = NT * KPT, nbatch = (V + span - 1) / span;
+  uint32_t kr[KPT];  // 0: no logit (no real logit has key 0)
+  auto load = [&](int b) {
+    const int base = b * span + tid * KPT;
+#pragma unroll
+    for (int e = 0; e < KPT; ++e) kr[e] = base + e < V ? sample_key(__ldcg(p.logits + base + e)) : 0u;
+  };
+  if (nbatch == 1) load(0);
   uint32_t prefix = 0u, mask = 0u;
   int krem = k, above = 0;
   for (int shift = 24; shift >= 0; shift -= 8) {
     for (int i = tid; i < 256; i += NT) hist[i] = 0;
     __syncthreads();
-    for (int i = tid; i < V; i += NT) {
-      const uint32_t key = sample_key(__ldcg(p.logits + i));
-      if ((key & mask) == prefix) atomicAdd(&hist[(key >> shift) & 255u], 1);
+    for (int b = 0; b < nbatch; ++b) {
+      if (nbatch > 1) load(b);
+      uint32_t run_bin = 0u;
+      int run = 0;
+#pragma unroll
+      for (int e = 0; e < KPT; ++e) {
+        const uint32_t key = kr[e];
+        if (key != 0u && (key & mask) == prefix) {
+          const uint32_t bin = (key >> shift) & 255u;
+          if (run > 0 && bin != run_bin) {
+            atomicAdd(&hist[run_bin], run);
+            run = 0;
+          }
+          run_bin = bin;
+          ++run;
+        }
+      }
+      if (run > 0) atomicAdd(&hist[run_bin], run);
     }
     __syncthreads();
     if (tid == 0) {  // the bin holding the krem-th largest of the keys still in play
@@ -136,32 +164,39 @@ __global__ void __launch_bounds__(kSampleThreads) sample_kernel(const SamplePara
     __syncthreads();
   }
   // keys above the threshold `prefix` (all of them) and `krem` keys equal to
-  // it, the lowest token ids first: gathered in token order from contiguous chunks
-  const int C = (V + NT - 1) / NT, i0 = min(V, tid * C), i1 = min(V, i0 + C);
-  int ngt = 0, neq = 0;
-  for (int i = i0; i < i1; ++i) {
-    const uint32_t key = sample_key(__ldcg(p.logits + i));
-    ngt += key > prefix;
-    neq += key == prefix;
-  }
-  int rgt = sample_scan(ngt, s_warp, &s_total);
-  int req = sample_scan(neq, s_warp, &s_total);
-  for (int i = i0; i < i1 && (ngt > 0 || (neq > 0 && req < krem)); ++i) {
-    const float x = __ldcg(p.logits + i);
-    const uint32_t key = sample_key(x);
-    if (key > prefix) {
-      cv[rgt] = x;
-      ci[rgt] = i;
-      ++rgt;
-      --ngt;
-    } else if (key == prefix) {
-      if (req < krem) {
-        cv[above + req] = x;
-        ci[above + req] = i;
-      }
-      ++req;
-      --neq;
+  // it, the lowest token ids first: gathered in token order (batch, thread,
+  // element) with block-wide scans
+  int gt_base = 0, eq_base = 0;
+  for (int b = 0; b < nbatch; ++b) {
+    if (nbatch > 1) load(b);
+    int ngt = 0, neq = 0;
+#pragma unroll
+    for (int e = 0; e < KPT; ++e) {
+      ngt += kr[e] != 0u && kr[e] > prefix;
+      neq += kr[e] != 0u && kr[e] == prefix;
     }
+    int rgt = gt_base + sample_scan(ngt, s_warp, &s_total);
+    const int tot_gt = s_total;
+    int req = eq_base + sample_scan(neq, s_warp, &s_total);
+    const int tot_eq = s_total;
+    const int base = b * span + tid * KPT;
+#pragma unroll
+    for (int e = 0; e < KPT; ++e) {
+      const uint32_t key = kr[e];
+      if (key != 0u && key > prefix) {
+        cv[rgt] = __ldcg(p.logits + base + e);
+        ci[rgt] = base + e;
+        ++rgt;
+      } else if (key != 0u && key == prefix) {
+        if (req < krem) {
+          cv[above + req] = __ldcg(p.logits + base + e);
+          ci[above + req] = base + e;
+        }
+        ++req;
+      }
+    }
+    gt_base += tot_gt;
+    eq_base += tot_eq;
   }
   __syncthreads();
   // ---- rank the k candidates: value descending, token id ascending
