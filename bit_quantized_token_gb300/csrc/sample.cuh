@@ -147,14 +147,28 @@ __global__ void __launch_bounds__(kSampleThreads) sample_kernel(const SamplePara
       if (run > 0) atomicAdd(&hist[run_bin], run);
     }
     __syncthreads();
-    if (tid == 0) {  // the bin holding the krem-th largest of the keys still in play
-      int acc = 0, b = 255;
-      for (; b > 0; --b) {
-        if (acc + hist[b] >= krem) break;
-        acc += hist[b];
+    if (tid < 32) {  // the bin holding the krem-th largest of the keys still in play
+      // lane l sums bins 255-8l .. 248-8l; a scan from the top finds the lane,
+      // that lane walks its 8 bins
+      int part = 0;
+#pragma unroll
+      for (int q = 0; q < 8; ++q) part += hist[255 - 8 * tid - q];
+      int incl = part;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (tid >= o) incl += y;
       }
-      s_bin = b;
-      s_acc = acc;
+      const unsigned hit = __ballot_sync(0xffffffffu, incl >= krem);
+      if (tid == __ffs(hit) - 1) {  // the first lane whose running count reaches krem
+        int acc = incl - part, b = 255 - 8 * tid;
+        for (int q = 0; q < 7; ++q, --b) {
+          if (acc + hist[b] >= krem) break;
+          acc += hist[b];
+        }
+        s_bin = b;
+        s_acc = acc;
+      }
     }
     __syncthreads();
     prefix |= (uint32_t)s_bin << shift;
