@@ -75,7 +75,11 @@ class Model(C.Structure):
 
 
 class Cache(C.Structure):
-    _fields_ = [("k", C.c_void_p), ("v", C.c_void_p), ("cap", C.c_int32), ("len", C.c_int32)]
+    _fields_ = [("k", C.c_void_p), ("v", C.c_void_p), ("cap", C.c_int32), ("len", C.c_int32),
+                ("k8", C.c_void_p), ("v8", C.c_void_p), ("ks", C.c_void_p), ("vs", C.c_void_p)]
+
+
+Q8_GROUP = 32
 
 
 def _declare(L: C.CDLL) -> None:
@@ -93,6 +97,11 @@ def _declare(L: C.CDLL) -> None:
         "orc_rope": (None, [P, i32, i32, d, i32]),
         "orc_silu_mul": (None, [P, P, i32, P]),
         "orc_attend": (None, [P, P, P, i32, i32, P]),
+        "orc_half_from_float": (C.c_uint16, [C.c_float]),
+        "orc_q8_quantize": (None, [P, i32, P, P]),
+        "orc_q8_value": (d, [C.c_int8, C.c_uint16]),
+        "orc_attend_q8": (None, [P, P, P, P, P, i32, i32, P]),
+        "orc_set_kv_q8": (None, [i32]),
         "orc_argmax_f32": (i32, [P, i64]),
         "orc_step": (i32, [P, P, i32, P, P]),
         "orc_full_prefix": (i32, [P, P, i32, P, P]),
@@ -132,6 +141,45 @@ def mutation(m: int | str):
 
 def half_to_double(bits: int) -> float:
     return float(lib().orc_half_to_double(int(bits)))
+
+
+def half_from_float(x: float) -> int:
+    return int(lib().orc_half_from_float(float(x)))
+
+
+def q8_quantize(x) -> tuple[np.ndarray, np.ndarray]:
+    """Grouped int8 codes [n] and fp16 scale bits [n / 32] of a vector (n a multiple of 32)."""
+    x = _f64(x)
+    assert x.size % Q8_GROUP == 0
+    q = np.empty(x.size, dtype=np.int8)
+    dd = np.empty(x.size // Q8_GROUP, dtype=np.uint16)
+    lib().orc_q8_quantize(_ptr(x), x.size, _ptr(q), _ptr(dd))
+    return q, dd
+
+
+def q8_values(q: np.ndarray, d: np.ndarray) -> np.ndarray:
+    """Stored values of grouped int8 codes: code x fp16 scale, exactly."""
+    return np.array([lib().orc_q8_value(int(c), int(d[i // Q8_GROUP])) for i, c in enumerate(q)])
+
+
+def attend_q8(q, k8, ks, v8, vs) -> np.ndarray:
+    """orc_attend over grouped-int8 rows: k8/v8 [n_pos][hd] int8, ks/vs [n_pos][hd/32] fp16 bits."""
+    q = _f64(q)
+    k8, v8 = (np.ascontiguousarray(a, dtype=np.int8) for a in (k8, v8))
+    ks, vs = (np.ascontiguousarray(a, dtype=np.uint16) for a in (ks, vs))
+    out = np.empty(q.size, dtype=np.float64)
+    lib().orc_attend_q8(_ptr(q), _ptr(k8), _ptr(ks), _ptr(v8), _ptr(vs), k8.shape[0], q.size, _ptr(out))
+    return out
+
+
+@contextlib.contextmanager
+def kv_q8():
+    """Full-prefix mode with grouped int8 K/V for the duration of a block."""
+    lib().orc_set_kv_q8(1)
+    try:
+        yield
+    finally:
+        lib().orc_set_kv_q8(0)
 
 
 def bf16_to_double(bits: int) -> float:
@@ -239,8 +287,8 @@ class OracleModel:
                       cfg["tied"], embed_bf16, 0, float(cfg["norm_eps"]), float(cfg["rope_theta"]))
         self._model = Model(conf, _ptr(e), _ptr(fn), lm, layers)
 
-    def new_cache(self, cap: int) -> "OracleCache":
-        return OracleCache(self.cfg, cap)
+    def new_cache(self, cap: int, kv: str = "bf16") -> "OracleCache":
+        return OracleCache(self.cfg, cap, kv)
 
     def step(self, cache: "OracleCache", tok: int, hidden: bool = False):
         cfg = self.cfg
@@ -266,13 +314,24 @@ class OracleModel:
 
 
 class OracleCache:
-    """bf16 K/V storage of one sequence: ``[n_layers][n_kv_heads][cap][head_dim]``."""
+    """K/V storage of one sequence: ``[n_layers][n_kv_heads][cap][head_dim]`` bf16,
+    or (kv="q8") int8 codes with fp16 scales ``[...][head_dim / 32]``."""
 
-    def __init__(self, cfg: dict, cap: int):
+    def __init__(self, cfg: dict, cap: int, kv: str = "bf16"):
         shape = (cfg["n_layers"], cfg["n_kv_heads"], cap, cfg["head_dim"])
         self.k = np.zeros(shape, dtype=np.uint16)
         self.v = np.zeros(shape, dtype=np.uint16)
         self.c = Cache(_ptr(self.k), _ptr(self.v), cap, 0)
+        if kv == "q8":
+            self.k8 = np.zeros(shape, dtype=np.int8)
+            self.v8 = np.zeros(shape, dtype=np.int8)
+            sshape = shape[:3] + (cfg["head_dim"] // Q8_GROUP,)
+            self.ks = np.zeros(sshape, dtype=np.uint16)
+            self.vs = np.zeros(sshape, dtype=np.uint16)
+            self.c.k8, self.c.v8 = _ptr(self.k8), _ptr(self.v8)
+            self.c.ks, self.c.vs = _ptr(self.ks), _ptr(self.vs)
+        else:
+            assert kv == "bf16", kv
 
     @property
     def len(self) -> int:

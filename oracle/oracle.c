@@ -9,7 +9,11 @@
  *     so k and v are rounded fp64 -> fp32 -> bf16 before they are stored and
  *     every position (the current one included) is read back from the cache;
  *   - the greedy choice is taken on fp32-rounded logits, the precision the GPU
- *     path decides in; lowest index wins a tie.
+ *     path decides in; lowest index wins a tie;
+ *   - optionally the cache holds K/V as grouped int8 (llmopt page, "grouped-Q8
+ *     attention/recurrent state"; the q8_0 block of GGUF files): groups of 32,
+ *     an fp16 scale amax/127 and round-to-nearest codes, all decided in fp32
+ *     (the precision the pages append from).
  * Pipeline and per-architecture variants follow the aot-llm page (sequence
  * diagram, "static pipeline", Qwen3 per-head q/k RMSNorm before RoPE, NEOX
  * pairing (i, i + rot_dim/2) versus adjacent pairs); GQA grouping and the
@@ -27,6 +31,9 @@
 #endif
 
 static int32_t g_mut = ORC_MUT_NONE;
+static int32_t g_kv_q8 = 0;
+
+void orc_set_kv_q8(int32_t on) { g_kv_q8 = on; }
 
 void orc_set_mutation(int32_t m) { g_mut = m; }
 
@@ -171,6 +178,72 @@ void orc_attend(const double* q, const uint16_t* k, const uint16_t* v, int32_t n
   free(s);
 }
 
+/* fp32 -> IEEE binary16, round to nearest even (11 significant bits; subnormal
+   spacing 2^-24; overflow to infinity). */
+uint16_t orc_half_from_float(float f) {
+  const double x = (double)f;
+  uint16_t sign = signbit(x) ? 0x8000 : 0;
+  double a = fabs(x), r;
+  if (isnan(x)) return 0x7E00;
+  if (a < ldexp(1.0, -14)) {
+    r = ldexp(nearbyint(ldexp(a, 24)), -24);
+  } else {
+    int e;
+    double m = frexp(a, &e);                          /* a = m * 2^e, m in [0.5, 1) */
+    r = ldexp(nearbyint(ldexp(m, 11)), e - 11);
+  }
+  if (r >= 65520.0 || isinf(a)) return (uint16_t)(sign | 0x7C00);
+  if (r < ldexp(1.0, -14)) return (uint16_t)(sign | (uint16_t)nearbyint(ldexp(r, 24)));
+  int e;
+  double m = frexp(r, &e);                            /* r = m * 2^e exactly */
+  const int E = e - 1 + 15;                           /* biased exponent of 1.f * 2^(e-1) */
+  const int F = (int)nearbyint(ldexp(m, 11)) - 1024;  /* 10 fraction bits */
+  return (uint16_t)(sign | (E << 10) | F);
+}
+
+void orc_q8_quantize(const double* x, int32_t n, int8_t* q, uint16_t* d) {
+  for (int32_t g = 0; g < n / ORC_Q8_GROUP; ++g) {
+    float xf[ORC_Q8_GROUP], amax = 0.0f;
+    for (int32_t i = 0; i < ORC_Q8_GROUP; ++i) {
+      xf[i] = (float)x[g * ORC_Q8_GROUP + i];
+      if (fabsf(xf[i]) > amax) amax = fabsf(xf[i]);
+    }
+    d[g] = orc_half_from_float(amax / 127.0f);
+    const float dq = (float)orc_half_to_double(d[g]);
+    for (int32_t i = 0; i < ORC_Q8_GROUP; ++i) {
+      float c = dq == 0.0f ? 0.0f : roundf(xf[i] / dq);
+      c = c > 127.0f ? 127.0f : (c < -127.0f ? -127.0f : c);
+      q[g * ORC_Q8_GROUP + i] = (int8_t)c;
+    }
+  }
+}
+
+double orc_q8_value(int8_t q, uint16_t d) { return (double)q * orc_half_to_double(d); }
+
+void orc_attend_q8(const double* q, const int8_t* k, const uint16_t* ks, const int8_t* v,
+                   const uint16_t* vs, int32_t n_pos, int32_t hd, double* out) {
+  const double scale = 1.0 / sqrt((double)hd);
+  const int32_t ng = hd / ORC_Q8_GROUP;
+  double* s = (double*)malloc((size_t)(n_pos > 0 ? n_pos : 1) * sizeof(double));
+  double mx = -INFINITY, l = 0.0;
+  for (int32_t t = 0; t < n_pos; ++t) {
+    double dot = 0.0;
+    for (int32_t d = 0; d < hd; ++d)
+      dot += q[d] * orc_q8_value(k[(int64_t)t * hd + d], ks[(int64_t)t * ng + d / ORC_Q8_GROUP]);
+    s[t] = dot * scale;
+    if (s[t] > mx) mx = s[t];
+  }
+  for (int32_t d = 0; d < hd; ++d) out[d] = 0.0;
+  for (int32_t t = 0; t < n_pos; ++t) {
+    double p = exp(s[t] - mx);
+    l += p;
+    for (int32_t d = 0; d < hd; ++d)
+      out[d] += p * orc_q8_value(v[(int64_t)t * hd + d], vs[(int64_t)t * ng + d / ORC_Q8_GROUP]);
+  }
+  for (int32_t d = 0; d < hd; ++d) out[d] /= l;
+  free(s);
+}
+
 /* Greedy choice on fp32-rounded logits; lowest index wins a tie; -1 on NaN. */
 int32_t orc_argmax_f32(const double* logits, int64_t n) {
   int64_t best = -1;
@@ -282,9 +355,15 @@ int32_t orc_step(const orc_model* m, orc_cache* cache, int32_t tok, double* logi
     orc_matvec(&L->wk, xn, k);
     orc_matvec(&L->wv, xn, v);
     qk_prepare(m, L, q, k, pos);
-    /* append this position's K and V (bf16) to the cache */
+    /* append this position's K and V (bf16, or grouped int8) to the cache */
     for (int32_t g = 0; g < Hkv; ++g) {
       int64_t base = (((int64_t)l * Hkv + g) * cache->cap + pos) * hd;
+      if (cache->k8) {
+        const int64_t sbase = base / ORC_Q8_GROUP;
+        orc_q8_quantize(k + (int64_t)g * hd, hd, cache->k8 + base, cache->ks + sbase);
+        orc_q8_quantize(v + (int64_t)g * hd, hd, cache->v8 + base, cache->vs + sbase);
+        continue;
+      }
       for (int32_t i = 0; i < hd; ++i) {
         cache->k[base + i] = orc_bf16_from_double(k[(int64_t)g * hd + i]);
         cache->v[base + i] = orc_bf16_from_double(v[(int64_t)g * hd + i]);
@@ -297,8 +376,12 @@ int32_t orc_step(const orc_model* m, orc_cache* cache, int32_t tok, double* logi
     for (int32_t h = 0; h < Hq; ++h) {
       int32_t g = kv_head_of(c, h);
       int64_t base = ((int64_t)l * Hkv + g) * cache->cap * hd;
-      orc_attend(q + (int64_t)h * hd, cache->k + base, cache->v + base, n_att, hd,
-                 o + (int64_t)h * hd);
+      if (cache->k8)
+        orc_attend_q8(q + (int64_t)h * hd, cache->k8 + base, cache->ks + base / ORC_Q8_GROUP, cache->v8 + base,
+                      cache->vs + base / ORC_Q8_GROUP, n_att, hd, o + (int64_t)h * hd);
+      else
+        orc_attend(q + (int64_t)h * hd, cache->k + base, cache->v + base, n_att, hd,
+                   o + (int64_t)h * hd);
     }
     orc_matvec(&L->wo, o, y);
     residual(x, y, d);
@@ -324,8 +407,10 @@ int32_t orc_full_prefix(const orc_model* m, const int32_t* toks, int32_t n, doub
   double* Q = (double*)malloc((size_t)n * qd * sizeof(double));
   double* K = (double*)malloc((size_t)n * kd * sizeof(double));
   double* Vv = (double*)malloc((size_t)n * kd * sizeof(double));
-  uint16_t* Kb = (uint16_t*)malloc((size_t)n * kd * sizeof(uint16_t));
-  uint16_t* Vb = (uint16_t*)malloc((size_t)n * kd * sizeof(uint16_t));
+  double* Kb = (double*)malloc((size_t)n * kd * sizeof(double));   /* K/V as read back from storage */
+  double* Vb = (double*)malloc((size_t)n * kd * sizeof(double));
+  int8_t q8[512];
+  uint16_t d8[512 / ORC_Q8_GROUP];
   double* xn = (double*)malloc((size_t)d * sizeof(double));
   double* o = (double*)malloc((size_t)qd * sizeof(double));
   double* y = (double*)malloc((size_t)d * sizeof(double));
@@ -346,20 +431,31 @@ int32_t orc_full_prefix(const orc_model* m, const int32_t* toks, int32_t n, doub
       orc_matvec(&L->wv, xn, Vv + (int64_t)t * kd);
       qk_prepare(m, L, Q + (int64_t)t * qd, K + (int64_t)t * kd, t);
     }
-    /* keys and values as the bf16 storage type: [kv_head][t][hd] */
+    /* keys and values as read back from the storage type (bf16 or grouped
+       int8): [kv_head][t][hd] */
     for (int32_t t = 0; t < n; ++t)
-      for (int32_t g = 0; g < Hkv; ++g)
-        for (int32_t i = 0; i < hd; ++i) {
-          Kb[((int64_t)g * n + t) * hd + i] = orc_bf16_from_double(K[(int64_t)t * kd + g * hd + i]);
-          Vb[((int64_t)g * n + t) * hd + i] = orc_bf16_from_double(Vv[(int64_t)t * kd + g * hd + i]);
+      for (int32_t g = 0; g < Hkv; ++g) {
+        double* kr = Kb + ((int64_t)g * n + t) * hd;
+        double* vr = Vb + ((int64_t)g * n + t) * hd;
+        if (g_kv_q8) {
+          orc_q8_quantize(K + (int64_t)t * kd + g * hd, hd, q8, d8);
+          for (int32_t i = 0; i < hd; ++i) kr[i] = orc_q8_value(q8[i], d8[i / ORC_Q8_GROUP]);
+          orc_q8_quantize(Vv + (int64_t)t * kd + g * hd, hd, q8, d8);
+          for (int32_t i = 0; i < hd; ++i) vr[i] = orc_q8_value(q8[i], d8[i / ORC_Q8_GROUP]);
+          continue;
         }
+        for (int32_t i = 0; i < hd; ++i) {
+          kr[i] = orc_bf16_to_double(orc_bf16_from_double(K[(int64_t)t * kd + g * hd + i]));
+          vr[i] = orc_bf16_to_double(orc_bf16_from_double(Vv[(int64_t)t * kd + g * hd + i]));
+        }
+      }
     /* causal attention, bottom-right aligned: key j visible to query t iff
        j <= t + (sk - sq); here sq == sk == n */
     for (int32_t t = 0; t < n; ++t) {
       for (int32_t h = 0; h < Hq; ++h) {
         int32_t g = kv_head_of(c, h);
-        const uint16_t* kg = Kb + (int64_t)g * n * hd;
-        const uint16_t* vg = Vb + (int64_t)g * n * hd;
+        const double* kg = Kb + (int64_t)g * n * hd;
+        const double* vg = Vb + (int64_t)g * n * hd;
         double mx = -INFINITY, lsum = 0.0;
         double* out = o + (int64_t)h * hd;
         for (int32_t j = 0; j < n; ++j) {
@@ -369,12 +465,10 @@ int32_t orc_full_prefix(const orc_model* m, const int32_t* toks, int32_t n, doub
           if (g_mut == ORC_MUT_QK_ORIENTATION) {
             /* planted: the roles of query and key rows exchanged */
             const double* qj = Q + (int64_t)j * qd + (int64_t)h * hd;
-            uint16_t kt[512];
-            for (int32_t i = 0; i < hd; ++i) kt[i] = kg[(int64_t)t * hd + i];
-            for (int32_t i = 0; i < hd; ++i) dot += qj[i] * orc_bf16_to_double(kt[i]);
+            for (int32_t i = 0; i < hd; ++i) dot += qj[i] * kg[(int64_t)t * hd + i];
           } else {
             const double* qt = Q + (int64_t)t * qd + (int64_t)h * hd;
-            for (int32_t i = 0; i < hd; ++i) dot += qt[i] * orc_bf16_to_double(kg[(int64_t)j * hd + i]);
+            for (int32_t i = 0; i < hd; ++i) dot += qt[i] * kg[(int64_t)j * hd + i];
           }
           s[j] = dot * scale;
           if (s[j] > mx) mx = s[j];
@@ -385,7 +479,7 @@ int32_t orc_full_prefix(const orc_model* m, const int32_t* toks, int32_t n, doub
           if (!visible) continue;
           double p = exp(s[j] - mx);
           lsum += p;
-          for (int32_t i = 0; i < hd; ++i) out[i] += p * orc_bf16_to_double(vg[(int64_t)j * hd + i]);
+          for (int32_t i = 0; i < hd; ++i) out[i] += p * vg[(int64_t)j * hd + i];
         }
         for (int32_t i = 0; i < hd; ++i) out[i] /= lsum;
       }

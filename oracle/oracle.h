@@ -53,7 +53,25 @@ typedef struct {            /* one sequence's cache, caller-owned storage */
   uint16_t* k;              /* bf16 bits [n_layers][n_kv_heads][cap][head_dim] */
   uint16_t* v;
   int32_t cap, len;
+  int8_t* k8;               /* grouped int8 instead (k, v unused): codes [n_layers][n_kv_heads][cap][head_dim] */
+  int8_t* v8;
+  uint16_t* ks;             /* fp16 scales [n_layers][n_kv_heads][cap][head_dim / 32] */
+  uint16_t* vs;
 } orc_cache;
+
+/* Grouped int8 storage of cached K/V (llmopt page, "grouped-Q8 attention
+   state"; GGUF's q8_0 block): groups of 32 values, an fp16 scale d =
+   fp16(amax / 127) from the fp32-rounded values, codes round(x / d) (half away
+   from zero, clamped to +-127; all zero when d is), value = code * d. */
+#define ORC_Q8_GROUP 32
+uint16_t orc_half_from_float(float f);     /* RNE */
+void     orc_q8_quantize(const double* x, int32_t n, int8_t* q, uint16_t* d);
+double   orc_q8_value(int8_t q, uint16_t d);
+/* orc_attend over grouped-int8 rows: codes [n_pos][hd], scales [n_pos][hd / 32]. */
+void orc_attend_q8(const double* q, const int8_t* k, const uint16_t* ks, const int8_t* v,
+                   const uint16_t* vs, int32_t n_pos, int32_t hd, double* out);
+/* Full-prefix mode keeps K/V as grouped int8 (1) or bf16 (0, the default). */
+void orc_set_kv_q8(int32_t on);
 
 /* Planted mistakes for the mutation tests (0 = none). */
 enum {
