@@ -37,7 +37,7 @@ def _reduce_worker(rank, world, port, out):
 
 def test_timed_region_is_the_slowest_rank():
     port = _free_port()
-    with mp.Manager() as man:
+    with mp.get_context("spawn").Manager() as man:  # no fork of a threaded process
         out = man.dict()
         mp.spawn(_reduce_worker, args=(2, port, out), nprocs=2, join=True)
         res = dict(out)
