@@ -23,14 +23,17 @@
 // build issues all of its loads before it uses any of them: one L2 round trip
 // per phase.
 //
-// Attention is flash-decoding over (kv head, split) items. An item loads its
-// K/V rows into padded shared-memory tiles in the same round trip as its q|k|v
-// gather; each warp then scores all GQ heads against 16 positions on the
-// tensor cores (attn_mma.cuh) and the item leaves an unnormalised partial
-// (o, max, sum) per split;
-// with few splits the o-projection's input build merges them, so the merge
-// costs no round trip of its own. With many splits (long caches) the last
-// split of a kv head merges them instead.
+// Attention is flash-decoding over (kv head, split) items. An item requests
+// its cached K/V rows (asynchronous copies into padded shared-memory tiles)
+// before the grid barrier that its q|k|v wait for; each warp then scores all
+// GQ heads against 16 positions on the tensor cores (attn_mma.cuh). In the
+// split variant the items run in their own phase and leave an unnormalised
+// partial (o, max, sum) per split; with few splits the o-projection's input
+// build merges them, so the merge costs no round trip of its own, and with
+// many splits (long caches) the last split of a kv head merges them. In the
+// FUSED variant (short caches, one kv head per o-projection range) every CTA
+// runs the one item of its range inside the o-projection's input build and
+// the attention phase is skipped.
 #pragma once
 #include "kernels.cuh"
 #include "attn_mma.cuh"
