@@ -18,11 +18,16 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 _ROOT = os.path.dirname(_HERE)
 LIB_PATH = os.path.join(_HERE, "libllmq.so")
 HEADER = os.path.join(_ROOT, "include", "llmq.h")
-SOURCES = [os.path.join(_HERE, "csrc", f) for f in ("llmq.cu", "kernels.cuh", "common.cuh")]
+CSRC = os.path.join(_HERE, "csrc")
+
+
+def sources() -> list[str]:
+    """Every file the library is compiled from: the translation unit, all headers it may include, the ABI header."""
+    return sorted(os.path.join(CSRC, f) for f in os.listdir(CSRC) if f.endswith((".cu", ".cuh", ".h"))) + [HEADER]
 
 ABI_VERSION = 1
 LLM_F32, LLM_BF16, LLM_F16, LLM_Q4G64 = 0, 1, 2, 3
-LLM_NO_GRAPH, LLM_NO_PDL, LLM_MULTI_KERNEL = 1, 2, 4
+LLM_NO_GRAPH, LLM_NO_PDL, LLM_MULTI_KERNEL, LLM_DATAFLOW_STEP = 1, 2, 4, 8
 STATUS = {0: "OK", -1: "INVALID_ARG", -2: "UNSUPPORTED", -3: "OOM", -4: "CTX_FULL", -5: "CUDA",
           -6: "TIMEOUT", -7: "NAN", -8: "NOT_FOUND"}
 
@@ -31,7 +36,7 @@ EXPORTS = ["llm_model_create", "llm_model_destroy", "llm_prefill", "llm_prefill_
            "llm_decode_greedy", "llm_set_sampling",
            "llm_decode_step_batch", "llm_kv_reset", "llm_kv_write", "llm_kv_read", "llm_kv_len",
            "llm_debug_hidden", "llm_debug_unpack", "llm_model_stats", "llm_profile_step", "llm_time_kernel", "llm_sync",
-           "llm_last_error", "llm_op_matvec", "llm_matvec_noalloc"]
+           "llm_last_error", "llm_op_matvec", "llm_matvec_noalloc", "llm_phase_times"]
 
 
 def nvcc_command(out: str = LIB_PATH) -> list[str]:
@@ -42,7 +47,7 @@ def nvcc_command(out: str = LIB_PATH) -> list[str]:
 
 def build(force: bool = False) -> str:
     """Compile libllmq.so in place for sm_103a (nvcc cross-compiles without a GPU)."""
-    newest = max(os.path.getmtime(f) for f in SOURCES + [HEADER])
+    newest = max(os.path.getmtime(f) for f in sources())
     if force or not os.path.exists(LIB_PATH) or os.path.getmtime(LIB_PATH) < newest:
         tmp = LIB_PATH + f".tmp{os.getpid()}"
         subprocess.check_call(nvcc_command(tmp))
@@ -115,6 +120,7 @@ def lib() -> C.CDLL:
             "llm_last_error": (C.c_char_p, [P]),
             "llm_op_matvec": (i32, [C.POINTER(Tensor), P, P]),
             "llm_matvec_noalloc": (i32, [P, C.c_char_p, P, P, P]),
+            "llm_phase_times": (i32, [P, i32, i32, i32, P, C.c_int64]),
         }
         for name, (res, args) in sig.items():
             f = getattr(L, name)
@@ -287,6 +293,20 @@ class Model:
         _check(lib().llm_time_kernel(self.h, seq, self.KERNELS[which], layer, n, C.byref(ms), C.byref(nb)),
                self.h)
         return float(ms.value), int(nb.value)
+
+    def phase_times(self, seq: int, token: int, n_steps: int) -> np.ndarray:
+        """Device timestamps (ns) of n_steps greedy steps through the flag-synchronised
+        step: [n_steps][phases][n_sm][16]: SM cycles (clock64) when the input build starts, its inputs
+        have arrived, the build is done, the units are done and the outputs are published; the largest
+        per-warp cycles waiting for units and in unit dots, and their sums over the warps. Record
+        [0][0][cta][12:16] holds (%globaltimer ns, clock64) at the kernel's start and end for the CTA."""
+        n_sm = self.stats()["n_sm"]
+        cap = 8 * 16 * 4096 * n_sm
+        buf = np.zeros(cap, np.uint64)
+        n = lib().llm_phase_times(self.h, seq, int(token), int(n_steps), buf.ctypes.data, cap)
+        if n < 0:
+            _check(n, self.h)
+        return buf[:16 * n].reshape(n_steps, -1, n_sm, 16)
 
     def sync(self) -> None:
         _check(lib().llm_sync(self.h), self.h)

@@ -21,6 +21,7 @@
 
 #include "kernels.cuh"
 #include "step.cuh"
+#include "stepll.cuh"
 #include "batch.cuh"
 #include "sample.cuh"
 #include "llmq.h"
@@ -245,6 +246,18 @@ struct llm_model {
   int n_phases = 0;
   int* d_step_sync = nullptr;                 // [2]: arrivals, abort
   size_t step_smem = 0;
+  // dataflow step kernel (stepll.cuh): several steps per launch
+  bool use_ll = false;
+  int ll_fuse_len = 0;                        // positions it covers (attention inside the o-projection's build)
+  LPhase* d_lphases = nullptr;
+  int n_lphases = 0;
+  uint64_t* d_ll = nullptr;                   // flagged words of every phase
+  uint32_t* d_epoch = nullptr;
+  int* d_ll_abort = nullptr;
+  uint64_t* d_cand = nullptr;
+  size_t ll_smem = 0;
+  unsigned long long* d_stamps = nullptr;     // per-phase timestamps of the last profiled launch
+  size_t stamps_steps = 0;
   // per-sequence state
   int *d_pos = nullptr, *d_tok = nullptr, *d_argmax = nullptr, *d_hist = nullptr, *d_hist_ctr = nullptr,
       *d_status = nullptr, *d_prompt = nullptr;
@@ -583,6 +596,100 @@ cudaError_t enqueue_persistent_step(llm_model* m, int seq, bool fused) {
   return launch_step_t<2, 128>(m, sp, fused);
 }
 
+
+// ---- the dataflow step: n steps of one sequence per cooperative launch
+template <int GQ, int HD>
+cudaError_t launch_ll_t(const llm_model* m, const StepLLParams& sp) {
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3(m->n_sm);
+  cfg.blockDim = dim3(kLThreads);
+  cfg.dynamicSmemBytes = m->ll_smem;
+  cfg.stream = m->stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeCooperative;  // CTAs wait on one another's words: all must be resident
+  attr[0].val.cooperative = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, stepll_kernel<GQ, HD>, sp);
+}
+
+template <typename F>
+cudaError_t with_ll_kernel(int gq, int hd, F f) {
+  if (gq == 2 && hd == 64) return f(stepll_kernel<2, 64>, stepll_smem_bytes<2, 64>());
+  if (gq == 8 && hd == 64) return f(stepll_kernel<8, 64>, stepll_smem_bytes<8, 64>());
+  return f(stepll_kernel<2, 128>, stepll_smem_bytes<2, 128>());
+}
+
+// Steps pos0 .. pos0+n-1 of sequence seq (pos0 = the sequence's device
+// position): the input token of step i < n_forced is forced[i] (device), the
+// others take the previous step's greedy choice (step 0: d_tok[seq]).
+cudaError_t enqueue_ll(llm_model* m, int seq, int n_steps, int n_forced, const int* forced,
+                       unsigned long long* stamps = nullptr) {
+  const llm_config& c = m->cfg;
+  StepLLParams sp{};
+  sp.phases = m->d_lphases;
+  sp.n_phases = m->n_lphases;
+  sp.n_steps = n_steps;
+  sp.n_forced = n_forced;
+  sp.forced = forced;
+  sp.dim = c.dim;
+  sp.vocab = c.vocab;
+  sp.eps = c.norm_eps;
+  sp.epoch = m->d_epoch;
+  sp.abort = m->d_ll_abort;
+  sp.status = m->d_status;
+  sp.embed = m->d_embed;
+  sp.q_dim = m->q_dim;
+  sp.kv_dim = m->kv_dim;
+  sp.Hkv = c.n_kv_heads;
+  sp.cap = c.max_seq;
+  sp.rope_neox = c.rope_neox;
+  sp.rope = m->d_rope;
+  sp.pos = m->d_pos + seq;
+  sp.layer_stride = (size_t)c.n_kv_heads * c.max_seq * c.head_dim;
+  sp.k_base = m->d_k + (size_t)seq * c.n_layers * sp.layer_stride;
+  sp.v_base = m->d_v + (size_t)seq * c.n_layers * sp.layer_stride;
+  sp.cand = m->d_cand;
+  sp.logits = m->d_logits;
+  sp.tok_io = m->d_tok + seq;
+  sp.argmax_out = m->d_argmax + seq;
+  sp.hist = m->d_hist;
+  sp.hist_ctr = m->d_hist_ctr;
+  sp.hist_cap = c.max_seq;
+  sp.stamps = stamps;
+  const int gq = m->gq, hd = c.head_dim;
+  if (gq == 2 && hd == 64) return launch_ll_t<2, 64>(m, sp);
+  if (gq == 8 && hd == 64) return launch_ll_t<8, 64>(m, sp);
+  return launch_ll_t<2, 128>(m, sp);
+}
+
+// Whether steps at positions pos0 .. pos0+n-1 run through the dataflow step.
+bool ll_covers(const llm_model* m, int pos0, int n) {
+  return m->use_ll && !m->sampling && n > 0 && pos0 + n <= m->ll_fuse_len;
+}
+
+// Group blocks per row tile for a phase: the (tile, block) items of the
+// CTA with the most tiles spread over the consumer warps with the fewest units
+// on the busiest warp (ties: fewer, larger blocks); at most kLRed items.
+// A block is at most bs_max units, so that one round of items (one block per
+// consumer warp) spans less than the ring minus one slot and every warp works
+// on slots the producer can have in flight together.
+int ll_blocks(int n_rt, int n_cta, int R, int GR, int bs_max) {
+  const int nr = std::max(1, n_cta / R);
+  const int nt = (n_rt + nr - 1) / nr;
+  int best = 0;
+  long best_cost = 0;
+  for (int nb = 1; nb <= GR; ++nb) {
+    if (GR % nb || (long)nt * nb > kLRed || GR / nb > bs_max) continue;
+    const long cost = (((long)nt * nb + kLWarps - 1) / kLWarps) * (GR / nb);
+    if (best == 0 || cost < best_cost) {
+      best = nb;
+      best_cost = cost;
+    }
+  }
+  return best;  // 0: no split fits
+}
+
 template <int GQ, int HD>
 cudaError_t launch_battn_t(const llm_model* m, const BAttnParams& b, int splits, int rows, bool pdl) {
   return launch(battn_mma_kernel<GQ, HD>, dim3(splits, m->cfg.n_kv_heads, rows), dim3(kBAttnThreads),
@@ -834,7 +941,24 @@ int check_status(llm_model* m) {
   CK(cudaMemsetAsync(m->d_status, 0, sizeof(int), m->stream), "status clear");
   if (st & ST_TIMEOUT) {
     m->poisoned = LLM_ERR_TIMEOUT;
-    return set_err(m, LLM_ERR_TIMEOUT, "a device-side wait exceeded its limit");
+    std::string msg = "a device-side wait exceeded its limit";
+    int where = 0;
+    if (m->d_ll_abort && cudaMemcpy(&where, m->d_ll_abort, 4, cudaMemcpyDeviceToHost) == cudaSuccess && where > 1) {
+      msg += " (flag-synchronised step: CTA " + std::to_string((where - 1) >> 8) + ", wait site " +
+             std::to_string((where - 1) & 255);
+      // where every CTA was: (step * phases + phase) * 4 + stage (0 build, 1 units, 2 publish)
+      std::vector<int> prog(m->n_sm);
+      if (cudaMemcpy(prog.data(), m->d_ll_abort + 1, 4 * (size_t)m->n_sm, cudaMemcpyDeviceToHost) == cudaSuccess) {
+        std::unordered_map<int, int> hist;
+        for (int v : prog) hist[v]++;
+        msg += "; CTAs at (phase.stage):";
+        for (auto& kv : hist)
+          msg += " " + std::to_string(kv.first / 4 % std::max(1, m->n_lphases)) + "." + std::to_string(kv.first % 4) +
+                 "x" + std::to_string(kv.second);
+      }
+      msg += ")";
+    }
+    return set_err(m, LLM_ERR_TIMEOUT, msg);
   }
   if (st & ST_NAN) return set_err(m, LLM_ERR_NAN, "NaN in the logits");
   if (st & ST_CTX_FULL) return set_err(m, LLM_ERR_CTX_FULL, "position reached max_seq on the device");
@@ -1263,6 +1387,134 @@ int llm_model_create(const llm_config* cfg, const llm_tensor* tensors, int32_t n
   m->n_phases = (int)phases.size();
   AL(m->d_phases, phases.size() * sizeof(Phase), "phase table");
   AL(m->d_step_sync, 2 * sizeof(int), "step barrier");
+  // ---- the dataflow step: the same GEMVs as phases whose outputs travel as
+  // flagged words (one region per phase), the LM head over whole rows
+  std::vector<LPhase> lph;
+  {
+    const int R = m->step_R;
+    const int hpr = R > 0 ? c.n_kv_heads / R : 0;
+    bool ok = m->use_step && (c.flags & LLM_DATAFLOW_STEP) && m->n_sm <= kLMaxCTAs && R >= 1 &&
+              c.n_kv_heads % R == 0 && hpr * gq * hd <= kSFuseOut && d / R <= kLMaxRes && d <= kLMaxKr;
+    auto lgemv = [&](const GemvPlan& g, int r) {
+      LPhase p{};
+      p.units = m->d_arena + g.m.off;
+      p.n_rt = g.m.n_rt;
+      p.G = g.m.G;
+      p.K = g.m.cols;
+      p.bf16 = g.m.bf16;
+      p.unit_bytes = g.m.unit_bytes();
+      p.R = r;
+      p.GR = g.m.G / r;
+      p.NB = ll_blocks(p.n_rt, m->n_sm, r, p.GR, (kLNSlot - 1) * (kLSlotBytes / p.unit_bytes) / kLWarps);
+      if (p.NB == 0 || g.m.G % r || g.m.cols / r > kLMaxKr) ok = false;
+      return p;
+    };
+    // word counts: per layer q|k|v, o, gate|up, down partials [n_rt][R][32],
+    // the two norms' range sums [4]; the last residual [dim]; the candidates [2N]
+    // every region starts on a 1 KB boundary: a row tile's 32 words then fill two
+    // whole cache lines, which no other CTA writes
+    size_t words = 0;
+    auto region = [&](size_t n) {
+      const size_t o = words;
+      words += (n + 127) / 128 * 128;
+      return o;
+    };
+    std::vector<size_t> o_qkv(L), o_wo(L), o_gu(L), o_dn(L), o_ssq(L), o_ssg(L);
+    for (int l = 0; l < L && ok; ++l) {
+      o_qkv[l] = region((size_t)m->qkv[l].m.n_rt * R * 32);
+      o_wo[l] = region((size_t)m->wo[l].m.n_rt * R * 32);
+      o_gu[l] = region((size_t)m->gu[l].m.n_rt * R * 32);
+      o_dn[l] = region((size_t)m->down[l].m.n_rt * R * 32);
+      o_ssq[l] = region(4);
+      o_ssg[l] = region(4);
+    }
+    const size_t o_res = region((size_t)d);
+    const size_t o_cand = region(2 * (size_t)m->n_sm);
+    if (ok) {
+      AL(m->d_ll, words * 8, "flagged words");
+      AL(m->d_epoch, 4, "step epoch");
+      AL(m->d_ll_abort, 4 * (1 + (size_t)m->n_sm), "abort flag and progress");
+      uint64_t* W = m->d_ll;
+      for (int l = 0; l < L; ++l) {
+        LPhase q = lgemv(m->qkv[l], R);
+        q.layer = l;
+        q.in_mode = l == 0 ? (m->embed_bf16 ? LIN_EMBED_BF16 : LIN_EMBED_F32) : LIN_RESID;
+        q.in_ll = l == 0 ? nullptr : W + o_dn[l - 1];
+        q.in_R = R;
+        q.norm_w = m->d_norms + m->off_attn_norm[l];
+        q.ss_out = W + o_ssq[l];
+        q.in_store = m->d_xbuf + (size_t)l * d;
+        q.out_ll = W + o_qkv[l];
+        LPhase o = lgemv(m->wo[l], R);
+        o.layer = l;
+        o.in_mode = LIN_ATTN;
+        o.in_ll = W + o_qkv[l];
+        o.in_R = R;
+        o.ss_in = W + o_ssq[l];
+        o.q_norm = c.qk_norm ? m->d_norms + m->off_q_norm[l] : nullptr;
+        o.k_norm = c.qk_norm ? m->d_norms + m->off_k_norm[l] : nullptr;
+        o.out_ll = W + o_wo[l];
+        LPhase gu = lgemv(m->gu[l], R);
+        gu.layer = l;
+        gu.in_mode = LIN_RESID;
+        gu.in_ll = W + o_wo[l];
+        gu.in_R = R;
+        gu.norm_w = m->d_norms + m->off_ffn_norm[l];
+        gu.ss_out = W + o_ssg[l];
+        gu.in_store = m->d_hbuf + (size_t)l * d;
+        gu.res_out = l == L - 1 ? W + o_res : nullptr;
+        gu.out_ll = W + o_gu[l];
+        LPhase dn = lgemv(m->down[l], R);
+        dn.layer = l;
+        dn.in_mode = LIN_SWIGLU;
+        dn.in_ll = W + o_gu[l];
+        dn.in_R = R;
+        dn.ss_in = W + o_ssg[l];
+        dn.out_ll = W + o_dn[l];
+        lph.insert(lph.end(), {q, o, gu, dn});
+      }
+      LPhase lm = lgemv(m->lm, 1);
+      lm.layer = -1;
+      lm.in_mode = LIN_FINAL;
+      lm.in_ll = W + o_dn[L - 1];
+      lm.in_R = R;
+      lm.res_ll = W + o_res;
+      lm.norm_w = m->d_norms + m->off_final_norm;
+      lm.in_store = m->d_xbuf + (size_t)L * d;
+      lm.out_ll = nullptr;
+      lph.push_back(lm);
+      m->d_cand = W + o_cand;
+    }
+    if (ok) {
+      with_ll_kernel(gq, hd, [&](auto kern, size_t smem) {
+        m->ll_smem = smem;
+        int per_sm = 0;
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e == cudaSuccess) e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kLThreads, smem);
+        if (e != cudaSuccess || per_sm < 1) {
+          cudaGetLastError();
+          ok = false;  // the barrier-synchronised step serves every call
+        }
+        return cudaSuccess;
+      });
+    }
+    m->use_ll = ok;
+    m->ll_fuse_len = ok ? 4 * step_attn_pp(hd) : 0;
+    if (ok) {
+      m->n_lphases = (int)lph.size();
+      AL(m->d_lphases, lph.size() * sizeof(LPhase), "dataflow phase table");
+      const size_t ll_bytes = words * 8;
+      cudaError_t e = cudaMemset(m->d_ll, 0, ll_bytes);  // flag 0: never a step's flag
+      const uint32_t one = 1;
+      if (e == cudaSuccess) e = cudaMemcpy(m->d_epoch, &one, 4, cudaMemcpyHostToDevice);
+      if (e == cudaSuccess) e = cudaMemset(m->d_ll_abort, 0, 4 * (1 + (size_t)m->n_sm));
+      if (e == cudaSuccess)
+        e = cudaMemcpy(m->d_lphases, lph.data(), lph.size() * sizeof(LPhase), cudaMemcpyHostToDevice);
+      if (e != cudaSuccess) return fail(cuda_fail(m, e, "dataflow step setup"));
+      m->stamps_steps = kLStampSteps;
+      AL(m->d_stamps, (size_t)kLStampSteps * m->n_lphases * m->n_sm * 16 * 8, "phase timestamps");
+    }
+  }
   // ---- the batched pipeline (one token for every sequence of a batch, or a
   // chunk of up to kBM prompt tokens of one sequence)
   size_t bcnt_total = 0;
@@ -1368,7 +1620,7 @@ int llm_model_create(const llm_config* cfg, const llm_tensor* tensors, int32_t n
   }
   m->len.assign(c.max_batch, 0);
   m->graphs.assign(2 * (size_t)c.max_batch, nullptr);  // per sequence: split, fused variant
-  m->kernels_per_step = m->use_step ? 1 : 5 * L + 1;
+  m->kernels_per_step = (m->use_step || m->use_ll) ? 1 : 5 * L + 1;
   *out = m;
   return LLM_OK;
 }
@@ -1381,7 +1633,11 @@ int llm_decode_step(llm_model* m, int32_t seq, int32_t token, float* logits_out,
   // pageable source: staged at call time, so back-to-back asynchronous calls cannot race
   const int32_t tok_host = token;
   CK(cudaMemcpyAsync(m->d_tok + seq, &tok_host, 4, cudaMemcpyHostToDevice, m->stream), "token upload");
-  if ((rc = run_step(m, seq, m->len[seq])) != LLM_OK) return rc;
+  if (ll_covers(m, m->len[seq], 1)) {
+    CK(enqueue_ll(m, seq, 1, 0, nullptr), "step launch");
+  } else if ((rc = run_step(m, seq, m->len[seq])) != LLM_OK) {
+    return rc;
+  }
   m->len[seq] += 1;
   bool host = false;
   if ((rc = copy_out(m, logits_out, m->d_logits, (size_t)m->cfg.vocab * 4, &host)) != LLM_OK) return rc;
@@ -1401,9 +1657,13 @@ int llm_prefill(llm_model* m, int32_t seq, const int32_t* tokens, int32_t n, flo
     if (host_toks[i] < 0 || host_toks[i] >= m->cfg.vocab)
       return set_err(m, LLM_ERR_INVALID_ARG, "prompt token out of range");
   CK(cudaMemcpyAsync(m->d_prompt, host_toks.data(), (size_t)n * 4, cudaMemcpyHostToDevice, m->stream), "prompt upload");
-  for (int i = 0; i < n; ++i) {
-    CK(cudaMemcpyAsync(m->d_tok + seq, m->d_prompt + i, 4, cudaMemcpyDeviceToDevice, m->stream), "token copy");
-    if ((rc = run_step(m, seq, m->len[seq] + i)) != LLM_OK) return rc;
+  if (ll_covers(m, m->len[seq], n)) {
+    CK(enqueue_ll(m, seq, n, n, m->d_prompt), "prefill launch");  // every step's token forced
+  } else {
+    for (int i = 0; i < n; ++i) {
+      CK(cudaMemcpyAsync(m->d_tok + seq, m->d_prompt + i, 4, cudaMemcpyDeviceToDevice, m->stream), "token copy");
+      if ((rc = run_step(m, seq, m->len[seq] + i)) != LLM_OK) return rc;
+    }
   }
   m->len[seq] += n;
   bool host = false;
@@ -1496,7 +1756,16 @@ int llm_decode_greedy(llm_model* m, int32_t seq, int32_t first_token, int32_t n_
   const int32_t tok_host = first_token;  // pageable: staged at call time
   CK(cudaMemcpyAsync(m->d_tok + seq, &tok_host, 4, cudaMemcpyHostToDevice, m->stream), "token upload");
   CK(cudaMemsetAsync(m->d_hist_ctr, 0, 4, m->stream), "history reset");
-  for (int i = 0; i < n_steps; ++i)
+  // the steps the dataflow kernel covers go in one launch, the rest step by step
+  int done = 0;
+  if (m->use_ll && !m->sampling) {
+    const int n1 = std::min(n_steps, m->ll_fuse_len - m->len[seq]);
+    if (n1 > 0) {
+      CK(enqueue_ll(m, seq, n1, 0, nullptr), "greedy launch");
+      done = n1;
+    }
+  }
+  for (int i = done; i < n_steps; ++i)
     if ((rc = run_step(m, seq, m->len[seq] + i)) != LLM_OK) return rc;
   m->len[seq] += n_steps;
   bool host = false;
@@ -1712,6 +1981,29 @@ int llm_time_kernel(llm_model* m, int32_t seq, int32_t which, int32_t layer, int
   *ms = t / (float)(n * seqn.size());
   *bytes = total_bytes / (int64_t)seqn.size();
   return check_status(m);
+}
+
+int llm_phase_times(llm_model* m, int32_t seq, int32_t first_token, int32_t n_steps, uint64_t* out,
+                    int64_t max_out) {
+  int rc = check_model(m, seq);
+  if (rc) return rc;
+  if (!m->use_ll) return set_err(m, LLM_ERR_UNSUPPORTED, "no flag-synchronised step on this model");
+  if (n_steps <= 0 || n_steps > (int)m->stamps_steps || !out)
+    return set_err(m, LLM_ERR_INVALID_ARG, "n_steps outside 1..8 or null output");
+  if (first_token < 0 || first_token >= m->cfg.vocab) return set_err(m, LLM_ERR_INVALID_ARG, "token out of range");
+  if (!ll_covers(m, m->len[seq], n_steps))
+    return set_err(m, LLM_ERR_UNSUPPORTED, "positions beyond the flag-synchronised step's range (or sampling on)");
+  const int64_t n = (int64_t)n_steps * m->n_lphases * m->n_sm * 16;
+  if (max_out < n) return set_err(m, LLM_ERR_INVALID_ARG, "output too small");
+  const int32_t tok_host = first_token;
+  CK(cudaMemcpyAsync(m->d_tok + seq, &tok_host, 4, cudaMemcpyHostToDevice, m->stream), "token upload");
+  CK(cudaMemsetAsync(m->d_stamps, 0, (size_t)n * 8, m->stream), "timestamp reset");
+  CK(enqueue_ll(m, seq, n_steps, 0, nullptr, m->d_stamps), "profiled launch");
+  m->len[seq] += n_steps;
+  CK(cudaMemcpyAsync(out, m->d_stamps, (size_t)n * 8, cudaMemcpyDeviceToHost, m->stream), "timestamps");
+  CK(cudaStreamSynchronize(m->stream), "profile sync");
+  rc = check_status(m);
+  return rc ? rc : (int)(n / 16);
 }
 
 int llm_sync(llm_model* m) {

@@ -51,6 +51,9 @@ typedef enum { LLM_F32 = 0, LLM_BF16 = 1, LLM_F16 = 2, LLM_Q4G64 = 3 } llm_dtype
 #define LLM_NO_GRAPH 1u       /* launch the step's kernels one by one (debugging) */
 #define LLM_NO_PDL   2u       /* no programmatic dependent launch between kernels */
 #define LLM_MULTI_KERNEL 4u   /* one kernel per phase instead of the persistent step kernel */
+#define LLM_DATAFLOW_STEP 8u  /* greedy batch-1 steps on the flag-synchronised persistent kernel (phases
+                                 wait on flagged words instead of grid barriers; slower than the
+                                 default grid-barrier step on GB300, kept for comparison) */
 
 typedef struct {
   int32_t abi_version;        /* must equal LLMQ_ABI_VERSION */
@@ -62,7 +65,7 @@ typedef struct {
   int32_t tied_embedding;     /* 1: LM head is the bf16 embedding table */
   int32_t max_seq;            /* KV capacity per sequence (positions) */
   int32_t max_batch;          /* number of sequences (independent caches) */
-  uint32_t flags;             /* LLM_NO_GRAPH | LLM_NO_PDL | LLM_MULTI_KERNEL */
+  uint32_t flags;             /* LLM_NO_GRAPH | LLM_NO_PDL | LLM_MULTI_KERNEL | LLM_DATAFLOW_STEP */
 } llm_config;
 
 /* One input tensor in the canonical layout, host memory, caller-owned, only
@@ -225,6 +228,23 @@ int llm_profile_step(llm_model* m, int32_t seq, int32_t token, llm_kernel_time* 
  * completed step of seq. */
 int llm_time_kernel(llm_model* m, int32_t seq, int32_t which, int32_t layer, int32_t n, float* ms,
                     int64_t* bytes);
+
+/* Run n_steps (1..8) greedy steps of sequence seq from first_token through the
+ * flag-synchronised step kernel in one launch and record, for every (step,
+ * phase, CTA), 16 values: the SM cycle counter (clock64) when the phase's
+ * input build starts, when its inputs have all arrived, when the build is
+ * done, when the phase's weight units are done and when its outputs are
+ * published (the LM head's stays 0); the largest and the summed per-warp
+ * cycles spent waiting for weight units and computing unit dots; values 12..15
+ * of the CTA's (step 0, phase 0) record hold (%globaltimer ns, clock64) at the
+ * kernel's start and end, which map its cycles onto one time line.
+ * out [n_steps][phases][n_sm][16] (host); phases are the four GEMVs of every
+ * layer (q|k|v, o with the attention in its build, gate|up, down) and the LM
+ * head. Returns the number of records (n_steps * phases * n_sm) or a negative
+ * llm_status (UNSUPPORTED when the step kernel does not cover these
+ * positions). len += n_steps. For measurement, not the token loop. */
+int llm_phase_times(llm_model* m, int32_t seq, int32_t first_token, int32_t n_steps, uint64_t* out,
+                    int64_t max_out);
 
 /* Wait for all queued work of the model and report device-side errors. */
 int llm_sync(llm_model* m);

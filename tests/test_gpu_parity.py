@@ -160,9 +160,9 @@ def check_against_oracle(cfg, toks, logits, hid, ref, greedy=True):
 
 
 @pytest.mark.parametrize("flags", [0, bq.LLM_NO_GRAPH, bq.LLM_MULTI_KERNEL, bq.LLM_MULTI_KERNEL | bq.LLM_NO_GRAPH,
-                                   bq.LLM_MULTI_KERNEL | bq.LLM_NO_PDL],
+                                   bq.LLM_MULTI_KERNEL | bq.LLM_NO_PDL, bq.LLM_DATAFLOW_STEP],
                          ids=["persistent", "persistent-eager", "multi-kernel-graph+pdl", "multi-kernel-eager+pdl",
-                              "multi-kernel-graph"])
+                              "multi-kernel-graph", "dataflow"])
 def test_tiny_llama_greedy_matches_oracle(flags):
     cfg = synth.workload(0)
     w = synth.make_weights(cfg)
@@ -191,14 +191,17 @@ def test_bit_reproducible():
     assert np.array_equal(outs[0], outs[1])
 
 
-def test_qwen_shape_two_layers_full_vocab():
+@pytest.mark.parametrize("flags", [0, bq.LLM_DATAFLOW_STEP], ids=["barrier", "dataflow"])
+def test_qwen_shape_two_layers_full_vocab(flags):
     # tied bf16 LM head over the full 151936-token vocabulary, q/k norm, NEOX
     cfg = synth.workload(2, n_layers=2)
     w = synth.make_weights(cfg)
     prompt = synth.make_prompt(cfg)
     ref = oracle.greedy_run(oracle.OracleModel(cfg, w), prompt, 20, hidden=True)
-    with bq.Model(cfg, w, max_seq=64) as m:
+    with bq.Model(cfg, w, max_seq=64, flags=flags) as m:
         toks, logits, hid = gpu_run(m, cfg, prompt, 20, hidden=True)
+        if flags:
+            assert m.stats()["kernels_per_step"] == 1
     check_against_oracle(cfg, toks, logits, hid, ref)
 
 
@@ -209,7 +212,7 @@ def test_full_size_greedy_matches_oracle(idx):
     prompt = synth.make_prompt(cfg)
     n = cfg["decode_steps"]
     ref = oracle.greedy_run(oracle.OracleModel(cfg, w), prompt, n, hidden=True)
-    for flags in (0, bq.LLM_MULTI_KERNEL):
+    for flags in (0, bq.LLM_MULTI_KERNEL, bq.LLM_DATAFLOW_STEP):
         with bq.Model(cfg, w, max_seq=len(prompt) + n + 1, flags=flags) as m:
             toks, logits, hid = gpu_run(m, cfg, prompt, n, hidden=True)
         check_against_oracle(cfg, toks, logits, hid, ref)
@@ -249,7 +252,8 @@ def test_long_context_teacher_forced():
 @pytest.mark.parametrize("cfg,n_pre", [(synth.workload(1, n_layers=2, vocab=4096), 500),
                                        (synth.workload(2, n_layers=2, vocab=4096), 370)],
                          ids=["tinyllama-shape-fused-then-split", "qwen3-shape-split"])
-def test_attention_paths_across_the_switch(cfg, n_pre):
+@pytest.mark.parametrize("flags", [0, bq.LLM_DATAFLOW_STEP], ids=["barrier", "dataflow"])
+def test_attention_paths_across_the_switch(cfg, n_pre, flags):
     # Short caches, one kv head per o-projection range (the TinyLlama shape):
     # every CTA of the persistent step attends over the cache inside the
     # o-projection's input build; from 4 passes of positions (512) on, the
@@ -261,7 +265,7 @@ def test_attention_paths_across_the_switch(cfg, n_pre):
     cap = n_pre + n + 1
     om = oracle.OracleModel(cfg, w)
     cache = om.new_cache(cap)
-    with bq.Model(cfg, w, max_seq=cap) as m:
+    with bq.Model(cfg, w, max_seq=cap, flags=flags) as m:
         for l in range(cfg["n_layers"]):
             k, v = synth.make_prefilled_kv(cfg, l, 0, n_pre)
             cache.fill(l, k, v)
