@@ -28,6 +28,8 @@ def sources() -> list[str]:
 ABI_VERSION = 1
 LLM_F32, LLM_BF16, LLM_F16, LLM_Q4G64 = 0, 1, 2, 3
 LLM_NO_GRAPH, LLM_NO_PDL, LLM_MULTI_KERNEL, LLM_DATAFLOW_STEP = 1, 2, 4, 8
+LLM_DEBUG_BATCH_HIDDEN = 16
+LLM_TEST_EXPIRE_WAIT = 0x80000000
 STATUS = {0: "OK", -1: "INVALID_ARG", -2: "UNSUPPORTED", -3: "OOM", -4: "CTX_FULL", -5: "CUDA",
           -6: "TIMEOUT", -7: "NAN", -8: "NOT_FOUND"}
 
@@ -36,7 +38,8 @@ EXPORTS = ["llm_model_create", "llm_model_destroy", "llm_prefill", "llm_prefill_
            "llm_decode_greedy", "llm_set_sampling",
            "llm_decode_step_batch", "llm_kv_reset", "llm_kv_write", "llm_kv_read", "llm_kv_len",
            "llm_debug_hidden", "llm_debug_unpack", "llm_model_stats", "llm_profile_step", "llm_time_kernel", "llm_sync",
-           "llm_last_error", "llm_op_matvec", "llm_matvec_noalloc", "llm_phase_times"]
+           "llm_last_error", "llm_op_matvec", "llm_matvec_noalloc", "llm_phase_times", "llm_debug_fail_alloc",
+           "llm_debug_hidden_batch"]
 
 
 def nvcc_command(out: str = LIB_PATH) -> list[str]:
@@ -121,6 +124,8 @@ def lib() -> C.CDLL:
             "llm_op_matvec": (i32, [C.POINTER(Tensor), P, P]),
             "llm_matvec_noalloc": (i32, [P, C.c_char_p, P, P, P]),
             "llm_phase_times": (i32, [P, i32, i32, i32, P, C.c_int64]),
+            "llm_debug_fail_alloc": (i32, [i32]),
+            "llm_debug_hidden_batch": (i32, [P, P]),
         }
         for name, (res, args) in sig.items():
             f = getattr(L, name)
@@ -263,6 +268,12 @@ class Model:
         _check(lib().llm_debug_hidden(self.h, out.ctypes.data), self.h)
         return out
 
+    def hidden_batch(self) -> np.ndarray:
+        """Per-layer residuals of the last batched step: [n_layers+1, max_batch, dim]."""
+        out = np.empty((self.cfg["n_layers"] + 1, self.max_batch, self.cfg["dim"]), np.float32)
+        _check(lib().llm_debug_hidden_batch(self.h, out.ctypes.data), self.h)
+        return out
+
     def unpack(self, name: str, rows: int, cols: int):
         codes = np.empty((rows, cols // 2), np.uint8)
         scales = np.empty((rows, cols // 64), np.uint16)
@@ -319,6 +330,11 @@ def matvec(t: dict, x) -> np.ndarray:
     y = np.empty(int(t["rows"]), np.float32)
     _check(lib().llm_op_matvec(table, x.ctypes.data, y.ctypes.data))
     return y
+
+
+def debug_fail_alloc(nth: int) -> None:
+    """Test hook: the nth device allocation of the models created next fails (0 disarms)."""
+    _check(lib().llm_debug_fail_alloc(int(nth)))
 
 
 def matvec_noalloc(model: Model, name: str, x, y, stream: int | None = None) -> None:

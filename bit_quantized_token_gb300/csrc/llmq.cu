@@ -10,6 +10,7 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <atomic>
 #include <cmath>
 #include <cstdio>
 #include <cstring>
@@ -231,6 +232,7 @@ struct llm_model {
   std::vector<BPlan> bqkv, bwo, bgu, bdown;
   BPlan blm;
   float *d_bss_x = nullptr, *d_bss_h = nullptr;  // batched: per-(row block, token) sums of squares
+  float* d_bhid = nullptr;  // [L+1][max_batch][dim] residual after the embedding and each layer (LLM_DEBUG_BATCH_HIDDEN)
   float *d_bx = nullptr, *d_bh = nullptr, *d_bqkv = nullptr, *d_bo = nullptr, *d_ba = nullptr,
         *d_blogits = nullptr, *d_bpart = nullptr, *d_battn_part = nullptr, *d_bcand_v = nullptr;
   int *d_bcand_i = nullptr, *d_bcnt = nullptr, *d_battn_cnt = nullptr, *d_bgreedy_cnt = nullptr;
@@ -298,9 +300,17 @@ int cuda_fail(llm_model* m, cudaError_t e, const char* what) {
     if (e_ != cudaSuccess) return cuda_fail(m, e_, what); \
   } while (0)
 
+// llm_debug_fail_alloc: the device allocation (counted from 1) of the models
+// created next that reports cudaErrorMemoryAllocation instead of allocating
+std::atomic<int> g_fail_alloc{0};
+
 template <typename T>
 cudaError_t dalloc(llm_model* m, T** p, size_t bytes) {
   void* q = nullptr;
+  int n = g_fail_alloc.load();
+  while (n > 0 && !g_fail_alloc.compare_exchange_weak(n, n - 1)) {
+  }
+  if (n == 1) return cudaErrorMemoryAllocation;
   cudaError_t e = cudaMalloc(&q, std::max<size_t>(bytes, 16));
   if (e != cudaSuccess) return e;
   m->allocs.push_back(q);
@@ -316,6 +326,20 @@ bool is_device_ptr(const void* p) {
     return false;
   }
   return a.type == cudaMemoryTypeDevice || a.type == cudaMemoryTypeManaged;
+}
+
+// A kernel's dynamic shared memory limit is process-wide state of the
+// device, shared by every model and call that launches the same kernel
+// instantiation with different sizes: it is only ever raised.
+std::mutex g_smem_limit_mu;
+template <typename Kern>
+cudaError_t raise_smem_limit(Kern kern, size_t bytes) {
+  std::lock_guard<std::mutex> lk(g_smem_limit_mu);
+  cudaFuncAttributes a{};
+  cudaError_t e = cudaFuncGetAttributes(&a, kern);
+  if (e != cudaSuccess) return e;
+  if ((size_t)a.maxDynamicSharedSizeBytes >= bytes) return cudaSuccess;
+  return cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
 }
 
 template <typename Kern, typename Params>
@@ -559,6 +583,10 @@ cudaError_t enqueue_persistent_step(llm_model* m, int seq, bool fused) {
   sp.dim = c.dim;
   sp.sync = m->d_step_sync;
   sp.status = m->d_status;
+  // the expiry test: a barrier no CTA set can reach, a 1 ms limit
+  const bool expire = (c.flags & LLM_TEST_EXPIRE_WAIT) != 0;
+  sp.bar_extra = expire ? 1 : 0;
+  sp.wait_ns = expire ? 1000000ull : kWaitLimitNs;
   sp.embed = m->d_embed;
   sp.tok = m->d_tok + seq;
   sp.vocab = c.vocab;
@@ -697,8 +725,7 @@ cudaError_t launch_battn_t(const llm_model* m, const BAttnParams& b, int splits,
 }
 template <int GQ, int HD>
 cudaError_t battn_smem_attr() {
-  return cudaFuncSetAttribute(battn_mma_kernel<GQ, HD>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              (int)sizeof(BAttnSmem<GQ, HD>));
+  return raise_smem_limit(battn_mma_kernel<GQ, HD>, sizeof(BAttnSmem<GQ, HD>));
 }
 cudaError_t battn_set_smem(int gq, int hd) {
   switch (gq * 1000 + hd) {
@@ -784,7 +811,14 @@ BatchedIO decode_io(llm_model* m) {
 cudaError_t enqueue_batched(llm_model* m, const BatchedIO& io) {
   const llm_config& c = m->cfg;
   const int L = c.n_layers, d = c.dim, B = io.M, F = c.ffn_dim;
-  const bool pdl = !(c.flags & LLM_NO_PDL);
+  // the hidden-state capture copies sit between the kernels: no programmatic launches then
+  const bool capture = m->d_bhid && !io.chunk && io.M == c.max_batch;
+  const bool pdl = !(c.flags & LLM_NO_PDL) && !capture;
+  auto capture_x = [&](int k) {  // the residual after the embedding (k = 0) or layer k - 1
+    return capture ? cudaMemcpyAsync(m->d_bhid + (size_t)k * B * d, m->d_bx, (size_t)B * d * 4,
+                                     cudaMemcpyDeviceToDevice, m->stream)
+                   : cudaSuccess;
+  };
   cudaError_t e;
   BEmbedParams ep{};
   ep.embed = m->d_embed;
@@ -797,6 +831,7 @@ cudaError_t enqueue_batched(llm_model* m, const BatchedIO& io) {
   ep.ss_out = m->d_bss_x;
   ep.status = m->d_status;
   if ((e = launch(bembed_kernel, dim3(B), dim3(256), 0, m->stream, false, ep)) != cudaSuccess) return e;
+  if ((e = capture_x(0)) != cudaSuccess) return e;
   const size_t kv_layer = (size_t)c.n_kv_heads * c.max_seq * c.head_dim;
   const int qkv_cols = m->q_dim + 2 * m->kv_dim;
   for (int l = 0; l < L; ++l) {
@@ -866,6 +901,7 @@ cudaError_t enqueue_batched(llm_model* m, const BatchedIO& io) {
     p.out = m->d_bx;
     p.out_cols = d;
     if ((e = launch_bgemv(m, m->bdown[l], p, pdl)) != cudaSuccess) return e;
+    if ((e = capture_x(l + 1)) != cudaSuccess) return e;
   }
   if (!io.lm) return cudaSuccess;
   BGemvParams p = bgemv_params(m, m->blm, B);  // logits, greedy choice per sequence, positions += 1
@@ -1297,7 +1333,7 @@ int llm_model_create(const llm_config* cfg, const llm_tensor* tensors, int32_t n
     with_step_kernel(gq, hd, fused, [&](auto kern, size_t smem) {
       m->step_smem = smem;
       int per_sm = 0;
-      cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+      cudaError_t e = raise_smem_limit(kern, smem);
       if (e == cudaSuccess) e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kSThreads, smem);
       if (e != cudaSuccess || per_sm < 1) {
         cudaGetLastError();
@@ -1489,7 +1525,7 @@ int llm_model_create(const llm_config* cfg, const llm_tensor* tensors, int32_t n
       with_ll_kernel(gq, hd, [&](auto kern, size_t smem) {
         m->ll_smem = smem;
         int per_sm = 0;
-        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        cudaError_t e = raise_smem_limit(kern, smem);
         if (e == cudaSuccess) e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kLThreads, smem);
         if (e != cudaSuccess || per_sm < 1) {
           cudaGetLastError();
@@ -1538,6 +1574,7 @@ int llm_model_create(const llm_config* cfg, const llm_tensor* tensors, int32_t n
     }
     bcnt_total = (size_t)max_blocks + (size_t)B * c.n_kv_heads + 1;
     AL(m->d_bx, (size_t)B * d * 4, "batched residual");
+    if (c.flags & LLM_DEBUG_BATCH_HIDDEN) AL(m->d_bhid, (size_t)(L + 1) * B * d * 4, "batched hidden-state capture");
     AL(m->d_bss_x, (size_t)max_blocks * kBM * 4, "batched sums of squares");
     AL(m->d_bss_h, (size_t)max_blocks * kBM * 4, "batched sums of squares");
     AL(m->d_bh, (size_t)B * d * 4, "batched residual");
@@ -1602,9 +1639,9 @@ int llm_model_create(const llm_config* cfg, const llm_tensor* tensors, int32_t n
     if (e == cudaSuccess) e = cudaMemset(m->d_status, 0, 4);
     if (e == cudaSuccess && m->d_bcnt) e = cudaMemset(m->d_bcnt, 0, bcnt_total * 4);
     if (e == cudaSuccess && m->bsmem_max)
-      e = cudaFuncSetAttribute(bgemv_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)m->bsmem_max);
+      e = raise_smem_limit(bgemv_kernel<false>, m->bsmem_max);
     if (e == cudaSuccess && m->bsmem_max)
-      e = cudaFuncSetAttribute(bgemv_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)m->bsmem_max);
+      e = raise_smem_limit(bgemv_kernel<true>, m->bsmem_max);
     if (e == cudaSuccess) e = battn_set_smem(gq, hd);
     if (e == cudaSuccess) e = cudaMemset(m->d_k, 0, kv_elems * 2);
     if (e == cudaSuccess) e = cudaMemset(m->d_v, 0, kv_elems * 2);
@@ -1612,9 +1649,9 @@ int llm_model_create(const llm_config* cfg, const llm_tensor* tensors, int32_t n
     for (int l = 0; l < L; ++l)
       smax = std::max({smax, m->qkv[l].smem, m->wo[l].smem, m->gu[l].smem, m->down[l].smem});
     if (e == cudaSuccess)
-      e = cudaFuncSetAttribute(gemv_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smax);
+      e = raise_smem_limit(gemv_kernel<false>, smax);
     if (e == cudaSuccess)
-      e = cudaFuncSetAttribute(gemv_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smax);
+      e = raise_smem_limit(gemv_kernel<true>, smax);
     if (e == cudaSuccess) e = cudaDeviceSynchronize();
     if (e != cudaSuccess) return fail(cuda_fail(m, e, "initialisation"));
   }
@@ -1887,6 +1924,22 @@ int llm_debug_hidden(llm_model* m, float* out) {
   return LLM_OK;
 }
 
+int llm_debug_hidden_batch(llm_model* m, float* out) {
+  int rc = check_model(m, 0);
+  if (rc) return rc;
+  if (!out) return set_err(m, LLM_ERR_INVALID_ARG, "null output");
+  if (!m->d_bhid) return set_err(m, LLM_ERR_UNSUPPORTED, "the model was not created with LLM_DEBUG_BATCH_HIDDEN");
+  const size_t n = (size_t)(m->cfg.n_layers + 1) * m->cfg.max_batch * m->cfg.dim;
+  CK(cudaMemcpyAsync(out, m->d_bhid, n * 4, cudaMemcpyDefault, m->stream), "hidden copy");
+  CK(cudaStreamSynchronize(m->stream), "hidden sync");
+  return LLM_OK;
+}
+
+int llm_debug_fail_alloc(int32_t nth) {
+  g_fail_alloc.store(nth > 0 ? nth : 0);
+  return LLM_OK;
+}
+
 int llm_debug_unpack(llm_model* m, const char* name, uint8_t* codes, uint16_t* scales, uint16_t* mins) {
   int rc = check_model(m, 0);
   if (rc) return rc;
@@ -2049,8 +2102,7 @@ int llm_op_matvec(const llm_tensor* w, const float* x, float* y) {
   if (e == cudaSuccess) e = cudaMemset(d_status, 0, 4);
   if (e == cudaSuccess) e = cudaMemset(d_cnt, 0, (size_t)mat.n_rt * 4);
   if (e == cudaSuccess)
-    e = cudaFuncSetAttribute(bf16 ? gemv_kernel<true> : gemv_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)g.smem);
+    e = bf16 ? raise_smem_limit(gemv_kernel<true>, g.smem) : raise_smem_limit(gemv_kernel<false>, g.smem);
   int st = 0;
   if (e == cudaSuccess) {
     GemvParams p{};
@@ -2110,8 +2162,19 @@ extern "C" int llm_matvec_noalloc(const llm_model* m, const char* name, const fl
   int dev = -1;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return cuda_fail(mm, e, "cudaGetDevice");
-  if (dev != m->device || dev >= kMaxDevices)
-    return set_err(mm, LLM_ERR_INVALID_ARG, "the model's device must be the current device");
+  if (dev != m->device) return set_err(mm, LLM_ERR_INVALID_ARG, "the model's device must be the current device");
+  if (dev >= kMaxDevices)
+    return set_err(mm, LLM_ERR_UNSUPPORTED, "device ordinal " + std::to_string(dev) + " is beyond the " +
+                                                std::to_string(kMaxDevices) + " devices this call serves");
+  cudaStream_t st = static_cast<cudaStream_t>(cuda_stream);
+  {
+    // the call reads its status back and synchronises: it cannot be captured
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    e = cudaStreamIsCapturing(st, &cs);
+    if (e != cudaSuccess) return cuda_fail(mm, e, "cudaStreamIsCapturing");
+    if (cs != cudaStreamCaptureStatusNone)
+      return set_err(mm, LLM_ERR_INVALID_ARG, "the stream is capturing: this call synchronises and cannot be captured");
+  }
   if (!is_device_ptr(x) || !is_device_ptr(y)) return set_err(mm, LLM_ERR_INVALID_ARG, "x and y must be device memory");
   // the weight rows: a 4-bit tensor stored as a contiguous row range, or the tied bf16 LM head
   const Mat* mat = nullptr;
@@ -2155,7 +2218,6 @@ extern "C" int llm_matvec_noalloc(const llm_model* m, const char* name, const fl
   float* part = static_cast<float*>(base);
   int* counters = reinterpret_cast<int*>(static_cast<unsigned char*>(base) + kNoAllocPartFloats * 4);
   int* status = counters + kNoAllocCounters;
-  cudaStream_t st = static_cast<cudaStream_t>(cuda_stream);
   // the array keeps the previous call's contents: counters and status must start at zero
   e = cudaMemsetAsync(counters, 0, (size_t)sub.n_rt * 4, st);
   if (e == cudaSuccess) e = cudaMemsetAsync(status, 0, 4, st);
@@ -2177,6 +2239,10 @@ extern "C" int llm_matvec_noalloc(const llm_model* m, const char* name, const fl
   p.part_buf = part;
   p.counters = counters;
   p.status = status;
+  // another model or call may have left the kernel's shared memory limit
+  // below this matrix's need: raise it (never lower it)
+  e = sub.bf16 ? raise_smem_limit(gemv_kernel<true>, g.smem) : raise_smem_limit(gemv_kernel<false>, g.smem);
+  if (e != cudaSuccess) return cuda_fail(mm, e, "shared memory limit");
   e = sub.bf16 ? launch(gemv_kernel<true>, dim3(g.part.N), dim3(kGemvThreads), g.smem, st, false, p)
                : launch(gemv_kernel<false>, dim3(g.part.N), dim3(kGemvThreads), g.smem, st, false, p);
   int h_status = 0;

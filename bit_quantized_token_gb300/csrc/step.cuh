@@ -116,6 +116,8 @@ struct StepParams {
   int dim;                // residual width (RMSNorm mean)
   int* sync;              // [0] arrivals (phases x CTAs), [1] abort; zeroed before each launch
   int* status;
+  int bar_extra;          // arrivals every grid barrier waits for beyond its CTAs (0; 1 in the expiry test)
+  unsigned long long wait_ns;  // limit of every wait on another CTA or on the ring
   const void* embed;
   const int* tok;
   int vocab;
@@ -188,6 +190,7 @@ __device__ __forceinline__ int log2_slots(int S) { return S >= 4 ? 2 : S >= 2 ? 
 // Consumer-side grid barrier: wait until `target` arrivals (bounded). Any
 // timeout sets the shared abort flag, which ends every other wait at once.
 __device__ bool grid_wait(const StepParams& sp, int target, int* s_flag) {
+  target += sp.bar_extra;
   if (threadIdx.x == 0) {
     int ok = 1;
     if (ld_acquire(sp.sync) < target) {
@@ -195,7 +198,7 @@ __device__ bool grid_wait(const StepParams& sp, int target, int* s_flag) {
       unsigned ns = 16;
       while (ld_acquire(sp.sync) < target) {
         if (*(volatile int*)(sp.sync + 1)) { ok = 0; break; }
-        if (globaltimer() - t0 > kWaitLimitNs) {
+        if (globaltimer() - t0 > sp.wait_ns) {
           atomicOr(sp.status, ST_TIMEOUT);
           atomicExch(sp.sync + 1, 1);
           ok = 0;
@@ -226,7 +229,7 @@ __device__ __forceinline__ bool ring_wait(uint64_t* bar, uint32_t parity, const 
   unsigned ns = 32;
   while (!mbar_try_wait(bar, parity)) {
     if (*(volatile int*)(sp.sync + 1)) return false;
-    if (globaltimer() - t0 > kWaitLimitNs) {
+    if (globaltimer() - t0 > sp.wait_ns) {
       atomicOr(sp.status, ST_TIMEOUT);
       atomicExch(sp.sync + 1, 1);
       return false;

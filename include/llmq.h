@@ -51,6 +51,11 @@ typedef enum { LLM_F32 = 0, LLM_BF16 = 1, LLM_F16 = 2, LLM_Q4G64 = 3 } llm_dtype
 #define LLM_NO_GRAPH 1u       /* launch the step's kernels one by one (debugging) */
 #define LLM_NO_PDL   2u       /* no programmatic dependent launch between kernels */
 #define LLM_MULTI_KERNEL 4u   /* one kernel per phase instead of the persistent step kernel */
+#define LLM_TEST_EXPIRE_WAIT 0x80000000u  /* test only: every grid barrier of the persistent step
+                                 waits for one arrival too many with a 1 ms limit, so the first one
+                                 expires; the call returns LLM_ERR_TIMEOUT (nothing faults or hangs) */
+#define LLM_DEBUG_BATCH_HIDDEN 16u  /* keep every layer's residual of the last batched decode step
+                                 for llm_debug_hidden_batch (adds L+1 device copies to the step) */
 #define LLM_DATAFLOW_STEP 8u  /* greedy batch-1 steps on the flag-synchronised persistent kernel (phases
                                  wait on flagged words instead of grid barriers; slower than the
                                  default grid-barrier step on GB300, kept for comparison) */
@@ -65,7 +70,8 @@ typedef struct {
   int32_t tied_embedding;     /* 1: LM head is the bf16 embedding table */
   int32_t max_seq;            /* KV capacity per sequence (positions) */
   int32_t max_batch;          /* number of sequences (independent caches) */
-  uint32_t flags;             /* LLM_NO_GRAPH | LLM_NO_PDL | LLM_MULTI_KERNEL | LLM_DATAFLOW_STEP */
+  uint32_t flags;             /* LLM_NO_GRAPH | LLM_NO_PDL | LLM_MULTI_KERNEL | LLM_DATAFLOW_STEP |
+                                 LLM_DEBUG_BATCH_HIDDEN | LLM_TEST_EXPIRE_WAIT */
 } llm_config;
 
 /* One input tensor in the canonical layout, host memory, caller-owned, only
@@ -193,10 +199,22 @@ int llm_kv_len(const llm_model* m, int32_t seq);
  * batch-1 step: out [(n_layers+1)][dim] fp32, host or device. */
 int llm_debug_hidden(llm_model* m, float* out);
 
+/* Residual stream of every sequence after the embedding and after every layer
+ * of the last llm_decode_step_batch: out [(n_layers+1)][max_batch][dim] fp32,
+ * host or device. Needs a model created with LLM_DEBUG_BATCH_HIDDEN
+ * (else LLM_ERR_UNSUPPORTED). */
+int llm_debug_hidden_batch(llm_model* m, float* out);
+
 /* Undo the repack of one 4-bit tensor: write its canonical codes [rows][cols/2],
  * scales and mins [rows][cols/64] (host) from the device copy. */
 int llm_debug_unpack(llm_model* m, const char* name, uint8_t* codes, uint16_t* scales,
                      uint16_t* mins);
+
+/* Test hook: the nth device allocation (counted from 1) made by the models
+ * created after this call fails as if cudaMalloc had run out of memory, so
+ * llm_model_create returns LLM_ERR_OOM naming the buffer and frees what it
+ * had allocated. nth <= 0 disarms it. Process-wide; returns LLM_OK. */
+int llm_debug_fail_alloc(int32_t nth);
 
 /* Sizes and counts of the model (host struct). */
 int llm_model_stats(const llm_model* m, llm_stats* out);
@@ -273,13 +291,18 @@ int llm_op_matvec(const llm_tensor* w, const float* x, float* y);
  * Scratch (split-row-tile partial sums, arrival counters, a status word) lives
  * in one file-scope device array of 4 MiB + 128 KiB + 256 B that every GPU
  * loading the library keeps until exit; a matrix needing more partial-sum or
- * counter space is rejected with LLM_ERR_UNSUPPORTED naming both sizes. The
- * first call on a device looks up the array's device address
- * (cudaGetSymbolAddress): make that first call before any stream capture.
+ * counter space is rejected with LLM_ERR_UNSUPPORTED naming both sizes (the
+ * model stays usable). The first call on a device looks up the array's device
+ * address (cudaGetSymbolAddress) and keeps it for the process: it does not
+ * survive cudaDeviceReset, after which this call must not be used again.
  * Every call shares the array and clears its counters and status on
  * `cuda_stream` (NULL: the legacy default stream) before the kernel: calls
- * whose work overlaps on the GPU race on it, so serialise them. The call
- * returns after y is written. */
+ * whose work overlaps on the GPU race on it, so serialise them. The call is
+ * synchronous -- it reads the status word back and synchronises
+ * `cuda_stream`, returning after y is written -- so it cannot be captured
+ * into a graph: on a capturing stream it returns LLM_ERR_INVALID_ARG without
+ * touching the stream or the model. Device ordinals of 64 and above:
+ * LLM_ERR_UNSUPPORTED. */
 int llm_matvec_noalloc(const llm_model* m, const char* name, const float* x, float* y, void* cuda_stream);
 
 #ifdef __cplusplus
