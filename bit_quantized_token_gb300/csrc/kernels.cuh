@@ -99,6 +99,110 @@ __device__ __forceinline__ float bf16_unit_dot(const uint8_t* __restrict__ ub, c
   return (a0 + a1) + (a2 + a3);
 }
 
+// ---- the 4-bit unit dot over byte limbs ------------------------------------
+// Exact integer form of the group's dot product: the group's inputs become
+// 32-bit fixed point X_j = rint(x_j 2^sh) with 2^sh chosen so the largest
+// |x_j| lands in [2^29, 2^30) (a relative rounding of at most 2^-30 of the
+// group's largest input, finer than fp32's own spacing for inputs within 2^6
+// of it); sum_j q_j X_j is then formed exactly from byte limbs of X with
+// dp4a and combined in 64-bit integers, and converted to fp32 once. The
+// scale/min affine map follows: s * 2^-sh * sum q X + m * sum x.
+// Unit layout as above: word j = 4h + k of lane l holds the codes of
+// inputs 8j .. 8j+3 in its low nibbles and 8j+4 .. 8j+7 in its high nibbles.
+// xl: the group's limbs, uint4 [4 limbs][4]; uint4 p of limb k is the byte k
+// of X for inputs 16p .. 16p+15 in the order (8j..8j+3, 8j+4..8j+7, 8j+8..,
+// 8j+12..) with j = 2p. fe = 2^e / 16, xsum = sum of the group's x.
+__device__ __forceinline__ uint32_t dp4a_uu(uint32_t a, uint32_t b, uint32_t c) {
+  uint32_t d;
+  asm("dp4a.u32.u32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+  return d;
+}
+__device__ __forceinline__ int dp4a_us(uint32_t a, uint32_t b, int c) {
+  int d;
+  asm("dp4a.u32.s32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+  return d;
+}
+__device__ __forceinline__ float q4_unit_dot_limbs(const uint8_t* __restrict__ ub, const uint4* __restrict__ xl,
+                                                   float fe, float xsum, int lane, uint32_t mlo, uint32_t mhi) {
+  const uint4 c0 = *reinterpret_cast<const uint4*>(ub + lane * 16);
+  const uint4 c1 = *reinterpret_cast<const uint4*>(ub + 512 + lane * 16);
+  const __half2 sm = *reinterpret_cast<const __half2*>(ub + 1024 + lane * 4);
+  const uint32_t words[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+  uint32_t lo0 = 0, lo1 = 0, lo2 = 0, hi0 = 0, hi1 = 0, hi2 = 0;
+  int lo3 = 0, hi3 = 0;
+#pragma unroll
+  for (int p = 0; p < 4; ++p) {
+    const uint32_t wa = words[2 * p], wb = words[2 * p + 1];
+    const uint32_t la = wa & mlo, ha = wa & mhi, lb = wb & mlo, hb = wb & mhi;  // hi: 16 x code
+    const uint4 x0 = xl[p], x1 = xl[4 + p], x2 = xl[8 + p], x3 = xl[12 + p];
+    lo0 = dp4a_uu(la, x0.x, lo0); hi0 = dp4a_uu(ha, x0.y, hi0); lo0 = dp4a_uu(lb, x0.z, lo0); hi0 = dp4a_uu(hb, x0.w, hi0);
+    lo1 = dp4a_uu(la, x1.x, lo1); hi1 = dp4a_uu(ha, x1.y, hi1); lo1 = dp4a_uu(lb, x1.z, lo1); hi1 = dp4a_uu(hb, x1.w, hi1);
+    lo2 = dp4a_uu(la, x2.x, lo2); hi2 = dp4a_uu(ha, x2.y, hi2); lo2 = dp4a_uu(lb, x2.z, lo2); hi2 = dp4a_uu(hb, x2.w, hi2);
+    lo3 = dp4a_us(la, x3.x, lo3); hi3 = dp4a_us(ha, x3.y, hi3); lo3 = dp4a_us(lb, x3.z, lo3); hi3 = dp4a_us(hb, x3.w, hi3);
+  }
+  // 16 x (sum over limb k) per limb, exact in 32 bits; their weighted sum in 64
+  const int c0k = (int)(16u * lo0 + hi0), c1k = (int)(16u * lo1 + hi1), c2k = (int)(16u * lo2 + hi2);
+  const int c3k = 16 * lo3 + hi3;
+  const int t32 = c3k * 256 + c2k;           // |.| < 2^30
+  const int u32 = c1k * 256 + c0k;           // < 2^30
+  const long long d64 = (long long)t32 * 65536 + u32;  // 16 * sum_j q_j X_j, exact
+  const float d = (float)d64;
+  const float2 s = __half22float2(sm);
+  return fmaf(s.x * fe, d, s.y * xsum);
+}
+
+// The GEMV input as the units read it, from float4 i4 of the (normed) input
+// in registers: for 4-bit units the limbs, the exponent factor and the sum of
+// each group of 64, for bf16 units the fp32 vector. The 16 threads of a
+// half-warp hold one group (every one of them calls this, valid or not). The
+// limbs of group g take the bytes of its 64 floats: xl may alias xh, the
+// group's threads read their inputs before the shuffles that precede the
+// stores.
+__device__ __forceinline__ void q4_build_group(float4 x, int i4, bool valid, bool bf16, uint4* xl, float* xh, float* fe,
+                                             float* xs) {
+  if (bf16) {
+    if (valid) reinterpret_cast<float4*>(xh)[i4] = x;
+    return;
+  }
+  float mx = fmaxf(fmaxf(fabsf(x.x), fabsf(x.y)), fmaxf(fabsf(x.z), fabsf(x.w)));
+  float gs = (x.x + x.y) + (x.z + x.w);
+#pragma unroll
+  for (int o = 8; o > 0; o >>= 1) {
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+    gs += __shfl_xor_sync(0xffffffffu, gs, o);
+  }
+  // mx = f * 2^E with f in [0.5, 1): X = x * 2^sh, sh = 30 - E, lies in [-2^30, 2^30]
+  // (subnormal mx: E from the scaled value; 2^sh as one or two exact powers of two)
+  const uint32_t mb = __float_as_uint(mx);
+  int E = (int)((mb >> 23) & 0xFF) - 126;
+  if ((mb >> 23) == 0) E = (int)((__float_as_uint(mx * 16777216.0f) >> 23) & 0xFF) - 126 - 24;
+  const int sh = 30 - E;
+  const int sh1 = sh > 126 ? 126 : sh, sh2 = sh - sh1;  // sh2 > 0 only for tiny groups
+  const float p1 = __uint_as_float((uint32_t)(sh1 + 127) << 23);
+  const float p2 = __uint_as_float((uint32_t)(sh2 + 127) << 23);
+  const bool nz = mx > 0.f;
+  const int X0 = nz ? __float2int_rn((x.x * p1) * p2) : 0;
+  const int X1 = nz ? __float2int_rn((x.y * p1) * p2) : 0;
+  const int X2 = nz ? __float2int_rn((x.z * p1) * p2) : 0;
+  const int X3 = nz ? __float2int_rn((x.w * p1) * p2) : 0;
+  const uint32_t a_lo = __byte_perm(X0, X1, 0x5140), a_hi = __byte_perm(X0, X1, 0x7362);
+  const uint32_t b_lo = __byte_perm(X2, X3, 0x5140), b_hi = __byte_perm(X2, X3, 0x7362);
+  if (valid) {
+    const int g = i4 >> 4, q = i4 & 15;  // group, quad of the group
+    uint32_t* w = reinterpret_cast<uint32_t*>(xl + 16 * g);
+    w[0 * 16 + q] = __byte_perm(a_lo, b_lo, 0x5410);
+    w[1 * 16 + q] = __byte_perm(a_lo, b_lo, 0x7632);
+    w[2 * 16 + q] = __byte_perm(a_hi, b_hi, 0x5410);
+    w[3 * 16 + q] = __byte_perm(a_hi, b_hi, 0x7632);
+    if (q == 0) {
+      const int fx = -sh - 4;  // 2^e / 16 with e = -sh
+      fe[g] = !nz ? 0.f : (fx >= -126 ? __uint_as_float((uint32_t)(fx + 127) << 23) : ldexpf(1.0f, fx));
+      xs[g] = gs;
+    }
+  }
+}
+
+
 // How a GEMV kernel gets its fp32 input vector (then optional RMSNorm).
 enum VecMode : int {
   VEC_PLAIN = 0,       // v = vin (written by an earlier kernel of the step)

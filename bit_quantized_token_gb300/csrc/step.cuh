@@ -260,8 +260,9 @@ template <int GQ, int HD>
 struct StepSmem {
   union {
     struct {
-      float xh[kMaxK];                     // input vector of the GEMV
+      float xh[kMaxK];                     // input vector of the GEMV (4-bit phases: its limbs, in place)
       float xs[kMaxK / 64];                // its per-group sums
+      float fe[kMaxK / 64];                // 2^-sh / 16 of each group's fixed point
       float red[kSRLoc][kSWarps][32];      // per-warp row-tile sums of a window
       float carry[2][32];
     } g;
@@ -615,6 +616,9 @@ __global__ void __launch_bounds__(kSThreads, 1) step_kernel(const StepParams sp)
   } else {
     // ================= consumers
     constexpr int NT = kSCThreads;
+    uint32_t mlo, mhi;  // the nibble masks of the unit dot, held in registers
+    asm volatile("mov.b32 %0, 0x0F0F0F0F;" : "=r"(mlo));
+    asm volatile("mov.b32 %0, 0xF0F0F0F0;" : "=r"(mhi));
     int gi = 0;
     // the position only changes at the very end of the step (greedy choice)
     const int spos = *sp.pos;
@@ -865,7 +869,9 @@ __global__ void __launch_bounds__(kSThreads, 1) step_kernel(const StepParams sp)
           for (int w = 0; w < kSWarps; ++w) t += sm.bred[w];
           P.ss_out[kr.r] = t;
         }
-        // x * w in place (RMSNorm without its 1/rms); per-group sums for the 4-bit units
+        // x * w (RMSNorm without its 1/rms), then what the units read: the
+        // fp32 vector (bf16 units) or each group's limbs, exponent and sum
+        // (4-bit units, in place of the group's floats)
 #pragma unroll
         for (int j = 0; j < kSMaxV; ++j) {
           const int i = tid + j * NT;
@@ -876,15 +882,10 @@ __global__ void __launch_bounds__(kSThreads, 1) step_kernel(const StepParams sp)
             if (P.norm_w && j < kSMaxW) {  // normed inputs are residual-wide
               const float4 w = w4[j];
               x = make_float4(x.x * w.x, x.y * w.y, x.z * w.z, x.w * w.w);
-              xh4[i] = x;
             }
           }
-          if (!P.bf16) {  // the 16 threads holding a group of 64 inputs
-            float gs = (x.x + x.y) + (x.z + x.w);
-#pragma unroll
-            for (int o = 8; o > 0; o >>= 1) gs += __shfl_xor_sync(0xffffffffu, gs, o);
-            if (i < n4 && (lane & 15) == 0) sm.u.g.xs[i / 16] = gs;
-          }
+          q4_build_group(x, i, i < n4, P.bf16 != 0, reinterpret_cast<uint4*>(sm.u.g.xh), sm.u.g.xh, sm.u.g.fe,
+                         sm.u.g.xs);
         }
         if (!red_clear)
           for (int i = tid; i < kSRLoc * kSWarps * 32; i += NT) (&sm.u.g.red[0][0][0])[i] = 0.f;
@@ -919,7 +920,9 @@ __global__ void __launch_bounds__(kSThreads, 1) step_kernel(const StepParams sp)
             }
             const uint8_t* ub = ring + s * kSSlot + warp * P.unit_bytes;
             if (P.bf16) acc += bf16_unit_dot(ub, sm.u.g.xh + k_g * EPU, lane);
-            else acc += q4_unit_dot(ub, sm.u.g.xh + k_g * EPU, sm.u.g.xs[k_g], lane);
+            else
+              acc += q4_unit_dot_limbs(ub, reinterpret_cast<const uint4*>(sm.u.g.xh) + 16 * k_g, sm.u.g.fe[k_g],
+                                       sm.u.g.xs[k_g], lane, mlo, mhi);
           }
           __syncwarp();
           if (lane == 0) mbar_arrive(&empty[s]);
