@@ -43,6 +43,8 @@ def args_():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--regions", type=int, default=5,
+                    help="timed regions of K steps each (same positions); value = the median region")
     ap.add_argument("--layers", type=int, default=0,
                     help="run only the first N layers of the workload (small profiling cases; not a bench line)")
     return ap.parse_args()
@@ -204,7 +206,7 @@ def run_batched(a, cfg, w, rank, world, local, dist):
     B = cfg["batch"]
     lens = synth.make_kv_lengths(cfg, B)
     n_e2e = 8
-    max_seq = int(lens.max()) + a.warmup + a.steps + n_e2e + 8
+    max_seq = int(lens.max()) + a.warmup + a.regions * a.steps + n_e2e + 8
     stream = torch.cuda.Stream()
     m = bq.Model(cfg, w, max_seq=max_seq, max_batch=B, stream=stream.cuda_stream)
     st = m.stats()
@@ -215,29 +217,33 @@ def run_batched(a, cfg, w, rank, world, local, dist):
     for _ in range(a.warmup - 1):
         m.decode_step_batch(None)
     m.sync()
-    pos0 = lens + a.warmup
+    per_pos = synth.kv_bytes_per_pos(cfg)
+    peak, peak_kind = peaks()
     clocks = ClockSampler(local)
     time.sleep(0.5)
-    if dist:
-        dist.barrier()
-    torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(a.steps):
-        m.decode_step_batch(None)  # greedy tokens fed back on the device
-    e1.record(stream)
-    torch.cuda.synchronize()
-    if dist:
-        dist.barrier()
-    ms = e0.elapsed_time(e1)
+    regions = []  # back to back: each region's caches are K positions longer than the last one's
+    for r in range(a.regions):
+        pos0 = lens + a.warmup + r * a.steps
+        if dist:
+            dist.barrier()
+        torch.cuda.synchronize()
+        e0.record(stream)
+        for _ in range(a.steps):
+            m.decode_step_batch(None)  # greedy tokens fed back on the device
+        e1.record(stream)
+        torch.cuda.synchronize()
+        if dist:
+            dist.barrier()
+        ms_r = max_over_ranks(e0.elapsed_time(e1), dist)
+        kv_r = float(np.mean([sum((int(pos0[b]) + i + 1) * per_pos for b in range(B)) for i in range(a.steps)]))
+        regions.append((ms_r, kv_r))
     clk = clocks.stop()
     m.sync()
-    ms = max_over_ranks(ms, dist)
+    order = sorted(range(len(regions)), key=lambda i: regions[i][0] / (st["weight_stream_bytes"] + regions[i][1]))
+    ms, kv_step = regions[order[len(order) // 2]]  # the median region by time per byte
     tok_s = job_rate(world, B * a.steps, ms)
-    per_pos = synth.kv_bytes_per_pos(cfg)
-    kv_step = float(np.mean([sum((int(pos0[b]) + i + 1) * per_pos for b in range(B)) for i in range(a.steps)]))
     bytes_step = st["weight_stream_bytes"] + kv_step
-    peak, peak_kind = peaks()
     gbs = bytes_step / (ms / a.steps / 1000.0) / 1e9
     # end to end: host tokens in, host greedy tokens out, every step
     am = np.zeros(B, np.int32)
@@ -262,6 +268,10 @@ def run_batched(a, cfg, w, rank, world, local, dist):
         "e2e": {"value": world * B * n_e2e / e2e_s, "unit": "tok/s", "h2d_bytes_per_step": 4 * B,
                 "d2h_bytes_per_step": 4 * B, "steps": n_e2e,
                 "call": "llm_decode_step_batch(host tokens -> host greedy tokens)"},
+        "regions": {"n": len(regions), "ms_per_step": [r[0] / a.steps for r in regions],
+                    "kv_bytes_per_step": [r[1] for r in regions],
+                    "note": "consecutive regions (caches grow by K positions each); value, hbm and roofline "
+                            "come from the median region by time per byte"},
         "gpu_launches": (5 * cfg["n_layers"] + 2) * a.steps,
         "clocks": clk,
     }
@@ -304,42 +314,50 @@ def main():
     if cfg.get("batch", 1) > 1:
         run_batched(a, cfg, w, rank, world, local, dist)
         return
-    n_e2e, n_kt, n_pf = 32, 3, 512
+    n_e2e, n_kt, n_pf = 128, 3, 512
     n_pre = max(0, cfg.get("prefill_kv", 0))
     max_seq = max(n_pre + len(prompt) + 2 * (a.warmup + a.steps) + n_e2e + 8, n_pf + 8)
     stream = torch.cuda.Stream()  # the library launches on it; events are recorded on it
     m = bq.Model(cfg, w, max_seq=max_seq, stream=stream.cuda_stream)
     st = m.stats()
-    am = np.zeros(1, np.int32)
-    if n_pre:  # pre-filled cache, seeded first token
-        for l in range(cfg["n_layers"]):
-            m.kv_write(0, l, 0, *synth.make_prefilled_kv(cfg, l, 0, n_pre))
-        am[0] = synth.make_first_tokens(cfg, 1)[0]
-    else:
-        m.prefill(0, prompt, None, am)
-    tok = int(am[0])
-    warm = m.decode_greedy(0, tok, a.warmup)
-    tok = int(warm[-1])
-    toks_dev = torch.empty(a.steps, dtype=torch.int32, device="cuda")
-    pos0 = m.kv_len(0)
-    positions = list(range(pos0, pos0 + a.steps))
+    kv_pre = [synth.make_prefilled_kv(cfg, l, 0, n_pre) for l in range(cfg["n_layers"])] if n_pre else None
 
+    def fresh_sequence():
+        # the same state before every timed region: the prompt (or the
+        # pre-filled cache and its seeded first token), then W warm-up steps
+        m.kv_reset(0)
+        am = np.zeros(1, np.int32)
+        if n_pre:
+            for l in range(cfg["n_layers"]):
+                m.kv_write(0, l, 0, *kv_pre[l])
+            am[0] = synth.make_first_tokens(cfg, 1)[0]
+        else:
+            m.prefill(0, prompt, None, am)
+        warm = m.decode_greedy(0, int(am[0]), a.warmup)
+        return int(warm[-1])
+
+    toks_dev = torch.empty(a.steps, dtype=torch.int32, device="cuda")
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     clocks = ClockSampler(local)
     time.sleep(0.5)
-    if dist:
-        dist.barrier()
-    torch.cuda.synchronize()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    m.decode_greedy(0, tok, a.steps, toks_dev)
-    e1.record(stream)
-    torch.cuda.synchronize()
-    if dist:
-        dist.barrier()
-    ms = e0.elapsed_time(e1)
+    region_ms = []
+    for r in range(a.regions):
+        tok = fresh_sequence()
+        pos0 = m.kv_len(0)
+        if dist:
+            dist.barrier()
+        torch.cuda.synchronize()
+        e0.record(stream)
+        m.decode_greedy(0, tok, a.steps, toks_dev)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        if dist:
+            dist.barrier()
+        region_ms.append(max_over_ranks(e0.elapsed_time(e1), dist))
     clk = clocks.stop()
     m.sync()
-    ms = max_over_ranks(ms, dist)
+    ms = statistics.median(region_ms)
+    positions = list(range(pos0, pos0 + a.steps))
     tok = int(toks_dev[-1].item())
     tok_s = job_rate(world, a.steps, ms)
     bytes_tok = st["weight_stream_bytes"] + kv_read_bytes(cfg, positions)
@@ -354,16 +372,36 @@ def main():
     share = {}
     for r in prof:
         share[r["kind"]] = share.get(r["kind"], 0.0) + r["ms"] / tot
-    # end to end through the public call: host token in, host argmax out, every step
+    # end to end through the public call: host token in, host argmax out,
+    # every step; the inter-token latency of that loop, on the host clock and
+    # between CUDA events recorded on the model's stream after each call
     am_h = np.zeros(1, np.int32)
     m.decode_step(0, tok, None, am_h)
     torch.cuda.synchronize()
-    t0 = time.perf_counter()
-    for _ in range(n_e2e):
+    evs = [torch.cuda.Event(enable_timing=True) for _ in range(n_e2e + 1)]
+    wall = []
+    evs[0].record(stream)
+    t0 = t_prev = time.perf_counter()
+    for i in range(n_e2e):
         m.decode_step(0, int(am_h[0]), None, am_h)
+        evs[i + 1].record(stream)
+        t = time.perf_counter()
+        wall.append(t - t_prev)
+        t_prev = t
     e2e_s = time.perf_counter() - t0
+    torch.cuda.synchronize()
+    dev = [evs[i].elapsed_time(evs[i + 1]) / 1000.0 for i in range(n_e2e)]
+
+    def pct(xs):
+        us = np.asarray(xs) * 1e6
+        return {"p50": float(np.percentile(us, 50)), "p95": float(np.percentile(us, 95)),
+                "p99": float(np.percentile(us, 99)), "mean": float(us.mean())}
+
     e2e = {"value": world * n_e2e / e2e_s, "unit": "tok/s", "h2d_bytes_per_step": 4, "d2h_bytes_per_step": 4,
            "steps": n_e2e, "call": "llm_decode_step(host token -> host argmax)"}
+    itl = {"steps": n_e2e, "wall_us": pct(wall), "device_us": pct(dev),
+           "positions": [pos0 + a.steps, pos0 + a.steps + n_e2e - 1],
+           "call": "llm_decode_step(host token -> host argmax), one call per token"}
 
     # sampled choice (temperature 0.8, top-k 40, top-p 0.95, Philox draw): the
     # same device-fed loop with the sampling kernel in each step's graph
@@ -430,6 +468,9 @@ def main():
                         "achieved": g_gbs, "unit": "GB/s", "frac": g_gbs / peak, "bytes_per_launch": g_bytes,
                         "ms_per_launch": g_ms},
         "kernel_share_eager": share,
+        "regions": {"n": len(region_ms), "ms_per_step": [r / a.steps for r in region_ms],
+                    "note": "each region decodes the same positions from a reset cache; value = the median"},
+        "itl": itl,
         "e2e": e2e,
         "gpu_launches": st["kernels_per_step"] * a.steps,
         "clocks": clk,

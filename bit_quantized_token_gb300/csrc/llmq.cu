@@ -8,6 +8,7 @@
 // as a CUDA graph whose kernels read the token and position from device
 // memory, so the same graph replays for every step.
 #include <cuda_runtime.h>
+#include <nvtx3/nvToolsExt.h>
 
 #include <algorithm>
 #include <atomic>
@@ -327,6 +328,14 @@ bool is_device_ptr(const void* p) {
   }
   return a.type == cudaMemoryTypeDevice || a.type == cudaMemoryTypeManaged;
 }
+
+// An NVTX range over one public call (a no-op unless a profiler listens).
+struct NvtxRange {
+  explicit NvtxRange(const char* name) { nvtxRangePushA(name); }
+  ~NvtxRange() { nvtxRangePop(); }
+  NvtxRange(const NvtxRange&) = delete;
+  NvtxRange& operator=(const NvtxRange&) = delete;
+};
 
 // A kernel's dynamic shared memory limit is process-wide state of the
 // device, shared by every model and call that launches the same kernel
@@ -1069,6 +1078,7 @@ void llm_model_destroy(llm_model* m) {
 
 int llm_model_create(const llm_config* cfg, const llm_tensor* tensors, int32_t n_tensors, void* cuda_stream,
                      llm_model** out) {
+  NvtxRange nvtx_("llm_model_create");
   llm_model* m = nullptr;
   if (out) *out = nullptr;
   if (!cfg || !tensors || !out || n_tensors <= 0)
@@ -1663,6 +1673,7 @@ int llm_model_create(const llm_config* cfg, const llm_tensor* tensors, int32_t n
 }
 
 int llm_decode_step(llm_model* m, int32_t seq, int32_t token, float* logits_out, int32_t* argmax_out) {
+  NvtxRange nvtx_("llm_decode_step");
   int rc = check_model(m, seq);
   if (rc) return rc;
   if (token < 0 || token >= m->cfg.vocab) return set_err(m, LLM_ERR_INVALID_ARG, "token out of range");
@@ -1684,6 +1695,7 @@ int llm_decode_step(llm_model* m, int32_t seq, int32_t token, float* logits_out,
 }
 
 int llm_prefill(llm_model* m, int32_t seq, const int32_t* tokens, int32_t n, float* logits_out, int32_t* argmax_out) {
+  NvtxRange nvtx_("llm_prefill");
   int rc = check_model(m, seq);
   if (rc) return rc;
   if (!tokens || n <= 0) return set_err(m, LLM_ERR_INVALID_ARG, "empty prompt");
@@ -1712,6 +1724,7 @@ int llm_prefill(llm_model* m, int32_t seq, const int32_t* tokens, int32_t n, flo
 
 int llm_prefill_batched(llm_model* m, int32_t seq, const int32_t* tokens, int32_t n, float* logits_out,
                         int32_t* argmax_out) {
+  NvtxRange nvtx_("llm_prefill_batched");
   int rc = check_model(m, seq);
   if (rc) return rc;
   if (!tokens || n <= 0) return set_err(m, LLM_ERR_INVALID_ARG, "empty prompt");
@@ -1785,6 +1798,7 @@ int llm_set_sampling(llm_model* m, float temperature, int32_t top_k, float top_p
 }
 
 int llm_decode_greedy(llm_model* m, int32_t seq, int32_t first_token, int32_t n_steps, int32_t* tokens_out) {
+  NvtxRange nvtx_("llm_decode_greedy");
   int rc = check_model(m, seq);
   if (rc) return rc;
   if (n_steps <= 0 || !tokens_out) return set_err(m, LLM_ERR_INVALID_ARG, "n_steps <= 0 or null tokens_out");
@@ -1812,6 +1826,7 @@ int llm_decode_greedy(llm_model* m, int32_t seq, int32_t first_token, int32_t n_
 }
 
 int llm_decode_step_batch(llm_model* m, const int32_t* tokens, int32_t n_seq, float* logits_out, int32_t* argmax_out) {
+  NvtxRange nvtx_("llm_decode_step_batch");
   int rc = check_model(m, 0);
   if (rc) return rc;
   const llm_config& c = m->cfg;
