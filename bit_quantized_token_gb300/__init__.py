@@ -29,6 +29,7 @@ ABI_VERSION = 1
 LLM_F32, LLM_BF16, LLM_F16, LLM_Q4G64 = 0, 1, 2, 3
 LLM_NO_GRAPH, LLM_NO_PDL, LLM_MULTI_KERNEL, LLM_DATAFLOW_STEP = 1, 2, 4, 8
 LLM_DEBUG_BATCH_HIDDEN = 16
+LLM_W4A8 = 64
 LLM_TEST_EXPIRE_WAIT = 0x80000000
 STATUS = {0: "OK", -1: "INVALID_ARG", -2: "UNSUPPORTED", -3: "OOM", -4: "CTX_FULL", -5: "CUDA",
           -6: "TIMEOUT", -7: "NAN", -8: "NOT_FOUND"}
@@ -38,24 +39,56 @@ EXPORTS = ["llm_model_create", "llm_model_destroy", "llm_prefill", "llm_prefill_
            "llm_decode_greedy", "llm_set_sampling",
            "llm_decode_step_batch", "llm_kv_reset", "llm_kv_write", "llm_kv_read", "llm_kv_len",
            "llm_debug_hidden", "llm_debug_unpack", "llm_model_stats", "llm_profile_step", "llm_time_kernel", "llm_sync",
-           "llm_last_error", "llm_op_matvec", "llm_matvec_noalloc", "llm_phase_times", "llm_debug_fail_alloc",
+           "llm_last_error", "llm_op_matvec", "llm_op_matvec_w4a8", "llm_matvec_noalloc", "llm_phase_times", "llm_debug_fail_alloc",
            "llm_debug_hidden_batch"]
 
 
-def nvcc_command(out: str = LIB_PATH) -> list[str]:
-    return ["nvcc", "-gencode", "arch=compute_103a,code=sm_103a", "-O3", "-lineinfo", "-std=c++17",
-            "-Xcompiler", "-fPIC,-pthread", "-shared", "-I", os.path.join(_ROOT, "include"),
-            "-o", out, os.path.join(_HERE, "csrc", "llmq.cu")]
+# translation units of the library, compiled in parallel and linked into one shared object
+UNITS = ["llmq.cu", "step_kernels.cu", "stepll_kernels.cu"]
+BUILD_DIR = os.path.join(_HERE, "_build")
+ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 
-def build(force: bool = False) -> str:
-    """Compile libllmq.so in place for sm_103a (nvcc cross-compiles without a GPU)."""
-    newest = max(os.path.getmtime(f) for f in sources())
-    if force or not os.path.exists(LIB_PATH) or os.path.getmtime(LIB_PATH) < newest:
-        tmp = LIB_PATH + f".tmp{os.getpid()}"
-        subprocess.check_call(nvcc_command(tmp))
-        os.replace(tmp, LIB_PATH)
-    return LIB_PATH
+def nvcc_compile_command(src: str, obj: str, defines=()) -> list[str]:
+    return (["nvcc"] + ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC,-pthread",
+                               "-I", os.path.join(_ROOT, "include")]
+            + [f"-D{d}" for d in defines] + ["-c", "-o", obj, src])
+
+
+def nvcc_link_command(objs: list[str], out: str) -> list[str]:
+    return ["nvcc"] + ARCH + ["-shared", "-Xcompiler", "-fPIC,-pthread", "-o", out] + list(objs)
+
+
+def build(force: bool = False, out: str | None = None, defines=()) -> str:
+    """Compile libllmq.so in place for sm_103a (nvcc cross-compiles without a GPU).
+
+    Rebuilds when the library is missing or older than any source; `out` and
+    `defines` build a variant elsewhere (always rebuilt).
+    """
+    from concurrent.futures import ThreadPoolExecutor
+
+    target = out or LIB_PATH
+    if out is None and not force and os.path.exists(LIB_PATH):
+        newest = max(os.path.getmtime(f) for f in sources())
+        if os.path.getmtime(LIB_PATH) >= newest:
+            return LIB_PATH
+    os.makedirs(BUILD_DIR, exist_ok=True)
+    tag = f"{os.getpid()}_{abs(hash(target)) % 100000}"
+    objs = [os.path.join(BUILD_DIR, f"{u[:-3]}.{tag}.o") for u in UNITS]
+    try:
+        with ThreadPoolExecutor(len(UNITS)) as ex:
+            futs = [ex.submit(subprocess.check_call, nvcc_compile_command(os.path.join(CSRC, u), o, defines))
+                    for u, o in zip(UNITS, objs)]
+            for f in futs:
+                f.result()
+        tmp = target + f".tmp{tag}"
+        subprocess.check_call(nvcc_link_command(objs, tmp))
+        os.replace(tmp, target)
+    finally:
+        for o in objs:
+            if os.path.exists(o):
+                os.unlink(o)
+    return target
 
 
 class LlmError(RuntimeError):
@@ -122,6 +155,7 @@ def lib() -> C.CDLL:
             "llm_sync": (i32, [P]),
             "llm_last_error": (C.c_char_p, [P]),
             "llm_op_matvec": (i32, [C.POINTER(Tensor), P, P]),
+            "llm_op_matvec_w4a8": (i32, [C.POINTER(Tensor), P, P]),
             "llm_matvec_noalloc": (i32, [P, C.c_char_p, P, P, P]),
             "llm_phase_times": (i32, [P, i32, i32, i32, P, C.c_int64]),
             "llm_debug_fail_alloc": (i32, [i32]),
@@ -329,6 +363,15 @@ def matvec(t: dict, x) -> np.ndarray:
     x = np.ascontiguousarray(x, np.float32)
     y = np.empty(int(t["rows"]), np.float32)
     _check(lib().llm_op_matvec(table, x.ctypes.data, y.ctypes.data))
+    return y
+
+
+def matvec_w4a8(t: dict, x) -> np.ndarray:
+    """y = W x in the W4A8 numerics (x quantized per 32-block to int8) through the GEMV kernel."""
+    table, keep = tensor_table({"w": t})
+    x = np.ascontiguousarray(x, np.float32)
+    y = np.empty(int(t["rows"]), np.float32)
+    _check(lib().llm_op_matvec_w4a8(table, x.ctypes.data, y.ctypes.data))
     return y
 
 

@@ -203,6 +203,68 @@ __device__ __forceinline__ void q4_build_group(float4 x, int i4, bool valid, boo
 }
 
 
+// ---- W4A8: 4-bit weights x int8 activations ---------------------------------
+// The GEMV input quantized once to 8-bit blocks of 32 (the Q8_0 scheme: an
+// fp16 scale d = fp16(amax / 127), codes clamp(round(x / d), +-127), rounded
+// half away from zero, all in fp32), then an integer dot per block. A group
+// of 64 inputs is two blocks; everything a unit reads of group g sits in the
+// group's 64-float slot: words 0..15 the codes (word q = inputs 4q .. 4q+3,
+// one byte each), word 16/17 the blocks' d / 16, word 18 the min term
+// d0 * sum(c of block 0) + d1 * sum(c of block 1).
+// Same threads and aliasing as q4_build_group (8 threads per block).
+__device__ __forceinline__ void q8_build_group(float4 x, int i4, bool valid, float* slots) {
+  float amax = fmaxf(fmaxf(fabsf(x.x), fabsf(x.y)), fmaxf(fabsf(x.z), fabsf(x.w)));
+#pragma unroll
+  for (int o = 4; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+  const float d = __half2float(__float2half_rn(amax / 127.0f));
+  auto code = [&](float v) {
+    const float c = d == 0.0f ? 0.0f : roundf(v / d);
+    return (int)fminf(fmaxf(c, -127.0f), 127.0f);
+  };
+  const int c0 = code(x.x), c1 = code(x.y), c2 = code(x.z), c3 = code(x.w);
+  const uint32_t packed = (uint32_t)(c0 & 0xFF) | ((uint32_t)(c1 & 0xFF) << 8) | ((uint32_t)(c2 & 0xFF) << 16) |
+                          ((uint32_t)(c3 & 0xFF) << 24);
+  int s2 = (c0 + c1) + (c2 + c3);
+#pragma unroll
+  for (int o = 4; o > 0; o >>= 1) s2 += __shfl_xor_sync(0xffffffffu, s2, o);
+  const float mterm = d * (float)s2;                              // this block's d * sum(c), exact
+  const float other = __shfl_xor_sync(0xffffffffu, mterm, 8);   // the group's other block
+  if (valid) {
+    const int g = i4 >> 4, q = i4 & 15;
+    uint32_t* w = reinterpret_cast<uint32_t*>(slots + 64 * g);
+    w[q] = packed;
+    if ((q & 7) == 0) slots[64 * g + 16 + (q >> 3)] = d * 0.0625f;
+    if (q == 0) slots[64 * g + 18] = mterm + other;
+  }
+}
+
+// One unit against a W4A8 group slot: sum over the two blocks of
+// d_b * (scale * sum q c + min * sum c). Lane word j of the unit covers inputs
+// 8j .. 8j+7 (low nibbles 8j .. 8j+3, high 8j+4 .. 8j+7): block 0 is words
+// 0..3, block 1 words 4..7; the high-nibble sums come out 16 x, which the
+// stored d / 16 takes back.
+__device__ __forceinline__ float q4a8_unit_dot(const uint8_t* __restrict__ ub, const float* __restrict__ slot,
+                                               int lane, uint32_t mlo, uint32_t mhi) {
+  const uint4 c0 = *reinterpret_cast<const uint4*>(ub + lane * 16);
+  const uint4 c1 = *reinterpret_cast<const uint4*>(ub + 512 + lane * 16);
+  const __half2 sm = *reinterpret_cast<const __half2*>(ub + 1024 + lane * 4);
+  const uint4* xq = reinterpret_cast<const uint4*>(slot);
+  const uint4 xa = xq[0], xb = xq[1], xc = xq[2], xd = xq[3];
+  const float4 dm = reinterpret_cast<const float4*>(slot)[4];  // d0 / 16, d1 / 16, min term
+  int l0 = 0, h0 = 0, l1 = 0, h1 = 0;
+  l0 = dp4a_us(c0.x & mlo, xa.x, l0); h0 = dp4a_us(c0.x & mhi, xa.y, h0);
+  l0 = dp4a_us(c0.y & mlo, xa.z, l0); h0 = dp4a_us(c0.y & mhi, xa.w, h0);
+  l0 = dp4a_us(c0.z & mlo, xb.x, l0); h0 = dp4a_us(c0.z & mhi, xb.y, h0);
+  l0 = dp4a_us(c0.w & mlo, xb.z, l0); h0 = dp4a_us(c0.w & mhi, xb.w, h0);
+  l1 = dp4a_us(c1.x & mlo, xc.x, l1); h1 = dp4a_us(c1.x & mhi, xc.y, h1);
+  l1 = dp4a_us(c1.y & mlo, xc.z, l1); h1 = dp4a_us(c1.y & mhi, xc.w, h1);
+  l1 = dp4a_us(c1.z & mlo, xd.x, l1); h1 = dp4a_us(c1.z & mhi, xd.y, h1);
+  l1 = dp4a_us(c1.w & mlo, xd.z, l1); h1 = dp4a_us(c1.w & mhi, xd.w, h1);
+  const int t0 = 16 * l0 + h0, t1 = 16 * l1 + h1;  // 16 x sum q c per block, exact
+  const float2 s = __half22float2(sm);
+  return fmaf(s.x, fmaf(dm.x, (float)t0, dm.y * (float)t1), s.y * dm.z);
+}
+
 // How a GEMV kernel gets its fp32 input vector (then optional RMSNorm).
 enum VecMode : int {
   VEC_PLAIN = 0,       // v = vin (written by an earlier kernel of the step)
@@ -231,6 +293,7 @@ struct GemvParams {
   float* vstore;         // VEC_EMBED_*: CTA 0 stores the gathered row here
   const float* norm_w;   // RMSNorm weight, or null
   float eps;
+  int w4a8;              // 4-bit units on int8 activation blocks (q8_build_group / q4a8_unit_dot)
   // output
   int epi;
   float* out;
@@ -349,6 +412,9 @@ __global__ void __launch_bounds__(kGemvThreads, 2) gemv_kernel(const GemvParams 
     // ---------------- consumers ------------------------------------------
     const int tid = threadIdx.x;
     const int K = p.K;
+    uint32_t mlo, mhi;  // the nibble masks of the W4A8 unit dot, held in registers
+    asm volatile("mov.b32 %0, 0x0F0F0F0F;" : "=r"(mlo));
+    asm volatile("mov.b32 %0, 0xF0F0F0F0;" : "=r"(mhi));
     // weights of the norm do not depend on earlier kernels: load before waiting
     if (p.norm_w)
       for (int i = tid; i < K / 4; i += kCWarps * 32)
@@ -419,10 +485,15 @@ __global__ void __launch_bounds__(kGemvThreads, 2) gemv_kernel(const GemvParams 
     }
     // (3) store, and per-group sums (the min term of every group) by
     // shuffles over the 16 threads holding a group
+    const bool a8 = !BF16 && p.w4a8 != 0;
 #pragma unroll
     for (int j = 0; j < MAXV; ++j) {
       const int i = tid + j * kCWarps * 32;
       if (j * kCWarps * 32 >= n4) break;  // uniform: no thread has work at this j
+      if (a8) {
+        q8_build_group(v[j], i, i < n4, xh);
+        continue;
+      }
       if (i < n4) reinterpret_cast<float4*>(xh)[i] = v[j];
       if (!BF16) {
         float gs = (i < n4) ? (v[j].x + v[j].y) + (v[j].z + v[j].w) : 0.f;
@@ -460,6 +531,7 @@ __global__ void __launch_bounds__(kGemvThreads, 2) gemv_kernel(const GemvParams 
         }
         const uint8_t* ub = ring + (s * kChunkUnits + warp) * UB;
         if (BF16) acc += bf16_unit_dot(ub, xh + g * kBF16UnitCols, lane);
+        else if (a8) acc += q4a8_unit_dot(ub, xh + g * 64, lane, mlo, mhi);
         else acc += q4_unit_dot(ub, xh + g * 64, xs[g], lane);
       }
       __syncwarp();

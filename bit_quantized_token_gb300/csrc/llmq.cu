@@ -248,7 +248,6 @@ struct llm_model {
   Phase* d_phases = nullptr;
   int n_phases = 0;
   int* d_step_sync = nullptr;                 // [2]: arrivals, abort
-  size_t step_smem = 0;
   // dataflow step kernel (stepll.cuh): several steps per launch
   bool use_ll = false;
   int ll_fuse_len = 0;                        // positions it covers (attention inside the o-projection's build)
@@ -258,7 +257,6 @@ struct llm_model {
   uint32_t* d_epoch = nullptr;
   int* d_ll_abort = nullptr;
   uint64_t* d_cand = nullptr;
-  size_t ll_smem = 0;
   unsigned long long* d_stamps = nullptr;     // per-phase timestamps of the last profiled launch
   size_t stamps_steps = 0;
   // per-sequence state
@@ -391,6 +389,7 @@ GemvParams gemv_params(const llm_model* m, const GemvPlan& g) {
   p.part_buf = g.part_buf;
   p.counters = g.counters;
   p.eps = m->cfg.norm_eps;
+  p.w4a8 = (m->cfg.flags & LLM_W4A8) ? 1 : 0;
   p.status = m->d_status;
   p.vocab = m->cfg.vocab;
   return p;
@@ -554,34 +553,26 @@ int kind_of(const llm_model* m, int which) {
   return (which == W_LM && m->lm.m.bf16) ? 1 : 0;
 }
 
-// The persistent step kernel for the model's (GQA group, head_dim).
-template <int GQ, int HD>
-cudaError_t launch_step_t(const llm_model* m, const StepParams& sp, bool fused) {
+// A cooperative launch of one of the persistent step kernels (all CTAs
+// co-resident: their grid barriers and flag waits are safe).
+template <typename Params>
+cudaError_t launch_cooperative(const llm_model* m, const KernelRef& k, int threads, const Params& prm) {
+  if (!k.fn) return cudaErrorInvalidDeviceFunction;
   cudaLaunchConfig_t cfg{};
   cfg.gridDim = dim3(m->n_sm);
-  cfg.blockDim = dim3(kSThreads);
-  cfg.dynamicSmemBytes = m->step_smem;
+  cfg.blockDim = dim3(threads);
+  cfg.dynamicSmemBytes = k.smem;
   cfg.stream = m->stream;
   cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeCooperative;  // all CTAs co-resident: the grid barriers are safe
+  attr[0].id = cudaLaunchAttributeCooperative;
   attr[0].val.cooperative = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  if (fused) return cudaLaunchKernelEx(&cfg, step_kernel<GQ, HD, true>, sp);
-  return cudaLaunchKernelEx(&cfg, step_kernel<GQ, HD, false>, sp);
+  void* args[] = {const_cast<Params*>(&prm)};
+  return cudaLaunchKernelExC(&cfg, k.fn, args);
 }
 
 bool step_supported(int gq, int hd) { return (gq == 2 && hd == 64) || (gq == 8 && hd == 64) || (gq == 2 && hd == 128); }
-
-template <typename F>
-cudaError_t with_step_kernel(int gq, int hd, bool fused, F f) {
-  if (gq == 2 && hd == 64) return fused ? f(step_kernel<2, 64, true>, step_smem_bytes<2, 64>())
-                                        : f(step_kernel<2, 64, false>, step_smem_bytes<2, 64>());
-  if (gq == 8 && hd == 64) return fused ? f(step_kernel<8, 64, true>, step_smem_bytes<8, 64>())
-                                        : f(step_kernel<8, 64, false>, step_smem_bytes<8, 64>());
-  return fused ? f(step_kernel<2, 128, true>, step_smem_bytes<2, 128>())
-               : f(step_kernel<2, 128, false>, step_smem_bytes<2, 128>());
-}
 
 cudaError_t enqueue_persistent_step(llm_model* m, int seq, bool fused) {
   const llm_config& c = m->cfg;
@@ -627,36 +618,11 @@ cudaError_t enqueue_persistent_step(llm_model* m, int seq, bool fused) {
   sp.hist_cap = c.max_seq;
   cudaError_t e = cudaMemsetAsync(m->d_step_sync, 0, 2 * sizeof(int), m->stream);
   if (e != cudaSuccess) return e;
-  const int gq = m->gq, hd = c.head_dim;
-  if (gq == 2 && hd == 64) return launch_step_t<2, 64>(m, sp, fused);
-  if (gq == 8 && hd == 64) return launch_step_t<8, 64>(m, sp, fused);
-  return launch_step_t<2, 128>(m, sp, fused);
+  return launch_cooperative(m, step_kernel_ref(m->gq, c.head_dim, fused, (c.flags & LLM_W4A8) != 0), kSThreads, sp);
 }
 
 
 // ---- the dataflow step: n steps of one sequence per cooperative launch
-template <int GQ, int HD>
-cudaError_t launch_ll_t(const llm_model* m, const StepLLParams& sp) {
-  cudaLaunchConfig_t cfg{};
-  cfg.gridDim = dim3(m->n_sm);
-  cfg.blockDim = dim3(kLThreads);
-  cfg.dynamicSmemBytes = m->ll_smem;
-  cfg.stream = m->stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeCooperative;  // CTAs wait on one another's words: all must be resident
-  attr[0].val.cooperative = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, stepll_kernel<GQ, HD>, sp);
-}
-
-template <typename F>
-cudaError_t with_ll_kernel(int gq, int hd, F f) {
-  if (gq == 2 && hd == 64) return f(stepll_kernel<2, 64>, stepll_smem_bytes<2, 64>());
-  if (gq == 8 && hd == 64) return f(stepll_kernel<8, 64>, stepll_smem_bytes<8, 64>());
-  return f(stepll_kernel<2, 128>, stepll_smem_bytes<2, 128>());
-}
-
 // Steps pos0 .. pos0+n-1 of sequence seq (pos0 = the sequence's device
 // position): the input token of step i < n_forced is forced[i] (device), the
 // others take the previous step's greedy choice (step 0: d_tok[seq]).
@@ -694,10 +660,7 @@ cudaError_t enqueue_ll(llm_model* m, int seq, int n_steps, int n_forced, const i
   sp.hist_ctr = m->d_hist_ctr;
   sp.hist_cap = c.max_seq;
   sp.stamps = stamps;
-  const int gq = m->gq, hd = c.head_dim;
-  if (gq == 2 && hd == 64) return launch_ll_t<2, 64>(m, sp);
-  if (gq == 8 && hd == 64) return launch_ll_t<8, 64>(m, sp);
-  return launch_ll_t<2, 128>(m, sp);
+  return launch_cooperative(m, stepll_kernel_ref(m->gq, c.head_dim), kLThreads, sp);
 }
 
 // Whether steps at positions pos0 .. pos0+n-1 run through the dataflow step.
@@ -1340,17 +1303,14 @@ int llm_model_create(const llm_config* cfg, const llm_tensor* tensors, int32_t n
                 std::min({d, m->q_dim, F}) >= 256;
   for (bool fused : {false, true}) {
     if (!m->use_step) break;
-    with_step_kernel(gq, hd, fused, [&](auto kern, size_t smem) {
-      m->step_smem = smem;
-      int per_sm = 0;
-      cudaError_t e = raise_smem_limit(kern, smem);
-      if (e == cudaSuccess) e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kSThreads, smem);
-      if (e != cudaSuccess || per_sm < 1) {
-        cudaGetLastError();
-        m->use_step = false;  // fall back to the per-kernel step
-      }
-      return cudaSuccess;
-    });
+    const KernelRef k = step_kernel_ref(gq, hd, fused, (c.flags & LLM_W4A8) != 0);
+    int per_sm = 0;
+    cudaError_t e = k.fn ? raise_smem_limit(k.fn, k.smem) : cudaErrorInvalidDeviceFunction;
+    if (e == cudaSuccess) e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k.fn, kSThreads, k.smem);
+    if (e != cudaSuccess || per_sm < 1) {
+      cudaGetLastError();
+      m->use_step = false;  // fall back to the per-kernel step
+    }
   }
   std::vector<Phase> phases;
   {
@@ -1439,7 +1399,7 @@ int llm_model_create(const llm_config* cfg, const llm_tensor* tensors, int32_t n
   {
     const int R = m->step_R;
     const int hpr = R > 0 ? c.n_kv_heads / R : 0;
-    bool ok = m->use_step && (c.flags & LLM_DATAFLOW_STEP) && m->n_sm <= kLMaxCTAs && R >= 1 &&
+    bool ok = m->use_step && (c.flags & LLM_DATAFLOW_STEP) && !(c.flags & LLM_W4A8) && m->n_sm <= kLMaxCTAs && R >= 1 &&
               c.n_kv_heads % R == 0 && hpr * gq * hd <= kSFuseOut && d / R <= kLMaxRes && d <= kLMaxKr;
     auto lgemv = [&](const GemvPlan& g, int r) {
       LPhase p{};
@@ -1532,17 +1492,14 @@ int llm_model_create(const llm_config* cfg, const llm_tensor* tensors, int32_t n
       m->d_cand = W + o_cand;
     }
     if (ok) {
-      with_ll_kernel(gq, hd, [&](auto kern, size_t smem) {
-        m->ll_smem = smem;
-        int per_sm = 0;
-        cudaError_t e = raise_smem_limit(kern, smem);
-        if (e == cudaSuccess) e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kLThreads, smem);
-        if (e != cudaSuccess || per_sm < 1) {
-          cudaGetLastError();
-          ok = false;  // the barrier-synchronised step serves every call
-        }
-        return cudaSuccess;
-      });
+      const KernelRef k = stepll_kernel_ref(gq, hd);
+      int per_sm = 0;
+      cudaError_t e = k.fn ? raise_smem_limit(k.fn, k.smem) : cudaErrorInvalidDeviceFunction;
+      if (e == cudaSuccess) e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k.fn, kLThreads, k.smem);
+      if (e != cudaSuccess || per_sm < 1) {
+        cudaGetLastError();
+        ok = false;  // the barrier-synchronised step serves every call
+      }
     }
     m->use_ll = ok;
     m->ll_fuse_len = ok ? 4 * step_attn_pp(hd) : 0;
@@ -2079,9 +2036,10 @@ int llm_sync(llm_model* m) {
   return check_status(m);
 }
 
-int llm_op_matvec(const llm_tensor* w, const float* x, float* y) {
+static int op_matvec(const llm_tensor* w, const float* x, float* y, bool w4a8) {
   if (!w || !x || !y) return set_err(nullptr, LLM_ERR_INVALID_ARG, "null argument");
   const bool bf16 = w->dtype == LLM_BF16;
+  if (w4a8 && bf16) return set_err(nullptr, LLM_ERR_UNSUPPORTED, "W4A8 needs a Q4G64 tensor");
   if (!bf16 && w->dtype != LLM_Q4G64) return set_err(nullptr, LLM_ERR_UNSUPPORTED, "dtype must be Q4G64 or BF16");
   if (w->rows <= 0 || w->cols <= 0 || w->cols % 64 || w->cols > kMaxK || w->rows > (1 << 24))
     return set_err(nullptr, LLM_ERR_UNSUPPORTED, "rows > 0 and cols a multiple of 64 up to 8192 required");
@@ -2132,6 +2090,7 @@ int llm_op_matvec(const llm_tensor* w, const float* x, float* y) {
     p.part = g.part;
     p.vec_mode = VEC_PLAIN;
     p.vin = d_x;
+    p.w4a8 = w4a8 ? 1 : 0;
     p.epi = EPI_STORE;
     p.out = d_y;
     p.part_buf = d_part;
@@ -2151,6 +2110,10 @@ int llm_op_matvec(const llm_tensor* w, const float* x, float* y) {
   if (st & ST_TIMEOUT) return set_err(nullptr, LLM_ERR_TIMEOUT, "a device-side wait exceeded its limit");
   return LLM_OK;
 }
+
+int llm_op_matvec(const llm_tensor* w, const float* x, float* y) { return op_matvec(w, x, y, false); }
+
+int llm_op_matvec_w4a8(const llm_tensor* w, const float* x, float* y) { return op_matvec(w, x, y, true); }
 
 }  // extern "C"
 

@@ -189,7 +189,7 @@ __device__ __forceinline__ int log2_slots(int S) { return S >= 4 ? 2 : S >= 2 ? 
 
 // Consumer-side grid barrier: wait until `target` arrivals (bounded). Any
 // timeout sets the shared abort flag, which ends every other wait at once.
-__device__ bool grid_wait(const StepParams& sp, int target, int* s_flag) {
+__device__ inline bool grid_wait(const StepParams& sp, int target, int* s_flag) {
   target += sp.bar_extra;
   if (threadIdx.x == 0) {
     int ok = 1;
@@ -560,7 +560,7 @@ __device__ void step_attn_item(const StepParams& sp, const Phase& P, int g, int 
 // FUSED: the variant for short caches (every CTA computes the attention of
 // its o-projection range in that GEMV's input build; no attention phase). The
 // two variants are separate kernels: either one alone keeps its registers.
-template <int GQ, int HD, bool FUSED>
+template <int GQ, int HD, bool FUSED, bool A8>
 __global__ void __launch_bounds__(kSThreads, 1) step_kernel(const StepParams sp) {
   extern __shared__ __align__(128) uint8_t smem_raw[];
   uint8_t* ring = smem_raw;
@@ -616,6 +616,7 @@ __global__ void __launch_bounds__(kSThreads, 1) step_kernel(const StepParams sp)
   } else {
     // ================= consumers
     constexpr int NT = kSCThreads;
+    constexpr bool a8 = A8;
     uint32_t mlo, mhi;  // the nibble masks of the unit dot, held in registers
     asm volatile("mov.b32 %0, 0x0F0F0F0F;" : "=r"(mlo));
     asm volatile("mov.b32 %0, 0xF0F0F0F0;" : "=r"(mhi));
@@ -884,8 +885,11 @@ __global__ void __launch_bounds__(kSThreads, 1) step_kernel(const StepParams sp)
               x = make_float4(x.x * w.x, x.y * w.y, x.z * w.z, x.w * w.w);
             }
           }
-          q4_build_group(x, i, i < n4, P.bf16 != 0, reinterpret_cast<uint4*>(sm.u.g.xh), sm.u.g.xh, sm.u.g.fe,
-                         sm.u.g.xs);
+          if (A8 && !P.bf16)
+            q8_build_group(x, i, i < n4, sm.u.g.xh);
+          else
+            q4_build_group(x, i, i < n4, P.bf16 != 0, reinterpret_cast<uint4*>(sm.u.g.xh), sm.u.g.xh, sm.u.g.fe,
+                           sm.u.g.xs);
         }
         if (!red_clear)
           for (int i = tid; i < kSRLoc * kSWarps * 32; i += NT) (&sm.u.g.red[0][0][0])[i] = 0.f;
@@ -920,6 +924,7 @@ __global__ void __launch_bounds__(kSThreads, 1) step_kernel(const StepParams sp)
             }
             const uint8_t* ub = ring + s * kSSlot + warp * P.unit_bytes;
             if (P.bf16) acc += bf16_unit_dot(ub, sm.u.g.xh + k_g * EPU, lane);
+            else if (a8) acc += q4a8_unit_dot(ub, sm.u.g.xh + 64 * k_g, lane, mlo, mhi);
             else
               acc += q4_unit_dot_limbs(ub, reinterpret_cast<const uint4*>(sm.u.g.xh) + 16 * k_g, sm.u.g.fe[k_g],
                                        sm.u.g.xs[k_g], lane, mlo, mhi);
@@ -1089,5 +1094,15 @@ template <int GQ, int HD>
 constexpr size_t step_smem_bytes() {
   return kSRing + ((sizeof(StepSmem<GQ, HD>) + 15) & ~size_t(15)) + 2 * kSNSlot * sizeof(uint64_t);
 }
+
+// A kernel of a shape, as the host launches it: entry point and dynamic shared memory.
+struct KernelRef {
+  const void* fn = nullptr;
+  size_t smem = 0;
+};
+// The step kernel for a GQA group, head_dim, variant and activation numerics
+// (defined in step_kernels.cu, which holds the instantiations); fn is null
+// for an unsupported shape.
+KernelRef step_kernel_ref(int gq, int hd, bool fused, bool w4a8);
 
 }  // namespace llmq

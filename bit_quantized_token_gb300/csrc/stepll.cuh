@@ -972,4 +972,8 @@ __global__ void __launch_bounds__(kLThreads, 1) stepll_kernel(const StepLLParams
   }
 }
 
+// The flag-synchronised step kernel for a GQA group and head_dim (defined in
+// stepll_kernels.cu); fn is null for an unsupported shape.
+KernelRef stepll_kernel_ref(int gq, int hd);
+
 }  // namespace llmq

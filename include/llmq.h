@@ -56,6 +56,10 @@ typedef enum { LLM_F32 = 0, LLM_BF16 = 1, LLM_F16 = 2, LLM_Q4G64 = 3 } llm_dtype
                                  expires; the call returns LLM_ERR_TIMEOUT (nothing faults or hangs) */
 #define LLM_DEBUG_BATCH_HIDDEN 16u  /* keep every layer's residual of the last batched decode step
                                  for llm_debug_hidden_batch (adds L+1 device copies to the step) */
+#define LLM_W4A8 64u          /* 4-bit weights x int8 activations in the batch-1 paths: every 4-bit GEMV
+                                 input quantized once per 32-input block (fp16 scale amax/127, codes
+                                 round(x/scale) clamped to +-127) and dotted in integers; the batched
+                                 kernels keep their fp16 tensor-core inputs. Not with LLM_DATAFLOW_STEP */
 #define LLM_DATAFLOW_STEP 8u  /* greedy batch-1 steps on the flag-synchronised persistent kernel (phases
                                  wait on flagged words instead of grid barriers; slower than the
                                  default grid-barrier step on GB300, kept for comparison) */
@@ -71,7 +75,7 @@ typedef struct {
   int32_t max_seq;            /* KV capacity per sequence (positions) */
   int32_t max_batch;          /* number of sequences (independent caches) */
   uint32_t flags;             /* LLM_NO_GRAPH | LLM_NO_PDL | LLM_MULTI_KERNEL | LLM_DATAFLOW_STEP |
-                                 LLM_DEBUG_BATCH_HIDDEN | LLM_TEST_EXPIRE_WAIT */
+                                 LLM_DEBUG_BATCH_HIDDEN | LLM_W4A8 | LLM_TEST_EXPIRE_WAIT */
 } llm_config;
 
 /* One input tensor in the canonical layout, host memory, caller-owned, only
@@ -277,6 +281,13 @@ const char* llm_last_error(const llm_model* m);
  * host arrays. Allocates and frees its
  * own device memory; not for the token loop. */
 int llm_op_matvec(const llm_tensor* w, const float* x, float* y);
+
+/* llm_op_matvec in the W4A8 numerics of LLM_W4A8 (Q4G64 tensors only): x is
+ * quantized per 32-input block to int8 with an fp16 scale (aot-llm README,
+ * implementation notes: the f32 activation vector quantized once to Q8_0,
+ * integer dot products scaled back to f32), each block's integer sums
+ * scaled by its d and the group's scale and min. */
+int llm_op_matvec_w4a8(const llm_tensor* w, const float* x, float* y);
 
 /* y = W x with one weight matrix already resident in model m, without any
  * device allocation. No page has a counterpart: it exists for callers that

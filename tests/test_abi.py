@@ -68,5 +68,8 @@ int main(void) {
 
 
 def test_build_command_targets_sm103a():
-    cmd = " ".join(bq.nvcc_command("x.so"))
-    assert "arch=compute_103a,code=sm_103a" in cmd and "-shared" in cmd
+    for u in bq.UNITS:
+        cmd = " ".join(bq.nvcc_compile_command(u, "x.o"))
+        assert "arch=compute_103a,code=sm_103a" in cmd and " -c " in cmd and "-O3" in cmd
+    link = " ".join(bq.nvcc_link_command(["a.o", "b.o"], "x.so"))
+    assert "arch=compute_103a,code=sm_103a" in link and "-shared" in link

@@ -42,13 +42,20 @@ def test_touching_any_source_rebuilds(tmp_path, monkeypatch):
     monkeypatch.setattr(bq, "CSRC", str(csrc))
     monkeypatch.setattr(bq, "HEADER", str(inc / "llmq.h"))
     monkeypatch.setattr(bq, "LIB_PATH", str(lib))
-    calls = []
+    monkeypatch.setattr(bq, "BUILD_DIR", str(tmp_path / "_build"))
+    calls = []  # one entry per library link (each preceded by a compile of every unit)
+    compiled = []
 
     def fake_compile(cmd, *a, **k):
         out = cmd[cmd.index("-o") + 1]
         with open(out, "w") as f:
             f.write("built")
-        calls.append(out)
+        if "-shared" in cmd:
+            assert len(compiled) == len(bq.UNITS) and all(o in cmd for o in compiled)
+            compiled.clear()
+            calls.append(out)
+        else:
+            compiled.append(out)
         return 0
 
     monkeypatch.setattr(bq.subprocess, "check_call", fake_compile)
