@@ -30,6 +30,7 @@ LLM_F32, LLM_BF16, LLM_F16, LLM_Q4G64 = 0, 1, 2, 3
 LLM_NO_GRAPH, LLM_NO_PDL, LLM_MULTI_KERNEL, LLM_DATAFLOW_STEP = 1, 2, 4, 8
 LLM_DEBUG_BATCH_HIDDEN = 16
 LLM_W4A8 = 64
+LLM_KV_Q8 = 128
 LLM_TEST_EXPIRE_WAIT = 0x80000000
 STATUS = {0: "OK", -1: "INVALID_ARG", -2: "UNSUPPORTED", -3: "OOM", -4: "CTX_FULL", -5: "CUDA",
           -6: "TIMEOUT", -7: "NAN", -8: "NOT_FOUND"}
@@ -37,14 +38,14 @@ STATUS = {0: "OK", -1: "INVALID_ARG", -2: "UNSUPPORTED", -3: "OOM", -4: "CTX_FUL
 # Every entry point include/llmq.h declares.
 EXPORTS = ["llm_model_create", "llm_model_destroy", "llm_prefill", "llm_prefill_batched", "llm_decode_step",
            "llm_decode_greedy", "llm_set_sampling",
-           "llm_decode_step_batch", "llm_kv_reset", "llm_kv_write", "llm_kv_read", "llm_kv_len",
+           "llm_decode_step_batch", "llm_kv_reset", "llm_kv_write", "llm_kv_read", "llm_kv_read_q8", "llm_kv_len",
            "llm_debug_hidden", "llm_debug_unpack", "llm_model_stats", "llm_profile_step", "llm_time_kernel", "llm_sync",
            "llm_last_error", "llm_op_matvec", "llm_op_matvec_w4a8", "llm_matvec_noalloc", "llm_phase_times", "llm_debug_fail_alloc",
            "llm_debug_hidden_batch"]
 
 
 # translation units of the library, compiled in parallel and linked into one shared object
-UNITS = ["llmq.cu", "step_kernels.cu", "stepll_kernels.cu"]
+UNITS = ["llmq.cu", "step_kernels.cu", "step_kernels_kv8.cu", "stepll_kernels.cu"]
 BUILD_DIR = os.path.join(_HERE, "_build")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
@@ -146,6 +147,7 @@ def lib() -> C.CDLL:
             "llm_kv_reset": (i32, [P, i32]),
             "llm_kv_write": (i32, [P, i32, i32, i32, i32, P, P]),
             "llm_kv_read": (i32, [P, i32, i32, i32, i32, P, P]),
+            "llm_kv_read_q8": (i32, [P, i32, i32, i32, i32, P, P, P, P]),
             "llm_kv_len": (i32, [P, i32]),
             "llm_debug_hidden": (i32, [P, P]),
             "llm_debug_unpack": (i32, [P, C.c_char_p, P, P, P]),
@@ -289,6 +291,15 @@ class Model:
         v = np.empty(shape, np.uint16)
         _check(lib().llm_kv_read(self.h, seq, layer, pos0, n, k.ctypes.data, v.ctypes.data), self.h)
         return k, v
+
+    def kv_read_q8(self, seq: int, layer: int, pos0: int, n: int):
+        """Codes [n, Hkv, hd] (int8) and fp16 scale bits [n, Hkv, hd/32] of K and V (int8 caches)."""
+        H, hd = self.cfg["n_kv_heads"], self.cfg["head_dim"]
+        k, v = np.empty((n, H, hd), np.int8), np.empty((n, H, hd), np.int8)
+        ks, vs = np.empty((n, H, hd // 32), np.uint16), np.empty((n, H, hd // 32), np.uint16)
+        _check(lib().llm_kv_read_q8(self.h, seq, layer, pos0, n, k.ctypes.data, ks.ctypes.data, v.ctypes.data,
+                                    vs.ctypes.data), self.h)
+        return k, ks, v, vs
 
     def kv_len(self, seq: int) -> int:
         r = lib().llm_kv_len(self.h, seq)

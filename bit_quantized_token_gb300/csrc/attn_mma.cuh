@@ -147,4 +147,97 @@ __device__ __forceinline__ void attn_block16(const float* q, const uint16_t* kt,
   }
 }
 
+// attn_block16 over int8 K/V (the grouped int8 cache): kt/vt hold the codes
+// as fp16 (exact), ks/vs the staged rows' fp16 group scales [row][HD / 32].
+// A key group's scale multiplies that group's partial scores per position
+// (the MMAs of a group's two 16-dim slices accumulate apart). A value
+// group's scale folds into the probabilities before P V; dividing it by the
+// block's largest scale of the group keeps the scaled probabilities in [0, 1]
+// for their fp16 high/low split, and that largest scale multiplies the MMA
+// result back. Same outputs as attn_block16.
+template <int GQ, int HD, int RS>
+__device__ __forceinline__ void attn_block16_q8(const float* q, const uint16_t* kt, const uint16_t* vt,
+                                                const uint16_t* ks, const uint16_t* vs, int row0, int nvalid,
+                                                int lane, float* out, int OS) {
+  constexpr int NG = HD / 32;
+  const int g = lane >> 2, t = lane & 3, r8 = lane & 7, mi = lane >> 3;
+  float s[NG][2][4];
+#pragma unroll
+  for (int k = 0; k < NG; ++k)
+#pragma unroll
+    for (int j = 0; j < 2; ++j)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) s[k][j][e] = 0.f;
+#pragma unroll
+  for (int kk = 0; kk < HD / 16; ++kk) {
+    uint32_t qf[4];
+    attn_q_frag<GQ, HD>(qf, q, kk, lane);
+    uint32_t b[4];
+    ldsm_x4(b, kt + (size_t)(row0 + 8 * (mi >> 1) + r8) * RS + 16 * kk + 8 * (mi & 1));
+    mma_f16_16816(s[kk / 2][0], qf, b[0], b[1]);
+    mma_f16_16816(s[kk / 2][1], qf, b[2], b[3]);
+  }
+  // this lane's positions: 2t, 2t+1, 2t+8, 2t+9 of the block (score / probability i)
+  int li[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) li[i] = 8 * (i >> 1) + 2 * t + (i & 1);
+  float sc[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int j = i >> 1, e = i & 1;
+    float v = 0.f;
+#pragma unroll
+    for (int k = 0; k < NG; ++k)
+      v += __half2float(__ushort_as_half(ks[(row0 + li[i]) * NG + k])) * (s[k][j][e] + s[k][j][e + 2]);
+    sc[i] = li[i] < nvalid ? v : -INFINITY;
+  }
+  float mx = fmaxf(fmaxf(sc[0], sc[1]), fmaxf(sc[2], sc[3]));
+  mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+  mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+  float p[4], sum = 0.f;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    p[i] = exp2f(sc[i] - mx);
+    sum += p[i];
+  }
+  sum += __shfl_xor_sync(0xffffffffu, sum, 1);
+  sum += __shfl_xor_sync(0xffffffffu, sum, 2);
+  float* o = out + g * OS;
+  const bool mine = g < GQ;
+#pragma unroll
+  for (int vg = 0; vg < NG; ++vg) {
+    float r[4], smax = 0.f;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      r[i] = __half2float(__ushort_as_half(vs[(row0 + li[i]) * NG + vg]));
+      smax = fmaxf(smax, r[i]);
+    }
+    smax = fmaxf(smax, __shfl_xor_sync(0xffffffffu, smax, 1));
+    smax = fmaxf(smax, __shfl_xor_sync(0xffffffffu, smax, 2));
+    const float inv = smax > 0.f ? 1.0f / smax : 0.f;
+    float ph[4], pl[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) split_f16(p[i] * (r[i] * inv), ph[i], pl[i]);
+    const uint32_t pa[4] = {pack_f16x2(ph[0], ph[1]), pack_f16x2(pl[0], pl[1]), pack_f16x2(ph[2], ph[3]),
+                            pack_f16x2(pl[2], pl[3])};
+#pragma unroll
+    for (int nt = 4 * vg; nt < 4 * vg + 4; nt += 2) {
+      uint32_t b[4];
+      ldsm_x4_t(b, vt + (size_t)(row0 + 8 * (mi & 1) + r8) * RS + 8 * (nt + (mi >> 1)));
+      float d0[4] = {0.f, 0.f, 0.f, 0.f}, d1[4] = {0.f, 0.f, 0.f, 0.f};
+      mma_f16_16816(d0, pa, b[0], b[1]);
+      mma_f16_16816(d1, pa, b[2], b[3]);
+      if (mine) {
+        *reinterpret_cast<float2*>(o + 8 * nt + 2 * t) = make_float2((d0[0] + d0[2]) * smax, (d0[1] + d0[3]) * smax);
+        *reinterpret_cast<float2*>(o + 8 * nt + 8 + 2 * t) =
+            make_float2((d1[0] + d1[2]) * smax, (d1[1] + d1[3]) * smax);
+      }
+    }
+  }
+  if (mine && t == 0) {
+    o[HD] = mx;
+    o[HD + 1] = sum;
+  }
+}
+
 }  // namespace llmq

@@ -213,6 +213,12 @@ struct llm_model {
   size_t off_final_norm = 0;
   uint16_t* d_k = nullptr;                    // [B][L][Hkv][cap][hd]
   uint16_t* d_v = nullptr;
+  bool kv8 = false;                           // LLM_KV_Q8: the grouped int8 cache instead of d_k / d_v
+  bool bkv8_ok = false;                       // the batched kernels read and append it
+  int8_t* d_k8 = nullptr;                     // codes [B][L][Hkv][cap][hd]
+  int8_t* d_v8 = nullptr;
+  uint16_t* d_ks = nullptr;                   // fp16 group scales [B][L][Hkv][cap][hd / 32]
+  uint16_t* d_vs = nullptr;
   float2* d_rope = nullptr;                   // [cap][hd/2]
 
   // step plans
@@ -600,8 +606,16 @@ cudaError_t enqueue_persistent_step(llm_model* m, int seq, bool fused) {
   sp.rope = m->d_rope;
   sp.pos = m->d_pos + seq;
   sp.layer_stride = (size_t)c.n_kv_heads * c.max_seq * c.head_dim;
-  sp.k_base = m->d_k + (size_t)seq * c.n_layers * sp.layer_stride;
-  sp.v_base = m->d_v + (size_t)seq * c.n_layers * sp.layer_stride;
+  const size_t seq_off = (size_t)seq * c.n_layers * sp.layer_stride;
+  if (m->kv8) {
+    sp.k8_base = m->d_k8 + seq_off;
+    sp.v8_base = m->d_v8 + seq_off;
+    sp.ks_base = m->d_ks + seq_off / 32;
+    sp.vs_base = m->d_vs + seq_off / 32;
+  } else {
+    sp.k_base = m->d_k + seq_off;
+    sp.v_base = m->d_v + seq_off;
+  }
   // the split partials of the step kernel share the multi-kernel path's buffer
   sp.attn_o = m->d_attn_part;
   sp.attn_ml = m->d_attn_part + (size_t)c.n_kv_heads * m->attn_P * m->gq * c.head_dim;
@@ -618,7 +632,8 @@ cudaError_t enqueue_persistent_step(llm_model* m, int seq, bool fused) {
   sp.hist_cap = c.max_seq;
   cudaError_t e = cudaMemsetAsync(m->d_step_sync, 0, 2 * sizeof(int), m->stream);
   if (e != cudaSuccess) return e;
-  return launch_cooperative(m, step_kernel_ref(m->gq, c.head_dim, fused, (c.flags & LLM_W4A8) != 0), kSThreads, sp);
+  return launch_cooperative(m, step_kernel_ref(m->gq, c.head_dim, fused, (c.flags & LLM_W4A8) != 0, m->kv8), kSThreads,
+                            sp);
 }
 
 
@@ -1221,8 +1236,16 @@ int llm_model_create(const llm_config* cfg, const llm_tensor* tensors, int32_t n
   AL(m->d_embed, emb_bytes, "embedding");
   AL(m->d_norms, norms.size() * 4, "norms");
   const size_t kv_elems = (size_t)c.max_batch * L * c.n_kv_heads * c.max_seq * hd;
-  AL(m->d_k, kv_elems * 2, "K cache");
-  AL(m->d_v, kv_elems * 2, "V cache");
+  m->kv8 = (c.flags & LLM_KV_Q8) != 0;
+  if (m->kv8) {
+    AL(m->d_k8, kv_elems, "int8 K cache");
+    AL(m->d_v8, kv_elems, "int8 V cache");
+    AL(m->d_ks, kv_elems / 32 * 2, "K cache scales");
+    AL(m->d_vs, kv_elems / 32 * 2, "V cache scales");
+  } else {
+    AL(m->d_k, kv_elems * 2, "K cache");
+    AL(m->d_v, kv_elems * 2, "V cache");
+  }
   AL(m->d_rope, (size_t)c.max_seq * (hd / 2) * sizeof(float2), "rope table");
 
   for (int l = 0; l < L; ++l) {
@@ -1303,7 +1326,7 @@ int llm_model_create(const llm_config* cfg, const llm_tensor* tensors, int32_t n
                 std::min({d, m->q_dim, F}) >= 256;
   for (bool fused : {false, true}) {
     if (!m->use_step) break;
-    const KernelRef k = step_kernel_ref(gq, hd, fused, (c.flags & LLM_W4A8) != 0);
+    const KernelRef k = step_kernel_ref(gq, hd, fused, (c.flags & LLM_W4A8) != 0, (c.flags & LLM_KV_Q8) != 0);
     int per_sm = 0;
     cudaError_t e = k.fn ? raise_smem_limit(k.fn, k.smem) : cudaErrorInvalidDeviceFunction;
     if (e == cudaSuccess) e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k.fn, kSThreads, k.smem);
@@ -1312,6 +1335,10 @@ int llm_model_create(const llm_config* cfg, const llm_tensor* tensors, int32_t n
       m->use_step = false;  // fall back to the per-kernel step
     }
   }
+  if (m->kv8 && !m->use_step)
+    return fail(set_err(m, LLM_ERR_UNSUPPORTED,
+                        "the int8 K/V cache (LLM_KV_Q8) runs in the persistent step only: not with LLM_MULTI_KERNEL, "
+                        "and the shape must fit it (head_dim 64 or 128, dim, q_dim and ffn_dim >= 256)"));
   std::vector<Phase> phases;
   {
     auto gemv_phase = [&](const GemvPlan& g, float* out_part) {
@@ -1399,7 +1426,7 @@ int llm_model_create(const llm_config* cfg, const llm_tensor* tensors, int32_t n
   {
     const int R = m->step_R;
     const int hpr = R > 0 ? c.n_kv_heads / R : 0;
-    bool ok = m->use_step && (c.flags & LLM_DATAFLOW_STEP) && !(c.flags & LLM_W4A8) && m->n_sm <= kLMaxCTAs && R >= 1 &&
+    bool ok = m->use_step && (c.flags & LLM_DATAFLOW_STEP) && !(c.flags & (LLM_W4A8 | LLM_KV_Q8)) && m->n_sm <= kLMaxCTAs && R >= 1 &&
               c.n_kv_heads % R == 0 && hpr * gq * hd <= kSFuseOut && d / R <= kLMaxRes && d <= kLMaxKr;
     auto lgemv = [&](const GemvPlan& g, int r) {
       LPhase p{};
@@ -1610,8 +1637,15 @@ int llm_model_create(const llm_config* cfg, const llm_tensor* tensors, int32_t n
     if (e == cudaSuccess && m->bsmem_max)
       e = raise_smem_limit(bgemv_kernel<true>, m->bsmem_max);
     if (e == cudaSuccess) e = battn_set_smem(gq, hd);
-    if (e == cudaSuccess) e = cudaMemset(m->d_k, 0, kv_elems * 2);
-    if (e == cudaSuccess) e = cudaMemset(m->d_v, 0, kv_elems * 2);
+    if (m->kv8) {
+      for (int8_t* z : {m->d_k8, m->d_v8})
+        if (e == cudaSuccess) e = cudaMemset(z, 0, kv_elems);
+      for (uint16_t* z : {m->d_ks, m->d_vs})
+        if (e == cudaSuccess) e = cudaMemset(z, 0, kv_elems / 32 * 2);
+    } else {
+      if (e == cudaSuccess) e = cudaMemset(m->d_k, 0, kv_elems * 2);
+      if (e == cudaSuccess) e = cudaMemset(m->d_v, 0, kv_elems * 2);
+    }
     size_t smax = m->lm.smem;
     for (int l = 0; l < L; ++l)
       smax = std::max({smax, m->qkv[l].smem, m->wo[l].smem, m->gu[l].smem, m->down[l].smem});
@@ -1684,6 +1718,7 @@ int llm_prefill_batched(llm_model* m, int32_t seq, const int32_t* tokens, int32_
   NvtxRange nvtx_("llm_prefill_batched");
   int rc = check_model(m, seq);
   if (rc) return rc;
+  if (m->kv8 && !m->bkv8_ok) return set_err(m, LLM_ERR_UNSUPPORTED, "batched prompt processing with the int8 K/V cache");
   if (!tokens || n <= 0) return set_err(m, LLM_ERR_INVALID_ARG, "empty prompt");
   if (m->len[seq] + n > m->cfg.max_seq) return set_err(m, LLM_ERR_CTX_FULL, "prompt would exceed max_seq");
   std::vector<int32_t> rows(3 * m->pf_cap);  // [tok | pos | seq]
@@ -1786,6 +1821,7 @@ int llm_decode_step_batch(llm_model* m, const int32_t* tokens, int32_t n_seq, fl
   NvtxRange nvtx_("llm_decode_step_batch");
   int rc = check_model(m, 0);
   if (rc) return rc;
+  if (m->kv8 && !m->bkv8_ok) return set_err(m, LLM_ERR_UNSUPPORTED, "batched decode with the int8 K/V cache");
   const llm_config& c = m->cfg;
   if (c.max_batch < 2) return set_err(m, LLM_ERR_UNSUPPORTED, "the model was created with max_batch < 2");
   if (n_seq != c.max_batch) return set_err(m, LLM_ERR_INVALID_ARG, "n_seq must equal max_batch");
@@ -1836,6 +1872,28 @@ int llm_kv_reset(llm_model* m, int32_t seq) {
   return LLM_OK;
 }
 
+// The cache's grouped int8 quantizer on the host (llm_kv_write into an int8
+// cache): each 32 values of a (position, head) row get the fp16 scale
+// fp16(amax / 127) and codes round(x / scale), half away from zero, clamped
+// to +-127 -- in fp32, the operations of the kernels' append.
+static void q8_quantize_host(const uint16_t* bf16, size_t n_vals, int8_t* codes, uint16_t* scales) {
+  for (size_t g = 0; g < n_vals / 32; ++g) {
+    float x[32], amax = 0.0f;
+    for (int i = 0; i < 32; ++i) {
+      const uint32_t u = (uint32_t)bf16[g * 32 + i] << 16;
+      std::memcpy(&x[i], &u, 4);
+      amax = std::max(amax, std::fabs(x[i]));
+    }
+    const __half dh = __float2half_rn(amax / 127.0f);
+    const float d = __half2float(dh);
+    for (int i = 0; i < 32; ++i) {
+      const float cf = d == 0.0f ? 0.0f : std::min(std::max(std::roundf(x[i] / d), -127.0f), 127.0f);
+      codes[g * 32 + i] = (int8_t)(int)cf;
+    }
+    std::memcpy(&scales[g], &dh, 2);
+  }
+}
+
 static int kv_copy(llm_model* m, int32_t seq, int32_t layer, int32_t pos0, int32_t n, const uint16_t* src_k,
                    const uint16_t* src_v, uint16_t* dst_k, uint16_t* dst_v, bool write) {
   int rc = check_model(m, seq);
@@ -1845,6 +1903,30 @@ static int kv_copy(llm_model* m, int32_t seq, int32_t layer, int32_t pos0, int32
   if (pos0 + n > c.max_seq) return set_err(m, LLM_ERR_CTX_FULL, "positions beyond max_seq");
   const int hd = c.head_dim, H = c.n_kv_heads;
   const size_t base = (((size_t)seq * c.n_layers + layer) * H) * c.max_seq * hd;
+  if (m->kv8) {
+    if (!write) return set_err(m, LLM_ERR_UNSUPPORTED, "the int8 K/V cache is read with llm_kv_read_q8");
+    if (!src_k || !src_v) return set_err(m, LLM_ERR_INVALID_ARG, "null key/value pointer");
+    const size_t nv = (size_t)n * H * hd;
+    std::vector<uint16_t> hb(nv);
+    std::vector<int8_t> codes(nv);
+    std::vector<uint16_t> scales(nv / 32);
+    for (int which = 0; which < 2; ++which) {
+      CK(cudaMemcpy(hb.data(), which ? src_v : src_k, nv * 2, cudaMemcpyDefault), "kv read-in");
+      q8_quantize_host(hb.data(), nv, codes.data(), scales.data());
+      for (int g = 0; g < H; ++g) {
+        const size_t off = base + ((size_t)g * c.max_seq + pos0) * hd;
+        CK(cudaMemcpy2D((which ? m->d_v8 : m->d_k8) + off, hd, codes.data() + (size_t)g * hd, (size_t)H * hd, hd, n,
+                        cudaMemcpyHostToDevice), "kv write");
+        CK(cudaMemcpy2D((which ? m->d_vs : m->d_ks) + off / 32, hd / 16, scales.data() + (size_t)g * (hd / 32),
+                        (size_t)H * (hd / 16), hd / 16, n, cudaMemcpyHostToDevice), "kv scale write");
+      }
+    }
+    m->len[seq] = std::max(m->len[seq], pos0 + n);
+    m->h_stage[1] = m->len[seq];
+    CK(cudaMemcpyAsync(m->d_pos + seq, m->h_stage + 1, 4, cudaMemcpyHostToDevice, m->stream), "position set");
+    CK(cudaStreamSynchronize(m->stream), "kv sync");
+    return LLM_OK;
+  }
   for (int g = 0; g < H; ++g) {
     const size_t cache_off = base + ((size_t)g * c.max_seq + pos0) * hd;
     for (int which = 0; which < 2; ++which) {
@@ -1878,6 +1960,31 @@ int llm_kv_write(llm_model* m, int32_t seq, int32_t layer, int32_t pos0, int32_t
 
 int llm_kv_read(llm_model* m, int32_t seq, int32_t layer, int32_t pos0, int32_t n, uint16_t* k, uint16_t* v) {
   return kv_copy(m, seq, layer, pos0, n, nullptr, nullptr, k, v, false);
+}
+
+int llm_kv_read_q8(llm_model* m, int32_t seq, int32_t layer, int32_t pos0, int32_t n, int8_t* k, uint16_t* ks,
+                   int8_t* v, uint16_t* vs) {
+  int rc = check_model(m, seq);
+  if (rc) return rc;
+  const llm_config& c = m->cfg;
+  if (!m->kv8) return set_err(m, LLM_ERR_UNSUPPORTED, "the model's K/V cache is bf16 (llm_kv_read)");
+  if (!k || !ks || !v || !vs) return set_err(m, LLM_ERR_INVALID_ARG, "null output");
+  if (layer < 0 || layer >= c.n_layers || pos0 < 0 || n <= 0) return set_err(m, LLM_ERR_INVALID_ARG, "bad layer/pos/n");
+  if (pos0 + n > c.max_seq) return set_err(m, LLM_ERR_CTX_FULL, "positions beyond max_seq");
+  const int hd = c.head_dim, H = c.n_kv_heads;
+  const size_t base = (((size_t)seq * c.n_layers + layer) * H) * c.max_seq * hd;
+  for (int g = 0; g < H; ++g) {
+    const size_t off = base + ((size_t)g * c.max_seq + pos0) * hd;
+    for (int which = 0; which < 2; ++which) {
+      CK(cudaMemcpy2DAsync((which ? v : k) + (size_t)g * hd, (size_t)H * hd, (which ? m->d_v8 : m->d_k8) + off, hd, hd,
+                           n, cudaMemcpyDefault, m->stream), "kv read");
+      CK(cudaMemcpy2DAsync((which ? vs : ks) + (size_t)g * (hd / 32), (size_t)H * (hd / 16),
+                           (which ? m->d_vs : m->d_ks) + off / 32, hd / 16, hd / 16, n, cudaMemcpyDefault, m->stream),
+         "kv scale read");
+    }
+  }
+  CK(cudaStreamSynchronize(m->stream), "kv sync");
+  return LLM_OK;
 }
 
 int llm_kv_len(const llm_model* m, int32_t seq) {
@@ -1933,7 +2040,8 @@ int llm_model_stats(const llm_model* m, llm_stats* out) {
   int64_t w = 0;
   for (const auto& x : m->mats) w += (int64_t)x.bytes();
   out->weight_stream_bytes = w;
-  out->kv_bytes_per_pos = (int64_t)2 * m->cfg.n_layers * m->cfg.n_kv_heads * m->cfg.head_dim * 2;
+  out->kv_bytes_per_pos = m->kv8 ? (int64_t)2 * m->cfg.n_layers * m->cfg.n_kv_heads * (m->cfg.head_dim + m->cfg.head_dim / 16)
+                                 : (int64_t)2 * m->cfg.n_layers * m->cfg.n_kv_heads * m->cfg.head_dim * 2;
   out->kernels_per_step = m->kernels_per_step;
   out->n_sm = m->n_sm;
   return LLM_OK;
@@ -1942,6 +2050,7 @@ int llm_model_stats(const llm_model* m, llm_stats* out) {
 int llm_profile_step(llm_model* m, int32_t seq, int32_t token, llm_kernel_time* out, int32_t max_out) {
   int rc = check_model(m, seq);
   if (rc) return rc;
+  if (m->kv8) return set_err(m, LLM_ERR_UNSUPPORTED, "the per-kernel profile runs the bf16 K/V cache's kernels");
   if (token < 0 || token >= m->cfg.vocab) return set_err(m, LLM_ERR_INVALID_ARG, "token out of range");
   if (m->len[seq] + 1 > m->cfg.max_seq) return set_err(m, LLM_ERR_CTX_FULL, "sequence is at max_seq");
   if (!out || max_out < 0) return set_err(m, LLM_ERR_INVALID_ARG, "null output");
@@ -1970,6 +2079,8 @@ int llm_time_kernel(llm_model* m, int32_t seq, int32_t which, int32_t layer, int
   if (which < 0 || which > 6 || n <= 0 || !ms || !bytes) return set_err(m, LLM_ERR_INVALID_ARG, "bad kernel/n");
   if (layer < -1 || layer >= L) return set_err(m, LLM_ERR_INVALID_ARG, "bad layer");
   if (m->len[seq] < 1) return set_err(m, LLM_ERR_INVALID_ARG, "run a step of the sequence first");
+  if (m->kv8 && which == W_ATTN)
+    return set_err(m, LLM_ERR_UNSUPPORTED, "the per-kernel attention reads the bf16 K/V cache");
   // attention re-reads position len-1 (and re-appends that slot with the values already there)
   m->h_stage[2] = m->len[seq] - 1;
   CK(cudaMemcpyAsync(m->d_pos + seq, m->h_stage + 2, 4, cudaMemcpyHostToDevice, m->stream), "position set");

@@ -128,6 +128,10 @@ struct StepParams {
   int* pos;               // position of the sequence (advanced by the greedy choice)
   uint16_t* k_base;       // layer 0 of this sequence's cache: [L][Hkv][cap][hd]
   uint16_t* v_base;
+  int8_t* k8_base;        // the grouped int8 cache instead (int8 K/V models): codes [L][Hkv][cap][hd]
+  int8_t* v8_base;
+  uint16_t* ks_base;      // and fp16 scales of each 32-element group [L][Hkv][cap][hd / 32]
+  uint16_t* vs_base;
   size_t layer_stride;    // elements per layer of the cache
   float* attn_o;          // [Hkv][P][GQ][hd] unnormalised split outputs
   float* attn_ml;         // [Hkv][P][GQ][2] (max, sum) of the splits
@@ -253,6 +257,9 @@ struct StepAttnSmem {
   float acc[GQ][HD];          // running output of the item over its passes
   float accm[GQ], accl[GQ];
   float fac[GQ][NBW + 1];
+  __align__(16) uint16_t ksc[PP][HD / 32];  // int8 K/V: fp16 group scales of the staged rows
+  __align__(16) uint16_t vsc[PP][HD / 32];
+  float cursc[2][HD / 32];    // int8 K/V: this step's k, v group scales (cur then holds their codes)
   int is_last;
 };
 
@@ -290,13 +297,31 @@ struct StepSmem {
 // steps, so this runs before the grid barrier that the item's q|k|v wait for;
 // row `pos` and the zero rows are written by the item. Thread-to-chunk map of
 // step_attn_item's tile loads.
-template <int GQ, int HD>
+template <int GQ, int HD, bool KV8>
 __device__ void step_attn_prefetch(const StepParams& sp, int layer, int g, int t0, int t1, int pos,
                                    StepAttnSmem<GQ, HD>& sa) {
   using SA = StepAttnSmem<GQ, HD>;
   constexpr int NT = kSCThreads, PP = SA::PP, CH = HD / 8;
   constexpr int TB = (2 * PP * CH + NT - 1) / NT;
   const int tid = threadIdx.x;
+  if constexpr (KV8) {
+    // one thread per staged row: its codes into the first HD bytes of the
+    // row's fp16 slot (widened in place by the same thread), its scales beside
+    static_assert(2 * PP <= NT, "one row per thread");
+    constexpr int NG = HD / 32;
+    const size_t cbase = (size_t)layer * sp.layer_stride + (size_t)g * sp.cap * HD;
+    const int n = min(PP, t1 - t0);
+    const int kv = tid / PP, row = tid - kv * PP;
+    if (kv < 2 && row < n && t0 + row != pos) {
+      const int8_t* src = (kv ? sp.v8_base : sp.k8_base) + cbase + (size_t)(t0 + row) * HD;
+      uint8_t* dst = reinterpret_cast<uint8_t*>(&(kv ? sa.vt : sa.kt)[row][0]);
+#pragma unroll
+      for (int c = 0; c < HD / 16; ++c) cp_async16(dst + 16 * c, src + 16 * c);
+      cp_async_small<2 * NG>(&(kv ? sa.vsc : sa.ksc)[row][0],
+                             (kv ? sp.vs_base : sp.ks_base) + cbase / 32 + (size_t)(t0 + row) * NG);
+    }
+    return;
+  }
   const uint16_t* kc = sp.k_base + (size_t)layer * sp.layer_stride + (size_t)g * sp.cap * HD;
   const uint16_t* vc = sp.v_base + (size_t)layer * sp.layer_stride + (size_t)g * sp.cap * HD;
   const int n = min(PP, t1 - t0);
@@ -314,7 +339,7 @@ __device__ void step_attn_prefetch(const StepParams& sp, int layer, int g, int t
 // leaves its split's unnormalised partial (o, max, sum) in global memory;
 // otherwise (one split over the whole cache) it writes the normalised output
 // of its GQ heads to fo[h * HD + d] in shared memory.
-template <int GQ, int HD>
+template <int GQ, int HD, bool KV8>
 __device__ void step_attn_item(const StepParams& sp, const Phase& P, int g, int split, int P_eff, int pos,
                                StepAttnSmem<GQ, HD>& sa, bool append, float* fo, bool prefetched) {
   using SA = StepAttnSmem<GQ, HD>;
@@ -325,14 +350,73 @@ __device__ void step_attn_item(const StepParams& sp, const Phase& P, int g, int 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int len = pos + 1;
   const int t0 = (int)((int64_t)len * split / P_eff), t1 = (int)((int64_t)len * (split + 1) / P_eff);
-  uint16_t* kc = sp.k_base + (size_t)P.layer * sp.layer_stride + (size_t)g * sp.cap * HD;
-  uint16_t* vc = sp.v_base + (size_t)P.layer * sp.layer_stride + (size_t)g * sp.cap * HD;
+  constexpr int NG = HD / 32;
+  const size_t cbase = (size_t)P.layer * sp.layer_stride + (size_t)g * sp.cap * HD;
+  uint16_t* kc = KV8 ? nullptr : sp.k_base + cbase;
+  uint16_t* vc = KV8 ? nullptr : sp.v_base + cbase;
+  int8_t* kc8 = KV8 ? sp.k8_base + cbase : nullptr;  // int8 K/V: codes and group scales
+  int8_t* vc8 = KV8 ? sp.v8_base + cbase : nullptr;
+  uint16_t* ks8 = KV8 ? sp.ks_base + cbase / 32 : nullptr;
+  uint16_t* vs8 = KV8 ? sp.vs_base + cbase / 32 : nullptr;
+  // int8 K/V: a row's HD codes (in registers) as fp16 halves (exact) into its tile row
+  auto write_row_f16 = [&](uint16_t* tr, const uint4 (&c)[HD / 16]) {
+#pragma unroll
+    for (int k = HD / 16 - 1; k >= 0; --k) {  // from the end: the codes may sit in the row's first bytes
+      const uint32_t w[4] = {c[k].x, c[k].y, c[k].z, c[k].w};
+      uint32_t h[8];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const float b0 = (float)(int8_t)(w[q] & 0xFF), b1 = (float)(int8_t)((w[q] >> 8) & 0xFF);
+        const float b2 = (float)(int8_t)((w[q] >> 16) & 0xFF), b3 = (float)(int8_t)(w[q] >> 24);
+        h[2 * q] = pack_f16x2(b0, b1);
+        h[2 * q + 1] = pack_f16x2(b2, b3);
+      }
+      reinterpret_cast<uint4*>(tr)[2 * k] = make_uint4(h[0], h[1], h[2], h[3]);
+      reinterpret_cast<uint4*>(tr)[2 * k + 1] = make_uint4(h[4], h[5], h[6], h[7]);
+    }
+  };
+  // int8 K/V, the first pass: one thread per staged row widens the codes its
+  // own asynchronous copies left in the first HD bytes of the row's slot, and
+  // zero-fills rows n .. `rows` (codes and scales); row `pos` is left to this
+  // step's k, v
+  auto widen_rows = [&](int n, int rows) {
+    const int kv = tid / PP, row = tid - kv * PP;
+    if (kv < 2 && row < rows && t0 + row != pos) {
+      uint16_t* tr = &(kv ? sa.vt : sa.kt)[row][0];
+      uint4 c[HD / 16];
+#pragma unroll
+      for (int k = 0; k < HD / 16; ++k)
+        c[k] = row < n ? reinterpret_cast<const uint4*>(tr)[k] : make_uint4(0u, 0u, 0u, 0u);
+      write_row_f16(tr, c);
+      if (row >= n)
+#pragma unroll
+        for (int k = 0; k < NG; ++k) (kv ? sa.vsc : sa.ksc)[row][k] = 0;
+    }
+  };
 
   // K/V rows tp .. tp+n-1 -> registers (zero beyond the split); stored into
   // the padded tiles once the previous readers are done. Row `pos` is left to
   // this step's k, v (another CTA may be appending it to the cache meanwhile).
-  uint4 tl[TB];
+  uint4 tl[KV8 ? HD / 16 : TB];
+  uint2 tsc = make_uint2(0u, 0u);  // int8 K/V: the row's group scales (NG halves)
   auto load_tile = [&](int tp) {
+    if constexpr (KV8) {
+      const int n = min(PP, t1 - tp);
+      const int kv = tid / PP, row = tid - kv * PP;
+      const bool ld = kv < 2 && row < n && tp + row != pos;
+      const int8_t* src = (kv ? vc8 : kc8) + (size_t)(tp + row) * HD;
+#pragma unroll
+      for (int k = 0; k < HD / 16; ++k) {
+        const float4 v = ldcg4_if(reinterpret_cast<const float*>(src + 16 * k), ld);
+        tl[k] = make_uint4(__float_as_uint(v.x), __float_as_uint(v.y), __float_as_uint(v.z), __float_as_uint(v.w));
+      }
+      const uint16_t* ssrc = (kv ? vs8 : ks8) + (size_t)(tp + row) * NG;
+      if (ld) {
+        if constexpr (NG == 2) tsc.x = __ldcg(reinterpret_cast<const unsigned int*>(ssrc));
+        else tsc = __ldcg(reinterpret_cast<const uint2*>(ssrc));
+      }
+      return;
+    }
     const int n = min(PP, t1 - tp);
 #pragma unroll
     for (int j = 0; j < TB; ++j) {
@@ -343,6 +427,20 @@ __device__ void step_attn_item(const StepParams& sp, const Phase& P, int g, int 
     }
   };
   auto store_tile = [&](int tp) {
+    if constexpr (KV8) {
+      const int n = min(PP, t1 - tp), rows = ((n + 15) / 16) * 16;
+      const int kv = tid / PP, row = tid - kv * PP;
+      if (kv < 2 && row < rows && tp + row != pos) {
+        if (row >= n)
+#pragma unroll
+          for (int k = 0; k < HD / 16; ++k) tl[k] = make_uint4(0u, 0u, 0u, 0u);
+        write_row_f16(&(kv ? sa.vt : sa.kt)[row][0], tl);
+        uint16_t* sc = &(kv ? sa.vsc : sa.ksc)[row][0];
+        if constexpr (NG == 2) *reinterpret_cast<unsigned int*>(sc) = row < n ? tsc.x : 0u;
+        else *reinterpret_cast<uint2*>(sc) = row < n ? tsc : make_uint2(0u, 0u);
+      }
+      return;
+    }
     const int rows = ((min(PP, t1 - tp) + 15) / 16) * 16;
 #pragma unroll
     for (int j = 0; j < TB; ++j) {
@@ -353,7 +451,7 @@ __device__ void step_attn_item(const StepParams& sp, const Phase& P, int g, int 
                        bf16x2_to_f16x2(tl[j].w));
     }
   };
-  if (!prefetched) step_attn_prefetch<GQ, HD>(sp, P.layer, g, t0, t1, pos, sa);
+  if (!prefetched) step_attn_prefetch<GQ, HD, KV8>(sp, P.layer, g, t0, t1, pos, sa);
 
   // RoPE factors and q/k norm weights do not depend on the step: load them
   // in the same round trip as the q|k|v gather and the first tile
@@ -398,8 +496,9 @@ __device__ void step_attn_item(const StepParams& sp, const Phase& P, int g, int 
     // (each thread its own chunks), zero rows up to the next multiple of 16
     cp_async_wait_all();
     const int n = min(PP, t1 - t0), rows = ((n + 15) / 16) * 16;
+    if constexpr (KV8) widen_rows(n, rows);
 #pragma unroll
-    for (int j = 0; j < TB; ++j) {
+    for (int j = 0; j < (KV8 ? 0 : TB); ++j) {
       const int idx = tid + j * NT, kv = idx / (PP * CH), rem = idx - kv * (PP * CH), row = rem / CH, ch = rem - row * CH;
       if (kv < 2 && row < rows && t0 + row != pos) {
         uint4* q = reinterpret_cast<uint4*>(&(kv ? sa.vt : sa.kt)[row][8 * ch]);
@@ -433,6 +532,10 @@ __device__ void step_attn_item(const StepParams& sp, const Phase& P, int g, int 
   const float qscale = 1.4426950408889634f / sqrtf((float)HD);
   const bool owner = t1 == len && pos - t0 < PP;  // the first pass's tile holds `pos`
   auto keep = [&](int r, int d, float x) {  // final value of cur[r][d], r >= GQ
+    if constexpr (KV8) {  // quantized per 32-element group below
+      sa.cur[r][d] = x;
+      return;
+    }
     const __nv_bfloat16 b = __float2bfloat16_rn(x);
     const float xr = __bfloat162float(b);
     sa.cur[r][d] = xr;
@@ -455,6 +558,32 @@ __device__ void step_attn_item(const StepParams& sp, const Phase& P, int g, int 
   } else if (tid < nrope + HD) {
     keep(GQ + 1, tid - nrope, sa.cur[GQ + 1][tid - nrope]);
   }
+  if constexpr (KV8) {
+    // the grouped int8 append: warp (kv, group) quantizes 32 elements of k or
+    // v (fp16 scale fp16(amax / 127), codes round(x / scale) half away from
+    // zero, clamped to +-127, all in fp32); cur keeps the codes, cursc the scales
+    ConsumerSync::sync();
+    if (warp < 2 * NG) {
+      const int kv = warp / NG, grp = warp - kv * NG, d = 32 * grp + lane;
+      const float x = sa.cur[GQ + kv][d];
+      float amax = fabsf(x);
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+      const __half dh = __float2half_rn(amax / 127.0f);
+      const float dq = __half2float(dh);
+      const float cf = dq == 0.0f ? 0.0f : fminf(fmaxf(roundf(x / dq), -127.0f), 127.0f);
+      sa.cur[GQ + kv][d] = cf;
+      if (lane == 0) sa.cursc[kv][grp] = dq;
+      if (append) {
+        (kv ? vc8 : kc8)[(size_t)pos * HD + d] = (int8_t)(int)cf;
+        if (lane == 0) (kv ? vs8 : ks8)[(size_t)pos * NG + grp] = __half_as_ushort(dh);
+      }
+      if (owner) {
+        (kv ? sa.vt : sa.kt)[pos - t0][d] = __half_as_ushort(__float2half_rn(cf));
+        if (lane == 0) (kv ? sa.vsc : sa.ksc)[pos - t0][grp] = __half_as_ushort(dh);
+      }
+    }
+  }
   for (int i = tid; i < GQ * HD; i += NT) sa.acc[i / HD][i % HD] = 0.f;
   if (tid < GQ) {
     sa.accm[tid] = -INFINITY;
@@ -468,16 +597,26 @@ __device__ void step_attn_item(const StepParams& sp, const Phase& P, int g, int 
     if (tp != t0) {
       load_tile(tp);
       store_tile(tp);
-      if (pos >= tp && pos < tp + n)
+      if (pos >= tp && pos < tp + n) {
         for (int d = tid; d < HD; d += NT) {
           sa.kt[pos - tp][d] = __half_as_ushort(__float2half_rn(sa.cur[GQ][d]));
           sa.vt[pos - tp][d] = __half_as_ushort(__float2half_rn(sa.cur[GQ + 1][d]));
         }
+        if constexpr (KV8)
+          if (tid < 2 * NG)
+            (tid < NG ? sa.ksc : sa.vsc)[pos - tp][tid % NG] =
+                __half_as_ushort(__float2half_rn(sa.cursc[tid / NG][tid % NG]));
+      }
       ConsumerSync::sync();
     }
-    if (warp < nb)
-      attn_block16<GQ, HD, RS>(&sa.cur[0][0], &sa.kt[0][0], &sa.vt[0][0], 16 * warp, n - 16 * warp, lane,
-                               &sa.tres[warp][0][0], HD + 2);
+    if (warp < nb) {
+      if constexpr (KV8)
+        attn_block16_q8<GQ, HD, RS>(&sa.cur[0][0], &sa.kt[0][0], &sa.vt[0][0], &sa.ksc[0][0], &sa.vsc[0][0],
+                                    16 * warp, n - 16 * warp, lane, &sa.tres[warp][0][0], HD + 2);
+      else
+        attn_block16<GQ, HD, RS>(&sa.cur[0][0], &sa.kt[0][0], &sa.vt[0][0], 16 * warp, n - 16 * warp, lane,
+                                 &sa.tres[warp][0][0], HD + 2);
+    }
     ConsumerSync::sync();
     // fold the pass into the running output. Warp h < GQ finds head h's
     // factors, lane w < nb for block w: new max, 2^(m_w - M), sum update
@@ -560,7 +699,7 @@ __device__ void step_attn_item(const StepParams& sp, const Phase& P, int g, int 
 // FUSED: the variant for short caches (every CTA computes the attention of
 // its o-projection range in that GEMV's input build; no attention phase). The
 // two variants are separate kernels: either one alone keeps its registers.
-template <int GQ, int HD, bool FUSED, bool A8>
+template <int GQ, int HD, bool FUSED, bool A8, bool KV8>
 __global__ void __launch_bounds__(kSThreads, 1) step_kernel(const StepParams sp) {
   extern __shared__ __align__(128) uint8_t smem_raw[];
   uint8_t* ring = smem_raw;
@@ -675,7 +814,7 @@ __global__ void __launch_bounds__(kSThreads, 1) step_kernel(const StepParams sp)
       if (spos >= 0 && spos < sp.cap) {
         if constexpr (FUSED) {
           if (P.type == PH_GEMV && P.in_mode == IN_ATTN) {
-            step_attn_prefetch<GQ, HD>(sp, P.layer, kr.r * (sp.Hkv / sp.R), 0, spos + 1, spos, sm.u.a);
+            step_attn_prefetch<GQ, HD, KV8>(sp, P.layer, kr.r * (sp.Hkv / sp.R), 0, spos + 1, spos, sm.u.a);
             pf = true;
           }
         } else if (P.type == PH_ATTN) {
@@ -683,7 +822,7 @@ __global__ void __launch_bounds__(kSThreads, 1) step_kernel(const StepParams sp)
           if (c < sp.Hkv * P_eff) {
             const int split = c % P_eff, len = spos + 1;
             const int t0 = (int)((int64_t)len * split / P_eff), t1 = (int)((int64_t)len * (split + 1) / P_eff);
-            step_attn_prefetch<GQ, HD>(sp, P.layer, c / P_eff, t0, t1, spos, sm.u.a);
+            step_attn_prefetch<GQ, HD, KV8>(sp, P.layer, c / P_eff, t0, t1, spos, sm.u.a);
             pf = true;
           }
         }
@@ -772,7 +911,7 @@ __global__ void __launch_bounds__(kSThreads, 1) step_kernel(const StepParams sp)
           if (!pos_ok && tid == 0 && c == 0) atomicOr(sp.status, ST_CTX_FULL);
           const int hpr = sp.Hkv / sp.R;
           for (int j = 0; j < hpr && pos_ok; ++j) {
-            step_attn_item<GQ, HD>(sp, P, kr.r * hpr + j, 0, 1, spos, sm.u.a, first, sm.fo + j * GQ * HD,
+            step_attn_item<GQ, HD, KV8>(sp, P, kr.r * hpr + j, 0, 1, spos, sm.u.a, first, sm.fo + j * GQ * HD,
                                    j == 0 && pf);
             ConsumerSync::sync();  // the next item and the input vector reuse the shared memory
           }
@@ -977,7 +1116,7 @@ __global__ void __launch_bounds__(kSThreads, 1) step_kernel(const StepParams sp)
           } else {
             const int P_eff = step_splits(pos + 1, sp.P, HD);
             for (int item = c; item < sp.Hkv * P_eff; item += N) {
-              step_attn_item<GQ, HD>(sp, P, item / P_eff, item % P_eff, P_eff, pos, sm.u.a,
+              step_attn_item<GQ, HD, KV8>(sp, P, item / P_eff, item % P_eff, P_eff, pos, sm.u.a,
                                      item % P_eff == P_eff - 1, nullptr, item == c && pf);
               ConsumerSync::sync();  // shared memory is reused by the next item
             }
@@ -1100,9 +1239,9 @@ struct KernelRef {
   const void* fn = nullptr;
   size_t smem = 0;
 };
-// The step kernel for a GQA group, head_dim, variant and activation numerics
-// (defined in step_kernels.cu, which holds the instantiations); fn is null
-// for an unsupported shape.
-KernelRef step_kernel_ref(int gq, int hd, bool fused, bool w4a8);
+// The step kernel for a GQA group, head_dim, variant, activation numerics and
+// cache format (defined in step_kernels.cu and step_kernels_kv8.cu, which
+// hold the instantiations); fn is null for an unsupported shape.
+KernelRef step_kernel_ref(int gq, int hd, bool fused, bool w4a8, bool kv8);
 
 }  // namespace llmq

@@ -60,6 +60,13 @@ typedef enum { LLM_F32 = 0, LLM_BF16 = 1, LLM_F16 = 2, LLM_Q4G64 = 3 } llm_dtype
                                  input quantized once per 32-input block (fp16 scale amax/127, codes
                                  round(x/scale) clamped to +-127) and dotted in integers; the batched
                                  kernels keep their fp16 tensor-core inputs. Not with LLM_DATAFLOW_STEP */
+#define LLM_KV_Q8 128u        /* grouped int8 K/V cache (llmopt README, "Current compiler and runtime":
+                                 grouped-Q8 attention state): each 32 values of a (position, kv head)
+                                 row stored as int8 codes with one fp16 scale fp16(amax/127), codes
+                                 round(x/scale) half away from zero clamped to +-127, decided in fp32;
+                                 attention reads the codes and scales. Persistent step only (not with
+                                 LLM_MULTI_KERNEL or LLM_DATAFLOW_STEP); llm_kv_write quantizes its bf16
+                                 rows the same way, llm_kv_read_q8 reads codes and scales */
 #define LLM_DATAFLOW_STEP 8u  /* greedy batch-1 steps on the flag-synchronised persistent kernel (phases
                                  wait on flagged words instead of grid barriers; slower than the
                                  default grid-barrier step on GB300, kept for comparison) */
@@ -75,7 +82,7 @@ typedef struct {
   int32_t max_seq;            /* KV capacity per sequence (positions) */
   int32_t max_batch;          /* number of sequences (independent caches) */
   uint32_t flags;             /* LLM_NO_GRAPH | LLM_NO_PDL | LLM_MULTI_KERNEL | LLM_DATAFLOW_STEP |
-                                 LLM_DEBUG_BATCH_HIDDEN | LLM_W4A8 | LLM_TEST_EXPIRE_WAIT */
+                                 LLM_DEBUG_BATCH_HIDDEN | LLM_W4A8 | LLM_KV_Q8 | LLM_TEST_EXPIRE_WAIT */
 } llm_config;
 
 /* One input tensor in the canonical layout, host memory, caller-owned, only
@@ -195,6 +202,11 @@ int llm_kv_write(llm_model* m, int32_t seq, int32_t layer, int32_t pos0, int32_t
 /* Read back bf16 keys/values [n][n_kv_heads][head_dim] (host or device). */
 int llm_kv_read(llm_model* m, int32_t seq, int32_t layer, int32_t pos0, int32_t n,
                 uint16_t* k_bf16, uint16_t* v_bf16);
+
+/* Read back an int8 cache (LLM_KV_Q8 models): codes k, v [n][n_kv_heads][head_dim]
+ * and fp16 scale bits ks, vs [n][n_kv_heads][head_dim / 32], host or device. */
+int llm_kv_read_q8(llm_model* m, int32_t seq, int32_t layer, int32_t pos0, int32_t n, int8_t* k, uint16_t* ks,
+                   int8_t* v, uint16_t* vs);
 
 /* Current cache length of sequence seq, or a negative llm_status. */
 int llm_kv_len(const llm_model* m, int32_t seq);

@@ -338,10 +338,22 @@ class OracleCache:
         return int(self.c.len)
 
     def fill(self, layer: int, k_bits: np.ndarray, v_bits: np.ndarray, pos0: int = 0) -> None:
-        """Write bf16 rows ``[n][n_kv_heads][hd]`` at positions pos0.. of one layer."""
+        """Write bf16 rows ``[n][n_kv_heads][hd]`` at positions pos0.. of one layer.
+
+        An int8 cache stores each (position, head) row through the grouped
+        int8 quantizer (q8_quantize) of its bf16 values.
+        """
         n = k_bits.shape[0]
         self.k[layer, :, pos0:pos0 + n, :] = np.transpose(k_bits, (1, 0, 2))
         self.v[layer, :, pos0:pos0 + n, :] = np.transpose(v_bits, (1, 0, 2))
+        if hasattr(self, "k8"):
+            for bits, codes, scales in ((k_bits, self.k8, self.ks), (v_bits, self.v8, self.vs)):
+                vals = (np.asarray(bits, np.uint16).astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+                rows = np.ascontiguousarray(np.transpose(vals, (1, 0, 2)))  # [head][position][hd]
+                c, d = q8_quantize(rows.reshape(-1))  # groups of 32 never straddle a row (hd % 32 == 0)
+                H, hd = rows.shape[0], rows.shape[2]
+                codes[layer, :, pos0:pos0 + n, :] = c.reshape(H, n, hd)
+                scales[layer, :, pos0:pos0 + n, :] = d.reshape(H, n, hd // Q8_GROUP)
 
     def set_len(self, n: int) -> None:
         self.c.len = int(n)

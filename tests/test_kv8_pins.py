@@ -103,3 +103,24 @@ def test_cached_equals_full_prefix_with_int8_kv():
     bf = om.full_prefix(prompt)
     rel = np.abs(full - bf).max(axis=1) / np.abs(bf).max(axis=1)
     assert 0 < rel.max() < 0.05
+
+
+def test_prefilled_int8_cache_holds_grid_rows_exactly():
+    # pre-filled rows whose values are codes times a power of two, with a
+    # largest code of 127 in every group: the int8 cache must hold exactly
+    # those codes at (layer, head, position), with the power of two as scale
+    cfg = synth.workload(0)
+    rng = np.random.default_rng(21)
+    n, H, hd, L = 12, cfg["n_kv_heads"], cfg["head_dim"], cfg["n_layers"]
+    c8 = oracle.OracleCache(cfg, n + 3, kv="q8")
+    to_bf16 = lambda a: (a.astype(np.float32).view(np.uint32) >> 16).astype(np.uint16)
+    for l in range(L):
+        codes = [rng.integers(-127, 128, (n, H, hd)) for _ in range(2)]
+        for c in codes:
+            c[:, :, ::32] = np.where(rng.random((n, H, hd // 32)) < 0.5, 127, -127)
+        e = (-5 - l, -2 + l)
+        c8.fill(l, to_bf16(codes[0] * 2.0 ** e[0]), to_bf16(codes[1] * 2.0 ** e[1]), pos0=2)
+        for c, stored, scales, ex in ((codes[0], c8.k8, c8.ks, e[0]), (codes[1], c8.v8, c8.vs, e[1])):
+            assert np.array_equal(stored[l, :, 2:2 + n, :], np.transpose(c, (1, 0, 2)).astype(np.int8))
+            assert np.all(scales[l, :, 2:2 + n, :] == int(np.float16(2.0 ** ex).view(np.uint16)))
+            assert not stored[l, :, :2].any() and not stored[l, :, 2 + n:].any()
