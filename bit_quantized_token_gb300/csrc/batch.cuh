@@ -483,6 +483,10 @@ struct BAttnParams {
                           // chunk), BA_APPEND for all rows, then BA_ATTEND over the cache
   size_t seq_kv_stride;   // cache elements per sequence
   size_t part_stride;     // attention partial floats per row
+  int8_t* k8;             // the grouped int8 cache instead of a.kc / a.vc (layer base): codes
+  int8_t* v8;
+  uint16_t* ks;           // and fp16 scales of each 32 values (layer base; elements / 32)
+  uint16_t* vs;
 };
 
 
@@ -499,6 +503,9 @@ struct BAttnSmem {
   float tres[NBW][GQ][HD + 2];    // per 16-position block and head: o, max, sum
   float acc[GQ][HD];
   float accm[GQ], accl[GQ], fac[GQ][NBW + 1];
+  __align__(16) uint16_t ksc[PP][HD / 32];  // int8 K/V: fp16 group scales of the staged rows
+  __align__(16) uint16_t vsc[PP][HD / 32];
+  float cursc[2][HD / 32];        // int8 K/V: this step's k, v group scales (cur then holds their codes)
   int is_last;
 };
 
@@ -507,10 +514,10 @@ struct BAttnSmem {
 // rows together; warp w < PP/16 scores all GQ heads against positions
 // 16w .. 16w+15 (attn_mma.cuh). The last split of a (sequence, kv head) to
 // finish merges the splits into the output row.
-template <int GQ, int HD>
+template <int GQ, int HD, bool KV8>
 __global__ void __launch_bounds__(kBAttnThreads) battn_mma_kernel(const BAttnParams bp) {
   using SA = BAttnSmem<GQ, HD>;
-  constexpr int NT = kBAttnThreads, PP = SA::PP, RS = SA::RS, CH = HD / 8, DPL = HD / 32;
+  constexpr int NT = kBAttnThreads, PP = SA::PP, RS = SA::RS, CH = HD / 8, DPL = HD / 32, NG = HD / 32;
   static_assert(GQ <= 8 && SA::NBW <= NT / 32, "layout");
   extern __shared__ __align__(16) uint8_t smraw[];
   SA& sa = *reinterpret_cast<SA*>(smraw);
@@ -530,8 +537,13 @@ __global__ void __launch_bounds__(kBAttnThreads) battn_mma_kernel(const BAttnPar
   if (split >= P_eff) return;
   const int t0 = (int)((int64_t)len * split / P_eff), t1 = (int)((int64_t)len * (split + 1) / P_eff);
   const int sb = bp.seq ? bp.seq[b] : b;  // this row's cache
-  uint16_t* kc = a.kc + (size_t)sb * bp.seq_kv_stride + (size_t)g * a.cap * HD;
-  uint16_t* vc = a.vc + (size_t)sb * bp.seq_kv_stride + (size_t)g * a.cap * HD;
+  const size_t cbase = (size_t)sb * bp.seq_kv_stride + (size_t)g * a.cap * HD;
+  uint16_t* kc = KV8 ? nullptr : a.kc + cbase;
+  uint16_t* vc = KV8 ? nullptr : a.vc + cbase;
+  int8_t* kc8 = KV8 ? bp.k8 + cbase : nullptr;  // int8 K/V: codes and group scales
+  int8_t* vc8 = KV8 ? bp.v8 + cbase : nullptr;
+  uint16_t* ks8 = KV8 ? bp.ks + cbase / 32 : nullptr;
+  uint16_t* vs8 = KV8 ? bp.vs + cbase / 32 : nullptr;
   const bool attend = bp.mode != BA_APPEND;
   const bool append = bp.mode == BA_APPEND || (bp.mode == BA_APPEND_ATTEND && split == P_eff - 1);
   const float* qkv = bp.qkv + (size_t)b * bp.qkv_cols;
@@ -542,27 +554,67 @@ __global__ void __launch_bounds__(kBAttnThreads) battn_mma_kernel(const BAttnPar
   constexpr int LCH = CH == 8 ? 3 : 4;
   auto stage = [&](int tp) {
     const int n = min(PP, t1 - tp), rows = ((n + 15) / 16) * 16;
+    if constexpr (KV8) {
+      // one thread per row: its codes into the first HD bytes of the row's
+      // fp16 slot, its scales beside (widened by the same thread in convert)
+      static_assert(2 * PP <= NT, "one row per thread");
+      const int kv = tid / PP, row = tid - kv * PP;
+      if (kv < 2 && row < n) {
+        const int8_t* src = (kv ? vc8 : kc8) + (size_t)(tp + row) * HD;
+        uint8_t* dst = reinterpret_cast<uint8_t*>(&(kv ? sa.vt : sa.kt)[row][0]);
 #pragma unroll
-    for (int kv = 0; kv < 2; ++kv) {
-      uint16_t(*tile)[RS] = kv ? sa.vt : sa.kt;
-      const uint16_t* src = (kv ? vc : kc) + (size_t)tp * HD;
-      for (int idx = tid; idx < rows * CH; idx += NT) {
-        const int row = idx >> LCH, ch = idx & (CH - 1);
-        if (row < n) cp_async16(&tile[row][8 * ch], src + (size_t)row * HD + 8 * ch);
-        else *reinterpret_cast<uint4*>(&tile[row][8 * ch]) = make_uint4(0u, 0u, 0u, 0u);
+        for (int c = 0; c < HD / 16; ++c) cp_async16(dst + 16 * c, src + 16 * c);
+        cp_async_small<2 * NG>(&(kv ? sa.vsc : sa.ksc)[row][0], (kv ? vs8 : ks8) + (size_t)(tp + row) * NG);
+      }
+    } else {
+#pragma unroll
+      for (int kv = 0; kv < 2; ++kv) {
+        uint16_t(*tile)[RS] = kv ? sa.vt : sa.kt;
+        const uint16_t* src = (kv ? vc : kc) + (size_t)tp * HD;
+        for (int idx = tid; idx < rows * CH; idx += NT) {
+          const int row = idx >> LCH, ch = idx & (CH - 1);
+          if (row < n) cp_async16(&tile[row][8 * ch], src + (size_t)row * HD + 8 * ch);
+          else *reinterpret_cast<uint4*>(&tile[row][8 * ch]) = make_uint4(0u, 0u, 0u, 0u);
+        }
       }
     }
   };
   auto convert = [&](int tp) {
     const int n = min(PP, t1 - tp), rows = ((n + 15) / 16) * 16;
     cp_async_wait_all();
+    if constexpr (KV8) {
+      const int kv = tid / PP, row = tid - kv * PP;
+      if (kv < 2 && row < rows) {
+        uint16_t* tr = &(kv ? sa.vt : sa.kt)[row][0];
+        uint4 c[HD / 16];
 #pragma unroll
-    for (int kv = 0; kv < 2; ++kv) {
-      uint16_t(*tile)[RS] = kv ? sa.vt : sa.kt;
-      for (int idx = tid; idx < rows * CH; idx += NT) {
-        uint4* q = reinterpret_cast<uint4*>(&tile[idx >> LCH][8 * (idx & (CH - 1))]);
-        const uint4 w = *q;
-        *q = make_uint4(bf16x2_to_f16x2(w.x), bf16x2_to_f16x2(w.y), bf16x2_to_f16x2(w.z), bf16x2_to_f16x2(w.w));
+        for (int k = 0; k < HD / 16; ++k)
+          c[k] = row < n ? reinterpret_cast<const uint4*>(tr)[k] : make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+        for (int k = HD / 16 - 1; k >= 0; --k) {  // from the end: the codes sit in the row's first bytes
+          const uint32_t w[4] = {c[k].x, c[k].y, c[k].z, c[k].w};
+          uint32_t h[8];
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            h[2 * q] = pack_f16x2((float)(int8_t)(w[q] & 0xFF), (float)(int8_t)((w[q] >> 8) & 0xFF));
+            h[2 * q + 1] = pack_f16x2((float)(int8_t)((w[q] >> 16) & 0xFF), (float)(int8_t)(w[q] >> 24));
+          }
+          reinterpret_cast<uint4*>(tr)[2 * k] = make_uint4(h[0], h[1], h[2], h[3]);
+          reinterpret_cast<uint4*>(tr)[2 * k + 1] = make_uint4(h[4], h[5], h[6], h[7]);
+        }
+        if (row >= n)
+#pragma unroll
+          for (int k = 0; k < NG; ++k) (kv ? sa.vsc : sa.ksc)[row][k] = 0;
+      }
+    } else {
+#pragma unroll
+      for (int kv = 0; kv < 2; ++kv) {
+        uint16_t(*tile)[RS] = kv ? sa.vt : sa.kt;
+        for (int idx = tid; idx < rows * CH; idx += NT) {
+          uint4* q = reinterpret_cast<uint4*>(&tile[idx >> LCH][8 * (idx & (CH - 1))]);
+          const uint4 w = *q;
+          *q = make_uint4(bf16x2_to_f16x2(w.x), bf16x2_to_f16x2(w.y), bf16x2_to_f16x2(w.z), bf16x2_to_f16x2(w.w));
+        }
       }
     }
   };
@@ -611,6 +663,10 @@ __global__ void __launch_bounds__(kBAttnThreads) battn_mma_kernel(const BAttnPar
   const float qscale = 1.4426950408889634f / sqrtf((float)HD);
   const bool owner = attend && split == P_eff - 1 && pos - t0 < PP;
   auto keep = [&](int r, int d, float x) {
+    if constexpr (KV8) {  // quantized per 32-element group below
+      sa.cur[r][d] = x;
+      return;
+    }
     const __nv_bfloat16 h = __float2bfloat16_rn(x);
     const float xr = __bfloat162float(h);
     sa.cur[r][d] = xr;
@@ -636,6 +692,32 @@ __global__ void __launch_bounds__(kBAttnThreads) battn_mma_kernel(const BAttnPar
       keep(GQ + 1, j - nrope, sa.cur[GQ + 1][j - nrope]);
     }
   }
+  if constexpr (KV8) {
+    // the grouped int8 append: warp (kv, group) quantizes 32 elements of k or
+    // v (fp16 scale fp16(amax / 127), codes round(x / scale) half away from
+    // zero, clamped to +-127, all in fp32); cur keeps the codes, cursc the scales
+    __syncthreads();
+    if (warp < 2 * NG) {
+      const int kv = warp / NG, grp = warp - kv * NG, d = 32 * grp + lane;
+      const float x = sa.cur[GQ + kv][d];
+      float amax = fabsf(x);
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+      const __half dh = __float2half_rn(amax / 127.0f);
+      const float dq = __half2float(dh);
+      const float cf = dq == 0.0f ? 0.0f : fminf(fmaxf(roundf(x / dq), -127.0f), 127.0f);
+      sa.cur[GQ + kv][d] = cf;
+      if (lane == 0) sa.cursc[kv][grp] = dq;
+      if (append) {
+        (kv ? vc8 : kc8)[(size_t)pos * HD + d] = (int8_t)(int)cf;
+        if (lane == 0) (kv ? vs8 : ks8)[(size_t)pos * NG + grp] = __half_as_ushort(dh);
+      }
+      if (owner) {
+        (kv ? sa.vt : sa.kt)[pos - t0][d] = __half_as_ushort(__float2half_rn(cf));
+        if (lane == 0) (kv ? sa.vsc : sa.ksc)[pos - t0][grp] = __half_as_ushort(dh);
+      }
+    }
+  }
   if (!attend) return;  // the rows' k, v are in the cache
   for (int i = tid; i < GQ * HD; i += NT) sa.acc[i / HD][i % HD] = 0.f;
   if (tid < GQ) {
@@ -651,16 +733,26 @@ __global__ void __launch_bounds__(kBAttnThreads) battn_mma_kernel(const BAttnPar
       stage(tp);
       convert(tp);
       __syncthreads();
-      if (pos >= tp && pos < tp + n)
+      if (pos >= tp && pos < tp + n) {
         for (int d = tid; d < HD; d += NT) {
           sa.kt[pos - tp][d] = __half_as_ushort(__float2half_rn(sa.cur[GQ][d]));
           sa.vt[pos - tp][d] = __half_as_ushort(__float2half_rn(sa.cur[GQ + 1][d]));
         }
+        if constexpr (KV8)
+          if (tid < 2 * NG)
+            (tid < NG ? sa.ksc : sa.vsc)[pos - tp][tid % NG] =
+                __half_as_ushort(__float2half_rn(sa.cursc[tid / NG][tid % NG]));
+      }
       __syncthreads();
     }
-    if (warp < nb)
-      attn_block16<GQ, HD, RS>(&sa.cur[0][0], &sa.kt[0][0], &sa.vt[0][0], 16 * warp, n - 16 * warp, lane,
-                               &sa.tres[warp][0][0], HD + 2);
+    if (warp < nb) {
+      if constexpr (KV8)
+        attn_block16_q8<GQ, HD, RS>(&sa.cur[0][0], &sa.kt[0][0], &sa.vt[0][0], &sa.ksc[0][0], &sa.vsc[0][0],
+                                    16 * warp, n - 16 * warp, lane, &sa.tres[warp][0][0], HD + 2);
+      else
+        attn_block16<GQ, HD, RS>(&sa.cur[0][0], &sa.kt[0][0], &sa.vt[0][0], 16 * warp, n - 16 * warp, lane,
+                                 &sa.tres[warp][0][0], HD + 2);
+    }
     __syncthreads();
     // fold the pass into the running output. Warp h < GQ finds head h's
     // factors, lane w < nb for block w: new max, 2^(m_w - M), sum update

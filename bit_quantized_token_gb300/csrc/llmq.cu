@@ -707,12 +707,18 @@ int ll_blocks(int n_rt, int n_cta, int R, int GR, int bs_max) {
 
 template <int GQ, int HD>
 cudaError_t launch_battn_t(const llm_model* m, const BAttnParams& b, int splits, int rows, bool pdl) {
-  return launch(battn_mma_kernel<GQ, HD>, dim3(splits, m->cfg.n_kv_heads, rows), dim3(kBAttnThreads),
-                sizeof(BAttnSmem<GQ, HD>), m->stream, pdl, b);
+  const dim3 grid(splits, m->cfg.n_kv_heads, rows);
+  if (m->kv8)
+    return launch(battn_mma_kernel<GQ, HD, true>, grid, dim3(kBAttnThreads), sizeof(BAttnSmem<GQ, HD>), m->stream,
+                  pdl, b);
+  return launch(battn_mma_kernel<GQ, HD, false>, grid, dim3(kBAttnThreads), sizeof(BAttnSmem<GQ, HD>), m->stream,
+                pdl, b);
 }
 template <int GQ, int HD>
 cudaError_t battn_smem_attr() {
-  return raise_smem_limit(battn_mma_kernel<GQ, HD>, sizeof(BAttnSmem<GQ, HD>));
+  cudaError_t e = raise_smem_limit(battn_mma_kernel<GQ, HD, false>, sizeof(BAttnSmem<GQ, HD>));
+  if (e == cudaSuccess) e = raise_smem_limit(battn_mma_kernel<GQ, HD, true>, sizeof(BAttnSmem<GQ, HD>));
+  return e;
 }
 cudaError_t battn_set_smem(int gq, int hd) {
   switch (gq * 1000 + hd) {
@@ -841,8 +847,15 @@ cudaError_t enqueue_batched(llm_model* m, const BatchedIO& io) {
     bp.a.q_norm = c.qk_norm ? m->d_norms + m->off_q_norm[l] : nullptr;
     bp.a.k_norm = c.qk_norm ? m->d_norms + m->off_k_norm[l] : nullptr;
     bp.a.eps = c.norm_eps;
-    bp.a.kc = m->d_k + (size_t)l * kv_layer;
-    bp.a.vc = m->d_v + (size_t)l * kv_layer;
+    if (m->kv8) {
+      bp.k8 = m->d_k8 + (size_t)l * kv_layer;
+      bp.v8 = m->d_v8 + (size_t)l * kv_layer;
+      bp.ks = m->d_ks + (size_t)l * kv_layer / 32;
+      bp.vs = m->d_vs + (size_t)l * kv_layer / 32;
+    } else {
+      bp.a.kc = m->d_k + (size_t)l * kv_layer;
+      bp.a.vc = m->d_v + (size_t)l * kv_layer;
+    }
     bp.a.cap = c.max_seq;
     bp.a.part = m->d_battn_part;
     bp.a.counter = m->d_battn_cnt;
@@ -1237,6 +1250,7 @@ int llm_model_create(const llm_config* cfg, const llm_tensor* tensors, int32_t n
   AL(m->d_norms, norms.size() * 4, "norms");
   const size_t kv_elems = (size_t)c.max_batch * L * c.n_kv_heads * c.max_seq * hd;
   m->kv8 = (c.flags & LLM_KV_Q8) != 0;
+  m->bkv8_ok = m->kv8;  // the batched attention reads and appends the int8 cache too
   if (m->kv8) {
     AL(m->d_k8, kv_elems, "int8 K cache");
     AL(m->d_v8, kv_elems, "int8 V cache");

@@ -63,11 +63,11 @@ def _teacher_forced(cfg, m, om, cache, toks, n_check_from=0):
     return worst
 
 
-def _appended_rows_match(cfg, m, cache, pos0, n):
+def _appended_rows_match(cfg, m, cache, pos0, n, seq=0):
     H, hd = cfg["n_kv_heads"], cfg["head_dim"]
     same = total = 0
     for l in range(cfg["n_layers"]):
-        k, ks, v, vs = m.kv_read_q8(0, l, pos0, n)
+        k, ks, v, vs = m.kv_read_q8(seq, l, pos0, n)
         for got_c, got_s, ref_c, ref_s, name in ((k, ks, cache.k8, cache.ks, "K"), (v, vs, cache.v8, cache.vs, "V")):
             rc = np.transpose(ref_c[l, :, pos0:pos0 + n], (1, 0, 2))
             rs = np.transpose(ref_s[l, :, pos0:pos0 + n], (1, 0, 2))
@@ -151,6 +151,36 @@ def test_kv8_long_context_teacher_forced(n_steps):
                     assert rel_l2(hid[l], ref_h[l]) <= HIDDEN_RL2, f"step {i} layer {l}"
             tok = oracle.argmax_f32(ref)
         _appended_rows_match(cfg, m, cache, n_pre, n_steps)
+
+
+@pytest.mark.parametrize("cfg,n_prompt", [(synth.workload(0), 70), (synth.workload(2, n_layers=2, vocab=4096), 45)],
+                         ids=["tiny-3-chunks", "qwen3-shape-2-layers"])
+def test_kv8_batched_prefill_matches_token_by_token(cfg, n_prompt):
+    # batched prompt processing into the int8 cache against the oracle's
+    # token-by-token prefill into its int8 cache: last logits and greedy
+    # token, every appended row, then greedy decoding from that cache
+    w = synth.make_weights(cfg)
+    prompt = synth.make_prompt(cfg, n=n_prompt)
+    n = 8
+    cap = n_prompt + n + 1
+    om = oracle.OracleModel(cfg, w)
+    cache = om.new_cache(cap, kv="q8")
+    ref = None
+    for t in prompt:
+        ref = om.step(cache, int(t))
+    toks = [oracle.argmax_f32(ref)]
+    with bq.Model(cfg, w, max_seq=cap, max_batch=2, flags=bq.LLM_KV_Q8) as m:
+        logits = np.empty(cfg["vocab"], np.float32)
+        am = np.zeros(1, np.int32)
+        m.prefill_batched(1, prompt, logits, am)
+        assert m.kv_len(1) == n_prompt
+        err = np.abs(logits - ref).max() / np.abs(ref).max()
+        assert err <= LOGIT_REL, f"last-token logit error {err:.3e}"
+        assert int(am[0]) == toks[0]
+        _appended_rows_match(cfg, m, cache, 0, n_prompt, seq=1)
+        for _ in range(n):
+            toks.append(oracle.argmax_f32(om.step(cache, toks[-1])))
+        assert np.array_equal(m.decode_greedy(1, int(am[0]), n), toks[1:])
 
 
 def test_kv8_refuses_the_paths_that_read_bf16():

@@ -435,7 +435,7 @@ def test_error_paths_leave_model_usable():
 
 # ---------------------------------------------------------------- batched decode
 
-def _batched_vs_oracle(cfg, lens, n_steps, seed_tokens, hidden=False):
+def _batched_vs_oracle(cfg, lens, n_steps, seed_tokens, hidden=False, kv8=False):
     """Ragged pre-filled caches, teacher-forced batched steps compared per sequence.
 
     Every step: logits at 5e-3 * max|logit|; the greedy choice equal to the
@@ -448,11 +448,11 @@ def _batched_vs_oracle(cfg, lens, n_steps, seed_tokens, hidden=False):
     om = oracle.OracleModel(cfg, w)
     cap = int(max(lens)) + n_steps + 1
     caches = []
-    flags = bq.LLM_DEBUG_BATCH_HIDDEN if hidden else 0
+    flags = (bq.LLM_DEBUG_BATCH_HIDDEN if hidden else 0) | (bq.LLM_KV_Q8 if kv8 else 0)
     near_ties = 0
     with bq.Model(cfg, w, max_seq=cap, max_batch=B, flags=flags) as m:
         for b in range(B):
-            c = om.new_cache(int(lens[b]) + n_steps + 1)
+            c = om.new_cache(int(lens[b]) + n_steps + 1, kv="q8" if kv8 else "bf16")
             for l in range(cfg["n_layers"]):
                 k, v = synth.make_prefilled_kv(cfg, l, b, int(lens[b]))
                 c.fill(l, k, v)
@@ -506,6 +506,18 @@ def test_batched_qwen_shape_ragged_two_layers():
     cfg = synth.workload(4, n_layers=2)
     lens = synth.make_kv_lengths(cfg, 32)
     _batched_vs_oracle(cfg, lens, 3, synth.make_first_tokens(cfg, 32), hidden=True)
+
+
+def test_batched_tiny_int8_kv_matches_oracle():
+    # the grouped int8 cache (LLM_KV_Q8) against the oracle's int8 caches
+    cfg = synth.workload(0)
+    _batched_vs_oracle(cfg, [3, 17, 1, 40], 6, synth.make_first_tokens(cfg, 4), hidden=True, kv8=True)
+
+
+def test_batched_workload_full_size_int8_kv():
+    cfg = synth.workload(4)
+    lens = synth.make_kv_lengths(cfg, 32)
+    _batched_vs_oracle(cfg, lens, 16, synth.make_first_tokens(cfg, 32), hidden=True, kv8=True)
 
 
 def test_batched_workload_full_size():
