@@ -43,6 +43,9 @@ def args_():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--kv", default="bf16", choices=["bf16", "q8"],
+                    help="K/V cache format: bf16, or the grouped int8 cache (LLM_KV_Q8)")
+    ap.add_argument("--w4a8", action="store_true", help="int8 activation blocks in the batch-1 GEMVs (LLM_W4A8)")
     ap.add_argument("--regions", type=int, default=5,
                     help="timed regions of K steps each (same positions); value = the median region")
     ap.add_argument("--layers", type=int, default=0,
@@ -81,18 +84,24 @@ def ncu_traffic(key):
     return t["traffic_bytes"] if t and t.get("src_sha") == src_sha(key.split()[0]) else None
 
 
-def workload_desc(cfg):
+def workload_desc(cfg, kv="bf16", w4a8=False):
     full = synth.workload(cfg["index"])["n_layers"] if "index" in cfg else cfg["n_layers"]
     layers = f"{cfg['n_layers']} layers" if cfg["n_layers"] == full else f"first {cfg['n_layers']} of {full} layers"
+    acts = "int8 activation blocks (W4A8)" if w4a8 else "fp32 activations"
+    cache = "grouped int8 KV (32-value groups, fp16 scales)" if kv == "q8" else "bf16 KV"
     return (f"{cfg['name']}: dim {cfg['dim']}, {layers}, {cfg['n_heads']}/{cfg['n_kv_heads']} heads, "
             f"head_dim {cfg['head_dim']}, ffn {cfg['ffn_dim']}, vocab {cfg['vocab']}, group-64 4-bit weights "
-            f"(fp16 scale/min), fp32 activations, bf16 KV" + (", tied bf16 LM head" if cfg["tied"] else ""))
+            f"(fp16 scale/min), {acts}, {cache}" + (", tied bf16 LM head" if cfg["tied"] else ""))
 
 
-def kv_read_bytes(cfg, positions):
+def kv_read_bytes(per_pos, positions):
     """Mean K/V bytes read per step when the steps run at the given positions."""
-    per_pos = synth.kv_bytes_per_pos(cfg)
     return float(np.mean([(p + 1) * per_pos for p in positions]))
+
+
+def model_flags(a):
+    import bit_quantized_token_gb300 as bq
+    return (bq.LLM_KV_Q8 if a.kv == "q8" else 0) | (bq.LLM_W4A8 if a.w4a8 else 0)
 
 
 class ClockSampler:
@@ -208,7 +217,7 @@ def run_batched(a, cfg, w, rank, world, local, dist):
     n_e2e = 8
     max_seq = int(lens.max()) + a.warmup + a.regions * a.steps + n_e2e + 8
     stream = torch.cuda.Stream()
-    m = bq.Model(cfg, w, max_seq=max_seq, max_batch=B, stream=stream.cuda_stream)
+    m = bq.Model(cfg, w, max_seq=max_seq, max_batch=B, stream=stream.cuda_stream, flags=model_flags(a))
     st = m.stats()
     for b in range(B):
         for l in range(cfg["n_layers"]):
@@ -217,7 +226,7 @@ def run_batched(a, cfg, w, rank, world, local, dist):
     for _ in range(a.warmup - 1):
         m.decode_step_batch(None)
     m.sync()
-    per_pos = synth.kv_bytes_per_pos(cfg)
+    per_pos = st["kv_bytes_per_pos"]  # the model's own cache format (bf16 or grouped int8)
     peak, peak_kind = peaks()
     clocks = ClockSampler(local)
     time.sleep(0.5)
@@ -256,8 +265,8 @@ def run_batched(a, cfg, w, rank, world, local, dist):
     line = {
         "metric": METRIC, "value": tok_s, "unit": "tok/s", "n_gpus": world, "steps": a.steps, "warmup": a.warmup,
         "ms_per_step": ms / a.steps, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": "f32", "data": "synthetic",
-        "config": {"workload": workload_desc(cfg), "batch": B, "kv_lengths": [int(lens.min()), int(lens.max())],
+        "dtype": "i8" if a.w4a8 else "f32", "data": "synthetic",
+        "config": {"workload": workload_desc(cfg, a.kv, a.w4a8), "batch": B, "kv_lengths": [int(lens.min()), int(lens.max())],
                    "kv_lengths_mean": float(lens.mean()), "l2": "inputs larger than L2: ~5.4 GB streamed per step",
                    "timed": "llm_decode_step_batch(NULL tokens): CUDA-graph replays, greedy tokens fed back on the device"},
         "hbm": {"bytes_per_step": bytes_step, "weight_bytes": st["weight_stream_bytes"], "kv_bytes_per_step": kv_step,
@@ -318,7 +327,7 @@ def main():
     n_pre = max(0, cfg.get("prefill_kv", 0))
     max_seq = max(n_pre + len(prompt) + 2 * (a.warmup + a.steps) + n_e2e + 8, n_pf + 8)
     stream = torch.cuda.Stream()  # the library launches on it; events are recorded on it
-    m = bq.Model(cfg, w, max_seq=max_seq, stream=stream.cuda_stream)
+    m = bq.Model(cfg, w, max_seq=max_seq, stream=stream.cuda_stream, flags=model_flags(a))
     st = m.stats()
     kv_pre = [synth.make_prefilled_kv(cfg, l, 0, n_pre) for l in range(cfg["n_layers"])] if n_pre else None
 
@@ -360,18 +369,20 @@ def main():
     positions = list(range(pos0, pos0 + a.steps))
     tok = int(toks_dev[-1].item())
     tok_s = job_rate(world, a.steps, ms)
-    bytes_tok = st["weight_stream_bytes"] + kv_read_bytes(cfg, positions)
+    bytes_tok = st["weight_stream_bytes"] + kv_read_bytes(st["kv_bytes_per_pos"], positions)
     peak, peak_kind = peaks()
 
     # dominant kernel: every 4-bit / bf16 GEMV of a step, back to back (582 MB > L2)
     g_ms, g_bytes = m.time_kernel(0, "all_gemv", -1, n_kt)
     g_gbs = g_bytes / (g_ms / 1000.0) / 1e9
     # kernel shares of one eagerly launched step (serialised, like an ncu launch list)
-    prof = m.profile_step(0, tok)
-    tot = sum(r["ms"] for r in prof)
-    share = {}
-    for r in prof:
-        share[r["kind"]] = share.get(r["kind"], 0.0) + r["ms"] / tot
+    share = None
+    if a.kv == "bf16":  # the eager per-kernel profile runs the bf16-cache kernels
+        prof = m.profile_step(0, tok)
+        tot = sum(r["ms"] for r in prof)
+        share = {}
+        for r in prof:
+            share[r["kind"]] = share.get(r["kind"], 0.0) + r["ms"] / tot
     # end to end through the public call: host token in, host argmax out,
     # every step; the inter-token latency of that loop, on the host clock and
     # between CUDA events recorded on the model's stream after each call
@@ -452,8 +463,9 @@ def main():
     line = {
         "metric": METRIC, "value": tok_s, "unit": "tok/s", "n_gpus": world, "steps": a.steps, "warmup": a.warmup,
         "ms_per_step": ms / a.steps, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": "f32", "data": "synthetic",
-        "config": {"workload": workload_desc(cfg), "batch": 1, "prompt_len": len(prompt), "prefilled_positions": n_pre,
+        "dtype": "i8" if a.w4a8 else "f32", "data": "synthetic",
+        "config": {"workload": workload_desc(cfg, a.kv, a.w4a8), "batch": 1, "prompt_len": len(prompt),
+                   "prefilled_positions": n_pre,
                    "positions": [positions[0], positions[-1]],
                    "l2": "inputs larger than L2: 582 MB of weights streamed per step vs 129 MB L2"
                    if a.workload in (1, 3) else "weights streamed per step exceed L2"
