@@ -555,17 +555,18 @@ __global__ void __launch_bounds__(kBAttnThreads) battn_mma_kernel(const BAttnPar
   auto stage = [&](int tp) {
     const int n = min(PP, t1 - tp), rows = ((n + 15) / 16) * 16;
     if constexpr (KV8) {
-      // one thread per row: its codes into the first HD bytes of the row's
-      // fp16 slot, its scales beside (widened by the same thread in convert)
-      static_assert(2 * PP <= NT, "one row per thread");
-      const int kv = tid / PP, row = tid - kv * PP;
-      if (kv < 2 && row < n) {
-        const int8_t* src = (kv ? vc8 : kc8) + (size_t)(tp + row) * HD;
-        uint8_t* dst = reinterpret_cast<uint8_t*>(&(kv ? sa.vt : sa.kt)[row][0]);
-#pragma unroll
-        for (int c = 0; c < HD / 16; ++c) cp_async16(dst + 16 * c, src + 16 * c);
-        cp_async_small<2 * NG>(&(kv ? sa.vsc : sa.ksc)[row][0], (kv ? vs8 : ks8) + (size_t)(tp + row) * NG);
+      // 16-byte chunks of codes into the first HD bytes of each row's fp16
+      // slot (widened in convert), one row's scales per thread
+      static_assert(2 * PP <= NT, "one scale row per thread");
+      constexpr int C8 = HD / 16, L8 = C8 == 4 ? 2 : 3;
+      for (int idx = tid; idx < 2 * n * C8; idx += NT) {
+        const int kv = idx >= n * C8, r = idx - kv * n * C8, row = r >> L8, ch = r & (C8 - 1);
+        cp_async16(reinterpret_cast<uint8_t*>(&(kv ? sa.vt : sa.kt)[row][0]) + 16 * ch,
+                   (kv ? vc8 : kc8) + (size_t)(tp + row) * HD + 16 * ch);
       }
+      const int kv = tid / PP, row = tid - kv * PP;
+      if (kv < 2 && row < n)
+        cp_async_small<2 * NG>(&(kv ? sa.vsc : sa.ksc)[row][0], (kv ? vs8 : ks8) + (size_t)(tp + row) * NG);
     } else {
 #pragma unroll
       for (int kv = 0; kv < 2; ++kv) {
@@ -583,29 +584,42 @@ __global__ void __launch_bounds__(kBAttnThreads) battn_mma_kernel(const BAttnPar
     const int n = min(PP, t1 - tp), rows = ((n + 15) / 16) * 16;
     cp_async_wait_all();
     if constexpr (KV8) {
-      const int kv = tid / PP, row = tid - kv * PP;
-      if (kv < 2 && row < rows) {
-        uint16_t* tr = &(kv ? sa.vt : sa.kt)[row][0];
-        uint4 c[HD / 16];
+      // every thread reads its chunks of codes (any row: the copies of all
+      // threads are complete after the barrier), then, after a second
+      // barrier, writes them back widened to fp16 over the same rows
+      constexpr int C8 = HD / 16, L8 = C8 == 4 ? 2 : 3, MAXC = (2 * PP * C8 + NT - 1) / NT;
+      __syncthreads();
+      uint4 c[MAXC];
 #pragma unroll
-        for (int k = 0; k < HD / 16; ++k)
-          c[k] = row < n ? reinterpret_cast<const uint4*>(tr)[k] : make_uint4(0u, 0u, 0u, 0u);
+      for (int j = 0; j < MAXC; ++j) {
+        const int idx = tid + j * NT, kv = idx >= rows * C8, r = idx - kv * rows * C8, row = r >> L8,
+                  ch = r & (C8 - 1);
+        c[j] = (idx < 2 * rows * C8 && row < n)
+                   ? reinterpret_cast<const uint4*>(&(kv ? sa.vt : sa.kt)[row][0])[ch]
+                   : make_uint4(0u, 0u, 0u, 0u);
+      }
+      __syncthreads();
 #pragma unroll
-        for (int k = HD / 16 - 1; k >= 0; --k) {  // from the end: the codes sit in the row's first bytes
-          const uint32_t w[4] = {c[k].x, c[k].y, c[k].z, c[k].w};
+      for (int j = 0; j < MAXC; ++j) {
+        const int idx = tid + j * NT, kv = idx >= rows * C8, r = idx - kv * rows * C8, row = r >> L8,
+                  ch = r & (C8 - 1);
+        if (idx < 2 * rows * C8) {
+          const uint32_t w[4] = {c[j].x, c[j].y, c[j].z, c[j].w};
           uint32_t h[8];
 #pragma unroll
           for (int q = 0; q < 4; ++q) {
             h[2 * q] = pack_f16x2((float)(int8_t)(w[q] & 0xFF), (float)(int8_t)((w[q] >> 8) & 0xFF));
             h[2 * q + 1] = pack_f16x2((float)(int8_t)((w[q] >> 16) & 0xFF), (float)(int8_t)(w[q] >> 24));
           }
-          reinterpret_cast<uint4*>(tr)[2 * k] = make_uint4(h[0], h[1], h[2], h[3]);
-          reinterpret_cast<uint4*>(tr)[2 * k + 1] = make_uint4(h[4], h[5], h[6], h[7]);
+          uint4* tr = reinterpret_cast<uint4*>(&(kv ? sa.vt : sa.kt)[row][0]);
+          tr[2 * ch] = make_uint4(h[0], h[1], h[2], h[3]);
+          tr[2 * ch + 1] = make_uint4(h[4], h[5], h[6], h[7]);
         }
-        if (row >= n)
-#pragma unroll
-          for (int k = 0; k < NG; ++k) (kv ? sa.vsc : sa.ksc)[row][k] = 0;
       }
+      const int kv = tid / PP, row = tid - kv * PP;
+      if (kv < 2 && row >= n && row < rows)
+#pragma unroll
+        for (int k = 0; k < NG; ++k) (kv ? sa.vsc : sa.ksc)[row][k] = 0;
     } else {
 #pragma unroll
       for (int kv = 0; kv < 2; ++kv) {
