@@ -147,6 +147,79 @@ __device__ __forceinline__ void attn_block16(const float* q, const uint16_t* kt,
   }
 }
 
+// attn_block16 on the CUDA cores (fp32 FMAs on the staged fp16 rows), the
+// same inputs and outputs: the comparison the tensor-core block is measured
+// against (step kernels built with LLMQ_ATTN_CUDA_CORES=1). Lane (position
+// p = lane % 16, head parity lane / 16) scores its position against heads
+// lane/16, lane/16 + 2, ...; the softmax of a head reduces over 16 lanes;
+// then lane d accumulates output dims d, d + 32, ... of every head, taking
+// each position's probability by a shuffle.
+template <int GQ, int HD, int RS>
+__device__ __forceinline__ void attn_block16_cc(const float* q, const uint16_t* kt, const uint16_t* vt, int row0,
+                                                int nvalid, int lane, float* out, int OS) {
+  constexpr int NH = (GQ + 1) / 2;  // heads per lane
+  const int p = lane & 15, hp = lane >> 4;
+  float sc[NH];
+  const __half2* kr = reinterpret_cast<const __half2*>(kt + (size_t)(row0 + p) * RS);
+#pragma unroll
+  for (int j = 0; j < NH; ++j) sc[j] = 0.f;
+#pragma unroll 8
+  for (int d2 = 0; d2 < HD / 2; ++d2) {
+    const float2 k = __half22float2(kr[d2]);
+#pragma unroll
+    for (int j = 0; j < NH; ++j) {
+      const int h = hp + 2 * j;
+      if (h < GQ) {
+        const float2 qq = *reinterpret_cast<const float2*>(q + h * HD + 2 * d2);
+        sc[j] = fmaf(qq.x, k.x, fmaf(qq.y, k.y, sc[j]));
+      }
+    }
+  }
+  float pr[NH], mx[NH], sm[NH];
+#pragma unroll
+  for (int j = 0; j < NH; ++j) {
+    const float v = p < nvalid ? sc[j] : -INFINITY;
+    float m = v;
+#pragma unroll
+    for (int o = 8; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+    pr[j] = exp2f(v - m);
+    float l = pr[j];
+#pragma unroll
+    for (int o = 8; o > 0; o >>= 1) l += __shfl_xor_sync(0xffffffffu, l, o);
+    mx[j] = m;
+    sm[j] = l;
+  }
+  float acc[GQ][HD / 32];
+#pragma unroll
+  for (int h = 0; h < GQ; ++h)
+#pragma unroll
+    for (int e = 0; e < HD / 32; ++e) acc[h][e] = 0.f;
+#pragma unroll 4
+  for (int pp = 0; pp < 16; ++pp) {
+    float v[HD / 32];
+#pragma unroll
+    for (int e = 0; e < HD / 32; ++e)
+      v[e] = __half2float(__ushort_as_half(vt[(size_t)(row0 + pp) * RS + lane + 32 * e]));
+#pragma unroll
+    for (int h = 0; h < GQ; ++h) {
+      const float w = __shfl_sync(0xffffffffu, pr[h / 2], pp + 16 * (h & 1));
+#pragma unroll
+      for (int e = 0; e < HD / 32; ++e) acc[h][e] = fmaf(w, v[e], acc[h][e]);
+    }
+  }
+#pragma unroll
+  for (int h = 0; h < GQ; ++h)
+#pragma unroll
+    for (int e = 0; e < HD / 32; ++e) out[h * OS + lane + 32 * e] = acc[h][e];
+  if (p == 0)
+#pragma unroll
+    for (int j = 0; j < NH; ++j)
+      if (hp + 2 * j < GQ) {
+        out[(hp + 2 * j) * OS + HD] = mx[j];
+        out[(hp + 2 * j) * OS + HD + 1] = sm[j];
+      }
+}
+
 // attn_block16 over int8 K/V (the grouped int8 cache): kt/vt hold the codes
 // as fp16 (exact), ks/vs the staged rows' fp16 group scales [row][HD / 32].
 // A key group's scale multiplies that group's partial scores per position

@@ -38,6 +38,10 @@
 #include "kernels.cuh"
 #include "attn_mma.cuh"
 
+#ifndef LLMQ_ATTN_CUDA_CORES
+#define LLMQ_ATTN_CUDA_CORES 0  // 1: the step's attention blocks on the CUDA cores (comparison build)
+#endif
+
 namespace llmq {
 
 // 15 consumer warps + 1 producer warp = 4 warps per scheduler, 128 registers each
@@ -614,8 +618,13 @@ __device__ void step_attn_item(const StepParams& sp, const Phase& P, int g, int 
         attn_block16_q8<GQ, HD, RS>(&sa.cur[0][0], &sa.kt[0][0], &sa.vt[0][0], &sa.ksc[0][0], &sa.vsc[0][0],
                                     16 * warp, n - 16 * warp, lane, &sa.tres[warp][0][0], HD + 2);
       else
+#if LLMQ_ATTN_CUDA_CORES
+        attn_block16_cc<GQ, HD, RS>(&sa.cur[0][0], &sa.kt[0][0], &sa.vt[0][0], 16 * warp, n - 16 * warp, lane,
+                                    &sa.tres[warp][0][0], HD + 2);
+#else
         attn_block16<GQ, HD, RS>(&sa.cur[0][0], &sa.kt[0][0], &sa.vt[0][0], 16 * warp, n - 16 * warp, lane,
                                  &sa.tres[warp][0][0], HD + 2);
+#endif
     }
     ConsumerSync::sync();
     // fold the pass into the running output. Warp h < GQ finds head h's
