@@ -123,17 +123,24 @@ typedef struct {
  * everything to the device, size all buffers and capture the step graph.
  * cuda_stream: cudaStream_t to run on, or NULL for a stream the model owns.
  * Errors: INVALID_ARG, UNSUPPORTED (head_dim not 64/128, cols % 64, heads not
- * divisible, missing tensor...), NOT_FOUND, OOM, CUDA. On error *out = NULL. */
+ * divisible, missing tensor...), NOT_FOUND, OOM, CUDA. On error *out = NULL.
+ * Source: aot-llm README, "Library output" and its C example (aot_open: the model opened once, weights
+ * ready); pytensor-ml issue #53, "Acceptance rules that apply to every PR" (fail at load with the
+ * missing capability named). */
 int llm_model_create(const llm_config* cfg, const llm_tensor* tensors, int32_t n_tensors,
                      void* cuda_stream, llm_model** out);
 
-/* Free every device allocation of the model. NULL is accepted. */
+/* Free every device allocation of the model. NULL is accepted.
+ * Source: no page counterpart: the model owns its device memory (pytensor-ml issue #53, "Already
+ * here": immutable model, mutable context). */
 void llm_model_destroy(llm_model* m);
 
 /* Append n tokens (host array) to sequence seq at positions len..len+n-1 and
  * return the last position's fp32 logits [vocab] and greedy token. Runs n
  * decode steps. logits_out / argmax_out: host or device, may be NULL.
- * Errors: INVALID_ARG, CTX_FULL (len + n > max_seq), NAN, CUDA, TIMEOUT. */
+ * Errors: INVALID_ARG, CTX_FULL (len + n > max_seq), NAN, CUDA, TIMEOUT.
+ * Source: aot-llm README C example (aot_eval of n prompt tokens, then aot_logits: n_vocab floats); the
+ * static pipeline emitted for every model (aot-llm README) run once per token. */
 int llm_prefill(llm_model* m, int32_t seq, const int32_t* tokens, int32_t n,
                 float* logits_out, int32_t* argmax_out);
 
@@ -151,13 +158,17 @@ int llm_prefill_batched(llm_model* m, int32_t seq, const int32_t* tokens, int32_
 
 /* One decode step of sequence seq for `token` at position len; len += 1.
  * logits_out [vocab] fp32 and argmax_out (lowest index wins ties): host or
- * device, may be NULL. Errors as llm_prefill. */
+ * device, may be NULL. Errors as llm_prefill.
+ * Source: aot-llm README, "The static pipeline emitted for every model" and its C example (one token
+ * through aot_eval, aot_logits); pytensor-ml issue #53 (one-token append to the cache). */
 int llm_decode_step(llm_model* m, int32_t seq, int32_t token, float* logits_out,
                     int32_t* argmax_out);
 
 /* n_steps greedy steps starting from first_token; each step's argmax feeds the
  * next step on the device (no host round trip per step). tokens_out
- * [n_steps] (host or device) receives the token chosen at each step. */
+ * [n_steps] (host or device) receives the token chosen at each step.
+ * Source: zynfer PR #100, stage M3 (one command buffer per forward, 2 waits per token instead of 476:
+ * the step runs on the device without a host round trip). */
 int llm_decode_greedy(llm_model* m, int32_t seq, int32_t first_token, int32_t n_steps,
                       int32_t* tokens_out);
 
@@ -185,54 +196,70 @@ int llm_set_sampling(llm_model* m, float temperature, int32_t top_k, float top_p
  * device), or NULL to continue every sequence from its previous greedy token
  * on the device; logits_out [n_seq][vocab] and argmax_out [n_seq]: host or
  * device, may be NULL. Synchronous when tokens or an output are host memory.
- * Errors: UNSUPPORTED (max_batch < 2), INVALID_ARG, CTX_FULL, NAN, CUDA. */
+ * Errors: UNSUPPORTED (max_batch < 2), INVALID_ARG, CTX_FULL, NAN, CUDA.
+ * Source: no page decodes several sequences at once; this applies the batched prompt path of the
+ * aot-llm README ("Batched prompt processing": each weight row read once for a chunk of tokens) to one
+ * token of each sequence. */
 int llm_decode_step_batch(llm_model* m, const int32_t* tokens, int32_t n_seq,
                           float* logits_out, int32_t* argmax_out);
 
-/* Forget the cache of sequence seq (-1: all); its length becomes 0. */
+/* Forget the cache of sequence seq (-1: all); its length becomes 0.
+ * Source: aot-llm README C example (aot_ctx_reset). */
 int llm_kv_reset(llm_model* m, int32_t seq);
 
 /* Copy bf16 keys/values [n][n_kv_heads][head_dim] (host or device) into
  * positions pos0..pos0+n-1 of one layer of sequence seq; keys are stored as
  * given (already rotated). The sequence length becomes max(len, pos0 + n).
- * Errors: INVALID_ARG, CTX_FULL. */
+ * Errors: INVALID_ARG, CTX_FULL.
+ * Source: aot-llm README (aot_ctx_save / aot_ctx_load move a conversation's cache between processes);
+ * zynfer PR #100, stage M4 (bf16 KV cache appended from f32). */
 int llm_kv_write(llm_model* m, int32_t seq, int32_t layer, int32_t pos0, int32_t n,
                  const uint16_t* k_bf16, const uint16_t* v_bf16);
 
-/* Read back bf16 keys/values [n][n_kv_heads][head_dim] (host or device). */
+/* Read back bf16 keys/values [n][n_kv_heads][head_dim] (host or device).
+ * Source: as llm_kv_write. */
 int llm_kv_read(llm_model* m, int32_t seq, int32_t layer, int32_t pos0, int32_t n,
                 uint16_t* k_bf16, uint16_t* v_bf16);
 
 /* Read back an int8 cache (LLM_KV_Q8 models): codes k, v [n][n_kv_heads][head_dim]
- * and fp16 scale bits ks, vs [n][n_kv_heads][head_dim / 32], host or device. */
+ * and fp16 scale bits ks, vs [n][n_kv_heads][head_dim / 32], host or device.
+ * Source: llmopt README, "Current compiler and runtime" (grouped-Q8 attention state). */
 int llm_kv_read_q8(llm_model* m, int32_t seq, int32_t layer, int32_t pos0, int32_t n, int8_t* k, uint16_t* ks,
                    int8_t* v, uint16_t* vs);
 
-/* Current cache length of sequence seq, or a negative llm_status. */
+/* Current cache length of sequence seq, or a negative llm_status.
+ * Source: pytensor-ml issue #53, "Already here" (the cache and its one-token append). */
 int llm_kv_len(const llm_model* m, int32_t seq);
 
 /* Residual stream after the embedding and after every layer of the last
- * batch-1 step: out [(n_layers+1)][dim] fp32, host or device. */
+ * batch-1 step: out [(n_layers+1)][dim] fp32, host or device.
+ * Source: pytensor-ml issue #53, "Acceptance rules that apply to every PR" (an independent oracle, the
+ * cached output checked at every step). */
 int llm_debug_hidden(llm_model* m, float* out);
 
 /* Residual stream of every sequence after the embedding and after every layer
  * of the last llm_decode_step_batch: out [(n_layers+1)][max_batch][dim] fp32,
  * host or device. Needs a model created with LLM_DEBUG_BATCH_HIDDEN
- * (else LLM_ERR_UNSUPPORTED). */
+ * (else LLM_ERR_UNSUPPORTED).
+ * Source: as llm_debug_hidden. */
 int llm_debug_hidden_batch(llm_model* m, float* out);
 
 /* Undo the repack of one 4-bit tensor: write its canonical codes [rows][cols/2],
- * scales and mins [rows][cols/64] (host) from the device copy. */
+ * scales and mins [rows][cols/64] (host) from the device copy.
+ * Source: aot-llm README, testing section (every dot product and weight type checked against a scalar
+ * reference). */
 int llm_debug_unpack(llm_model* m, const char* name, uint8_t* codes, uint16_t* scales,
                      uint16_t* mins);
 
 /* Test hook: the nth device allocation (counted from 1) made by the models
  * created after this call fails as if cudaMalloc had run out of memory, so
  * llm_model_create returns LLM_ERR_OOM naming the buffer and frees what it
- * had allocated. nth <= 0 disarms it. Process-wide; returns LLM_OK. */
+ * had allocated. nth <= 0 disarms it. Process-wide; returns LLM_OK.
+ * Source: zynfer PR #100, stage M6 (allocation behaviour tested with a failing allocator). */
 int llm_debug_fail_alloc(int32_t nth);
 
-/* Sizes and counts of the model (host struct). */
+/* Sizes and counts of the model (host struct).
+ * Source: zynfer PR #100, stages M2-M4 (bytes per token for the roofline estimate). */
 int llm_model_stats(const llm_model* m, llm_stats* out);
 
 /* One launch of a decode step, as timed by llm_profile_step. */
@@ -247,7 +274,8 @@ typedef struct {
  * without programmatic dependent launch, with a CUDA event pair around every
  * kernel. Writes up to max_out records (launch order) and returns the number
  * of launches, or a negative llm_status. Meant for measurement, not the token
- * loop (it creates and destroys events). */
+ * loop (it creates and destroys events).
+ * Source: zynfer PR #100, stage M2 (per-family timing and a roofline JSON). */
 int llm_profile_step(llm_model* m, int32_t seq, int32_t token, llm_kernel_time* out, int32_t max_out);
 
 /* Time back-to-back launches of the batch-1 step's kernels of sequence seq
@@ -259,7 +287,8 @@ int llm_profile_step(llm_model* m, int32_t seq, int32_t token, llm_kernel_time* 
  * step order. The list is launched n times. Attention launches re-append the
  * last position with the values already there. Writes the mean milliseconds
  * per launch and the mean algorithmic bytes per launch. Needs at least one
- * completed step of seq. */
+ * completed step of seq.
+ * Source: as llm_profile_step. */
 int llm_time_kernel(llm_model* m, int32_t seq, int32_t which, int32_t layer, int32_t n, float* ms,
                     int64_t* bytes);
 
@@ -276,22 +305,27 @@ int llm_time_kernel(llm_model* m, int32_t seq, int32_t which, int32_t layer, int
  * layer (q|k|v, o with the attention in its build, gate|up, down) and the LM
  * head. Returns the number of records (n_steps * phases * n_sm) or a negative
  * llm_status (UNSUPPORTED when the step kernel does not cover these
- * positions). len += n_steps. For measurement, not the token loop. */
+ * positions). len += n_steps. For measurement, not the token loop.
+ * Source: as llm_profile_step. */
 int llm_phase_times(llm_model* m, int32_t seq, int32_t first_token, int32_t n_steps, uint64_t* out,
                     int64_t max_out);
 
-/* Wait for all queued work of the model and report device-side errors. */
+/* Wait for all queued work of the model and report device-side errors.
+ * Source: pytensor-ml issue #53, "Acceptance rules that apply to every PR" (errors reported, not
+ * swallowed). */
 int llm_sync(llm_model* m);
 
 /* Last error text of the model (m may be NULL: the last create error of this
- * thread). Never NULL; owned by the library. */
+ * thread). Never NULL; owned by the library.
+ * Source: as llm_sync. */
 const char* llm_last_error(const llm_model* m);
 
 /* Kernel-level check: y = W x through the same repack and dequant-GEMV kernel
  * the decode step uses (plain store epilogue). w: one LLM_Q4G64 or LLM_BF16
  * tensor (host, cols a multiple of 64 up to 8192); x [cols], y [rows] fp32
  * host arrays. Allocates and frees its
- * own device memory; not for the token loop. */
+ * own device memory; not for the token loop.
+ * Source: aot-llm README, testing section (every matrix product against a float reference). */
 int llm_op_matvec(const llm_tensor* w, const float* x, float* y);
 
 /* llm_op_matvec in the W4A8 numerics of LLM_W4A8 (Q4G64 tensors only): x is
