@@ -195,6 +195,12 @@ __device__ __forceinline__ float4 slot_sum(float4 a, int lgS) {
 }
 __device__ __forceinline__ int log2_slots(int S) { return S >= 4 ? 2 : S >= 2 ? 1 : 0; }
 
+// A wait's limit in SM cycles: the time limit at 2.1 cycles per ns (GB300's
+// top clock; at lower clocks the limit only lasts longer).
+__device__ __forceinline__ long long wait_cycles(const StepParams& sp) {
+  return (long long)(sp.wait_ns * 21ull / 10ull);
+}
+
 // Consumer-side grid barrier: wait until `target` arrivals (bounded). Any
 // timeout sets the shared abort flag, which ends every other wait at once.
 __device__ inline bool grid_wait(const StepParams& sp, int target, int* s_flag) {
@@ -202,18 +208,18 @@ __device__ inline bool grid_wait(const StepParams& sp, int target, int* s_flag) 
   if (threadIdx.x == 0) {
     int ok = 1;
     if (ld_acquire(sp.sync) < target) {
-      const unsigned long long t0 = globaltimer();
-      unsigned ns = 16;
-      while (ld_acquire(sp.sync) < target) {
+      // polled without pauses (a pause only delays seeing the last arrival);
+      // the abort word and the clock are read every 16th poll
+      const long long c0 = clock64();
+      for (unsigned it = 1; ld_acquire(sp.sync) < target; ++it) {
+        if (it & 15) continue;
         if (*(volatile int*)(sp.sync + 1)) { ok = 0; break; }
-        if (globaltimer() - t0 > sp.wait_ns) {
+        if (clock64() - c0 > wait_cycles(sp)) {
           atomicOr(sp.status, ST_TIMEOUT);
           atomicExch(sp.sync + 1, 1);
           ok = 0;
           break;
         }
-        __nanosleep(ns);
-        ns = ns < 64 ? 2 * ns : 64;
       }
     }
     *s_flag = ok;
@@ -233,17 +239,15 @@ __device__ __forceinline__ void grid_arrive(const StepParams& sp) {
 // Bounded mbarrier wait that also gives up when another CTA aborted the step.
 __device__ __forceinline__ bool ring_wait(uint64_t* bar, uint32_t parity, const StepParams& sp) {
   if (mbar_try_wait(bar, parity)) return true;
-  const unsigned long long t0 = globaltimer();
-  unsigned ns = 32;
-  while (!mbar_try_wait(bar, parity)) {
+  const long long c0 = clock64();
+  for (unsigned it = 1; !mbar_try_wait(bar, parity); ++it) {
+    if (it & 63) continue;  // the abort word and the clock every 64th try
     if (*(volatile int*)(sp.sync + 1)) return false;
-    if (globaltimer() - t0 > sp.wait_ns) {
+    if (clock64() - c0 > wait_cycles(sp)) {
       atomicOr(sp.status, ST_TIMEOUT);
       atomicExch(sp.sync + 1, 1);
       return false;
     }
-    __nanosleep(ns);
-    ns = ns < 256 ? 2 * ns : 256;
   }
   return true;
 }
