@@ -46,6 +46,9 @@ def args_():
     ap.add_argument("--kv", default="bf16", choices=["bf16", "q8"],
                     help="K/V cache format: bf16, or the grouped int8 cache (LLM_KV_Q8)")
     ap.add_argument("--w4a8", action="store_true", help="int8 activation blocks in the batch-1 GEMVs (LLM_W4A8)")
+    ap.add_argument("--phases", action="store_true",
+                    help="per-phase breakdown of one grid-barrier step (builds a stamps variant of the library); "
+                         "prints a table, not a bench line")
     ap.add_argument("--regions", type=int, default=5,
                     help="timed regions of K steps each (same positions); value = the median region")
     ap.add_argument("--layers", type=int, default=0,
@@ -294,6 +297,56 @@ def run_batched(a, cfg, w, rank, world, local, dist):
         dist.destroy_process_group()
 
 
+def run_phases(a, cfg, w, prompt):
+    """Where one batch-1 step's time goes, phase by phase (clock stamps of the grid-barrier step)."""
+    import torch
+
+    import bit_quantized_token_gb300 as bq
+
+    lib = os.path.join(os.path.dirname(bq.LIB_PATH), "libllmq_phase_stamps.so")
+    bq.build(out=lib, defines=["LLMQ_PHASE_STAMPS=1", "LLMQ_UNIT_STAMPS=1"])
+    bq.LIB_PATH = lib
+    torch.cuda.set_device(0)
+    with bq.Model(cfg, w, max_seq=len(prompt) + 32, flags=model_flags(a)) as m:
+        am = np.zeros(1, np.int32)
+        m.prefill(0, prompt, None, am)
+        g = m.decode_greedy(0, int(am[0]), 8)
+        t = m.phase_times(0, int(g[-1]), 1).astype(np.float64)[0]  # [phase][cta][16]
+    gt0, c0, gt1, c1 = t[0, :, 12], t[0, :, 13], t[0, :, 14], t[0, :, 15]
+    rate = (gt1 - gt0) / (c1 - c0)  # ns per cycle, per SM
+    T = lambda k: gt0[None, :] + (t[:, :, k] - c0[None, :]) * rate[None, :]
+    bar, blt, und, arr = T(1), T(2), T(3), T(4)
+    ghz = 1.0 / rate.mean()
+    rows, prev = [], None
+    for ph in range(t.shape[0]):
+        if not (t[ph, :, 4] > 0).all():
+            continue  # a phase the fused variant skips
+        units = (t[ph, :, 3] > 0).all()
+        r = {"phase": ph, "units": bool(units)}
+        if prev is not None:
+            last = arr[prev].max()
+            r["barrier_after_last_arrival_us"] = float(np.median(bar[ph]) - last) / 1000
+            r["span_us"] = float(arr[ph].max() - last) / 1000
+        if units:
+            r["build_us"] = float(np.median(blt[ph] - bar[ph])) / 1000
+            r["units_us"] = float(np.median(und[ph] - blt[ph])) / 1000
+            r["busiest_warp_wait_us"] = float(np.median(t[ph, :, 5])) / ghz / 1000
+            r["busiest_warp_dot_us"] = float(np.median(t[ph, :, 6])) / ghz / 1000
+        r["arrive_us"] = float(np.median(arr[ph] - (und[ph] if units else bar[ph]))) / 1000
+        r["arrival_spread_us"] = float(arr[ph].max() - arr[ph].min()) / 1000
+        rows.append(r)
+        prev = ph
+    print(f"{cfg['name']}: {len(rows)} phases, step {(gt1.max() - gt0.min()) / 1000:.1f} us (stamps build)")
+    keys = ["barrier_after_last_arrival_us", "build_us", "units_us", "busiest_warp_wait_us", "busiest_warp_dot_us",
+            "arrive_us", "arrival_spread_us", "span_us"]
+    per = 4 if len(rows) % 4 == 1 else 5  # phases per layer (+ the LM head / logits tail)
+    print("phase-in-layer | " + " | ".join(k[:-3] for k in keys))
+    for j in range(per):
+        sel = [r for i, r in enumerate(rows[:-(len(rows) % per) or None]) if i % per == j]
+        vals = [np.mean([r[k] for r in sel if k in r]) if any(k in r for r in sel) else float("nan") for k in keys]
+        print(f"{j} (n={len(sel)}) | " + " | ".join(f"{v:.2f}" for v in vals))
+
+
 def main():
     a = args_()
     rank = int(os.environ.get("RANK", "0"))
@@ -306,6 +359,9 @@ def main():
     cfg = synth.workload(a.workload, **({"n_layers": a.layers} if a.layers else {}))
     w = synth.make_weights(cfg)
     prompt = synth.make_prompt(cfg)
+    if a.phases:
+        run_phases(a, cfg, w, prompt)
+        return
     if a.impl == "reference":
         run_reference(a, cfg, w, prompt, rank, world)
         if dist:

@@ -580,7 +580,7 @@ cudaError_t launch_cooperative(const llm_model* m, const KernelRef& k, int threa
 
 bool step_supported(int gq, int hd) { return (gq == 2 && hd == 64) || (gq == 8 && hd == 64) || (gq == 2 && hd == 128); }
 
-cudaError_t enqueue_persistent_step(llm_model* m, int seq, bool fused) {
+cudaError_t enqueue_persistent_step(llm_model* m, int seq, bool fused, unsigned long long* stamps = nullptr) {
   const llm_config& c = m->cfg;
   StepParams sp{};
   sp.phases = m->d_phases;
@@ -592,6 +592,7 @@ cudaError_t enqueue_persistent_step(llm_model* m, int seq, bool fused) {
   // the expiry test: a barrier no CTA set can reach, a 1 ms limit
   const bool expire = (c.flags & LLM_TEST_EXPIRE_WAIT) != 0;
   sp.bar_extra = expire ? 1 : 0;
+  sp.stamps = stamps;
   sp.wait_ns = expire ? 1000000ull : kWaitLimitNs;
   sp.embed = m->d_embed;
   sp.tok = m->d_tok + seq;
@@ -1559,6 +1560,8 @@ int llm_model_create(const llm_config* cfg, const llm_tensor* tensors, int32_t n
       AL(m->d_stamps, (size_t)kLStampSteps * m->n_lphases * m->n_sm * 16 * 8, "phase timestamps");
     }
   }
+  if (LLMQ_PHASE_STAMPS && m->use_step && !m->use_ll)  // llm_phase_times on the grid-barrier step: one step
+    AL(m->d_stamps, (size_t)m->n_phases * m->n_sm * 16 * 8, "phase timestamps");
   // ---- the batched pipeline (one token for every sequence of a batch, or a
   // chunk of up to kBM prompt tokens of one sequence)
   size_t bcnt_total = 0;
@@ -2137,7 +2140,28 @@ int llm_phase_times(llm_model* m, int32_t seq, int32_t first_token, int32_t n_st
                     int64_t max_out) {
   int rc = check_model(m, seq);
   if (rc) return rc;
-  if (!m->use_ll) return set_err(m, LLM_ERR_UNSUPPORTED, "no flag-synchronised step on this model");
+  if (!m->use_ll) {
+    // the grid-barrier step: one step per launch, [phase][CTA][16]
+    if (!m->use_step) return set_err(m, LLM_ERR_UNSUPPORTED, "no persistent step on this model");
+    if (!m->d_stamps)
+      return set_err(m, LLM_ERR_UNSUPPORTED, "the grid-barrier step records stamps in a build with LLMQ_PHASE_STAMPS=1");
+    if (n_steps != 1 || !out) return set_err(m, LLM_ERR_INVALID_ARG, "one step at a time on the grid-barrier step");
+    if (first_token < 0 || first_token >= m->cfg.vocab) return set_err(m, LLM_ERR_INVALID_ARG, "token out of range");
+    if (m->len[seq] + 1 > m->cfg.max_seq) return set_err(m, LLM_ERR_CTX_FULL, "sequence at max_seq");
+    if (m->sampling) return set_err(m, LLM_ERR_UNSUPPORTED, "sampling on");
+    const int64_t n = (int64_t)m->n_phases * m->n_sm * 16;
+    if (max_out < n) return set_err(m, LLM_ERR_INVALID_ARG, "output too small");
+    const bool fused = m->len[seq] + 1 <= m->step_fuse_len;
+    const int32_t tok_host = first_token;
+    CK(cudaMemcpyAsync(m->d_tok + seq, &tok_host, 4, cudaMemcpyHostToDevice, m->stream), "token upload");
+    CK(cudaMemsetAsync(m->d_stamps, 0, (size_t)n * 8, m->stream), "timestamp reset");
+    CK(enqueue_persistent_step(m, seq, fused, m->d_stamps), "profiled launch");
+    m->len[seq] += 1;
+    CK(cudaMemcpyAsync(out, m->d_stamps, (size_t)n * 8, cudaMemcpyDeviceToHost, m->stream), "timestamps");
+    CK(cudaStreamSynchronize(m->stream), "profile sync");
+    rc = check_status(m);
+    return rc ? rc : (int)(n / 16);
+  }
   if (n_steps <= 0 || n_steps > (int)m->stamps_steps || !out)
     return set_err(m, LLM_ERR_INVALID_ARG, "n_steps outside 1..8 or null output");
   if (first_token < 0 || first_token >= m->cfg.vocab) return set_err(m, LLM_ERR_INVALID_ARG, "token out of range");

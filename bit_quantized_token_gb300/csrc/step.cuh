@@ -38,6 +38,13 @@
 #include "kernels.cuh"
 #include "attn_mma.cuh"
 
+#ifndef LLMQ_PHASE_STAMPS
+#define LLMQ_PHASE_STAMPS 0  // 1: per-phase clock stamps for llm_phase_times (a measurement build: they cost
+                             // the fused kernel registers, ~14 us per TinyLlama-1.1B token)
+#endif
+#ifndef LLMQ_UNIT_STAMPS
+#define LLMQ_UNIT_STAMPS 0  // 1: llm_phase_times also records per-warp unit wait / dot cycles (measurement build)
+#endif
 #ifndef LLMQ_ATTN_CUDA_CORES
 #define LLMQ_ATTN_CUDA_CORES 0  // 1: the step's attention blocks on the CUDA cores (comparison build)
 #endif
@@ -45,6 +52,7 @@
 namespace llmq {
 
 // 15 consumer warps + 1 producer warp = 4 warps per scheduler, 128 registers each
+constexpr bool kUnitStamps = LLMQ_UNIT_STAMPS != 0;
 constexpr int kSWarps = 15;                      // consumer warps
 constexpr int kSCThreads = kSWarps * 32;         // consumer threads
 constexpr int kSThreads = kSCThreads + 32;       // + one producer warp
@@ -121,6 +129,7 @@ struct StepParams {
   int* sync;              // [0] arrivals (phases x CTAs), [1] abort; zeroed before each launch
   int* status;
   int bar_extra;          // arrivals every grid barrier waits for beyond its CTAs (0; 1 in the expiry test)
+  unsigned long long* stamps;  // measurement: [phase][CTA][16] clock64 stamps, or null
   unsigned long long wait_ns;  // limit of every wait on another CTA or on the ring
   const void* embed;
   const int* tok;
@@ -734,6 +743,10 @@ __global__ void __launch_bounds__(kSThreads, 1) step_kernel(const StepParams sp)
   __syncthreads();
 
   const KRange kr(c, N, sp.R);  // this CTA's input range in every GEMV phase
+  if (LLMQ_PHASE_STAMPS && sp.stamps && tid == 0) {  // (%globaltimer, clock64) pairs map this SM's cycles onto one time line
+    sp.stamps[(size_t)c * 16 + 12] = globaltimer();
+    sp.stamps[(size_t)c * 16 + 13] = clock64();
+  }
   if (warp == kSWarps) {
     // ================= producer: every GEMV phase's units, in phase order
     if (lane == 0) {
@@ -793,6 +806,11 @@ __global__ void __launch_bounds__(kSThreads, 1) step_kernel(const StepParams sp)
     int bars = 0;  // grid barriers this CTA arrived at
     for (int ph = 0; ph < sp.n_phases; ++ph) {
       const Phase& P = sm.ph[ph & 1];
+      // measurement stamps (tid 0): 0 phase start, 1 barrier passed, 2 input
+      // built, 3 units done, 4 arrival issued
+      unsigned long long* st =
+          (LLMQ_PHASE_STAMPS && sp.stamps) ? sp.stamps + ((size_t)ph * N + c) * 16 : nullptr;
+      if (st && tid == 0) st[0] = clock64();
       if (P.type == PH_ATTN && fuse) {
         fetch_phase(ph + 1);
         ConsumerSync::sync();
@@ -845,6 +863,7 @@ __global__ void __launch_bounds__(kSThreads, 1) step_kernel(const StepParams sp)
         sm.abort = 1;
         break;
       }
+      if (st && tid == 0) st[1] = clock64();
       if (P.type == PH_GEMV) {
         // ---------------- build this CTA's range of the input vector (inputs
         // r*K .. r*K+K-1 of the GEMV): every load of the build in one round trip
@@ -1047,6 +1066,7 @@ __global__ void __launch_bounds__(kSThreads, 1) step_kernel(const StepParams sp)
           for (int i = tid; i < kSRLoc * kSWarps * 32; i += NT) (&sm.u.g.red[0][0][0])[i] = 0.f;
         if (tid < 2) sm.carry_rt[tid] = -1;
         ConsumerSync::sync();
+        if (st && tid == 0) st[2] = clock64();
 
         // ---------------- stream the units; chunk i = units u0+15i .. u0+15i+14
         const int G = P.GR, EPU = P.bf16 ? kBF16UnitCols : 64;
@@ -1061,12 +1081,15 @@ __global__ void __launch_bounds__(kSThreads, 1) step_kernel(const StepParams sp)
         int win_first = 0, win_idx = 0, win_rt0 = rt0, cur_rt = -1;
         float acc = 0.f;
         bool ok = true;
+        long long t_wait = 0, t_dot = 0;  // measurement build (LLMQ_UNIT_STAMPS): cycles waiting / in unit dots
         for (int i = 0; i < n_chunks; ++i, ++gi) {
           const int s = gi % kSNSlot;
+          const long long ta = (kUnitStamps && st) ? clock64() : 0;
           if (ok) {
             ok = ring_wait(&full[s], (gi / kSNSlot) & 1, sp);
             if (!ok) *(volatile int*)&sm.abort = 1;
           }
+          const long long tb = (kUnitStamps && st) ? clock64() : 0;
           const int k = u0 + i * kSChunk + warp;
           if (ok && k < u1) {
             if (k_rt != cur_rt) {
@@ -1083,6 +1106,10 @@ __global__ void __launch_bounds__(kSThreads, 1) step_kernel(const StepParams sp)
           }
           __syncwarp();
           if (lane == 0) mbar_arrive(&empty[s]);
+          if (kUnitStamps && st) {
+            t_wait += tb - ta;
+            t_dot += clock64() - tb;
+          }
           k_g += kSChunk;
           while (k_g >= G) {
             k_g -= G;
@@ -1120,6 +1147,32 @@ __global__ void __launch_bounds__(kSThreads, 1) step_kernel(const StepParams sp)
         }
         // every warp passed the last window's closing barrier: the flag is uniform
         if (*(volatile int*)&sm.abort) break;
+        if (kUnitStamps && st) {
+          if (lane == 0) {
+            sm.u.g.red[0][warp][0] = (float)t_wait;  // (the windows are closed: red is free)
+            sm.u.g.red[0][warp][1] = (float)t_dot;
+          }
+          ConsumerSync::sync();
+          if (tid == 0) {
+            float mw = 0.f, md = 0.f, sw = 0.f, sd = 0.f;
+            for (int w = 0; w < kSWarps; ++w) {
+              mw = fmaxf(mw, sm.u.g.red[0][w][0]);
+              md = fmaxf(md, sm.u.g.red[0][w][1]);
+              sw += sm.u.g.red[0][w][0];
+              sd += sm.u.g.red[0][w][1];
+            }
+            st[5] = (unsigned long long)mw;
+            st[6] = (unsigned long long)md;
+            st[7] = (unsigned long long)sw;
+            st[8] = (unsigned long long)sd;
+          }
+          ConsumerSync::sync();
+          if (lane == 0) {
+            sm.u.g.red[0][warp][0] = 0.f;
+            sm.u.g.red[0][warp][1] = 0.f;
+          }
+        }
+        if (st && tid == 0) st[3] = clock64();
       } else if (P.type == PH_ATTN) {
         if constexpr (!FUSED) {
           // ---------------- attention items (kv head, split) over the CTAs
@@ -1228,9 +1281,14 @@ __global__ void __launch_bounds__(kSThreads, 1) step_kernel(const StepParams sp)
         grid_arrive(sp);  // its CTA barrier also retires this phase's reads of sm.ph
         ++bars;
       }
+      if (st && tid == 0) st[4] = clock64();
     }
   }
   __syncthreads();
+  if (LLMQ_PHASE_STAMPS && sp.stamps && tid == 0) {
+    sp.stamps[(size_t)c * 16 + 14] = globaltimer();
+    sp.stamps[(size_t)c * 16 + 15] = clock64();
+  }
   // After an abort, wait (bounded) for copies still landing in the ring.
   if (sm.abort && tid == kSWarps * 32) {
     const int issued = sm.issued;

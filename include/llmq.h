@@ -292,7 +292,15 @@ int llm_profile_step(llm_model* m, int32_t seq, int32_t token, llm_kernel_time* 
 int llm_time_kernel(llm_model* m, int32_t seq, int32_t which, int32_t layer, int32_t n, float* ms,
                     int64_t* bytes);
 
-/* Run n_steps (1..8) greedy steps of sequence seq from first_token through the
+/* On a model without LLM_DATAFLOW_STEP, in a library built with
+ * LLMQ_PHASE_STAMPS=1 (else LLM_ERR_UNSUPPORTED): one step (n_steps = 1) of
+ * the grid-barrier persistent step, recording per (phase, CTA) the clock64
+ * stamps 0 phase start, 1 grid barrier passed, 2 input built, 3 weight units
+ * done, 4 arrival issued (0 where a phase has no such point), and with
+ * LLMQ_UNIT_STAMPS=1 also 5..8 the largest and summed per-warp cycles waiting
+ * for units and in unit dots; values 12..15 of phase 0's records hold
+ * (%globaltimer, clock64) at each CTA's start and end; out [phases][n_sm][16].
+ * Otherwise: run n_steps (1..8) greedy steps of sequence seq from first_token through the
  * flag-synchronised step kernel in one launch and record, for every (step,
  * phase, CTA), 16 values: the SM cycle counter (clock64) when the phase's
  * input build starts, when its inputs have all arrived, when the build is
