@@ -490,6 +490,10 @@ struct BAttnParams {
 };
 
 
+#ifndef LLMQ_BATTN_SPLITS
+#define LLMQ_BATTN_SPLITS 8  // measured on the 32-sequence workload: 24 -> 8791, 12 -> 9115, 8 -> 9274, 4 -> 9005 tok/s
+#endif
+static_assert(LLMQ_BATTN_SPLITS >= 1 && LLMQ_BATTN_SPLITS <= 24, "splits of a batched attention item");
 constexpr int kBAttnThreads = 256;
 constexpr int kBAttnPP = 64;  // cache positions per pass (~42 KB of tiles: 4 CTAs per SM)
 
@@ -532,8 +536,8 @@ __global__ void __launch_bounds__(kBAttnThreads) battn_mma_kernel(const BAttnPar
     return;
   }
   const int len = pos + 1;
-  constexpr int PMAX = 24;  // splits a (sequence, kv head) merges at most (longer splits take several passes)
-  const int P_eff = min(min(a.P, PMAX), (len + PP - 1) / PP);
+  constexpr int PMAX = 24;  // merge scratch: splits a (sequence, kv head) may have (LLMQ_BATTN_SPLITS <= PMAX)
+  const int P_eff = min(min(a.P, LLMQ_BATTN_SPLITS), (len + PP - 1) / PP);
   if (split >= P_eff) return;
   const int t0 = (int)((int64_t)len * split / P_eff), t1 = (int)((int64_t)len * (split + 1) / P_eff);
   const int sb = bp.seq ? bp.seq[b] : b;  // this row's cache
