@@ -65,7 +65,7 @@ def peaks():
 
 
 # the sources a kernel's code comes from (the step kernel is defined in these headers)
-KERNEL_SOURCES = {"step_kernel": ("common.cuh", "kernels.cuh", "attn_mma.cuh", "step.cuh")}
+KERNEL_SOURCES = {"step_kernel": ("common.cuh", "kernels.cuh", "attn_mma.cuh", "step.cuh", "step_kernels.cu")}
 
 
 def src_sha(kernel="step_kernel"):
@@ -339,12 +339,18 @@ def run_phases(a, cfg, w, prompt):
     print(f"{cfg['name']}: {len(rows)} phases, step {(gt1.max() - gt0.min()) / 1000:.1f} us (stamps build)")
     keys = ["barrier_after_last_arrival_us", "build_us", "units_us", "busiest_warp_wait_us", "busiest_warp_dot_us",
             "arrive_us", "arrival_spread_us", "span_us"]
-    per = 4 if len(rows) % 4 == 1 else 5  # phases per layer (+ the LM head / logits tail)
-    print("phase-in-layer | " + " | ".join(k[:-3] for k in keys))
+    L = cfg["n_layers"]
+    per = (len(rows) - 2) // L  # phases per layer; the last two are the LM head and the logit reduction
+    names = (["q|k|v", "o (+attention)", "gate|up", "down"] if per == 4
+             else ["q|k|v", "attention", "o", "gate|up", "down"])[:per]
+    print("phase | " + " | ".join(k[:-3] for k in keys) + "  (us, median CTA, mean over layers 1..L-1)")
+    fmt = lambda sel: " | ".join(
+        f"{np.mean([r[k] for r in sel if k in r]):.2f}" if any(k in r for r in sel) else "-" for k in keys)
     for j in range(per):
-        sel = [r for i, r in enumerate(rows[:-(len(rows) % per) or None]) if i % per == j]
-        vals = [np.mean([r[k] for r in sel if k in r]) if any(k in r for r in sel) else float("nan") for k in keys]
-        print(f"{j} (n={len(sel)}) | " + " | ".join(f"{v:.2f}" for v in vals))
+        sel = [rows[l * per + j] for l in range(1, L)]
+        print(f"{names[j]} | " + fmt(sel))
+    print("LM head | " + fmt([rows[L * per]]))
+    print("logits | " + fmt([rows[L * per + 1]]))
 
 
 def main():
