@@ -272,7 +272,9 @@ struct llm_model {
   SampleCfg* d_samp = nullptr;                // sampling options (temperature 0: greedy)
   bool sampling = false;
   size_t pf_cap = 0;
-  int* h_stage = nullptr;                     // pinned staging
+  int* h_stage = nullptr;                     // pinned staging (slots: kStage*)
+  float* h_logits = nullptr;                  // pinned logits of a batch-1 call with host outputs
+  size_t h_logits_n = 0;
   std::vector<int> len;
   std::vector<cudaGraphExec_t> graphs;
   int kernels_per_step = 0;
@@ -969,11 +971,19 @@ cudaError_t enqueue_step_only(llm_model* m, int seq, Prof* prof, bool fused) {
   return one(W_LM, -1, pdl);
 }
 
+int status_of(llm_model* m, int st);
+
 int check_status(llm_model* m) {
   if (m->poisoned) return m->poisoned;
   int st = 0;
   CK(cudaMemcpyAsync(&st, m->d_status, sizeof(int), cudaMemcpyDeviceToHost, m->stream), "status read");
   CK(cudaStreamSynchronize(m->stream), "stream sync");
+  return status_of(m, st);
+}
+
+// The llm_status of a device status word the host has read after a synchronization.
+int status_of(llm_model* m, int st) {
+  if (m->poisoned) return m->poisoned;
   if (st == 0) return LLM_OK;
   CK(cudaMemsetAsync(m->d_status, 0, sizeof(int), m->stream), "status clear");
   if (st & ST_TIMEOUT) {
@@ -1051,6 +1061,53 @@ int copy_out(llm_model* m, void* dst, const void* src, size_t bytes, bool* host)
   return LLM_OK;
 }
 
+// Pinned staging slots (ints of h_stage): the batch-1 token in, the status
+// word, and up to 32 tokens in and 32 choices out of a batched call.
+constexpr int kStageTok = 8, kStageStatus = 10, kStageToks = 128, kStageChoice = 160, kStageInts = 256;
+
+// Whether a call's outputs include host memory: such a call ends with one
+// synchronization, so its small transfers can go through the pinned slots.
+bool host_outputs(const void* a, const void* b) {
+  return (a && !is_device_ptr(a)) || (b && !is_device_ptr(b));
+}
+
+// Upload n tokens: through a pinned slot when the call synchronizes before
+// it returns (the slot is free again by then), else from the caller's memory.
+int upload_tokens(llm_model* m, int32_t* dst, const int32_t* src, int n, bool sync_call, int slot) {
+  if (sync_call && n <= 32) {
+    std::memcpy(m->h_stage + slot, src, (size_t)n * 4);
+    CK(cudaMemcpyAsync(dst, m->h_stage + slot, (size_t)n * 4, cudaMemcpyHostToDevice, m->stream), "token upload");
+  } else {
+    CK(cudaMemcpyAsync(dst, src, (size_t)n * 4, cudaMemcpyDefault, m->stream), "token upload");
+  }
+  return LLM_OK;
+}
+
+// The end of a decode call: device outputs are copied asynchronously; host
+// outputs, with the status word, come back through pinned memory after one
+// synchronization (large ones directly). Returns the call's llm_status.
+int finish_call(llm_model* m, float* logits_out, const float* d_logits, size_t n_logits, int32_t* choice_out,
+                const int32_t* d_choice, size_t n_choice) {
+  const bool hl = logits_out && !is_device_ptr(logits_out);
+  const bool hc = choice_out && !is_device_ptr(choice_out);
+  if (logits_out && !hl)
+    CK(cudaMemcpyAsync(logits_out, d_logits, n_logits * 4, cudaMemcpyDeviceToDevice, m->stream), "output copy");
+  if (choice_out && !hc)
+    CK(cudaMemcpyAsync(choice_out, d_choice, n_choice * 4, cudaMemcpyDeviceToDevice, m->stream), "output copy");
+  if (!hl && !hc) return LLM_OK;  // asynchronous: a later synchronizing call reports the status
+  float* lst = (hl && n_logits <= m->h_logits_n) ? m->h_logits : nullptr;
+  int32_t* cst = (hc && n_choice <= 32) ? m->h_stage + kStageChoice : nullptr;
+  if (hl) CK(cudaMemcpyAsync(lst ? lst : logits_out, d_logits, n_logits * 4, cudaMemcpyDeviceToHost, m->stream),
+             "logits copy");
+  if (hc) CK(cudaMemcpyAsync(cst ? cst : choice_out, d_choice, n_choice * 4, cudaMemcpyDeviceToHost, m->stream),
+             "choice copy");
+  CK(cudaMemcpyAsync(m->h_stage + kStageStatus, m->d_status, 4, cudaMemcpyDeviceToHost, m->stream), "status read");
+  CK(cudaStreamSynchronize(m->stream), "stream sync");
+  if (lst) std::memcpy(logits_out, lst, n_logits * 4);
+  if (cst) std::memcpy(choice_out, cst, n_choice * 4);
+  return status_of(m, m->h_stage[kStageStatus]);
+}
+
 }  // namespace
 
 extern "C" {
@@ -1064,6 +1121,7 @@ void llm_model_destroy(llm_model* m) {
   if (m->bgraph) cudaGraphExecDestroy(m->bgraph);
   for (void* p : m->allocs) cudaFree(p);
   if (m->h_stage) cudaFreeHost(m->h_stage);
+  if (m->h_logits) cudaFreeHost(m->h_logits);
   if (m->own_stream && m->stream) cudaStreamDestroy(m->stream);
   delete m;
 }
@@ -1616,8 +1674,10 @@ int llm_model_create(const llm_config* cfg, const llm_tensor* tensors, int32_t n
   }
 #undef AL
   {
-    cudaError_t e = cudaMallocHost(&m->h_stage, 64 * sizeof(int));
+    cudaError_t e = cudaMallocHost(&m->h_stage, kStageInts * sizeof(int));
+    if (e == cudaSuccess) e = cudaMallocHost(&m->h_logits, (size_t)V * sizeof(float));
     if (e != cudaSuccess) return fail(cuda_fail(m, e, "pinned staging"));
+    m->h_logits_n = V;
   }
 
   // ---- uploads
@@ -1686,20 +1746,18 @@ int llm_decode_step(llm_model* m, int32_t seq, int32_t token, float* logits_out,
   if (rc) return rc;
   if (token < 0 || token >= m->cfg.vocab) return set_err(m, LLM_ERR_INVALID_ARG, "token out of range");
   if (m->len[seq] + 1 > m->cfg.max_seq) return set_err(m, LLM_ERR_CTX_FULL, "sequence is at max_seq");
-  // pageable source: staged at call time, so back-to-back asynchronous calls cannot race
+  // an asynchronous call uploads from its pageable argument (staged at call
+  // time, so back-to-back calls cannot race); a synchronous one via pinned memory
+  const bool sync_call = host_outputs(logits_out, argmax_out);
   const int32_t tok_host = token;
-  CK(cudaMemcpyAsync(m->d_tok + seq, &tok_host, 4, cudaMemcpyHostToDevice, m->stream), "token upload");
+  if ((rc = upload_tokens(m, m->d_tok + seq, &tok_host, 1, sync_call, kStageTok)) != LLM_OK) return rc;
   if (ll_covers(m, m->len[seq], 1)) {
     CK(enqueue_ll(m, seq, 1, 0, nullptr), "step launch");
   } else if ((rc = run_step(m, seq, m->len[seq])) != LLM_OK) {
     return rc;
   }
   m->len[seq] += 1;
-  bool host = false;
-  if ((rc = copy_out(m, logits_out, m->d_logits, (size_t)m->cfg.vocab * 4, &host)) != LLM_OK) return rc;
-  if ((rc = copy_out(m, argmax_out, m->d_argmax + seq, 4, &host)) != LLM_OK) return rc;
-  if (host) return check_status(m);
-  return LLM_OK;
+  return finish_call(m, logits_out, m->d_logits, (size_t)m->cfg.vocab, argmax_out, m->d_argmax + seq, 1);
 }
 
 int llm_prefill(llm_model* m, int32_t seq, const int32_t* tokens, int32_t n, float* logits_out, int32_t* argmax_out) {
@@ -1723,9 +1781,9 @@ int llm_prefill(llm_model* m, int32_t seq, const int32_t* tokens, int32_t n, flo
     }
   }
   m->len[seq] += n;
-  bool host = false;
-  if ((rc = copy_out(m, logits_out, m->d_logits, (size_t)m->cfg.vocab * 4, &host)) != LLM_OK) return rc;
-  if ((rc = copy_out(m, argmax_out, m->d_argmax + seq, 4, &host)) != LLM_OK) return rc;
+  if ((rc = finish_call(m, logits_out, m->d_logits, (size_t)m->cfg.vocab, argmax_out, m->d_argmax + seq, 1)) !=
+      LLM_OK)
+    return rc;
   CK(cudaStreamSynchronize(m->stream), "prefill sync");  // host_toks outlives the upload
   return check_status(m);
 }
@@ -1813,8 +1871,9 @@ int llm_decode_greedy(llm_model* m, int32_t seq, int32_t first_token, int32_t n_
   if (n_steps <= 0 || !tokens_out) return set_err(m, LLM_ERR_INVALID_ARG, "n_steps <= 0 or null tokens_out");
   if (first_token < 0 || first_token >= m->cfg.vocab) return set_err(m, LLM_ERR_INVALID_ARG, "token out of range");
   if (m->len[seq] + n_steps > m->cfg.max_seq) return set_err(m, LLM_ERR_CTX_FULL, "steps would exceed max_seq");
-  const int32_t tok_host = first_token;  // pageable: staged at call time
-  CK(cudaMemcpyAsync(m->d_tok + seq, &tok_host, 4, cudaMemcpyHostToDevice, m->stream), "token upload");
+  const int32_t tok_host = first_token;
+  if ((rc = upload_tokens(m, m->d_tok + seq, &tok_host, 1, host_outputs(tokens_out, nullptr), kStageTok)) != LLM_OK)
+    return rc;
   CK(cudaMemsetAsync(m->d_hist_ctr, 0, 4, m->stream), "history reset");
   // the steps the dataflow kernel covers go in one launch, the rest step by step
   int done = 0;
@@ -1828,10 +1887,7 @@ int llm_decode_greedy(llm_model* m, int32_t seq, int32_t first_token, int32_t n_
   for (int i = done; i < n_steps; ++i)
     if ((rc = run_step(m, seq, m->len[seq] + i)) != LLM_OK) return rc;
   m->len[seq] += n_steps;
-  bool host = false;
-  if ((rc = copy_out(m, tokens_out, m->d_hist, (size_t)n_steps * 4, &host)) != LLM_OK) return rc;
-  if (host) return check_status(m);
-  return LLM_OK;
+  return finish_call(m, nullptr, nullptr, 0, tokens_out, m->d_hist, (size_t)n_steps);
 }
 
 int llm_decode_step_batch(llm_model* m, const int32_t* tokens, int32_t n_seq, float* logits_out, int32_t* argmax_out) {
@@ -1850,8 +1906,8 @@ int llm_decode_step_batch(llm_model* m, const int32_t* tokens, int32_t n_seq, fl
     CK(cudaMemcpy(host_toks.data(), tokens, (size_t)n_seq * 4, cudaMemcpyDefault), "token read");
     for (int b = 0; b < n_seq; ++b)
       if (host_toks[b] < 0 || host_toks[b] >= c.vocab) return set_err(m, LLM_ERR_INVALID_ARG, "token out of range");
-    CK(cudaMemcpyAsync(m->d_tok, host_toks.data(), (size_t)n_seq * 4, cudaMemcpyHostToDevice, m->stream),
-       "token upload");
+    // a call given tokens synchronizes before it returns: the pinned slot is free again by then
+    if ((rc = upload_tokens(m, m->d_tok, host_toks.data(), n_seq, true, kStageToks)) != LLM_OK) return rc;
   }
   if (c.flags & LLM_NO_GRAPH) {
     CK(enqueue_batched(m, decode_io(m)), "batched step launch");
@@ -1870,10 +1926,11 @@ int llm_decode_step_batch(llm_model* m, const int32_t* tokens, int32_t n_seq, fl
     CK(cudaGraphLaunch(m->bgraph, m->stream), "graph launch");
   }
   for (int b = 0; b < n_seq; ++b) m->len[b] += 1;
-  bool host = false;
-  if ((rc = copy_out(m, logits_out, m->d_blogits, (size_t)n_seq * c.vocab * 4, &host)) != LLM_OK) return rc;
-  if ((rc = copy_out(m, argmax_out, m->d_argmax, (size_t)n_seq * 4, &host)) != LLM_OK) return rc;
-  if (host || tokens) return check_status(m);  // (pageable uploads are staged at call time)
+  const bool host = host_outputs(logits_out, argmax_out);
+  if ((rc = finish_call(m, logits_out, m->d_blogits, (size_t)n_seq * c.vocab, argmax_out, m->d_argmax,
+                        (size_t)n_seq)) != LLM_OK)
+    return rc;
+  if (tokens && !host) return check_status(m);
   return LLM_OK;
 }
 
