@@ -478,9 +478,11 @@ def main():
 
     # sampled choice (temperature 0.8, top-k 40, top-p 0.95, Philox draw): the
     # same device-fed loop with the sampling kernel in each step's graph
+    # (from the same reset cache as the greedy regions: the same positions)
     m.set_sampling(0.8, 40, 0.95, 42)
     toks_s = torch.empty(a.steps, dtype=torch.int32, device="cuda")
-    warm_s = m.decode_greedy(0, int(am_h[0]), a.warmup)
+    tok_s0 = fresh_sequence()
+    warm_s = np.array([tok_s0], np.int32)
     torch.cuda.synchronize()
     e0.record(stream)
     m.decode_greedy(0, int(warm_s[-1]), a.steps, toks_s)
