@@ -16,7 +16,11 @@ import numpy as np
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _ROOT = os.path.dirname(_HERE)
-LIB_PATH = os.path.join(_HERE, "libllmq.so")
+# LLMQ_CHECKED=1 selects the checked build: every computed index into a weight
+# stream, K/V cache row or partial-sum array is tested on the device, and one
+# outside its buffer fails the call (LLM_ERR_CUDA, "an index left its buffer")
+CHECKED = os.environ.get("LLMQ_CHECKED") == "1"
+LIB_PATH = os.path.join(_HERE, "libllmq_checked.so" if CHECKED else "libllmq.so")
 HEADER = os.path.join(_ROOT, "include", "llmq.h")
 CSRC = os.path.join(_HERE, "csrc")
 
@@ -69,6 +73,8 @@ def build(force: bool = False, out: str | None = None, defines=()) -> str:
     from concurrent.futures import ThreadPoolExecutor
 
     target = out or LIB_PATH
+    if CHECKED and out is None:
+        defines = list(defines) + ["LLMQ_CHECKED=1"]
     if out is None and not force and os.path.exists(LIB_PATH):
         newest = max(os.path.getmtime(f) for f in sources())
         if os.path.getmtime(LIB_PATH) >= newest:

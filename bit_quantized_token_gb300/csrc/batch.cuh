@@ -108,10 +108,13 @@ __global__ void __launch_bounds__(kBThreads, 2) bgemv_kernel(const BGemvParams p
     const int nk = min(p.kc, g1 - ga), b = ((ga - g0) / p.kc) & 1;
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // earlier reads of this buffer
     mbar_expect_tx(&s_bar[b], p.rtb * nk * p.unit_bytes);
-    for (int r = 0; r < p.rtb; ++r)
+    for (int r = 0; r < p.rtb; ++r) {
+      // (checked build: an index outside the stream copies its first units instead)
+      const bool okc = in_bounds(p.status, rt0 + r < p.n_rt && ga + nk <= p.G);
       bulk_g2s(wbuf + b * wchunk + (size_t)r * p.kc * p.unit_bytes,
-               p.units + ((size_t)(rt0 + r) * p.G + ga) * p.unit_bytes, nk * p.unit_bytes, &s_bar[b],
+               p.units + (okc ? ((size_t)(rt0 + r) * p.G + ga) * p.unit_bytes : 0), nk * p.unit_bytes, &s_bar[b],
                policy_evict_first());
+    }
   };
   if (tid == 0) {
     mbar_init(&s_bar[0], 1);
@@ -308,7 +311,9 @@ __global__ void __launch_bounds__(kBThreads, 2) bgemv_kernel(const BGemvParams p
 #pragma unroll
       for (int k = 0; k < 4; ++k) {
         const int mm = warp + 8 * k;
-        p.part[((size_t)ksi * kBM + mm) * rows_pad + row0 + rl * 32 + lane] = cta_sum(rl * 32 + lane, mm);
+        const float v = cta_sum(rl * 32 + lane, mm);
+        if (in_bounds(p.status, ksi < p.ks && row0 + rl * 32 + lane < rows_pad))
+          p.part[((size_t)ksi * kBM + mm) * rows_pad + row0 + rl * 32 + lane] = v;
       }
     __threadfence();
     __syncthreads();
@@ -565,8 +570,9 @@ __global__ void __launch_bounds__(kBAttnThreads) battn_mma_kernel(const BAttnPar
       constexpr int C8 = HD / 16, L8 = C8 == 4 ? 2 : 3;
       for (int idx = tid; idx < 2 * n * C8; idx += NT) {
         const int kv = idx >= n * C8, r = idx - kv * n * C8, row = r >> L8, ch = r & (C8 - 1);
-        cp_async16(reinterpret_cast<uint8_t*>(&(kv ? sa.vt : sa.kt)[row][0]) + 16 * ch,
-                   (kv ? vc8 : kc8) + (size_t)(tp + row) * HD + 16 * ch);
+        if (in_bounds(a.status, tp + row < a.cap))
+          cp_async16(reinterpret_cast<uint8_t*>(&(kv ? sa.vt : sa.kt)[row][0]) + 16 * ch,
+                     (kv ? vc8 : kc8) + (size_t)(tp + row) * HD + 16 * ch);
       }
       const int kv = tid / PP, row = tid - kv * PP;
       if (kv < 2 && row < n)
@@ -578,7 +584,8 @@ __global__ void __launch_bounds__(kBAttnThreads) battn_mma_kernel(const BAttnPar
         const uint16_t* src = (kv ? vc : kc) + (size_t)tp * HD;
         for (int idx = tid; idx < rows * CH; idx += NT) {
           const int row = idx >> LCH, ch = idx & (CH - 1);
-          if (row < n) cp_async16(&tile[row][8 * ch], src + (size_t)row * HD + 8 * ch);
+          if (row < n && in_bounds(a.status, tp + row < a.cap))
+            cp_async16(&tile[row][8 * ch], src + (size_t)row * HD + 8 * ch);
           else *reinterpret_cast<uint4*>(&tile[row][8 * ch]) = make_uint4(0u, 0u, 0u, 0u);
         }
       }
@@ -688,7 +695,7 @@ __global__ void __launch_bounds__(kBAttnThreads) battn_mma_kernel(const BAttnPar
     const __nv_bfloat16 h = __float2bfloat16_rn(x);
     const float xr = __bfloat162float(h);
     sa.cur[r][d] = xr;
-    if (append) (r == GQ ? kc : vc)[(size_t)pos * HD + d] = __bfloat16_as_ushort(h);
+    if (append && in_bounds(a.status, pos < a.cap)) (r == GQ ? kc : vc)[(size_t)pos * HD + d] = __bfloat16_as_ushort(h);
     if (owner) (r == GQ ? sa.kt : sa.vt)[pos - t0][d] = __half_as_ushort(__float2half_rn(xr));
   };
   for (int j = tid; j < nrope + HD; j += NT) {  // RoPE pairs of the q heads and k, then v elements
@@ -726,7 +733,7 @@ __global__ void __launch_bounds__(kBAttnThreads) battn_mma_kernel(const BAttnPar
       const float cf = dq == 0.0f ? 0.0f : fminf(fmaxf(roundf(x / dq), -127.0f), 127.0f);
       sa.cur[GQ + kv][d] = cf;
       if (lane == 0) sa.cursc[kv][grp] = dq;
-      if (append) {
+      if (append && in_bounds(a.status, pos < a.cap)) {
         (kv ? vc8 : kc8)[(size_t)pos * HD + d] = (int8_t)(int)cf;
         if (lane == 0) (kv ? vs8 : ks8)[(size_t)pos * NG + grp] = __half_as_ushort(dh);
       }

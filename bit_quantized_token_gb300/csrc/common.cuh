@@ -20,7 +20,22 @@ constexpr int kMaxK = 8192;          // widest GEMV input (held in registers in 
 constexpr int kAttnThreads = 128;
 
 // Device status bits (OR-ed into the model's status word).
-enum : int { ST_TIMEOUT = 1, ST_NAN = 2, ST_BAD_TOKEN = 4, ST_CTX_FULL = 8 };
+enum : int { ST_TIMEOUT = 1, ST_NAN = 2, ST_BAD_TOKEN = 4, ST_CTX_FULL = 8, ST_BOUNDS = 16 };
+
+// The checked build (-DLLMQ_CHECKED=1): every computed index into a weight
+// stream, a K/V cache row or a partial-sum array is tested against its
+// buffer first; one outside sets ST_BOUNDS in the status word and its access
+// is skipped (no trap). In the normal build the test compiles away.
+#ifndef LLMQ_CHECKED
+#define LLMQ_CHECKED 0
+#endif
+__device__ __forceinline__ bool in_bounds(int* status, bool ok) {
+  if (LLMQ_CHECKED && !ok) {
+    atomicOr(status, ST_BOUNDS);
+    return false;
+  }
+  return true;
+}
 
 constexpr unsigned long long kWaitLimitNs = 2000000000ull;  // 2 s for any device wait
 

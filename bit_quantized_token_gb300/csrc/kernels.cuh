@@ -404,7 +404,9 @@ __global__ void __launch_bounds__(kGemvThreads, 2) gemv_kernel(const GemvParams 
         const int ub = u0 + i * kChunkUnits;
         const int nu = min(kChunkUnits, u1 - ub);
         mbar_expect_tx(&full[s], nu * UB);
-        bulk_g2s(ring + s * kChunkUnits * UB, p.units + (size_t)ub * UB, nu * UB, &full[s], pol);
+        // (checked build: an index outside the stream copies its first units instead)
+        const bool okc = in_bounds(p.status, ub + nu <= p.n_rt * p.G);
+        bulk_g2s(ring + s * kChunkUnits * UB, p.units + (okc ? (size_t)ub * UB : 0), nu * UB, &full[s], pol);
         flags[3] = i + 1;  // chunks issued
       }
     }
@@ -566,7 +568,8 @@ __global__ void __launch_bounds__(kGemvThreads, 2) gemv_kernel(const GemvParams 
           if (r == next_rt) {
             cout[lane] = sum;
           } else if (r * G < u0 || (r + 1) * G > u1) {
-            p.part_buf[((size_t)r * p.part.S + (c - p.part.first_cta(r))) * 32 + lane] = sum;
+            if (in_bounds(p.status, r < p.n_rt && c - p.part.first_cta(r) < p.part.S))
+              p.part_buf[((size_t)r * p.part.S + (c - p.part.first_cta(r))) * 32 + lane] = sum;
           } else {
             gemv_epilogue(p, r, lane, sum, bv, bi, nan);
           }

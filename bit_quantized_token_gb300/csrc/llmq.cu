@@ -1007,6 +1007,10 @@ int status_of(llm_model* m, int st) {
     }
     return set_err(m, LLM_ERR_TIMEOUT, msg);
   }
+  if (st & ST_BOUNDS) {
+    m->poisoned = LLM_ERR_CUDA;
+    return set_err(m, LLM_ERR_CUDA, "an index left its buffer (checked build)");
+  }
   if (st & ST_NAN) return set_err(m, LLM_ERR_NAN, "NaN in the logits");
   if (st & ST_CTX_FULL) return set_err(m, LLM_ERR_CTX_FULL, "position reached max_seq on the device");
   return set_err(m, LLM_ERR_INVALID_ARG, "token id out of range on the device");

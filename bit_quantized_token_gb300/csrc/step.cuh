@@ -329,7 +329,7 @@ __device__ void step_attn_prefetch(const StepParams& sp, int layer, int g, int t
     const size_t cbase = (size_t)layer * sp.layer_stride + (size_t)g * sp.cap * HD;
     const int n = min(PP, t1 - t0);
     const int kv = tid / PP, row = tid - kv * PP;
-    if (kv < 2 && row < n && t0 + row != pos) {
+    if (kv < 2 && row < n && t0 + row != pos && in_bounds(sp.status, t0 + row < sp.cap)) {
       const int8_t* src = (kv ? sp.v8_base : sp.k8_base) + cbase + (size_t)(t0 + row) * HD;
       uint8_t* dst = reinterpret_cast<uint8_t*>(&(kv ? sa.vt : sa.kt)[row][0]);
 #pragma unroll
@@ -345,7 +345,7 @@ __device__ void step_attn_prefetch(const StepParams& sp, int layer, int g, int t
 #pragma unroll
   for (int j = 0; j < TB; ++j) {
     const int idx = tid + j * NT, kv = idx / (PP * CH), rem = idx - kv * (PP * CH), row = rem / CH, ch = rem - row * CH;
-    if (kv < 2 && row < n && t0 + row != pos)
+    if (kv < 2 && row < n && t0 + row != pos && in_bounds(sp.status, t0 + row < sp.cap))
       cp_async16(&(kv ? sa.vt : sa.kt)[row][8 * ch], (kv ? vc : kc) + (size_t)(t0 + row) * HD + 8 * ch);
   }
 }
@@ -420,7 +420,7 @@ __device__ void step_attn_item(const StepParams& sp, const Phase& P, int g, int 
     if constexpr (KV8) {
       const int n = min(PP, t1 - tp);
       const int kv = tid / PP, row = tid - kv * PP;
-      const bool ld = kv < 2 && row < n && tp + row != pos;
+      const bool ld = kv < 2 && row < n && tp + row != pos && in_bounds(sp.status, tp + row < sp.cap);
       const int8_t* src = (kv ? vc8 : kc8) + (size_t)(tp + row) * HD;
 #pragma unroll
       for (int k = 0; k < HD / 16; ++k) {
@@ -439,7 +439,7 @@ __device__ void step_attn_item(const StepParams& sp, const Phase& P, int g, int 
     for (int j = 0; j < TB; ++j) {
       const int idx = tid + j * NT, kv = idx / (PP * CH), rem = idx - kv * (PP * CH), row = rem / CH, ch = rem - row * CH;
       const float4 v = ldcg4_if(reinterpret_cast<const float*>((kv ? vc : kc) + (size_t)(tp + row) * HD + 8 * ch),
-                                kv < 2 && row < n && tp + row != pos);
+                                kv < 2 && row < n && tp + row != pos && in_bounds(sp.status, tp + row < sp.cap));
       tl[j] = make_uint4(__float_as_uint(v.x), __float_as_uint(v.y), __float_as_uint(v.z), __float_as_uint(v.w));
     }
   };
@@ -556,7 +556,7 @@ __device__ void step_attn_item(const StepParams& sp, const Phase& P, int g, int 
     const __nv_bfloat16 b = __float2bfloat16_rn(x);
     const float xr = __bfloat162float(b);
     sa.cur[r][d] = xr;
-    if (append) (r == GQ ? kc : vc)[(size_t)pos * HD + d] = __bfloat16_as_ushort(b);
+    if (append && in_bounds(sp.status, pos < sp.cap)) (r == GQ ? kc : vc)[(size_t)pos * HD + d] = __bfloat16_as_ushort(b);
     if (owner) (r == GQ ? sa.kt : sa.vt)[pos - t0][d] = __half_as_ushort(__float2half_rn(xr));
   };
   if (tid < nrope) {
@@ -591,7 +591,7 @@ __device__ void step_attn_item(const StepParams& sp, const Phase& P, int g, int 
       const float cf = dq == 0.0f ? 0.0f : fminf(fmaxf(roundf(x / dq), -127.0f), 127.0f);
       sa.cur[GQ + kv][d] = cf;
       if (lane == 0) sa.cursc[kv][grp] = dq;
-      if (append) {
+      if (append && in_bounds(sp.status, pos < sp.cap)) {
         (kv ? vc8 : kc8)[(size_t)pos * HD + d] = (int8_t)(int)cf;
         if (lane == 0) (kv ? vs8 : ks8)[(size_t)pos * NG + grp] = __half_as_ushort(dh);
       }
@@ -770,8 +770,12 @@ __global__ void __launch_bounds__(kSThreads, 1) step_kernel(const StepParams sp)
           // one copy per row tile touched: the range's units of a tile are contiguous
           for (int v = ub; v < ue;) {
             const int rt = v / GR, gp = v - rt * GR, run = min(ue - v, GR - gp);
-            bulk_g2s(ring + s * kSSlot + (v - ub) * UB, P.units + ((size_t)rt * P.G + kr.r * GR + gp) * UB,
-                     run * UB, &full[s], pol);
+            // (checked build: an index outside the stream copies its first units instead, so
+            // the slot still completes; the status word reports the error)
+            const bool okc = in_bounds(sp.status, rt < P.n_rt && kr.r * GR + gp + run <= P.G &&
+                                                      (v - ub + run) * UB <= kSSlot);
+            bulk_g2s(ring + s * kSSlot + (v - ub) * UB,
+                     P.units + (okc ? ((size_t)rt * P.G + kr.r * GR + gp) * UB : 0), run * UB, &full[s], pol);
             v += run;
           }
           sm.issued = gi + 1;
@@ -1136,7 +1140,7 @@ __global__ void __launch_bounds__(kSThreads, 1) step_kernel(const StepParams sp)
                 sm.u.g.red[li][w2][lane] = 0.f;
               }
               if (t == next_rt) sm.u.g.carry[win_idx & 1][lane] = sum;
-              else P.out_part[((size_t)t * sp.R + kr.r) * 32 + lane] = sum;
+              else if (in_bounds(sp.status, t < P.n_rt)) P.out_part[((size_t)t * sp.R + kr.r) * 32 + lane] = sum;
             }
             if (tid == 0) sm.carry_rt[win_idx & 1] = (next_rt == rt_b) ? rt_b : -1;
             ConsumerSync::sync();
@@ -1212,7 +1216,7 @@ __global__ void __launch_bounds__(kSThreads, 1) step_kernel(const StepParams sp)
 #pragma unroll
           for (int j = 0; j < RR; ++j) {
             const int r = rb + tid + j * NT;
-            if (r < r1) {
+            if (r < r1 && in_bounds(sp.status, r < V)) {
               const float v = ((y[j][0] + y[j][1]) + (y[j][2] + y[j][3])) * inv;
               sp.logits[r] = v;
               if (v != v) nan = true;

@@ -360,15 +360,15 @@ class OracleCache:
 
 
 def greedy_run(model: OracleModel, prompt, n_steps: int, cap: int | None = None,
-               hidden: bool = False):
+               hidden: bool = False, kv: str = "bf16"):
     """prefill(prompt) -> t0 = argmax, then n_steps cached steps feeding back argmax.
 
     Returns tokens [n_steps+1], logits [n_steps+1][vocab] and, if asked, the
-    hidden states of every step.
+    hidden states of every step. kv: the cache's storage ("bf16" or "q8").
     """
     prompt = list(int(t) for t in prompt)
     cap = cap or (len(prompt) + n_steps + 1)
-    cache = model.new_cache(cap)
+    cache = model.new_cache(cap, kv)
     hids = []
     for t in prompt[:-1]:
         model.step(cache, t)
