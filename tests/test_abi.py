@@ -73,3 +73,16 @@ def test_build_command_targets_sm103a():
         assert "arch=compute_103a,code=sm_103a" in cmd and " -c " in cmd and "-O3" in cmd
     link = " ".join(bq.nvcc_link_command(["a.o", "b.o"], "x.so"))
     assert "arch=compute_103a,code=sm_103a" in link and "-shared" in link
+
+
+def test_flags_statuses_and_dtypes_match_the_header():
+    import re
+    text = open(bq.HEADER).read()
+    flags = {n: int(v, 0) for n, v in re.findall(r"^#define (LLM_[A-Z0-9_]+)\s+(0x[0-9a-fA-F]+|\d+)u", text, re.M)}
+    assert flags, "no flags found"
+    for name, value in flags.items():
+        assert getattr(bq, name) == value, name
+    statuses = {int(v): n for n, v in re.findall(r"(LLM_(?:OK|ERR_[A-Z_]+))\s*=\s*(-?\d+)", text)}
+    assert {k: v.replace("LLM_ERR_", "").replace("LLM_", "") for k, v in statuses.items()} == bq.STATUS
+    dtypes = dict(re.findall(r"(LLM_(?:F32|BF16|F16|Q4G64))\s*=\s*(\d+)", text))
+    assert dtypes and all(getattr(bq, n) == int(v) for n, v in dtypes.items())
