@@ -81,15 +81,30 @@ __device__ __forceinline__ void attn_q_frag(uint32_t (&qf)[4], const float* q, i
   qf[3] = pack_f16x2(l[2], l[3]);
 }
 
+// Offset (in halves) of dims 8c .. 8c+7 of row r of a K/V tile. Padded tiles
+// (BF = false): rows of RS > HD halves. Unpadded tiles (BF = true, rows of HD
+// halves): chunk c of row r sits at chunk c ^ (r & 7), so the 8 rows of an
+// ldmatrix fetch still hit distinct bank groups.
+template <int HD, int RS, bool BF>
+__device__ __forceinline__ int tile_off(int r, int c) {
+  if constexpr (BF) return r * HD + 8 * (c ^ (r & 7));
+  else return r * RS + 8 * c;
+}
+
 // One warp, the GQ heads of q ([GQ][HD], scaled) against the 16 staged rows
 // row0 .. row0+15 (rows at or beyond `nvalid` are zero-filled and masked).
 // Scores are in the log2 domain (q carries log2(e)/sqrt(hd)). Lane (head
 // g = lane/4 < GQ, t = lane%4) writes to out[g*OS ..]: o at dims 8nt+2t(+1)
 // (sum over the 16 positions of 2^(s - m) v), and lane t = 0 writes m (max
 // score) at [HD] and l (sum of 2^(s - m)) at [HD+1].
-template <int GQ, int HD, int RS>
+// BF = false: the tiles hold fp16 rows, padded to RS halves. BF = true: they
+// hold the cache's bf16 rows as they are (tile_off's permuted chunks), and
+// every fragment is converted to fp16 in registers after its ldmatrix: the
+// same fp16 operands as the padded path.
+template <int GQ, int HD, int RS, bool BF = false>
 __device__ __forceinline__ void attn_block16(const float* q, const uint16_t* kt, const uint16_t* vt, int row0,
                                              int nvalid, int lane, float* out, int OS) {
+  static_assert(!BF || RS == HD, "bf16 tiles are unpadded");
   const int g = lane >> 2, t = lane & 3, r8 = lane & 7, mi = lane >> 3;
   float s[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
 #pragma unroll
@@ -98,7 +113,10 @@ __device__ __forceinline__ void attn_block16(const float* q, const uint16_t* kt,
     attn_q_frag<GQ, HD>(qf, q, ks, lane);
     // matrices: positions 0-7 / 8-15 (n-tile j = mi/2) x dims 16ks + 8*(mi%2) .. +7
     uint32_t b[4];
-    ldsm_x4(b, kt + (size_t)(row0 + 8 * (mi >> 1) + r8) * RS + 16 * ks + 8 * (mi & 1));
+    ldsm_x4(b, kt + tile_off<HD, RS, BF>(row0 + 8 * (mi >> 1) + r8, 2 * ks + (mi & 1)));
+    if constexpr (BF)
+#pragma unroll
+      for (int i = 0; i < 4; ++i) b[i] = bf16x2_to_f16x2(b[i]);
     mma_f16_16816(s[0], qf, b[0], b[1]);
     mma_f16_16816(s[1], qf, b[2], b[3]);
   }
@@ -132,7 +150,10 @@ __device__ __forceinline__ void attn_block16(const float* q, const uint16_t* kt,
   for (int nt = 0; nt < HD / 8; nt += 2) {
     // matrices (transposed): positions 8*(mi%2) .. +7 x dims 8*(nt + mi/2) .. +7
     uint32_t b[4];
-    ldsm_x4_t(b, vt + (size_t)(row0 + 8 * (mi & 1) + r8) * RS + 8 * (nt + (mi >> 1)));
+    ldsm_x4_t(b, vt + tile_off<HD, RS, BF>(row0 + 8 * (mi & 1) + r8, nt + (mi >> 1)));
+    if constexpr (BF)
+#pragma unroll
+      for (int i = 0; i < 4; ++i) b[i] = bf16x2_to_f16x2(b[i]);
     float d0[4] = {0.f, 0.f, 0.f, 0.f}, d1[4] = {0.f, 0.f, 0.f, 0.f};
     mma_f16_16816(d0, pa, b[0], b[1]);
     mma_f16_16816(d1, pa, b[2], b[3]);

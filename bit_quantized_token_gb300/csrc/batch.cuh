@@ -18,6 +18,8 @@
 // adds the partials in CTA order and runs the epilogue (store, residual,
 // SwiGLU, or logits with the per-sequence greedy choice).
 #pragma once
+#include <type_traits>
+
 #include "kernels.cuh"
 #include "attn_mma.cuh"
 
@@ -436,6 +438,280 @@ __global__ void __launch_bounds__(kBThreads, 2) bgemv_kernel(const BGemvParams p
   if (tid == 0) *p.gcounter = 0;
 }
 
+// ---- the batched LM head over a bf16 table (the tied embedding) ------------
+// Persistent: one CTA per SM walks a contiguous range of row tiles with the
+// 32-token input staged once for the whole launch (RMSNorm applied, split
+// into bf16 high parts and remainders, resident in shared memory). Consumer
+// warp w owns row tile w of each group of kHWarps and accumulates it over all
+// of K (both 16-row halves share the input fragments). A producer warp
+// streams the group's units through a ring of kHSlots slots (kHUC units of
+// every row tile of the group per slot), running ahead across groups. Each
+// warp stores its row tile's logits when it finishes it and keeps the best
+// logit of each token; the CTA's best goes to cand_v/cand_i[token][CTA], and
+// the last CTA to arrive picks each sequence's greedy choice.
+constexpr int kHWarps = 8;                        // consumer warps = row tiles in flight
+constexpr int kHThreads = (kHWarps + 1) * 32;     // + the producer warp
+constexpr int kHUC = 2;                           // units of each row tile per ring slot
+constexpr int kHSlots = 5;
+constexpr int kHUnitBytes = 32 * kBF16UnitCols * 2;
+constexpr size_t kHSlotBytes = (size_t)kHWarps * kHUC * kHUnitBytes;
+
+// Dynamic shared memory: the ring, then the inputs [64][K+8] halves.
+__host__ __device__ inline size_t bhead_smem_bytes(int K) {
+  return (size_t)kHSlots * kHSlotBytes + (size_t)2 * kBM * (K + 8) * 2;
+}
+
+__device__ __forceinline__ void consumers_sync() {  // the kHWarps consumer warps only
+  asm volatile("bar.sync 1, %0;" ::"n"(kHWarps * 32) : "memory");
+}
+
+__global__ void __launch_bounds__(kHThreads, 1) bhead_kernel(const BGemvParams p) {
+  extern __shared__ __align__(128) uint8_t smem[];
+  __shared__ uint64_t s_full[kHSlots], s_empty[kHSlots];
+  __shared__ float s_inv[kBM];
+  __shared__ float s_bv[kHWarps][kBM];
+  __shared__ int s_bi[kHWarps][kBM];
+  __shared__ int s_last, s_fail;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int XS = p.K + 8;  // staged input row (halves): conflict-free ldmatrix rows
+  uint8_t* ring = smem;
+  uint16_t* xh = reinterpret_cast<uint16_t*>(smem + (size_t)kHSlots * kHSlotBytes);
+  const int nc = gridDim.x, c = blockIdx.x;
+  const int rt_a = (int)((int64_t)p.n_rt * c / nc), rt_b = (int)((int64_t)p.n_rt * (c + 1) / nc);
+  const int n_groups = (rt_b - rt_a + kHWarps - 1) / kHWarps;
+  if (tid == 0) {
+    for (int i = 0; i < kHSlots; ++i) {
+      mbar_init(&s_full[i], 1);
+      mbar_init(&s_empty[i], kHWarps);
+    }
+    mbar_fence_init();
+    s_fail = 0;
+  }
+  __syncthreads();
+
+  if (warp == kHWarps) {  // ---- producer: weights only (no wait on the previous kernel)
+    if (lane == 0) {
+      const uint64_t pol = policy_evict_first();
+      int ci = 0;
+      for (int gi = 0; gi < n_groups; ++gi) {
+        const int rt0 = rt_a + gi * kHWarps, nrt = min(kHWarps, rt_b - rt0);
+        for (int u0 = 0; u0 < p.G; u0 += kHUC, ++ci) {
+          const int slot = ci % kHSlots;
+          if (ci >= kHSlots) {
+            if (!mbar_wait_spin(&s_empty[slot], ((ci / kHSlots) - 1) & 1, p.status)) return;
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // the consumers' reads of the slot
+          }
+          mbar_expect_tx(&s_full[slot], (uint32_t)(nrt * kHUC * kHUnitBytes));
+          for (int r = 0; r < nrt; ++r) {
+            const bool okc = in_bounds(p.status, rt0 + r < p.n_rt && u0 + kHUC <= p.G);
+            bulk_g2s(ring + slot * kHSlotBytes + (size_t)r * kHUC * kHUnitBytes,
+                     p.units + (okc ? ((size_t)(rt0 + r) * p.G + u0) * kHUnitBytes : 0), kHUC * kHUnitBytes,
+                     &s_full[slot], pol);
+          }
+        }
+      }
+    }
+    return;
+  }
+
+  // ---- consumers: RMSNorm factor per token from the producer's partial sums
+  // of squares (thread: token tid % 32, partials tid/32, +8, ...; fixed order)
+  pdl_trigger();
+  pdl_wait();
+  if (p.norm_w) {
+    const int m = tid & 31, sub = tid >> 5;
+    float v[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) v[j] = ldcg1_if(p.ss_in + (size_t)(sub + 8 * j) * kBM + m, sub + 8 * j < p.ss_n);
+    float ss = ((v[0] + v[1]) + (v[2] + v[3])) + ((v[4] + v[5]) + (v[6] + v[7]));
+    for (int b = sub + 64; b < p.ss_n; b += 8) ss += __ldcg(p.ss_in + (size_t)b * kBM + m);  // > 64 partials
+    s_bv[sub][m] = ss;
+    consumers_sync();
+    if (tid < kBM) {
+      float t = 0.f;
+#pragma unroll
+      for (int w = 0; w < kHWarps; ++w) t += s_bv[w][tid];
+      s_inv[tid] = 1.0f / sqrtf(t / (float)p.K + p.eps);
+    }
+    consumers_sync();
+  }
+  // the whole input, once: x * inv * w -> bf16 high part (row m) and remainder (row 32 + m)
+  {
+    const int k4n = p.K / 4;
+    constexpr int UN = 8;  // loads in flight per thread
+    for (int i0 = tid; i0 < kBM * k4n; i0 += UN * kHWarps * 32) {
+      float4 xv[UN], wv[UN];
+#pragma unroll
+      for (int j = 0; j < UN; ++j) {
+        const int i = i0 + j * kHWarps * 32, m = i / k4n, k4 = i - m * k4n;
+        xv[j] = ldcg4_if(p.x + (size_t)m * p.K + 4 * k4, i < kBM * k4n && m < p.M);
+        wv[j] = ldnc4_if(p.norm_w ? p.norm_w + 4 * k4 : nullptr, p.norm_w != nullptr && i < kBM * k4n);
+      }
+#pragma unroll
+      for (int j = 0; j < UN; ++j) {
+        const int i = i0 + j * kHWarps * 32, m = i / k4n, k4 = i - m * k4n;
+        if (i >= kBM * k4n) continue;
+        float4 v = xv[j];
+        if (p.norm_w) {
+          const float inv = m < p.M ? s_inv[m] : 0.f;
+          v = make_float4(v.x * inv * wv[j].x, v.y * inv * wv[j].y, v.z * inv * wv[j].z, v.w * inv * wv[j].w);
+        }
+        const float hx = __bfloat162float(__float2bfloat16_rn(v.x)), hy = __bfloat162float(__float2bfloat16_rn(v.y));
+        const float hz = __bfloat162float(__float2bfloat16_rn(v.z)), hw = __bfloat162float(__float2bfloat16_rn(v.w));
+        *reinterpret_cast<uint2*>(xh + (size_t)m * XS + 4 * k4) =
+            make_uint2(pack_bf16x2(hx, hy), pack_bf16x2(hz, hw));
+        *reinterpret_cast<uint2*>(xh + (size_t)(kBM + m) * XS + 4 * k4) =
+            make_uint2(pack_bf16x2(v.x - hx, v.y - hy), pack_bf16x2(v.z - hz, v.w - hw));
+      }
+    }
+  }
+  consumers_sync();
+
+  // lane (g, t): rows 16h + g (+8) of its row tile, tokens 8nt + 2t + e; the
+  // accumulators hold the high-part columns (nt < 4) and the remainders (nt >= 4)
+  const int g = lane >> 2, t = lane & 3, r8 = lane & 7, mi = lane >> 3;
+  float bv[4][2];
+  int bi[4][2];
+#pragma unroll
+  for (int nt = 0; nt < 4; ++nt)
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+      bv[nt][e] = -INFINITY;
+      bi[nt][e] = 0x7fffffff;
+    }
+  bool ok = true, nan = false;
+  int ci = 0;
+  for (int gi = 0; gi < n_groups; ++gi) {
+    const int rt = rt_a + gi * kHWarps + warp;
+    const bool mine = rt < rt_b;
+    float d[2][8][4];
+#pragma unroll
+    for (int h = 0; h < 2; ++h)
+#pragma unroll
+      for (int nt = 0; nt < 8; ++nt) d[h][nt][0] = d[h][nt][1] = d[h][nt][2] = d[h][nt][3] = 0.f;
+    for (int u0 = 0; u0 < p.G; u0 += kHUC, ++ci) {
+      const int slot = ci % kHSlots;
+      if (ok) ok = mbar_wait_spin(&s_full[slot], (ci / kHSlots) & 1, p.status);
+      if (ok && mine) {
+        const uint8_t* wb = ring + slot * kHSlotBytes + (size_t)warp * kHUC * kHUnitBytes;
+#pragma unroll
+        for (int uu = 0; uu < kHUC; ++uu) {
+          uint32_t bx[4][4];
+#pragma unroll
+          for (int q = 0; q < 4; ++q)
+            ldsm_x4(bx[q], xh + (size_t)(8 * (2 * q + (mi >> 1)) + r8) * XS + (u0 + uu) * kBF16UnitCols + 8 * (mi & 1));
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            // bf16 unit [k half][row][8 k]: the A fragment of rows 16h .. 16h+15 is one ldmatrix
+            uint32_t a[4];
+            ldsm_x4(a, wb + (size_t)uu * kHUnitBytes + ((mi >> 1) * 32 + 16 * h + 8 * (mi & 1) + r8) * 16);
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              mma_bf16_16816(d[h][2 * q], a, bx[q][0], bx[q][1]);
+              mma_bf16_16816(d[h][2 * q + 1], a, bx[q][2], bx[q][3]);
+            }
+          }
+        }
+      }
+      __syncwarp();
+      if (ok && lane == 0) mbar_arrive(&s_empty[slot]);
+    }
+    if (!ok || !mine) continue;
+    // this row tile's logits (4 tokens x 8 consecutive rows per store: whole 32-B sectors)
+#pragma unroll
+    for (int h = 0; h < 2; ++h)
+#pragma unroll
+      for (int hh = 0; hh < 2; ++hh) {
+        const int row = rt * 32 + 16 * h + 8 * hh + g;
+#pragma unroll
+        for (int nt = 0; nt < 4; ++nt)
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            const int mm = 8 * nt + 2 * t + e;
+            const float y = d[h][nt][2 * hh + e] + d[h][nt + 4][2 * hh + e];
+            if (mm >= p.M || row >= p.rows) continue;
+            p.out[(size_t)mm * p.out_cols + row] = y;
+            if (y != y) nan = true;
+            else if (better(y, row, bv[nt][e], bi[nt][e])) {
+              bv[nt][e] = y;
+              bi[nt][e] = row;
+            }
+          }
+      }
+  }
+  // ---- greedy choice: best per token over the lanes of a warp, the warps, then the CTAs
+  if (!ok) s_fail = 1;
+  if (nan) atomicOr(p.status, ST_NAN);
+#pragma unroll
+  for (int nt = 0; nt < 4; ++nt)
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+#pragma unroll
+      for (int o = 4; o < 32; o <<= 1) {  // lanes of equal t hold the same tokens
+        const float ov = __shfl_xor_sync(0xffffffffu, bv[nt][e], o);
+        const int oi = __shfl_xor_sync(0xffffffffu, bi[nt][e], o);
+        if (better(ov, oi, bv[nt][e], bi[nt][e])) {
+          bv[nt][e] = ov;
+          bi[nt][e] = oi;
+        }
+      }
+      if (g == 0) {
+        s_bv[warp][8 * nt + 2 * t + e] = bv[nt][e];
+        s_bi[warp][8 * nt + 2 * t + e] = bi[nt][e];
+      }
+    }
+  consumers_sync();
+  if (s_fail) return;  // every consumer warp has passed its last barrier; the status word says why
+  const int n_blocks = nc;
+  if (warp == 0) {
+    float b2 = -INFINITY;
+    int i2 = 0x7fffffff;
+#pragma unroll
+    for (int w = 0; w < kHWarps; ++w)
+      if (better(s_bv[w][lane], s_bi[w][lane], b2, i2)) {
+        b2 = s_bv[w][lane];
+        i2 = s_bi[w][lane];
+      }
+    p.cand_v[(size_t)lane * n_blocks + c] = b2;
+    p.cand_i[(size_t)lane * n_blocks + c] = i2;
+  }
+  __threadfence();
+  consumers_sync();
+  if (tid == 0) s_last = atomicAdd(p.gcounter, 1) == n_blocks - 1;
+  consumers_sync();
+  if (!s_last) return;
+  __threadfence();
+  // warp w handles sequences w, w+8, ...; lanes stride over the CTAs
+  for (int q = warp; q < p.M; q += kHWarps) {
+    float b2 = -INFINITY;
+    int i2 = 0x7fffffff;
+    for (int k = lane; k < n_blocks; k += 32) {
+      const float v = __ldcg(p.cand_v + (size_t)q * n_blocks + k);
+      const int ix = __ldcg(p.cand_i + (size_t)q * n_blocks + k);
+      if (better(v, ix, b2, i2)) {
+        b2 = v;
+        i2 = ix;
+      }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const float ov = __shfl_xor_sync(0xffffffffu, b2, o);
+      const int oi = __shfl_xor_sync(0xffffffffu, i2, o);
+      if (better(ov, oi, b2, i2)) {
+        b2 = ov;
+        i2 = oi;
+      }
+    }
+    if (lane == 0) {
+      if (i2 < 0 || i2 >= p.rows) i2 = 0;  // every logit NaN (status already says so)
+      p.argmax_out[q] = i2;
+      p.tok_io[q] = i2;
+      p.pos[q] = p.pos[q] + 1;
+    }
+  }
+  if (tid == 0) *p.gcounter = 0;
+}
+
 // x[m][:] = embedding row of token[m] (fp32 or bf16 table)
 struct BEmbedParams {
   const void* embed;
@@ -499,6 +775,9 @@ struct BAttnParams {
 #define LLMQ_BATTN_SPLITS 8  // measured on the 32-sequence workload: 24 -> 8791, 12 -> 9115, 8 -> 9274, 4 -> 9005 tok/s
 #endif
 static_assert(LLMQ_BATTN_SPLITS >= 1 && LLMQ_BATTN_SPLITS <= 24, "splits of a batched attention item");
+#ifndef LLMQ_BATTN_SPLIT_LEN
+#define LLMQ_BATTN_SPLIT_LEN 256  // bf16 cache: cached positions per split (at most 24 splits)
+#endif
 constexpr int kBAttnThreads = 256;
 constexpr int kBAttnPP = 64;  // cache positions per pass (~42 KB of tiles: 4 CTAs per SM)
 
@@ -517,17 +796,39 @@ struct BAttnSmem {
   float cursc[2][HD / 32];        // int8 K/V: this step's k, v group scales (cur then holds their codes)
   int is_last;
 };
+// The same over the bf16 cache: each warp streams its own blocks of 16
+// positions through a private stage (bf16 rows as cached, unpadded, chunks
+// permuted by tile_off) and keeps its own running softmax state, so no CTA
+// barrier separates two blocks (~75 KB for Qwen3's GQ 2, hd 128: 3 CTAs per SM).
+template <int GQ, int HD>
+struct BAttnWarpSmem {
+  static constexpr int NW = kBAttnThreads / 32, RS = HD;
+  uint16_t kt[NW][16][HD];
+  uint16_t vt[NW][16][HD];
+  float cur[GQ + 2][HD];          // q heads (scaled), k, v of this step
+  float tres[NW][GQ][HD + 2];     // per warp: the block's o, max, sum; at the end the warp's state
+  int is_last;
+};
+template <int GQ, int HD, bool KV8>
+using BAttnSmemT = std::conditional_t<KV8, BAttnSmem<GQ, HD>, BAttnWarpSmem<GQ, HD>>;
 
 // Flash-decoding attention of every sequence of the batch on the tensor
 // cores: grid (split, kv head, sequence), 8 warps that stage the pass's K/V
 // rows together; warp w < PP/16 scores all GQ heads against positions
 // 16w .. 16w+15 (attn_mma.cuh). The last split of a (sequence, kv head) to
 // finish merges the splits into the output row.
+//   bf16 cache: splits of LLMQ_BATTN_SPLIT_LEN positions; warp w takes
+//   blocks w, w+8, ... of 16 positions, each copied into its private stage as
+//   cached (converted to fp16 fragment by fragment in attn_block16), folds
+//   them into its own (max, sum, o), and requests its next block as soon as
+//   the stage has been read. The 8 warp states merge once per split.
+//   int8 cache: passes of 64 positions in one CTA-wide stage, widened to
+//   fp16 in place after its copies land; warp w < 4 scores 16 of them.
 template <int GQ, int HD, bool KV8>
 __global__ void __launch_bounds__(kBAttnThreads) battn_mma_kernel(const BAttnParams bp) {
-  using SA = BAttnSmem<GQ, HD>;
-  constexpr int NT = kBAttnThreads, PP = SA::PP, RS = SA::RS, CH = HD / 8, DPL = HD / 32, NG = HD / 32;
-  static_assert(GQ <= 8 && SA::NBW <= NT / 32, "layout");
+  using SA = BAttnSmemT<GQ, HD, KV8>;
+  constexpr int NT = kBAttnThreads, PP = kBAttnPP, RS = SA::RS, CH = HD / 8, DPL = HD / 32, NG = HD / 32;
+  static_assert(GQ <= 8 && PP / 16 <= NT / 32, "layout");
   extern __shared__ __align__(16) uint8_t smraw[];
   SA& sa = *reinterpret_cast<SA*>(smraw);
   pdl_trigger();
@@ -542,7 +843,8 @@ __global__ void __launch_bounds__(kBAttnThreads) battn_mma_kernel(const BAttnPar
   }
   const int len = pos + 1;
   constexpr int PMAX = 24;  // merge scratch: splits a (sequence, kv head) may have (LLMQ_BATTN_SPLITS <= PMAX)
-  const int P_eff = min(min(a.P, LLMQ_BATTN_SPLITS), (len + PP - 1) / PP);
+  const int P_eff = KV8 ? min(min(a.P, LLMQ_BATTN_SPLITS), (len + PP - 1) / PP)
+                       : min(min(a.P, PMAX), (len + LLMQ_BATTN_SPLIT_LEN - 1) / LLMQ_BATTN_SPLIT_LEN);
   if (split >= P_eff) return;
   const int t0 = (int)((int64_t)len * split / P_eff), t1 = (int)((int64_t)len * (split + 1) / P_eff);
   const int sb = bp.seq ? bp.seq[b] : b;  // this row's cache
@@ -558,11 +860,12 @@ __global__ void __launch_bounds__(kBAttnThreads) battn_mma_kernel(const BAttnPar
   const float* qkv = bp.qkv + (size_t)b * bp.qkv_cols;
 
   // rows tp .. tp+n-1 of K and V -> tiles (async copies; zero rows up to the
-  // next multiple of 16), then bf16 -> fp16 in place by the same threads
+  // next multiple of 16): stage bi of the bf16 cache's two, or the int8
+  // cache's one stage, which convert then widens to fp16 in place
   static_assert((CH & (CH - 1)) == 0, "16-B chunks per row: a power of two");
   constexpr int LCH = CH == 8 ? 3 : 4;
-  auto stage = [&](int tp) {
-    const int n = min(PP, t1 - tp), rows = ((n + 15) / 16) * 16;
+  auto stage = [&](int tp, int bi) {
+    const int n = min(PP, t1 - tp);
     if constexpr (KV8) {
       // 16-byte chunks of codes into the first HD bytes of each row's fp16
       // slot (widened in convert), one row's scales per thread
@@ -577,21 +880,17 @@ __global__ void __launch_bounds__(kBAttnThreads) battn_mma_kernel(const BAttnPar
       const int kv = tid / PP, row = tid - kv * PP;
       if (kv < 2 && row < n)
         cp_async_small<2 * NG>(&(kv ? sa.vsc : sa.ksc)[row][0], (kv ? vs8 : ks8) + (size_t)(tp + row) * NG);
-    } else {
-#pragma unroll
-      for (int kv = 0; kv < 2; ++kv) {
-        uint16_t(*tile)[RS] = kv ? sa.vt : sa.kt;
-        const uint16_t* src = (kv ? vc : kc) + (size_t)tp * HD;
-        for (int idx = tid; idx < rows * CH; idx += NT) {
-          const int row = idx >> LCH, ch = idx & (CH - 1);
-          if (row < n && in_bounds(a.status, tp + row < a.cap))
-            cp_async16(&tile[row][8 * ch], src + (size_t)row * HD + 8 * ch);
-          else *reinterpret_cast<uint4*>(&tile[row][8 * ch]) = make_uint4(0u, 0u, 0u, 0u);
-        }
+    } else {  // the warp's block of 16 rows from tp into its stage bi (= the warp)
+      for (int idx = lane; idx < 2 * 16 * CH; idx += 32) {
+        const int kv = idx >= 16 * CH, r = idx - kv * 16 * CH, row = r >> LCH, ch = r & (CH - 1);
+        uint16_t* dst = (kv ? &sa.vt[bi][0][0] : &sa.kt[bi][0][0]) + tile_off<HD, HD, true>(row, ch);
+        if (row < n && in_bounds(a.status, tp + row < a.cap))
+          cp_async16(dst, (kv ? vc : kc) + (size_t)(tp + row) * HD + 8 * ch);
+        else *reinterpret_cast<uint4*>(dst) = make_uint4(0u, 0u, 0u, 0u);
       }
     }
   };
-  auto convert = [&](int tp) {
+  auto convert = [&](int tp) {  // the int8 cache's stage
     const int n = min(PP, t1 - tp), rows = ((n + 15) / 16) * 16;
     cp_async_wait_all();
     if constexpr (KV8) {
@@ -631,19 +930,12 @@ __global__ void __launch_bounds__(kBAttnThreads) battn_mma_kernel(const BAttnPar
       if (kv < 2 && row >= n && row < rows)
 #pragma unroll
         for (int k = 0; k < NG; ++k) (kv ? sa.vsc : sa.ksc)[row][k] = 0;
-    } else {
-#pragma unroll
-      for (int kv = 0; kv < 2; ++kv) {
-        uint16_t(*tile)[RS] = kv ? sa.vt : sa.kt;
-        for (int idx = tid; idx < rows * CH; idx += NT) {
-          uint4* q = reinterpret_cast<uint4*>(&tile[idx >> LCH][8 * (idx & (CH - 1))]);
-          const uint4 w = *q;
-          *q = make_uint4(bf16x2_to_f16x2(w.x), bf16x2_to_f16x2(w.y), bf16x2_to_f16x2(w.z), bf16x2_to_f16x2(w.w));
-        }
-      }
     }
   };
-  if (attend) stage(t0);
+  if (attend) {
+    if constexpr (KV8) stage(t0, 0);
+    else if (t0 + 16 * warp < t1) stage(t0 + 16 * warp, warp);  // each warp's first block, during the prologue
+  }
   // q heads, k, v of this kv head; RoPE factors and q/k norm weights
   for (int i = tid; i < (GQ + 2) * HD; i += NT) {
     const int r = i / HD, d = i % HD;
@@ -660,7 +952,8 @@ __global__ void __launch_bounds__(kBAttnThreads) battn_mma_kernel(const BAttnPar
       const int h = warp + 8 * k2;
       wn[k2][e] = (a.q_norm && h <= GQ) ? __ldg((h < GQ ? a.q_norm : a.k_norm) + lane + 32 * e) : 1.f;
     }
-  if (attend) convert(t0);
+  if constexpr (KV8)
+    if (attend) convert(t0);
   __syncthreads();
   if (a.q_norm) {  // per-head RMSNorm of the q heads and k
 #pragma unroll
@@ -690,13 +983,12 @@ __global__ void __launch_bounds__(kBAttnThreads) battn_mma_kernel(const BAttnPar
   auto keep = [&](int r, int d, float x) {
     if constexpr (KV8) {  // quantized per 32-element group below
       sa.cur[r][d] = x;
-      return;
+    } else {  // the pass holding `pos` puts the row into its stage once its copies have landed
+      const __nv_bfloat16 h = __float2bfloat16_rn(x);
+      sa.cur[r][d] = __bfloat162float(h);
+      if (append && in_bounds(a.status, pos < a.cap))
+        (r == GQ ? kc : vc)[(size_t)pos * HD + d] = __bfloat16_as_ushort(h);
     }
-    const __nv_bfloat16 h = __float2bfloat16_rn(x);
-    const float xr = __bfloat162float(h);
-    sa.cur[r][d] = xr;
-    if (append && in_bounds(a.status, pos < a.cap)) (r == GQ ? kc : vc)[(size_t)pos * HD + d] = __bfloat16_as_ushort(h);
-    if (owner) (r == GQ ? sa.kt : sa.vt)[pos - t0][d] = __half_as_ushort(__float2half_rn(xr));
   };
   for (int j = tid; j < nrope + HD; j += NT) {  // RoPE pairs of the q heads and k, then v elements
     if (j < nrope) {
@@ -744,83 +1036,160 @@ __global__ void __launch_bounds__(kBAttnThreads) battn_mma_kernel(const BAttnPar
     }
   }
   if (!attend) return;  // the rows' k, v are in the cache
-  for (int i = tid; i < GQ * HD; i += NT) sa.acc[i / HD][i % HD] = 0.f;
-  if (tid < GQ) {
-    sa.accm[tid] = -INFINITY;
-    sa.accl[tid] = 0.f;
-  }
-  __syncthreads();
-
   float* gpart = a.part + (size_t)b * bp.part_stride + (((size_t)g * a.P + split) * GQ) * (HD + 2);
-  for (int tp = t0; tp < t1; tp += PP) {
-    const int n = min(PP, t1 - tp), nb = (n + 15) / 16;
-    if (tp != t0) {
-      stage(tp);
-      convert(tp);
-      __syncthreads();
-      if (pos >= tp && pos < tp + n) {
-        for (int d = tid; d < HD; d += NT) {
-          sa.kt[pos - tp][d] = __half_as_ushort(__float2half_rn(sa.cur[GQ][d]));
-          sa.vt[pos - tp][d] = __half_as_ushort(__float2half_rn(sa.cur[GQ + 1][d]));
-        }
-        if constexpr (KV8)
+  if constexpr (KV8) {
+    for (int i = tid; i < GQ * HD; i += NT) sa.acc[i / HD][i % HD] = 0.f;
+    if (tid < GQ) {
+      sa.accm[tid] = -INFINITY;
+      sa.accl[tid] = 0.f;
+    }
+    __syncthreads();
+    for (int tp = t0; tp < t1; tp += PP) {
+      const int n = min(PP, t1 - tp), nb = (n + 15) / 16;
+      if (tp != t0) {
+        stage(tp, 0);
+        convert(tp);
+        __syncthreads();
+        if (pos >= tp && pos < tp + n) {
+          for (int d = tid; d < HD; d += NT) {
+            sa.kt[pos - tp][d] = __half_as_ushort(__float2half_rn(sa.cur[GQ][d]));
+            sa.vt[pos - tp][d] = __half_as_ushort(__float2half_rn(sa.cur[GQ + 1][d]));
+          }
           if (tid < 2 * NG)
             (tid < NG ? sa.ksc : sa.vsc)[pos - tp][tid % NG] =
                 __half_as_ushort(__float2half_rn(sa.cursc[tid / NG][tid % NG]));
+        }
+        __syncthreads();
       }
-      __syncthreads();
-    }
-    if (warp < nb) {
-      if constexpr (KV8)
+      if (warp < nb)
         attn_block16_q8<GQ, HD, RS>(&sa.cur[0][0], &sa.kt[0][0], &sa.vt[0][0], &sa.ksc[0][0], &sa.vsc[0][0],
                                     16 * warp, n - 16 * warp, lane, &sa.tres[warp][0][0], HD + 2);
-      else
-        attn_block16<GQ, HD, RS>(&sa.cur[0][0], &sa.kt[0][0], &sa.vt[0][0], 16 * warp, n - 16 * warp, lane,
-                                 &sa.tres[warp][0][0], HD + 2);
-    }
-    __syncthreads();
-    // fold the pass into the running output. Warp h < GQ finds head h's
-    // factors, lane w < nb for block w: new max, 2^(m_w - M), sum update
-    if (warp < GQ) {
-      const int h = warp;
-      const float am = sa.accm[h], al = sa.accl[h];
-      const float mw = lane < nb ? sa.tres[lane][h][HD] : -INFINITY;
-      const float lw = lane < nb ? sa.tres[lane][h][HD + 1] : 0.f;
-      float M = fmaxf(mw, am);
+      __syncthreads();
+      // fold the pass into the running output. Warp h < GQ finds head h's
+      // factors, lane w < nb for block w: new max, 2^(m_w - M), sum update
+      if (warp < GQ) {
+        const int h = warp;
+        const float am = sa.accm[h], al = sa.accl[h];
+        const float mw = lane < nb ? sa.tres[lane][h][HD] : -INFINITY;
+        const float lw = lane < nb ? sa.tres[lane][h][HD + 1] : 0.f;
+        float M = fmaxf(mw, am);
 #pragma unroll
-      for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
-      const float f = lane < nb ? exp2f(mw - M) : 0.f;
-      float L = lw * f;
+        for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+        const float f = lane < nb ? exp2f(mw - M) : 0.f;
+        float L = lw * f;
 #pragma unroll
-      for (int o = 16; o > 0; o >>= 1) L += __shfl_xor_sync(0xffffffffu, L, o);
-      const float fa = am == -INFINITY ? 0.f : exp2f(am - M);
-      __syncwarp();
-      if (lane < SA::NBW) sa.fac[h][1 + lane] = f;
-      if (lane == 0) {
-        sa.fac[h][0] = fa;
-        sa.accm[h] = M;
-        sa.accl[h] = al * fa + L;
+        for (int o = 16; o > 0; o >>= 1) L += __shfl_xor_sync(0xffffffffu, L, o);
+        const float fa = am == -INFINITY ? 0.f : exp2f(am - M);
+        __syncwarp();
+        if (lane < SA::NBW) sa.fac[h][1 + lane] = f;
+        if (lane == 0) {
+          sa.fac[h][0] = fa;
+          sa.accm[h] = M;
+          sa.accl[h] = al * fa + L;
+        }
       }
+      __syncthreads();
+      const bool last_pass = tp + PP >= t1;
+      for (int i = tid; i < GQ * HD; i += NT) {
+        const int h = i / HD, d = i % HD;
+        float O = sa.acc[h][d] * sa.fac[h][0];
+#pragma unroll
+        for (int w = 0; w < SA::NBW; ++w)
+          if (w < nb) O += sa.tres[w][h][d] * sa.fac[h][1 + w];
+        if (last_pass) {  // the split's partial: o, max, sum
+          gpart[h * (HD + 2) + d] = O;
+          if (d == 0) {
+            gpart[h * (HD + 2) + HD] = sa.accm[h];
+            gpart[h * (HD + 2) + HD + 1] = sa.accl[h];
+          }
+        } else {
+          sa.acc[h][d] = O;
+        }
+      }
+      // the next pass writes its tiles and blocks after the barriers of its staging
+    }
+  } else {
+    // ---- warp w: blocks w, w + NW, ... of the split, each folded into the
+    // warp's running (max, sum) per head and its share of o: lane holds
+    // elements lane + 32e of the [GQ][HD] output
+    constexpr int NW = SA::NW, OE = GQ * HD / 32;
+    static_assert(GQ * HD % 32 == 0, "output elements per lane");
+    __syncthreads();  // q, k, v of this step (cur) are complete
+    float* wt = &sa.tres[warp][0][0];
+    float m_run[GQ], l_run[GQ], o_run[OE];
+#pragma unroll
+    for (int h = 0; h < GQ; ++h) {
+      m_run[h] = -INFINITY;
+      l_run[h] = 0.f;
+    }
+#pragma unroll
+    for (int e = 0; e < OE; ++e) o_run[e] = 0.f;
+    for (int tp = t0 + 16 * warp; tp < t1; tp += 16 * NW) {
+      const int n = min(16, t1 - tp);
+      cp_async_wait_all();
+      __syncwarp();
+      if (pos >= tp && pos < tp + n) {  // this step's k, v row (its copy from the cache may predate the append)
+        for (int i = lane; i < 2 * HD; i += 32) {
+          const int kv = i >= HD, d = i - kv * HD;
+          (kv ? &sa.vt[warp][0][0] : &sa.kt[warp][0][0])[tile_off<HD, HD, true>(pos - tp, d >> 3) + (d & 7)] =
+              (uint16_t)(__float_as_uint(sa.cur[GQ + kv][d]) >> 16);  // bf16-exact value
+        }
+        __syncwarp();
+      }
+      attn_block16<GQ, HD, HD, true>(&sa.cur[0][0], &sa.kt[warp][0][0], &sa.vt[warp][0][0], 0, n, lane, wt, HD + 2);
+      __syncwarp();  // the stage has been read and the block's results written
+      if (tp + 16 * NW < t1) stage(tp + 16 * NW, warp);
+      float fr[GQ], fb[GQ];
+#pragma unroll
+      for (int h = 0; h < GQ; ++h) {
+        const float mb = wt[h * (HD + 2) + HD], lb = wt[h * (HD + 2) + HD + 1];
+        const float M = fmaxf(m_run[h], mb);
+        fr[h] = m_run[h] == -INFINITY ? 0.f : exp2f(m_run[h] - M);
+        fb[h] = exp2f(mb - M);
+        l_run[h] = l_run[h] * fr[h] + lb * fb[h];
+        m_run[h] = M;
+      }
+#pragma unroll
+      for (int e = 0; e < OE; ++e) {
+        const int i = lane + 32 * e, h = i / HD, d = i % HD;
+        o_run[e] = o_run[e] * fr[h] + wt[h * (HD + 2) + d] * fb[h];
+      }
+      __syncwarp();  // the next block's results overwrite wt
+    }
+    // the warps' states -> tres, then the split's partial (warps in order)
+#pragma unroll
+    for (int e = 0; e < OE; ++e) {
+      const int i = lane + 32 * e;
+      wt[(i / HD) * (HD + 2) + i % HD] = o_run[e];
+    }
+    if (lane < GQ) {
+#pragma unroll
+      for (int h = 0; h < GQ; ++h)
+        if (h == lane) {
+          wt[h * (HD + 2) + HD] = m_run[h];
+          wt[h * (HD + 2) + HD + 1] = l_run[h];
+        }
     }
     __syncthreads();
-    const bool last_pass = tp + PP >= t1;
     for (int i = tid; i < GQ * HD; i += NT) {
       const int h = i / HD, d = i % HD;
-      float O = sa.acc[h][d] * sa.fac[h][0];
+      float M = -INFINITY;
 #pragma unroll
-      for (int w = 0; w < SA::NBW; ++w)
-        if (w < nb) O += sa.tres[w][h][d] * sa.fac[h][1 + w];
-      if (last_pass) {  // the split's partial: o, max, sum
-        gpart[h * (HD + 2) + d] = O;
-        if (d == 0) {
-          gpart[h * (HD + 2) + HD] = sa.accm[h];
-          gpart[h * (HD + 2) + HD + 1] = sa.accl[h];
-        }
-      } else {
-        sa.acc[h][d] = O;
+      for (int w = 0; w < NW; ++w) M = fmaxf(M, sa.tres[w][h][HD]);
+      float O = 0.f, L = 0.f;
+#pragma unroll
+      for (int w = 0; w < NW; ++w) {
+        const float mw = sa.tres[w][h][HD];
+        const float f = mw == -INFINITY ? 0.f : exp2f(mw - M);
+        O += sa.tres[w][h][d] * f;
+        L += sa.tres[w][h][HD + 1] * f;
+      }
+      gpart[h * (HD + 2) + d] = O;
+      if (d == 0) {
+        gpart[h * (HD + 2) + HD] = M;
+        gpart[h * (HD + 2) + HD + 1] = L;
       }
     }
-    // the next pass writes its tiles and blocks after the barriers of its staging
   }
   // ---- the last split of this (sequence, kv head) merges the splits (no waiting)
   int* counter = a.counter + (size_t)b * a.Hkv + g;

@@ -99,6 +99,23 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int* s
   }
   return true;
 }
+// The same bound for a consumer of a copy ring, without pauses (its data is
+// usually under a microsecond away): the clock is read every 64th poll.
+__device__ __forceinline__ bool mbar_wait_spin(uint64_t* bar, uint32_t parity, int* status) {
+  unsigned long long t0 = 0;
+  for (uint32_t i = 0;; ++i) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((i & 63) == 63) {
+      const unsigned long long t = globaltimer();
+      if (t0 == 0) {
+        t0 = t;
+      } else if (t - t0 > kWaitLimitNs) {
+        atomicOr(status, ST_TIMEOUT);
+        return false;
+      }
+    }
+  }
+}
 // Global -> shared bulk copy completing on `bar` (addresses 16-B aligned,
 // bytes a multiple of 16). Weights are read once per step: evict first.
 __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar,
@@ -197,6 +214,14 @@ __device__ __forceinline__ void cp_async_small(void* dst, const void* src) {
   asm volatile("cp.async.ca.shared.global [%0], [%1], %2;" ::"r"(smem_u32(dst)), "l"(src), "n"(BYTES) : "memory");
 }
 __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+// Groups of copies: commit closes the thread's copies issued since the last
+// commit into one group; wait_group<N> returns once at most the N most recent
+// groups are still in flight.
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait_group() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
 
 struct Part {
   int U, N, G, S;  // units, CTAs, units per row tile, slots per row tile

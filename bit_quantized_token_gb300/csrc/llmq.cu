@@ -245,6 +245,7 @@ struct llm_model {
   int *d_bcand_i = nullptr, *d_bcnt = nullptr, *d_battn_cnt = nullptr, *d_bgreedy_cnt = nullptr;
   cudaGraphExec_t bgraph = nullptr;
   size_t bsmem_max = 0;
+  int bhead_grid = 0;  // > 0: the batched LM head runs as bhead_kernel on this many CTAs
   // persistent step kernel
   bool use_step = false;
   int step_R = 1;                             // input ranges of the persistent step's GEMVs
@@ -712,15 +713,15 @@ template <int GQ, int HD>
 cudaError_t launch_battn_t(const llm_model* m, const BAttnParams& b, int splits, int rows, bool pdl) {
   const dim3 grid(splits, m->cfg.n_kv_heads, rows);
   if (m->kv8)
-    return launch(battn_mma_kernel<GQ, HD, true>, grid, dim3(kBAttnThreads), sizeof(BAttnSmem<GQ, HD>), m->stream,
-                  pdl, b);
-  return launch(battn_mma_kernel<GQ, HD, false>, grid, dim3(kBAttnThreads), sizeof(BAttnSmem<GQ, HD>), m->stream,
-                pdl, b);
+    return launch(battn_mma_kernel<GQ, HD, true>, grid, dim3(kBAttnThreads), sizeof(BAttnSmemT<GQ, HD, true>),
+                  m->stream, pdl, b);
+  return launch(battn_mma_kernel<GQ, HD, false>, grid, dim3(kBAttnThreads), sizeof(BAttnSmemT<GQ, HD, false>),
+                m->stream, pdl, b);
 }
 template <int GQ, int HD>
 cudaError_t battn_smem_attr() {
-  cudaError_t e = raise_smem_limit(battn_mma_kernel<GQ, HD, false>, sizeof(BAttnSmem<GQ, HD>));
-  if (e == cudaSuccess) e = raise_smem_limit(battn_mma_kernel<GQ, HD, true>, sizeof(BAttnSmem<GQ, HD>));
+  cudaError_t e = raise_smem_limit(battn_mma_kernel<GQ, HD, false>, sizeof(BAttnSmemT<GQ, HD, false>));
+  if (e == cudaSuccess) e = raise_smem_limit(battn_mma_kernel<GQ, HD, true>, sizeof(BAttnSmemT<GQ, HD, true>));
   return e;
 }
 cudaError_t battn_set_smem(int gq, int hd) {
@@ -921,6 +922,8 @@ cudaError_t enqueue_batched(llm_model* m, const BatchedIO& io) {
   p.tok_io = io.tok_io;
   p.argmax_out = io.argmax_out;
   p.pos = io.pos;
+  if (m->bhead_grid)
+    return launch(bhead_kernel, dim3(m->bhead_grid), dim3(kHThreads), bhead_smem_bytes(p.K), m->stream, pdl, p);
   return launch_bgemv(m, m->blm, p, pdl);
 }
 
@@ -1646,6 +1649,18 @@ int llm_model_create(const llm_config* cfg, const llm_tensor* tensors, int32_t n
       m->bsmem_max = std::max(m->bsmem_max, b->smem);
     }
     bcnt_total = (size_t)max_blocks + (size_t)B * c.n_kv_heads + 1;
+    // a bf16 LM head whose 32-token input fits in shared memory beside the
+    // ring runs persistent, one CTA per SM (the candidates need one slot per CTA)
+    if (m->blm.m.bf16 && m->blm.m.G % kHUC == 0) {
+      int optin = 0, dev = 0;
+      cudaFuncAttributes fa{};
+      if (cudaGetDevice(&dev) == cudaSuccess &&
+          cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) == cudaSuccess &&
+          cudaFuncGetAttributes(&fa, bhead_kernel) == cudaSuccess &&
+          bhead_smem_bytes(m->blm.m.cols) + fa.sharedSizeBytes <= (size_t)optin)
+        m->bhead_grid = std::min({m->n_sm, m->blm.m.n_rt, m->blm.n_blocks});
+      cudaGetLastError();
+    }
     AL(m->d_bx, (size_t)B * d * 4, "batched residual");
     if (c.flags & LLM_DEBUG_BATCH_HIDDEN) AL(m->d_bhid, (size_t)(L + 1) * B * d * 4, "batched hidden-state capture");
     AL(m->d_bss_x, (size_t)max_blocks * kBM * 4, "batched sums of squares");
@@ -1717,6 +1732,7 @@ int llm_model_create(const llm_config* cfg, const llm_tensor* tensors, int32_t n
       e = raise_smem_limit(bgemv_kernel<false>, m->bsmem_max);
     if (e == cudaSuccess && m->bsmem_max)
       e = raise_smem_limit(bgemv_kernel<true>, m->bsmem_max);
+    if (e == cudaSuccess && m->bhead_grid) e = raise_smem_limit(bhead_kernel, bhead_smem_bytes(m->blm.m.cols));
     if (e == cudaSuccess) e = battn_set_smem(gq, hd);
     if (m->kv8) {
       for (int8_t* z : {m->d_k8, m->d_v8})

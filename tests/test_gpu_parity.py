@@ -508,6 +508,14 @@ def test_batched_qwen_shape_ragged_two_layers():
     _batched_vs_oracle(cfg, lens, 3, synth.make_first_tokens(cfg, 32), hidden=True)
 
 
+def test_batched_tied_head_ragged_vocabulary():
+    # the tied bf16 LM head with a vocabulary that is not a multiple of 32
+    # rows (126 row tiles over the persistent head's CTAs, the last tile
+    # partly masked), 3 sequences (29 padding token rows), caches of 1..3 passes
+    cfg = synth.workload(2, n_layers=1, vocab=4001)
+    _batched_vs_oracle(cfg, [70, 130, 5], 3, synth.make_first_tokens(cfg, 3), hidden=True)
+
+
 def test_batched_tiny_int8_kv_matches_oracle():
     # the grouped int8 cache (LLM_KV_Q8) against the oracle's int8 caches
     cfg = synth.workload(0)
