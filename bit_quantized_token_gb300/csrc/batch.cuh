@@ -6,14 +6,20 @@
 // 1-D bulk copies and the normalised inputs in shared memory.
 //   * 4-bit units run on the tensor cores (mma.sync m16n8k16, fp16, fp32
 //     accumulation): the 4-bit codes become exact fp16 integers, the inputs
-//     are split into fp16 high parts and remainders (64 columns: 32 tokens x
-//     2, a 22-bit-mantissa input), and each group's fp16 scale and min are
-//     applied to the fp32 MMA result: y = s * sum_k q_k x_k + m * sum_k x_k.
+//     are bf16 high parts and remainders (64 columns: 32 tokens x 2, a
+//     16-bit-mantissa input), and each group's fp16 scale and min are
+//     applied to the fp32 MMA result: y = s * sum_k q_k x_k + m * sum_k x_k
+//     (the group sums of x by one more MMA against a block of ones).
 //     Warp w owns 16 rows of one row tile (with several warps per 16 rows
 //     when the block has fewer row tiles, each taking every wp-th unit).
 //   * bf16 units (the tied LM head): the same with bf16 operands; the weight
 //     fragments are single ldmatrix loads and the inputs are split into bf16
 //     high parts and remainders (16-bit mantissa).
+// Inputs arrive staged: the producer of a GEMV's input (the embedding, an
+// epilogue below, the attention merge) writes it once as XL[64][K], bf16
+// high parts of the 32 tokens then their remainders, of x' = x * w with the
+// RMSNorm weights w already applied; the consumer copies its rows as they
+// are and multiplies each token's result by 1/rms(x) in its epilogue.
 // When K is split over several CTAs the last CTA of a row block to arrive
 // adds the partials in CTA order and runs the epilogue (store, residual,
 // SwiGLU, or logits with the per-sequence greedy choice).
@@ -36,10 +42,9 @@ struct BGemvParams {
   int M;                   // live tokens (<= 32)
   int rtb, kc;             // row tiles per CTA, units per chunk (per row tile)
   int ks;                  // K splits (CTAs per row block)
-  // input: X [M][K] fp32 (+ optional RMSNorm per token, whose sums of squares
-  // come as ss_n partials per token: ss_in[b * 32 + m])
-  const float* x;
-  const float* norm_w;
+  // input: XL [64][K] (see above); with ss_in, RMSNorm: each token's result
+  // is scaled by 1/rms(x), from ss_n partial sums of squares ss_in[b * 32 + m]
+  const uint16_t* xl;
   const float* ss_in;
   int ss_n;
   float eps;
@@ -49,6 +54,8 @@ struct BGemvParams {
   int out_cols;
   const float* resid;      // [M][rows] (EPI_RESID)
   float* ss_out;           // EPI_RESID: [n_blocks][32] sums of squares of the written rows
+  uint16_t* out_hl;        // EPI_RESID / EPI_SWIGLU: the output staged for the next GEMV, XL [64][out_cols]
+  const float* out_norm;   // RMSNorm weights that the next GEMV applies to it (null: none)
   float* part;             // [ks][M][rows] partials
   int* counters;           // [n_rt / rtb] arrival counters (zero between launches)
   // EPI_LOGITS: per-token best over the row blocks, then the greedy choice
@@ -61,12 +68,12 @@ struct BGemvParams {
   int* status;
 };
 
-// Dynamic shared memory of one CTA: two buffers of RT_B*kc units (256 inputs per row tile),
-// the staged inputs [64][256+8] halves and the 4-bit per-group input sums
-// [4][32]; after the last chunk the per-warp results [8][32][20] fp32.
+// Dynamic shared memory of one CTA: two buffers of RT_B*kc units (256 inputs
+// per row tile) and two of the chunk's staged inputs [64][256+8] halves; after
+// the last chunk the per-warp results [8][32][20] fp32.
 __host__ __device__ inline size_t bgemv_stage_bytes(int rtb, int kc, int unit_bytes, int epu) {
   const size_t w = (size_t)2 * rtb * kc * unit_bytes;  // two alternating weight buffers
-  const size_t x = (size_t)2 * kBM * (256 + 8) * 2 + (size_t)(256 / 64) * kBM * 4;
+  const size_t x = (size_t)2 * 2 * kBM * (256 + 8) * 2;  // two alternating input buffers
   const size_t red = (size_t)kBWarps * kBM * 20 * 4;
   return (w + x) > red ? (w + x) : red;
 }
@@ -80,6 +87,22 @@ __device__ __forceinline__ uint32_t q4_pair_f16(uint32_t w, int sh) {
   __half2 h = *reinterpret_cast<const __half2*>(&v);
   h = __hsub2(h, __float2half2_rn(1024.f));
   return *reinterpret_cast<const uint32_t*>(&h);
+}
+// The same as a bf16 pair: under the exponent of 128 (0x4300) the nibble q
+// reads 128 + q (7 mantissa bits: exact), and subtracting 128 is exact.
+__device__ __forceinline__ uint32_t q4_pair_bf16(uint32_t w, int sh) {
+  uint32_t v = __byte_perm(w >> sh, 0u, 0x4140u);
+  v = (v & 0x000F000Fu) | 0x43004300u;
+  __nv_bfloat162 h = *reinterpret_cast<const __nv_bfloat162*>(&v);
+  h = __hsub2(h, __float2bfloat162_rn(128.f));
+  return *reinterpret_cast<const uint32_t*>(&h);
+}
+// Token m's value v at column col of a staged input XL [64][K]: the bf16 high
+// part in row m, the bf16 remainder (v - high, rounded) in row 32 + m.
+__device__ __forceinline__ void store_hl(uint16_t* xl, int K, int m, int col, float v) {
+  const __nv_bfloat16 h = __float2bfloat16_rn(v);
+  xl[(size_t)m * K + col] = __bfloat16_as_ushort(h);
+  xl[(size_t)(kBM + m) * K + col] = __bfloat16_as_ushort(__float2bfloat16_rn(v - __bfloat162float(h)));
 }
 
 template <bool BF16>
@@ -98,9 +121,9 @@ __global__ void __launch_bounds__(kBThreads, 2) bgemv_kernel(const BGemvParams p
   constexpr int XS = KW + 8;       // staged input row (halves): conflict-free ldmatrix rows
   constexpr int EPU = BF16 ? kBF16UnitCols : 64;
   uint8_t* wbuf = smem;
-  // inputs of the chunk: xh[token][k] (fp16 or bf16) high parts, xh[32 + token][k] the remainders
+  // inputs of a chunk: xh[token][k] bf16 high parts, xh[32 + token][k] the remainders (two buffers)
   uint16_t* xh = reinterpret_cast<uint16_t*>(smem + (size_t)2 * p.rtb * p.kc * p.unit_bytes);
-  float* xsm = reinterpret_cast<float*>(xh + (size_t)2 * kBM * XS);  // 4-bit: [group][token] input sums
+  constexpr size_t XB = (size_t)2 * kBM * (KW + 8);  // halves per input buffer
 
   // the weight units of every row tile of the block (one bulk copy per row
   // tile); weights do not depend on the previous kernel: the first chunk is
@@ -129,25 +152,32 @@ __global__ void __launch_bounds__(kBThreads, 2) bgemv_kernel(const BGemvParams p
   pdl_trigger();
   pdl_wait();
 
-  // the first chunk's inputs are requested in the same round trip as the
-  // RMSNorm statistics (they are normalised once those are known)
-  constexpr int NL = kBM * (KW / 4) / kBThreads;  // float4 per thread (k fastest: coalesced reads)
-  static_assert(kBThreads % (KW / 4) == 0, "a thread stages one input column (k4) for NL tokens");
-  float4 xv[NL], wv;
-  auto load_inputs = [&](int ga) {
-    const int kw = min(p.kc, g1 - ga) * EPU, kbase = ga * EPU, k4 = tid % (KW / 4);
+  // a chunk's inputs, copied as they are (cp.async, 16 B = 8 inputs of a
+  // token's high parts or remainders) into input buffer bi; absent tokens
+  // and columns past the chunk read zero. The first chunk's copies go out in
+  // the same round trip as the RMSNorm statistics.
+  constexpr int NL = kBM * (KW / 8) / kBThreads;  // copies per thread and half (k fastest: coalesced)
+  static_assert(kBThreads % (KW / 8) == 0, "a thread stages one input column (k8) for NL tokens");
+  const int k8 = tid % (KW / 8);
+  auto load_inputs = [&](int ga, int bi) {
+    const int kw = min(p.kc, g1 - ga) * EPU, kbase = ga * EPU;
 #pragma unroll
     for (int it = 0; it < NL; ++it) {
-      const int m = (tid + it * kBThreads) / (KW / 4);
-      xv[it] = ldcg4_if(p.x + (size_t)m * p.K + kbase + 4 * k4, m < p.M && k4 < kw / 4);
+      const int m = (tid + it * kBThreads) / (KW / 8);
+#pragma unroll
+      for (int hl = 0; hl < 2; ++hl) {
+        uint16_t* dst = xh + bi * XB + (size_t)(hl * kBM + m) * XS + 8 * k8;
+        if (m < p.M && k8 < kw / 8) cp_async16(dst, p.xl + (size_t)(hl * kBM + m) * p.K + kbase + 8 * k8);
+        else *reinterpret_cast<uint4*>(dst) = make_uint4(0u, 0u, 0u, 0u);
+      }
     }
-    wv = ldnc4_if(p.norm_w ? p.norm_w + kbase + 4 * k4 : nullptr, p.norm_w != nullptr && k4 < kw / 4);
   };
-  load_inputs(g0);
+  load_inputs(g0, 0);
+  cp_async_commit();
 
   // ---- RMSNorm factor per token from the producer's partial sums of squares
   // (thread: token tid % 32, partials tid/32, +8, ...; added in a fixed order)
-  if (p.norm_w) {
+  if (p.ss_in) {
     const int m = tid & 31, sub = tid >> 5;
     float v[8];
 #pragma unroll
@@ -179,41 +209,10 @@ __global__ void __launch_bounds__(kBThreads, 2) bgemv_kernel(const BGemvParams p
   for (int ga = g0, ci = 0; ga < g1 && ok; ga += p.kc, ++ci) {
     const int nk = min(p.kc, g1 - ga);
     const uint8_t* wb = wbuf + (ci & 1) * wchunk;
-    {
-      // stage the (normalised) inputs of the chunk, loaded during the previous chunk
-#pragma unroll
-      for (int it = 0; it < NL; ++it) {
-        const int i = tid + it * kBThreads, m = i / (KW / 4), k4 = i % (KW / 4);
-        float4 v = xv[it];
-        if (p.norm_w) {
-          const float4 w = wv;
-          const float inv = m < p.M ? s_inv[m] : 0.f;
-          v = make_float4(v.x * inv * w.x, v.y * inv * w.y, v.z * inv * w.z, v.w * inv * w.w);
-        }
-        uint2 hv, lv;
-        if constexpr (!BF16) {
-          const float hx = __half2float(__float2half_rn(v.x)), hy = __half2float(__float2half_rn(v.y));
-          const float hz = __half2float(__float2half_rn(v.z)), hw = __half2float(__float2half_rn(v.w));
-          hv = make_uint2(pack_f16x2(hx, hy), pack_f16x2(hz, hw));
-          lv = make_uint2(pack_f16x2(v.x - hx, v.y - hy), pack_f16x2(v.z - hz, v.w - hw));
-        } else {
-          const float hx = __bfloat162float(__float2bfloat16_rn(v.x)), hy = __bfloat162float(__float2bfloat16_rn(v.y));
-          const float hz = __bfloat162float(__float2bfloat16_rn(v.z)), hw = __bfloat162float(__float2bfloat16_rn(v.w));
-          hv = make_uint2(pack_bf16x2(hx, hy), pack_bf16x2(hz, hw));
-          lv = make_uint2(pack_bf16x2(v.x - hx, v.y - hy), pack_bf16x2(v.z - hz, v.w - hw));
-        }
-        *reinterpret_cast<uint2*>(xh + (size_t)m * XS + 4 * k4) = hv;
-        *reinterpret_cast<uint2*>(xh + (size_t)(kBM + m) * XS + 4 * k4) = lv;
-        if constexpr (!BF16) {  // sum of each group of 64 inputs (16 consecutive lanes) per token
-          float gs = (v.x + v.y) + (v.z + v.w);
-#pragma unroll
-          for (int o = 8; o > 0; o >>= 1) gs += __shfl_xor_sync(0xffffffffu, gs, o);
-          if ((k4 & 15) == 0) xsm[(k4 >> 4) * kBM + m] = gs;
-        }
-      }
-    }
-    if (ga + p.kc < g1) load_inputs(ga + p.kc);  // in flight while this chunk computes
-    __syncthreads();
+    const uint16_t* xb = xh + (ci & 1) * XB;
+    if (ga + p.kc < g1) load_inputs(ga + p.kc, (ci + 1) & 1);  // in flight while this chunk computes
+    cp_async_commit();
+    cp_async_wait_group<1>();  // this chunk's inputs
     ok = __syncthreads_and(mbar_wait(&s_bar[ci & 1], (ci >> 1) & 1, p.status));  // uniform across the CTA
     if (ok) {
       for (int u = usub; u < nk; u += wp) {
@@ -221,6 +220,11 @@ __global__ void __launch_bounds__(kBThreads, 2) bgemv_kernel(const BGemvParams p
 #pragma unroll
         for (int nt = 0; nt < 8; ++nt) d[nt][0] = d[nt][1] = d[nt][2] = d[nt][3] = 0.f;
         if constexpr (!BF16) {
+          // ds[j]: the group's input sums (high parts + remainders) of tokens 8j .. 8j+7, by MMAs
+          // against a block of ones (every row of the result holds them)
+          float ds[4][4];
+#pragma unroll
+          for (int j = 0; j < 4; ++j) ds[j][0] = ds[j][1] = ds[j][2] = ds[j][3] = 0.f;
           const uint8_t* ub = wb + ((size_t)rt_q * p.kc + u) * p.unit_bytes;
           // rows R0 and R0 + 8: 16 B of codes per input half (inputs 0-31, 32-63)
           const uint4 c00 = *reinterpret_cast<const uint4*>(ub + R0 * 16);
@@ -235,14 +239,18 @@ __global__ void __launch_bounds__(kBThreads, 2) bgemv_kernel(const BGemvParams p
             const uint4 w0 = ks < 2 ? c00 : c01, w1 = ks < 2 ? c10 : c11;
             const uint32_t w0a = (ks & 1) ? w0.z : w0.x, w0b = (ks & 1) ? w0.w : w0.y;
             const uint32_t w1a = (ks & 1) ? w1.z : w1.x, w1b = (ks & 1) ? w1.w : w1.y;
-            const uint32_t a[4] = {q4_pair_f16(w0a, sh), q4_pair_f16(w1a, sh), q4_pair_f16(w0b, sh),
-                                   q4_pair_f16(w1b, sh)};
+            const uint32_t a[4] = {q4_pair_bf16(w0a, sh), q4_pair_bf16(w1a, sh), q4_pair_bf16(w0b, sh),
+                                   q4_pair_bf16(w1b, sh)};
+            constexpr uint32_t kOne2 = 0x3F803F80u;  // bf16 (1, 1)
+            const uint32_t ones[4] = {kOne2, kOne2, kOne2, kOne2};
 #pragma unroll
             for (int nt = 0; nt < 8; nt += 2) {
               uint32_t b[4];
-              ldsm_x4(b, xh + (size_t)(8 * (nt + (mi >> 1)) + r8) * XS + u * 64 + 16 * ks + 8 * (mi & 1));
-              mma_f16_16816(d[nt], a, b[0], b[1]);
-              mma_f16_16816(d[nt + 1], a, b[2], b[3]);
+              ldsm_x4(b, xb + (size_t)(8 * (nt + (mi >> 1)) + r8) * XS + u * 64 + 16 * ks + 8 * (mi & 1));
+              mma_bf16_16816(d[nt], a, b[0], b[1]);
+              mma_bf16_16816(d[nt + 1], a, b[2], b[3]);
+              mma_bf16_16816(ds[nt & 3], ones, b[0], b[1]);
+              mma_bf16_16816(ds[(nt + 1) & 3], ones, b[2], b[3]);
             }
           }
           // y += s * (high + remainder columns) + m * sum(x)
@@ -250,7 +258,7 @@ __global__ void __launch_bounds__(kBThreads, 2) bgemv_kernel(const BGemvParams p
           for (int nt = 0; nt < 4; ++nt)
 #pragma unroll
             for (int e = 0; e < 2; ++e) {
-              const float X = xsm[u * kBM + 8 * nt + 2 * t + e];
+              const float X = ds[nt][e];
               qacc[nt][e][0] = fmaf(sm0.x, d[nt][e] + d[nt + 4][e], fmaf(sm0.y, X, qacc[nt][e][0]));
               qacc[nt][e][1] = fmaf(sm1.x, d[nt][2 + e] + d[nt + 4][2 + e], fmaf(sm1.y, X, qacc[nt][e][1]));
             }
@@ -262,7 +270,7 @@ __global__ void __launch_bounds__(kBThreads, 2) bgemv_kernel(const BGemvParams p
 #pragma unroll
           for (int nt = 0; nt < 8; nt += 2) {
             uint32_t b[4];
-            ldsm_x4(b, xh + (size_t)(8 * (nt + (mi >> 1)) + r8) * XS + u * 16 + 8 * (mi & 1));
+            ldsm_x4(b, xb + (size_t)(8 * (nt + (mi >> 1)) + r8) * XS + u * 16 + 8 * (mi & 1));
             mma_bf16_16816(d[nt], a, b[0], b[1]);
             mma_bf16_16816(d[nt + 1], a, b[2], b[3]);
           }
@@ -279,7 +287,10 @@ __global__ void __launch_bounds__(kBThreads, 2) bgemv_kernel(const BGemvParams p
     __syncthreads();  // the buffers are restaged by the next chunks
     if (tid == 0 && ok && ga + 2 * p.kc < g1) stage_weights(ga + 2 * p.kc);  // into this chunk's buffer
   }
-  if (!ok) return;  // every wait is bounded; the status word carries the timeout
+  if (!ok) {  // every wait is bounded; the status word carries the timeout
+    cp_async_wait_all();
+    return;
+  }
 
   // ---- each warp's results -> shared memory [warp][32 tokens][QS] (16 rows,
   // padded: both the fragment stores and the row-contiguous reads below are
@@ -358,18 +369,27 @@ __global__ void __launch_bounds__(kBThreads, 2) bgemv_kernel(const BGemvParams p
         }
       }
     }
+    if (p.ss_in)  // RMSNorm of the input: 1/rms per token on the result
+#pragma unroll
+      for (int k = 0; k < 4; ++k) y[k] *= s_inv[warp + 8 * k];
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
       const int mm = warp + 8 * k;
       if (p.epi == EPI_SWIGLU) {  // lanes 0-15: gate rows; their up rows are lanes 16-31
         const float up = __shfl_down_sync(0xffffffffu, y[k], 16);
-        if (mm < p.M && lane < 16) p.out[(size_t)mm * p.out_cols + (row >> 5) * 16 + lane] = silu(y[k]) * up;
+        if (mm < p.M && lane < 16) {
+          const int col = (row >> 5) * 16 + lane;
+          const float av = silu(y[k]) * up;
+          if (p.out) p.out[(size_t)mm * p.out_cols + col] = av;
+          if (p.out_hl) store_hl(p.out_hl, p.out_cols, mm, col, av);
+        }
         continue;
       }
       if (mm >= p.M || row >= p.rows) continue;
       if (p.epi == EPI_RESID) {
         const float xn = __ldcg(p.resid + (size_t)mm * p.out_cols + row) + y[k];
         p.out[(size_t)mm * p.out_cols + row] = xn;
+        if (p.out_hl) store_hl(p.out_hl, p.out_cols, mm, row, p.out_norm ? xn * __ldg(p.out_norm + row) : xn);
         ssq[k] += xn * xn;
       } else {
         p.out[(size_t)mm * p.out_cols + row] = y[k];
@@ -440,8 +460,8 @@ __global__ void __launch_bounds__(kBThreads, 2) bgemv_kernel(const BGemvParams p
 
 // ---- the batched LM head over a bf16 table (the tied embedding) ------------
 // Persistent: one CTA per SM walks a contiguous range of row tiles with the
-// 32-token input staged once for the whole launch (RMSNorm applied, split
-// into bf16 high parts and remainders, resident in shared memory). Consumer
+// 32-token staged input (XL, above) copied once for the whole launch and
+// resident in shared memory; 1/rms scales each logit. Consumer
 // warp w owns row tile w of each group of kHWarps and accumulates it over all
 // of K (both 16-row halves share the input fragments). A producer warp
 // streams the group's units through a ring of kHSlots slots (kHUC units of
@@ -518,7 +538,7 @@ __global__ void __launch_bounds__(kHThreads, 1) bhead_kernel(const BGemvParams p
   // of squares (thread: token tid % 32, partials tid/32, +8, ...; fixed order)
   pdl_trigger();
   pdl_wait();
-  if (p.norm_w) {
+  if (p.ss_in) {
     const int m = tid & 31, sub = tid >> 5;
     float v[8];
 #pragma unroll
@@ -533,35 +553,23 @@ __global__ void __launch_bounds__(kHThreads, 1) bhead_kernel(const BGemvParams p
       for (int w = 0; w < kHWarps; ++w) t += s_bv[w][tid];
       s_inv[tid] = 1.0f / sqrtf(t / (float)p.K + p.eps);
     }
-    consumers_sync();
   }
-  // the whole input, once: x * inv * w -> bf16 high part (row m) and remainder (row 32 + m)
+  // the whole staged input, once: 16 B (8 inputs) of a token's high parts or remainders per load
   {
-    const int k4n = p.K / 4;
+    const int k8n = p.K / 8;
     constexpr int UN = 8;  // loads in flight per thread
-    for (int i0 = tid; i0 < kBM * k4n; i0 += UN * kHWarps * 32) {
-      float4 xv[UN], wv[UN];
+    for (int i0 = tid; i0 < 2 * kBM * k8n; i0 += UN * kHWarps * 32) {
+      float4 xv[UN];
 #pragma unroll
       for (int j = 0; j < UN; ++j) {
-        const int i = i0 + j * kHWarps * 32, m = i / k4n, k4 = i - m * k4n;
-        xv[j] = ldcg4_if(p.x + (size_t)m * p.K + 4 * k4, i < kBM * k4n && m < p.M);
-        wv[j] = ldnc4_if(p.norm_w ? p.norm_w + 4 * k4 : nullptr, p.norm_w != nullptr && i < kBM * k4n);
+        const int i = i0 + j * kHWarps * 32, r = i / k8n, k8 = i - r * k8n;
+        xv[j] = ldcg4_if(reinterpret_cast<const float*>(p.xl + (size_t)r * p.K + 8 * k8),
+                         i < 2 * kBM * k8n && (r & (kBM - 1)) < p.M);
       }
 #pragma unroll
       for (int j = 0; j < UN; ++j) {
-        const int i = i0 + j * kHWarps * 32, m = i / k4n, k4 = i - m * k4n;
-        if (i >= kBM * k4n) continue;
-        float4 v = xv[j];
-        if (p.norm_w) {
-          const float inv = m < p.M ? s_inv[m] : 0.f;
-          v = make_float4(v.x * inv * wv[j].x, v.y * inv * wv[j].y, v.z * inv * wv[j].z, v.w * inv * wv[j].w);
-        }
-        const float hx = __bfloat162float(__float2bfloat16_rn(v.x)), hy = __bfloat162float(__float2bfloat16_rn(v.y));
-        const float hz = __bfloat162float(__float2bfloat16_rn(v.z)), hw = __bfloat162float(__float2bfloat16_rn(v.w));
-        *reinterpret_cast<uint2*>(xh + (size_t)m * XS + 4 * k4) =
-            make_uint2(pack_bf16x2(hx, hy), pack_bf16x2(hz, hw));
-        *reinterpret_cast<uint2*>(xh + (size_t)(kBM + m) * XS + 4 * k4) =
-            make_uint2(pack_bf16x2(v.x - hx, v.y - hy), pack_bf16x2(v.z - hz, v.w - hw));
+        const int i = i0 + j * kHWarps * 32, r = i / k8n, k8 = i - r * k8n;
+        if (i < 2 * kBM * k8n) *reinterpret_cast<float4*>(xh + (size_t)r * XS + 8 * k8) = xv[j];
       }
     }
   }
@@ -628,8 +636,9 @@ __global__ void __launch_bounds__(kHThreads, 1) bhead_kernel(const BGemvParams p
 #pragma unroll
           for (int e = 0; e < 2; ++e) {
             const int mm = 8 * nt + 2 * t + e;
-            const float y = d[h][nt][2 * hh + e] + d[h][nt + 4][2 * hh + e];
+            float y = d[h][nt][2 * hh + e] + d[h][nt + 4][2 * hh + e];
             if (mm >= p.M || row >= p.rows) continue;
+            if (p.ss_in) y *= s_inv[mm];  // RMSNorm of the input: 1/rms per token
             p.out[(size_t)mm * p.out_cols + row] = y;
             if (y != y) nan = true;
             else if (better(y, row, bv[nt][e], bi[nt][e])) {
@@ -718,7 +727,9 @@ struct BEmbedParams {
   int bf16, dim, vocab, M;
   const int* tok;
   float* x;
-  float* ss_out;  // [32]: sum of squares of each token's row
+  float* ss_out;         // [32]: sum of squares of each token's row
+  uint16_t* x_hl;        // the rows staged for the first GEMV, XL [64][dim], with
+  const float* norm_w;   // its RMSNorm weights applied
   int* status;
 };
 
@@ -736,6 +747,7 @@ __global__ void __launch_bounds__(256) bembed_kernel(const BEmbedParams p) {
     const float v = p.bf16 ? bf16_bits_to_f32(static_cast<const uint16_t*>(p.embed)[(size_t)t * p.dim + i])
                            : static_cast<const float*>(p.embed)[(size_t)t * p.dim + i];
     p.x[(size_t)m * p.dim + i] = v;
+    store_hl(p.x_hl, p.dim, m, i, v * __ldg(p.norm_w + i));
     ss += v * v;
   }
   // sum of squares of the row (the first RMSNorm): warps, then warp sums in order
@@ -764,6 +776,7 @@ struct BAttnParams {
                           // chunk), BA_APPEND for all rows, then BA_ATTEND over the cache
   size_t seq_kv_stride;   // cache elements per sequence
   size_t part_stride;     // attention partial floats per row
+  uint16_t* o_hl;         // the output, staged for the o-projection: XL [64][o_cols]
   int8_t* k8;             // the grouped int8 cache instead of a.kc / a.vc (layer base): codes
   int8_t* v8;
   uint16_t* ks;           // and fp16 scales of each 32 values (layer base; elements / 32)
@@ -776,7 +789,10 @@ struct BAttnParams {
 #endif
 static_assert(LLMQ_BATTN_SPLITS >= 1 && LLMQ_BATTN_SPLITS <= 24, "splits of a batched attention item");
 #ifndef LLMQ_BATTN_SPLIT_LEN
-#define LLMQ_BATTN_SPLIT_LEN 256  // bf16 cache: cached positions per split (at most 24 splits)
+// bf16 cache: cached positions per split (at most 24 splits). Measured on the
+// 32-sequence workload: 128 -> 9408, 256 -> 10005, 512 -> 10826, 768 -> 10176,
+// 1024 -> 10735 tok/s
+#define LLMQ_BATTN_SPLIT_LEN 512
 #endif
 constexpr int kBAttnThreads = 256;
 constexpr int kBAttnPP = 64;  // cache positions per pass (~42 KB of tiles: 4 CTAs per SM)
@@ -1202,7 +1218,6 @@ __global__ void __launch_bounds__(kBAttnThreads) battn_mma_kernel(const BAttnPar
   // the last split: (max, sum) of every split and head to shared memory while
   // each thread loads its output element of every split (one round trip)
   const float* hp = a.part + (size_t)b * bp.part_stride + ((size_t)g * a.P * GQ) * (HD + 2);
-  float* out = a.out + (size_t)b * bp.o_cols;
   float* ml = &sa.tres[0][0][0];  // [P_eff][GQ][2] (the block results are no longer needed)
   static_assert(sizeof(sa.tres) >= PMAX * GQ * 2 * sizeof(float), "merge scratch");
   for (int i = tid; i < P_eff * GQ * 2; i += NT) {
@@ -1227,7 +1242,7 @@ __global__ void __launch_bounds__(kBAttnThreads) battn_mma_kernel(const BAttnPar
           L += ml[(s2 * GQ + h) * 2 + 1] * f;
           O += ov[s2] * f;
         }
-      out[(g * GQ + h) * HD + d] = O / L;
+      store_hl(bp.o_hl, bp.o_cols, b, (g * GQ + h) * HD + d, O / L);
     }
   }
   if (tid == 0) *counter = 0;

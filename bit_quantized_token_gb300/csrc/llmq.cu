@@ -240,7 +240,9 @@ struct llm_model {
   BPlan blm;
   float *d_bss_x = nullptr, *d_bss_h = nullptr;  // batched: per-(row block, token) sums of squares
   float* d_bhid = nullptr;  // [L+1][max_batch][dim] residual after the embedding and each layer (LLM_DEBUG_BATCH_HIDDEN)
-  float *d_bx = nullptr, *d_bh = nullptr, *d_bqkv = nullptr, *d_bo = nullptr, *d_ba = nullptr,
+  // batched GEMV inputs staged as XL [64][K] (bf16 high parts, remainders)
+  uint16_t *d_bx_hl = nullptr, *d_bh_hl = nullptr, *d_bo_hl = nullptr, *d_ba_hl = nullptr;
+  float *d_bx = nullptr, *d_bh = nullptr, *d_bqkv = nullptr,
         *d_blogits = nullptr, *d_bpart = nullptr, *d_battn_part = nullptr, *d_bcand_v = nullptr;
   int *d_bcand_i = nullptr, *d_bcnt = nullptr, *d_battn_cnt = nullptr, *d_bgreedy_cnt = nullptr;
   cudaGraphExec_t bgraph = nullptr;
@@ -826,15 +828,16 @@ cudaError_t enqueue_batched(llm_model* m, const BatchedIO& io) {
   ep.tok = io.tok;
   ep.x = m->d_bx;
   ep.ss_out = m->d_bss_x;
+  ep.x_hl = m->d_bx_hl;
+  ep.norm_w = m->d_norms + m->off_attn_norm[0];
   ep.status = m->d_status;
   if ((e = launch(bembed_kernel, dim3(B), dim3(256), 0, m->stream, false, ep)) != cudaSuccess) return e;
   if ((e = capture_x(0)) != cudaSuccess) return e;
   const size_t kv_layer = (size_t)c.n_kv_heads * c.max_seq * c.head_dim;
   const int qkv_cols = m->q_dim + 2 * m->kv_dim;
   for (int l = 0; l < L; ++l) {
-    BGemvParams p = bgemv_params(m, m->bqkv[l], B);
-    p.x = m->d_bx;
-    p.norm_w = m->d_norms + m->off_attn_norm[l];
+    BGemvParams p = bgemv_params(m, m->bqkv[l], B);  // the input staged with attn_norm[l] applied
+    p.xl = m->d_bx_hl;
     p.ss_in = m->d_bss_x;
     p.ss_n = l == 0 ? 1 : m->bdown[l - 1].n_blocks;
     p.epi = EPI_STORE;
@@ -863,7 +866,7 @@ cudaError_t enqueue_batched(llm_model* m, const BatchedIO& io) {
     bp.a.cap = c.max_seq;
     bp.a.part = m->d_battn_part;
     bp.a.counter = m->d_battn_cnt;
-    bp.a.out = m->d_bo;
+    bp.o_hl = m->d_bo_hl;
     bp.a.status = m->d_status;
     bp.qkv = m->d_bqkv;
     bp.qkv_cols = qkv_cols;
@@ -880,37 +883,39 @@ cudaError_t enqueue_batched(llm_model* m, const BatchedIO& io) {
       bp.mode = BA_APPEND_ATTEND;
     }
     if ((e = launch_battn(m, bp, m->attn_P, B, pdl)) != cudaSuccess) return e;
-    p = bgemv_params(m, m->bwo[l], B);  // h = x + Wo o
-    p.x = m->d_bo;
+    p = bgemv_params(m, m->bwo[l], B);  // h = x + Wo o (staged for gate|up with ffn_norm[l])
+    p.xl = m->d_bo_hl;
     p.epi = EPI_RESID;
     p.resid = m->d_bx;
     p.ss_out = m->d_bss_h;
     p.out = m->d_bh;
+    p.out_hl = m->d_bh_hl;
+    p.out_norm = m->d_norms + m->off_ffn_norm[l];
     p.out_cols = d;
     if ((e = launch_bgemv(m, m->bwo[l], p, pdl)) != cudaSuccess) return e;
     p = bgemv_params(m, m->bgu[l], B);  // a = silu(Wg rmsnorm(h)) * (Wu rmsnorm(h))
-    p.x = m->d_bh;
-    p.norm_w = m->d_norms + m->off_ffn_norm[l];
+    p.xl = m->d_bh_hl;
     p.ss_in = m->d_bss_h;
     p.ss_n = m->bwo[l].n_blocks;
     p.epi = EPI_SWIGLU;
-    p.out = m->d_ba;
+    p.out_hl = m->d_ba_hl;
     p.out_cols = F;
     if ((e = launch_bgemv(m, m->bgu[l], p, pdl)) != cudaSuccess) return e;
-    p = bgemv_params(m, m->bdown[l], B);  // x = h + Wd a
-    p.x = m->d_ba;
+    p = bgemv_params(m, m->bdown[l], B);  // x = h + Wd a (staged with the next RMSNorm applied)
+    p.xl = m->d_ba_hl;
     p.epi = EPI_RESID;
     p.resid = m->d_bh;
     p.ss_out = m->d_bss_x;
     p.out = m->d_bx;
+    p.out_hl = m->d_bx_hl;
+    p.out_norm = m->d_norms + (l + 1 < L ? m->off_attn_norm[l + 1] : m->off_final_norm);
     p.out_cols = d;
     if ((e = launch_bgemv(m, m->bdown[l], p, pdl)) != cudaSuccess) return e;
     if ((e = capture_x(l + 1)) != cudaSuccess) return e;
   }
   if (!io.lm) return cudaSuccess;
   BGemvParams p = bgemv_params(m, m->blm, B);  // logits, greedy choice per sequence, positions += 1
-  p.x = m->d_bx;
-  p.norm_w = m->d_norms + m->off_final_norm;
+  p.xl = m->d_bx_hl;  // staged with the final norm applied
   p.ss_in = m->d_bss_x;
   p.ss_n = m->bdown[L - 1].n_blocks;
   p.epi = EPI_LOGITS;
@@ -1667,8 +1672,10 @@ int llm_model_create(const llm_config* cfg, const llm_tensor* tensors, int32_t n
     AL(m->d_bss_h, (size_t)max_blocks * kBM * 4, "batched sums of squares");
     AL(m->d_bh, (size_t)B * d * 4, "batched residual");
     AL(m->d_bqkv, (size_t)B * (m->q_dim + 2 * m->kv_dim) * 4, "batched q|k|v");
-    AL(m->d_bo, (size_t)B * m->q_dim * 4, "batched attention output");
-    AL(m->d_ba, (size_t)B * F * 4, "batched SwiGLU output");
+    AL(m->d_bx_hl, (size_t)2 * kBM * d * 2, "batched staged inputs");
+    AL(m->d_bh_hl, (size_t)2 * kBM * d * 2, "batched staged inputs");
+    AL(m->d_bo_hl, (size_t)2 * kBM * m->q_dim * 2, "batched staged inputs");
+    AL(m->d_ba_hl, (size_t)2 * kBM * F * 2, "batched staged inputs");
     AL(m->d_blogits, (size_t)B * V * 4, "batched logits");
     AL(m->d_bpart, std::max<size_t>(part_floats, 1) * 4, "batched partials");
     AL(m->d_battn_part, (size_t)B * c.n_kv_heads * m->attn_P * gq * (hd + 2) * 4, "batched attention partials");
