@@ -248,8 +248,9 @@ __device__ __forceinline__ void attn_block16_cc(const float* q, const uint16_t* 
 // group's scale folds into the probabilities before P V; dividing it by the
 // block's largest scale of the group keeps the scaled probabilities in [0, 1]
 // for their fp16 high/low split, and that largest scale multiplies the MMA
-// result back. Same outputs as attn_block16.
-template <int GQ, int HD, int RS>
+// result back. Same outputs as attn_block16. SWZ: unpadded fp16 rows with
+// tile_off's permuted chunks instead of padded rows.
+template <int GQ, int HD, int RS, bool SWZ = false>
 __device__ __forceinline__ void attn_block16_q8(const float* q, const uint16_t* kt, const uint16_t* vt,
                                                 const uint16_t* ks, const uint16_t* vs, int row0, int nvalid,
                                                 int lane, float* out, int OS) {
@@ -267,7 +268,7 @@ __device__ __forceinline__ void attn_block16_q8(const float* q, const uint16_t* 
     uint32_t qf[4];
     attn_q_frag<GQ, HD>(qf, q, kk, lane);
     uint32_t b[4];
-    ldsm_x4(b, kt + (size_t)(row0 + 8 * (mi >> 1) + r8) * RS + 16 * kk + 8 * (mi & 1));
+    ldsm_x4(b, kt + tile_off<HD, RS, SWZ>(row0 + 8 * (mi >> 1) + r8, 2 * kk + (mi & 1)));
     mma_f16_16816(s[kk / 2][0], qf, b[0], b[1]);
     mma_f16_16816(s[kk / 2][1], qf, b[2], b[3]);
   }
@@ -317,7 +318,7 @@ __device__ __forceinline__ void attn_block16_q8(const float* q, const uint16_t* 
 #pragma unroll
     for (int nt = 4 * vg; nt < 4 * vg + 4; nt += 2) {
       uint32_t b[4];
-      ldsm_x4_t(b, vt + (size_t)(row0 + 8 * (mi & 1) + r8) * RS + 8 * (nt + (mi >> 1)));
+      ldsm_x4_t(b, vt + tile_off<HD, RS, SWZ>(row0 + 8 * (mi & 1) + r8, nt + (mi >> 1)));
       float d0[4] = {0.f, 0.f, 0.f, 0.f}, d1[4] = {0.f, 0.f, 0.f, 0.f};
       mma_f16_16816(d0, pa, b[0], b[1]);
       mma_f16_16816(d1, pa, b[2], b[3]);

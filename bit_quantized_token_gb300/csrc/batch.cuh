@@ -784,67 +784,61 @@ struct BAttnParams {
 };
 
 
-#ifndef LLMQ_BATTN_SPLITS
-#define LLMQ_BATTN_SPLITS 8  // measured on the 32-sequence workload: 24 -> 8791, 12 -> 9115, 8 -> 9274, 4 -> 9005 tok/s
-#endif
-static_assert(LLMQ_BATTN_SPLITS >= 1 && LLMQ_BATTN_SPLITS <= 24, "splits of a batched attention item");
 #ifndef LLMQ_BATTN_SPLIT_LEN
-// bf16 cache: cached positions per split (at most 24 splits). Measured on the
-// 32-sequence workload: 128 -> 9408, 256 -> 10005, 512 -> 10826, 768 -> 10176,
-// 1024 -> 10735 tok/s
+// Cached positions per split (at most 24 splits per (sequence, kv head)).
+// Measured on the 32-sequence workload, bf16 cache: 128 -> 9408, 256 -> 10005,
+// 512 -> 10826, 768 -> 10176, 1024 -> 10735 tok/s
 #define LLMQ_BATTN_SPLIT_LEN 512
 #endif
 constexpr int kBAttnThreads = 256;
-constexpr int kBAttnPP = 64;  // cache positions per pass (~42 KB of tiles: 4 CTAs per SM)
 
-// Shared memory of one batched attention item (sequence, kv head, split).
-template <int GQ, int HD>
-struct BAttnSmem {
-  static constexpr int PP = kBAttnPP, RS = HD + 8, NBW = PP / 16;
-  uint16_t kt[PP][RS];            // K rows of the pass (fp16, padded rows)
-  uint16_t vt[PP][RS];
-  float cur[GQ + 2][HD];          // q heads (scaled), k, v of this step
-  float tres[NBW][GQ][HD + 2];    // per 16-position block and head: o, max, sum
-  float acc[GQ][HD];
-  float accm[GQ], accl[GQ], fac[GQ][NBW + 1];
-  __align__(16) uint16_t ksc[PP][HD / 32];  // int8 K/V: fp16 group scales of the staged rows
-  __align__(16) uint16_t vsc[PP][HD / 32];
-  float cursc[2][HD / 32];        // int8 K/V: this step's k, v group scales (cur then holds their codes)
-  int is_last;
-};
-// The same over the bf16 cache: each warp streams its own blocks of 16
-// positions through a private stage (bf16 rows as cached, unpadded, chunks
-// permuted by tile_off) and keeps its own running softmax state, so no CTA
-// barrier separates two blocks (~75 KB for Qwen3's GQ 2, hd 128: 3 CTAs per SM).
+// Shared memory of one batched attention item (sequence, kv head, split) over
+// the bf16 cache: each warp streams its own blocks of 16 positions through a
+// private stage (bf16 rows as cached, unpadded, chunks permuted by tile_off)
+// and keeps its own running softmax state, so no CTA barrier separates two
+// blocks (~76 KB for Qwen3's GQ 2, hd 128: 3 CTAs per SM).
 template <int GQ, int HD>
 struct BAttnWarpSmem {
-  static constexpr int NW = kBAttnThreads / 32, RS = HD;
+  static constexpr int NW = kBAttnThreads / 32;
   uint16_t kt[NW][16][HD];
   uint16_t vt[NW][16][HD];
   float cur[GQ + 2][HD];          // q heads (scaled), k, v of this step
   float tres[NW][GQ][HD + 2];     // per warp: the block's o, max, sum; at the end the warp's state
   int is_last;
 };
+// The same over the grouped int8 cache: a warp's stage holds its block's
+// codes widened to fp16 (exact) in the same permuted rows, and their fp16
+// group scales (~78 KB for GQ 2, hd 128: 2 CTAs per SM).
+template <int GQ, int HD>
+struct BAttnWarpSmem8 {
+  static constexpr int NW = kBAttnThreads / 32, NG = HD / 32;
+  uint16_t kt[NW][16][HD];
+  uint16_t vt[NW][16][HD];
+  __align__(16) uint16_t ksc[NW][16][NG];
+  __align__(16) uint16_t vsc[NW][16][NG];
+  float cur[GQ + 2][HD];          // q heads (scaled), k, v of this step (k, v: their codes)
+  float cursc[2][NG];             // this step's k, v group scales
+  float tres[NW][GQ][HD + 2];
+  int is_last;
+};
 template <int GQ, int HD, bool KV8>
-using BAttnSmemT = std::conditional_t<KV8, BAttnSmem<GQ, HD>, BAttnWarpSmem<GQ, HD>>;
+using BAttnSmemT = std::conditional_t<KV8, BAttnWarpSmem8<GQ, HD>, BAttnWarpSmem<GQ, HD>>;
 
 // Flash-decoding attention of every sequence of the batch on the tensor
-// cores: grid (split, kv head, sequence), 8 warps that stage the pass's K/V
-// rows together; warp w < PP/16 scores all GQ heads against positions
-// 16w .. 16w+15 (attn_mma.cuh). The last split of a (sequence, kv head) to
-// finish merges the splits into the output row.
-//   bf16 cache: splits of LLMQ_BATTN_SPLIT_LEN positions; warp w takes
-//   blocks w, w+8, ... of 16 positions, each copied into its private stage as
-//   cached (converted to fp16 fragment by fragment in attn_block16), folds
-//   them into its own (max, sum, o), and requests its next block as soon as
-//   the stage has been read. The 8 warp states merge once per split.
-//   int8 cache: passes of 64 positions in one CTA-wide stage, widened to
-//   fp16 in place after its copies land; warp w < 4 scores 16 of them.
+// cores: grid (split, kv head, sequence), splits of LLMQ_BATTN_SPLIT_LEN
+// positions. Warp w takes blocks w, w+8, ... of 16 positions of the split:
+// it copies each into its private stage (bf16 rows as cached, converted to
+// fp16 fragment by fragment in attn_block16; int8 codes widened to fp16 in
+// the stage), scores all GQ heads on the tensor cores (attn_mma.cuh), folds
+// the block into its own running (max, sum, o), and requests its next block
+// as soon as the stage has been read. The 8 warp states merge once per
+// split, and the last split of a (sequence, kv head) to finish merges the
+// splits into the output row.
 template <int GQ, int HD, bool KV8>
 __global__ void __launch_bounds__(kBAttnThreads) battn_mma_kernel(const BAttnParams bp) {
   using SA = BAttnSmemT<GQ, HD, KV8>;
-  constexpr int NT = kBAttnThreads, PP = kBAttnPP, RS = SA::RS, CH = HD / 8, DPL = HD / 32, NG = HD / 32;
-  static_assert(GQ <= 8 && PP / 16 <= NT / 32, "layout");
+  constexpr int NT = kBAttnThreads, NW = SA::NW, CH = HD / 8, DPL = HD / 32, NG = HD / 32;
+  static_assert(GQ <= 8 && NW == 8, "layout");
   extern __shared__ __align__(16) uint8_t smraw[];
   SA& sa = *reinterpret_cast<SA*>(smraw);
   pdl_trigger();
@@ -858,9 +852,8 @@ __global__ void __launch_bounds__(kBAttnThreads) battn_mma_kernel(const BAttnPar
     return;
   }
   const int len = pos + 1;
-  constexpr int PMAX = 24;  // merge scratch: splits a (sequence, kv head) may have (LLMQ_BATTN_SPLITS <= PMAX)
-  const int P_eff = KV8 ? min(min(a.P, LLMQ_BATTN_SPLITS), (len + PP - 1) / PP)
-                       : min(min(a.P, PMAX), (len + LLMQ_BATTN_SPLIT_LEN - 1) / LLMQ_BATTN_SPLIT_LEN);
+  constexpr int PMAX = 24;  // merge scratch: splits a (sequence, kv head) may have
+  const int P_eff = min(min(a.P, PMAX), (len + LLMQ_BATTN_SPLIT_LEN - 1) / LLMQ_BATTN_SPLIT_LEN);
   if (split >= P_eff) return;
   const int t0 = (int)((int64_t)len * split / P_eff), t1 = (int)((int64_t)len * (split + 1) / P_eff);
   const int sb = bp.seq ? bp.seq[b] : b;  // this row's cache
@@ -875,83 +868,73 @@ __global__ void __launch_bounds__(kBAttnThreads) battn_mma_kernel(const BAttnPar
   const bool append = bp.mode == BA_APPEND || (bp.mode == BA_APPEND_ATTEND && split == P_eff - 1);
   const float* qkv = bp.qkv + (size_t)b * bp.qkv_cols;
 
-  // rows tp .. tp+n-1 of K and V -> tiles (async copies; zero rows up to the
-  // next multiple of 16): stage bi of the bf16 cache's two, or the int8
-  // cache's one stage, which convert then widens to fp16 in place
+  // the warp's block: rows tp .. tp+n-1 (n <= 16) of K and V into its stage
+  // (async copies). bf16: the rows as cached, rows past n zero. int8: each
+  // row's codes into the first HD bytes of its fp16 row, its scales beside;
+  // widen() then makes them fp16 in place
   static_assert((CH & (CH - 1)) == 0, "16-B chunks per row: a power of two");
   constexpr int LCH = CH == 8 ? 3 : 4;
-  auto stage = [&](int tp, int bi) {
-    const int n = min(PP, t1 - tp);
+  auto stage = [&](int tp) {
+    const int n = min(16, t1 - tp);
     if constexpr (KV8) {
-      // 16-byte chunks of codes into the first HD bytes of each row's fp16
-      // slot (widened in convert), one row's scales per thread
-      static_assert(2 * PP <= NT, "one scale row per thread");
       constexpr int C8 = HD / 16, L8 = C8 == 4 ? 2 : 3;
-      for (int idx = tid; idx < 2 * n * C8; idx += NT) {
-        const int kv = idx >= n * C8, r = idx - kv * n * C8, row = r >> L8, ch = r & (C8 - 1);
-        if (in_bounds(a.status, tp + row < a.cap))
-          cp_async16(reinterpret_cast<uint8_t*>(&(kv ? sa.vt : sa.kt)[row][0]) + 16 * ch,
+      for (int idx = lane; idx < 2 * 16 * C8; idx += 32) {
+        const int kv = idx >= 16 * C8, r = idx - kv * 16 * C8, row = r >> L8, ch = r & (C8 - 1);
+        if (row < n && in_bounds(a.status, tp + row < a.cap))
+          cp_async16(reinterpret_cast<uint8_t*>(&(kv ? sa.vt : sa.kt)[warp][row][0]) + 16 * ch,
                      (kv ? vc8 : kc8) + (size_t)(tp + row) * HD + 16 * ch);
       }
-      const int kv = tid / PP, row = tid - kv * PP;
-      if (kv < 2 && row < n)
-        cp_async_small<2 * NG>(&(kv ? sa.vsc : sa.ksc)[row][0], (kv ? vs8 : ks8) + (size_t)(tp + row) * NG);
-    } else {  // the warp's block of 16 rows from tp into its stage bi (= the warp)
+      const int kv = lane >> 4, row = lane & 15;  // one row's scales per lane
+      if (row < n && in_bounds(a.status, tp + row < a.cap))
+        cp_async_small<2 * NG>(&(kv ? sa.vsc : sa.ksc)[warp][row][0], (kv ? vs8 : ks8) + (size_t)(tp + row) * NG);
+    } else {
       for (int idx = lane; idx < 2 * 16 * CH; idx += 32) {
         const int kv = idx >= 16 * CH, r = idx - kv * 16 * CH, row = r >> LCH, ch = r & (CH - 1);
-        uint16_t* dst = (kv ? &sa.vt[bi][0][0] : &sa.kt[bi][0][0]) + tile_off<HD, HD, true>(row, ch);
+        uint16_t* dst = &(kv ? sa.vt : sa.kt)[warp][0][0] + tile_off<HD, HD, true>(row, ch);
         if (row < n && in_bounds(a.status, tp + row < a.cap))
           cp_async16(dst, (kv ? vc : kc) + (size_t)(tp + row) * HD + 8 * ch);
         else *reinterpret_cast<uint4*>(dst) = make_uint4(0u, 0u, 0u, 0u);
       }
     }
   };
-  auto convert = [&](int tp) {  // the int8 cache's stage
-    const int n = min(PP, t1 - tp), rows = ((n + 15) / 16) * 16;
-    cp_async_wait_all();
+  // int8: after the block's copies have landed, every lane reads its chunks
+  // of codes, then (after __syncwarp) writes them back as fp16 over the
+  // whole rows; rows past n become zero (codes and scales)
+  auto widen = [&](int n) {
     if constexpr (KV8) {
-      // every thread reads its chunks of codes (any row: the copies of all
-      // threads are complete after the barrier), then, after a second
-      // barrier, writes them back widened to fp16 over the same rows
-      constexpr int C8 = HD / 16, L8 = C8 == 4 ? 2 : 3, MAXC = (2 * PP * C8 + NT - 1) / NT;
-      __syncthreads();
+      constexpr int C8 = HD / 16, L8 = C8 == 4 ? 2 : 3, MAXC = 2 * 16 * C8 / 32;
       uint4 c[MAXC];
 #pragma unroll
       for (int j = 0; j < MAXC; ++j) {
-        const int idx = tid + j * NT, kv = idx >= rows * C8, r = idx - kv * rows * C8, row = r >> L8,
+        const int idx = lane + 32 * j, kv = idx >= 16 * C8, r = idx - kv * 16 * C8, row = r >> L8,
                   ch = r & (C8 - 1);
-        c[j] = (idx < 2 * rows * C8 && row < n)
-                   ? reinterpret_cast<const uint4*>(&(kv ? sa.vt : sa.kt)[row][0])[ch]
-                   : make_uint4(0u, 0u, 0u, 0u);
+        c[j] = row < n ? reinterpret_cast<const uint4*>(&(kv ? sa.vt : sa.kt)[warp][row][0])[ch]
+                       : make_uint4(0u, 0u, 0u, 0u);
       }
-      __syncthreads();
+      __syncwarp();
 #pragma unroll
       for (int j = 0; j < MAXC; ++j) {
-        const int idx = tid + j * NT, kv = idx >= rows * C8, r = idx - kv * rows * C8, row = r >> L8,
+        const int idx = lane + 32 * j, kv = idx >= 16 * C8, r = idx - kv * 16 * C8, row = r >> L8,
                   ch = r & (C8 - 1);
-        if (idx < 2 * rows * C8) {
-          const uint32_t w[4] = {c[j].x, c[j].y, c[j].z, c[j].w};
-          uint32_t h[8];
+        const uint32_t w[4] = {c[j].x, c[j].y, c[j].z, c[j].w};
+        uint32_t h[8];
 #pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            h[2 * q] = pack_f16x2((float)(int8_t)(w[q] & 0xFF), (float)(int8_t)((w[q] >> 8) & 0xFF));
-            h[2 * q + 1] = pack_f16x2((float)(int8_t)((w[q] >> 16) & 0xFF), (float)(int8_t)(w[q] >> 24));
-          }
-          uint4* tr = reinterpret_cast<uint4*>(&(kv ? sa.vt : sa.kt)[row][0]);
-          tr[2 * ch] = make_uint4(h[0], h[1], h[2], h[3]);
-          tr[2 * ch + 1] = make_uint4(h[4], h[5], h[6], h[7]);
+        for (int q = 0; q < 4; ++q) {
+          h[2 * q] = pack_f16x2((float)(int8_t)(w[q] & 0xFF), (float)(int8_t)((w[q] >> 8) & 0xFF));
+          h[2 * q + 1] = pack_f16x2((float)(int8_t)((w[q] >> 16) & 0xFF), (float)(int8_t)(w[q] >> 24));
         }
+        uint16_t* tile = &(kv ? sa.vt : sa.kt)[warp][0][0];
+        *reinterpret_cast<uint4*>(tile + tile_off<HD, HD, true>(row, 2 * ch)) = make_uint4(h[0], h[1], h[2], h[3]);
+        *reinterpret_cast<uint4*>(tile + tile_off<HD, HD, true>(row, 2 * ch + 1)) =
+            make_uint4(h[4], h[5], h[6], h[7]);
       }
-      const int kv = tid / PP, row = tid - kv * PP;
-      if (kv < 2 && row >= n && row < rows)
+      const int kv = lane >> 4, row = lane & 15;
+      if (row >= n)
 #pragma unroll
-        for (int k = 0; k < NG; ++k) (kv ? sa.vsc : sa.ksc)[row][k] = 0;
+        for (int k = 0; k < NG; ++k) (kv ? sa.vsc : sa.ksc)[warp][row][k] = 0;
     }
   };
-  if (attend) {
-    if constexpr (KV8) stage(t0, 0);
-    else if (t0 + 16 * warp < t1) stage(t0 + 16 * warp, warp);  // each warp's first block, during the prologue
-  }
+  if (attend && t0 + 16 * warp < t1) stage(t0 + 16 * warp);  // each warp's first block, during the prologue
   // q heads, k, v of this kv head; RoPE factors and q/k norm weights
   for (int i = tid; i < (GQ + 2) * HD; i += NT) {
     const int r = i / HD, d = i % HD;
@@ -968,8 +951,6 @@ __global__ void __launch_bounds__(kBAttnThreads) battn_mma_kernel(const BAttnPar
       const int h = warp + 8 * k2;
       wn[k2][e] = (a.q_norm && h <= GQ) ? __ldg((h < GQ ? a.q_norm : a.k_norm) + lane + 32 * e) : 1.f;
     }
-  if constexpr (KV8)
-    if (attend) convert(t0);
   __syncthreads();
   if (a.q_norm) {  // per-head RMSNorm of the q heads and k
 #pragma unroll
@@ -995,7 +976,6 @@ __global__ void __launch_bounds__(kBAttnThreads) battn_mma_kernel(const BAttnPar
   // RoPE of q and k; q scaled by log2(e)/sqrt(hd); k, v rounded to bf16 (the
   // split owning `pos` appends them and puts them into its tile)
   const float qscale = 1.4426950408889634f / sqrtf((float)HD);
-  const bool owner = attend && split == P_eff - 1 && pos - t0 < PP;
   auto keep = [&](int r, int d, float x) {
     if constexpr (KV8) {  // quantized per 32-element group below
       sa.cur[r][d] = x;
@@ -1045,90 +1025,15 @@ __global__ void __launch_bounds__(kBAttnThreads) battn_mma_kernel(const BAttnPar
         (kv ? vc8 : kc8)[(size_t)pos * HD + d] = (int8_t)(int)cf;
         if (lane == 0) (kv ? vs8 : ks8)[(size_t)pos * NG + grp] = __half_as_ushort(dh);
       }
-      if (owner) {
-        (kv ? sa.vt : sa.kt)[pos - t0][d] = __half_as_ushort(__float2half_rn(cf));
-        if (lane == 0) (kv ? sa.vsc : sa.ksc)[pos - t0][grp] = __half_as_ushort(dh);
-      }
     }
   }
   if (!attend) return;  // the rows' k, v are in the cache
   float* gpart = a.part + (size_t)b * bp.part_stride + (((size_t)g * a.P + split) * GQ) * (HD + 2);
-  if constexpr (KV8) {
-    for (int i = tid; i < GQ * HD; i += NT) sa.acc[i / HD][i % HD] = 0.f;
-    if (tid < GQ) {
-      sa.accm[tid] = -INFINITY;
-      sa.accl[tid] = 0.f;
-    }
-    __syncthreads();
-    for (int tp = t0; tp < t1; tp += PP) {
-      const int n = min(PP, t1 - tp), nb = (n + 15) / 16;
-      if (tp != t0) {
-        stage(tp, 0);
-        convert(tp);
-        __syncthreads();
-        if (pos >= tp && pos < tp + n) {
-          for (int d = tid; d < HD; d += NT) {
-            sa.kt[pos - tp][d] = __half_as_ushort(__float2half_rn(sa.cur[GQ][d]));
-            sa.vt[pos - tp][d] = __half_as_ushort(__float2half_rn(sa.cur[GQ + 1][d]));
-          }
-          if (tid < 2 * NG)
-            (tid < NG ? sa.ksc : sa.vsc)[pos - tp][tid % NG] =
-                __half_as_ushort(__float2half_rn(sa.cursc[tid / NG][tid % NG]));
-        }
-        __syncthreads();
-      }
-      if (warp < nb)
-        attn_block16_q8<GQ, HD, RS>(&sa.cur[0][0], &sa.kt[0][0], &sa.vt[0][0], &sa.ksc[0][0], &sa.vsc[0][0],
-                                    16 * warp, n - 16 * warp, lane, &sa.tres[warp][0][0], HD + 2);
-      __syncthreads();
-      // fold the pass into the running output. Warp h < GQ finds head h's
-      // factors, lane w < nb for block w: new max, 2^(m_w - M), sum update
-      if (warp < GQ) {
-        const int h = warp;
-        const float am = sa.accm[h], al = sa.accl[h];
-        const float mw = lane < nb ? sa.tres[lane][h][HD] : -INFINITY;
-        const float lw = lane < nb ? sa.tres[lane][h][HD + 1] : 0.f;
-        float M = fmaxf(mw, am);
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
-        const float f = lane < nb ? exp2f(mw - M) : 0.f;
-        float L = lw * f;
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) L += __shfl_xor_sync(0xffffffffu, L, o);
-        const float fa = am == -INFINITY ? 0.f : exp2f(am - M);
-        __syncwarp();
-        if (lane < SA::NBW) sa.fac[h][1 + lane] = f;
-        if (lane == 0) {
-          sa.fac[h][0] = fa;
-          sa.accm[h] = M;
-          sa.accl[h] = al * fa + L;
-        }
-      }
-      __syncthreads();
-      const bool last_pass = tp + PP >= t1;
-      for (int i = tid; i < GQ * HD; i += NT) {
-        const int h = i / HD, d = i % HD;
-        float O = sa.acc[h][d] * sa.fac[h][0];
-#pragma unroll
-        for (int w = 0; w < SA::NBW; ++w)
-          if (w < nb) O += sa.tres[w][h][d] * sa.fac[h][1 + w];
-        if (last_pass) {  // the split's partial: o, max, sum
-          gpart[h * (HD + 2) + d] = O;
-          if (d == 0) {
-            gpart[h * (HD + 2) + HD] = sa.accm[h];
-            gpart[h * (HD + 2) + HD + 1] = sa.accl[h];
-          }
-        } else {
-          sa.acc[h][d] = O;
-        }
-      }
-      // the next pass writes its tiles and blocks after the barriers of its staging
-    }
-  } else {
+  {
     // ---- warp w: blocks w, w + NW, ... of the split, each folded into the
     // warp's running (max, sum) per head and its share of o: lane holds
     // elements lane + 32e of the [GQ][HD] output
-    constexpr int NW = SA::NW, OE = GQ * HD / 32;
+    constexpr int OE = GQ * HD / 32;
     static_assert(GQ * HD % 32 == 0, "output elements per lane");
     __syncthreads();  // q, k, v of this step (cur) are complete
     float* wt = &sa.tres[warp][0][0];
@@ -1144,17 +1049,30 @@ __global__ void __launch_bounds__(kBAttnThreads) battn_mma_kernel(const BAttnPar
       const int n = min(16, t1 - tp);
       cp_async_wait_all();
       __syncwarp();
+      widen(n);
+      __syncwarp();
       if (pos >= tp && pos < tp + n) {  // this step's k, v row (its copy from the cache may predate the append)
         for (int i = lane; i < 2 * HD; i += 32) {
           const int kv = i >= HD, d = i - kv * HD;
-          (kv ? &sa.vt[warp][0][0] : &sa.kt[warp][0][0])[tile_off<HD, HD, true>(pos - tp, d >> 3) + (d & 7)] =
-              (uint16_t)(__float_as_uint(sa.cur[GQ + kv][d]) >> 16);  // bf16-exact value
+          // bf16: the bf16-exact value; int8: its code, exactly in fp16
+          const uint16_t v = KV8 ? __half_as_ushort(__float2half_rn(sa.cur[GQ + kv][d]))
+                                 : (uint16_t)(__float_as_uint(sa.cur[GQ + kv][d]) >> 16);
+          (kv ? &sa.vt[warp][0][0] : &sa.kt[warp][0][0])[tile_off<HD, HD, true>(pos - tp, d >> 3) + (d & 7)] = v;
         }
+        if constexpr (KV8)
+          if (lane < 2 * NG)
+            (lane < NG ? sa.ksc : sa.vsc)[warp][pos - tp][lane % NG] =
+                __half_as_ushort(__float2half_rn(sa.cursc[lane / NG][lane % NG]));
         __syncwarp();
       }
-      attn_block16<GQ, HD, HD, true>(&sa.cur[0][0], &sa.kt[warp][0][0], &sa.vt[warp][0][0], 0, n, lane, wt, HD + 2);
+      if constexpr (KV8)
+        attn_block16_q8<GQ, HD, HD, true>(&sa.cur[0][0], &sa.kt[warp][0][0], &sa.vt[warp][0][0], &sa.ksc[warp][0][0],
+                                          &sa.vsc[warp][0][0], 0, n, lane, wt, HD + 2);
+      else
+        attn_block16<GQ, HD, HD, true>(&sa.cur[0][0], &sa.kt[warp][0][0], &sa.vt[warp][0][0], 0, n, lane, wt,
+                                       HD + 2);
       __syncwarp();  // the stage has been read and the block's results written
-      if (tp + 16 * NW < t1) stage(tp + 16 * NW, warp);
+      if (tp + 16 * NW < t1) stage(tp + 16 * NW);
       float fr[GQ], fb[GQ];
 #pragma unroll
       for (int h = 0; h < GQ; ++h) {
