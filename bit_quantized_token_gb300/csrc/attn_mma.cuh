@@ -82,13 +82,115 @@ __device__ __forceinline__ void attn_q_frag(uint32_t (&qf)[4], const float* q, i
 }
 
 // Offset (in halves) of dims 8c .. 8c+7 of row r of a K/V tile. Padded tiles
-// (BF = false): rows of RS > HD halves. Unpadded tiles (BF = true, rows of HD
-// halves): chunk c of row r sits at chunk c ^ (r & 7), so the 8 rows of an
+// (SWZ = false): rows of RS > HD halves. Unpadded tiles (SWZ = true, rows of
+// HD halves): chunk c of row r sits at chunk c ^ (r & 7), so the 8 rows of an
 // ldmatrix fetch still hit distinct bank groups.
-template <int HD, int RS, bool BF>
+template <int HD, int RS, bool SWZ>
 __device__ __forceinline__ int tile_off(int r, int c) {
-  if constexpr (BF) return r * HD + 8 * (c ^ (r & 7));
+  if constexpr (SWZ) return r * HD + 8 * (c ^ (r & 7));
   else return r * RS + 8 * c;
+}
+
+// The query block's A fragments, built once per attention item: entry
+// ks * 4 GQ + 4 g + t holds lane (g, t)'s four registers for dims 16ks ..
+// 16ks+15 (as attn_q_frag), high parts and remainders as bf16 (BF) or fp16
+// pairs. Lanes with g >= GQ take zeros.
+template <int GQ, int HD, bool BF>
+__device__ __forceinline__ uint4 attn_q_pack(const float* q, int f) {
+  const int ks = f / (4 * GQ), g = (f / 4) % GQ, t = f % 4;
+  const float* r = q + g * HD + 16 * ks + 2 * t;
+  const float x[4] = {r[0], r[1], r[8], r[9]};
+  float h[4], l[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    if constexpr (BF) {
+      h[i] = __bfloat162float(__float2bfloat16_rn(x[i]));
+      l[i] = x[i] - h[i];
+    } else {
+      split_f16(x[i], h[i], l[i]);
+    }
+  }
+  if constexpr (BF)
+    return make_uint4(pack_bf16x2(h[0], h[1]), pack_bf16x2(l[0], l[1]), pack_bf16x2(h[2], h[3]),
+                      pack_bf16x2(l[2], l[3]));
+  else
+    return make_uint4(pack_f16x2(h[0], h[1]), pack_f16x2(l[0], l[1]), pack_f16x2(h[2], h[3]),
+                      pack_f16x2(l[2], l[3]));
+}
+template <int GQ>
+__device__ __forceinline__ void attn_q_load(uint32_t (&qf)[4], const uint4* qp, int ks, int lane) {
+  const int g = lane >> 2, t = lane & 3;
+  const uint4 v = g < GQ ? qp[ks * 4 * GQ + 4 * g + t] : make_uint4(0u, 0u, 0u, 0u);
+  qf[0] = v.x;
+  qf[1] = v.y;
+  qf[2] = v.z;
+  qf[3] = v.w;
+}
+
+// attn_block16 on bf16 operands: the cache's bf16 K/V rows as they are
+// (unpadded, tile_off's permuted chunks, rows 0..15), the query's packed bf16
+// fragments (attn_q_pack), the probabilities split into bf16 high part and
+// remainder (16-bit mantissa, relative error ~2^-17), fp32 accumulation.
+// Same outputs as attn_block16.
+template <int GQ, int HD>
+__device__ __forceinline__ void attn_block16_bf(const uint4* qp, const uint16_t* kt, const uint16_t* vt, int nvalid,
+                                                int lane, float* out, int OS) {
+  const int g = lane >> 2, t = lane & 3, r8 = lane & 7, mi = lane >> 3;
+  float s[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+#pragma unroll
+  for (int ks = 0; ks < HD / 16; ++ks) {
+    uint32_t qf[4];
+    attn_q_load<GQ>(qf, qp, ks, lane);
+    uint32_t b[4];
+    ldsm_x4(b, kt + tile_off<HD, HD, true>(8 * (mi >> 1) + r8, 2 * ks + (mi & 1)));
+    mma_bf16_16816(s[0], qf, b[0], b[1]);
+    mma_bf16_16816(s[1], qf, b[2], b[3]);
+  }
+  float sc[4];
+#pragma unroll
+  for (int j = 0; j < 2; ++j)
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+      const int li = 8 * j + 2 * t + e;
+      sc[2 * j + e] = li < nvalid ? s[j][e] + s[j][e + 2] : -INFINITY;  // high rows + remainder rows
+    }
+  float mx = fmaxf(fmaxf(sc[0], sc[1]), fmaxf(sc[2], sc[3]));
+  mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+  mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+  float p[4], sum = 0.f;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    p[i] = exp2f(sc[i] - mx);
+    sum += p[i];
+  }
+  sum += __shfl_xor_sync(0xffffffffu, sum, 1);
+  sum += __shfl_xor_sync(0xffffffffu, sum, 2);
+  float ph[4], pl[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    ph[i] = __bfloat162float(__float2bfloat16_rn(p[i]));
+    pl[i] = p[i] - ph[i];
+  }
+  const uint32_t pa[4] = {pack_bf16x2(ph[0], ph[1]), pack_bf16x2(pl[0], pl[1]), pack_bf16x2(ph[2], ph[3]),
+                          pack_bf16x2(pl[2], pl[3])};
+  float* o = out + g * OS;
+  const bool mine = g < GQ;
+#pragma unroll
+  for (int nt = 0; nt < HD / 8; nt += 2) {
+    uint32_t b[4];
+    ldsm_x4_t(b, vt + tile_off<HD, HD, true>(8 * (mi & 1) + r8, nt + (mi >> 1)));
+    float d0[4] = {0.f, 0.f, 0.f, 0.f}, d1[4] = {0.f, 0.f, 0.f, 0.f};
+    mma_bf16_16816(d0, pa, b[0], b[1]);
+    mma_bf16_16816(d1, pa, b[2], b[3]);
+    if (mine) {
+      *reinterpret_cast<float2*>(o + 8 * nt + 2 * t) = make_float2(d0[0] + d0[2], d0[1] + d0[3]);
+      *reinterpret_cast<float2*>(o + 8 * nt + 8 + 2 * t) = make_float2(d1[0] + d1[2], d1[1] + d1[3]);
+    }
+  }
+  if (mine && t == 0) {
+    o[HD] = mx;
+    o[HD + 1] = sum;
+  }
 }
 
 // One warp, the GQ heads of q ([GQ][HD], scaled) against the 16 staged rows
@@ -97,14 +199,9 @@ __device__ __forceinline__ int tile_off(int r, int c) {
 // g = lane/4 < GQ, t = lane%4) writes to out[g*OS ..]: o at dims 8nt+2t(+1)
 // (sum over the 16 positions of 2^(s - m) v), and lane t = 0 writes m (max
 // score) at [HD] and l (sum of 2^(s - m)) at [HD+1].
-// BF = false: the tiles hold fp16 rows, padded to RS halves. BF = true: they
-// hold the cache's bf16 rows as they are (tile_off's permuted chunks), and
-// every fragment is converted to fp16 in registers after its ldmatrix: the
-// same fp16 operands as the padded path.
-template <int GQ, int HD, int RS, bool BF = false>
+template <int GQ, int HD, int RS>
 __device__ __forceinline__ void attn_block16(const float* q, const uint16_t* kt, const uint16_t* vt, int row0,
                                              int nvalid, int lane, float* out, int OS) {
-  static_assert(!BF || RS == HD, "bf16 tiles are unpadded");
   const int g = lane >> 2, t = lane & 3, r8 = lane & 7, mi = lane >> 3;
   float s[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
 #pragma unroll
@@ -113,10 +210,7 @@ __device__ __forceinline__ void attn_block16(const float* q, const uint16_t* kt,
     attn_q_frag<GQ, HD>(qf, q, ks, lane);
     // matrices: positions 0-7 / 8-15 (n-tile j = mi/2) x dims 16ks + 8*(mi%2) .. +7
     uint32_t b[4];
-    ldsm_x4(b, kt + tile_off<HD, RS, BF>(row0 + 8 * (mi >> 1) + r8, 2 * ks + (mi & 1)));
-    if constexpr (BF)
-#pragma unroll
-      for (int i = 0; i < 4; ++i) b[i] = bf16x2_to_f16x2(b[i]);
+    ldsm_x4(b, kt + (size_t)(row0 + 8 * (mi >> 1) + r8) * RS + 16 * ks + 8 * (mi & 1));
     mma_f16_16816(s[0], qf, b[0], b[1]);
     mma_f16_16816(s[1], qf, b[2], b[3]);
   }
@@ -150,10 +244,7 @@ __device__ __forceinline__ void attn_block16(const float* q, const uint16_t* kt,
   for (int nt = 0; nt < HD / 8; nt += 2) {
     // matrices (transposed): positions 8*(mi%2) .. +7 x dims 8*(nt + mi/2) .. +7
     uint32_t b[4];
-    ldsm_x4_t(b, vt + tile_off<HD, RS, BF>(row0 + 8 * (mi & 1) + r8, nt + (mi >> 1)));
-    if constexpr (BF)
-#pragma unroll
-      for (int i = 0; i < 4; ++i) b[i] = bf16x2_to_f16x2(b[i]);
+    ldsm_x4_t(b, vt + (size_t)(row0 + 8 * (mi & 1) + r8) * RS + 8 * (nt + (mi >> 1)));
     float d0[4] = {0.f, 0.f, 0.f, 0.f}, d1[4] = {0.f, 0.f, 0.f, 0.f};
     mma_f16_16816(d0, pa, b[0], b[1]);
     mma_f16_16816(d1, pa, b[2], b[3]);
@@ -249,7 +340,8 @@ __device__ __forceinline__ void attn_block16_cc(const float* q, const uint16_t* 
 // block's largest scale of the group keeps the scaled probabilities in [0, 1]
 // for their fp16 high/low split, and that largest scale multiplies the MMA
 // result back. Same outputs as attn_block16. SWZ: unpadded fp16 rows with
-// tile_off's permuted chunks instead of padded rows.
+// tile_off's permuted chunks instead of padded rows, and q holds the packed
+// fp16 fragments (attn_q_pack) instead of the query.
 template <int GQ, int HD, int RS, bool SWZ = false>
 __device__ __forceinline__ void attn_block16_q8(const float* q, const uint16_t* kt, const uint16_t* vt,
                                                 const uint16_t* ks, const uint16_t* vs, int row0, int nvalid,
@@ -266,7 +358,8 @@ __device__ __forceinline__ void attn_block16_q8(const float* q, const uint16_t* 
 #pragma unroll
   for (int kk = 0; kk < HD / 16; ++kk) {
     uint32_t qf[4];
-    attn_q_frag<GQ, HD>(qf, q, kk, lane);
+    if constexpr (SWZ) attn_q_load<GQ>(qf, reinterpret_cast<const uint4*>(q), kk, lane);
+    else attn_q_frag<GQ, HD>(qf, q, kk, lane);
     uint32_t b[4];
     ldsm_x4(b, kt + tile_off<HD, RS, SWZ>(row0 + 8 * (mi >> 1) + r8, 2 * kk + (mi & 1)));
     mma_f16_16816(s[kk / 2][0], qf, b[0], b[1]);

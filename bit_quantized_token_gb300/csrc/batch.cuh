@@ -827,11 +827,12 @@ using BAttnSmemT = std::conditional_t<KV8, BAttnWarpSmem8<GQ, HD>, BAttnWarpSmem
 // Flash-decoding attention of every sequence of the batch on the tensor
 // cores: grid (split, kv head, sequence), splits of LLMQ_BATTN_SPLIT_LEN
 // positions. Warp w takes blocks w, w+8, ... of 16 positions of the split:
-// it copies each into its private stage (bf16 rows as cached, converted to
-// fp16 fragment by fragment in attn_block16; int8 codes widened to fp16 in
-// the stage), scores all GQ heads on the tensor cores (attn_mma.cuh), folds
-// the block into its own running (max, sum, o), and requests its next block
-// as soon as the stage has been read. The 8 warp states merge once per
+// it copies each into its private stage (bf16 rows as cached; int8 codes
+// widened to fp16 in the stage), scores all GQ heads on the tensor cores
+// (attn_mma.cuh: bf16 operands for the bf16 cache, fp16 for the widened
+// codes; the query's fragments packed once per item), folds the block into
+// its own running (max, sum, o), and requests its next block as soon as the
+// stage has been read. The 8 warp states merge once per
 // split, and the last split of a (sequence, kv head) to finish merges the
 // splits into the output row.
 template <int GQ, int HD, bool KV8>
@@ -1035,7 +1036,17 @@ __global__ void __launch_bounds__(kBAttnThreads) battn_mma_kernel(const BAttnPar
     // elements lane + 32e of the [GQ][HD] output
     constexpr int OE = GQ * HD / 32;
     static_assert(GQ * HD % 32 == 0, "output elements per lane");
+    // the query's A fragments, packed once over the query rows of cur (the
+    // same bytes: GQ * HD / 4 entries of 16 B): bf16 pairs for the bf16
+    // cache's bf16 MMAs, fp16 pairs for the widened int8 codes
+    constexpr int NF = GQ * HD / 4;
+    static_assert(NF <= NT, "one fragment entry per thread");
     __syncthreads();  // q, k, v of this step (cur) are complete
+    const uint4 qv = tid < NF ? attn_q_pack<GQ, HD, !KV8>(&sa.cur[0][0], tid) : make_uint4(0u, 0u, 0u, 0u);
+    __syncthreads();
+    if (tid < NF) reinterpret_cast<uint4*>(&sa.cur[0][0])[tid] = qv;
+    __syncthreads();
+    const uint4* qp = reinterpret_cast<const uint4*>(&sa.cur[0][0]);
     float* wt = &sa.tres[warp][0][0];
     float m_run[GQ], l_run[GQ], o_run[OE];
 #pragma unroll
@@ -1066,11 +1077,10 @@ __global__ void __launch_bounds__(kBAttnThreads) battn_mma_kernel(const BAttnPar
         __syncwarp();
       }
       if constexpr (KV8)
-        attn_block16_q8<GQ, HD, HD, true>(&sa.cur[0][0], &sa.kt[warp][0][0], &sa.vt[warp][0][0], &sa.ksc[warp][0][0],
-                                          &sa.vsc[warp][0][0], 0, n, lane, wt, HD + 2);
+        attn_block16_q8<GQ, HD, HD, true>(reinterpret_cast<const float*>(qp), &sa.kt[warp][0][0], &sa.vt[warp][0][0],
+                                          &sa.ksc[warp][0][0], &sa.vsc[warp][0][0], 0, n, lane, wt, HD + 2);
       else
-        attn_block16<GQ, HD, HD, true>(&sa.cur[0][0], &sa.kt[warp][0][0], &sa.vt[warp][0][0], 0, n, lane, wt,
-                                       HD + 2);
+        attn_block16_bf<GQ, HD>(qp, &sa.kt[warp][0][0], &sa.vt[warp][0][0], n, lane, wt, HD + 2);
       __syncwarp();  // the stage has been read and the block's results written
       if (tp + 16 * NW < t1) stage(tp + 16 * NW);
       float fr[GQ], fb[GQ];
