@@ -975,12 +975,12 @@ __global__ void __launch_bounds__(kBAttnThreads) battn_mma_kernel(const BAttnPar
     __syncthreads();
   }
   // RoPE of q and k; q scaled by log2(e)/sqrt(hd); k, v rounded to bf16 (the
-  // split owning `pos` appends them and puts them into its tile)
+  // last split appends them to the cache)
   const float qscale = 1.4426950408889634f / sqrtf((float)HD);
   auto keep = [&](int r, int d, float x) {
     if constexpr (KV8) {  // quantized per 32-element group below
       sa.cur[r][d] = x;
-    } else {  // the pass holding `pos` puts the row into its stage once its copies have landed
+    } else {  // the warp whose block holds `pos` puts the row into its stage once its copies have landed
       const __nv_bfloat16 h = __float2bfloat16_rn(x);
       sa.cur[r][d] = __bfloat162float(h);
       if (append && in_bounds(a.status, pos < a.cap))
