@@ -35,6 +35,7 @@ constexpr int kBWarps = 8;
 constexpr int kBThreads = kBWarps * 32;
 constexpr int kBM = 32;  // tokens per step (sequences), padded to 32
 constexpr int kQKC = 4;  // 4-bit units per chunk (256 inputs) of the tensor-core path
+constexpr int kBKsMax = 6;  // K splits (CTAs per row block) at most
 
 struct BGemvParams {
   const uint8_t* units;    // [n_rt][G] units
@@ -328,14 +329,16 @@ __global__ void __launch_bounds__(kBThreads, 2) bgemv_kernel(const BGemvParams p
         if (in_bounds(p.status, ksi < p.ks && row0 + rl * 32 + lane < rows_pad))
           p.part[((size_t)ksi * kBM + mm) * rows_pad + row0 + rl * 32 + lane] = v;
       }
-    __threadfence();
     __syncthreads();
-    if (tid == 0) s_last = atomicAdd(&p.counters[blk], 1) == p.ks - 1;
+    if (tid == 0) {  // one release for the CTA's partials (ordered after them by the barrier)
+      __threadfence();
+      s_last = atomicAdd(&p.counters[blk], 1) == p.ks - 1;
+    }
     __syncthreads();
     if (!s_last) return;
     __threadfence();
   }
-  constexpr int KSMAX = 16;
+  static_assert(kBKsMax <= 6, "partials of 4 tokens in flight per thread");
   float ssq[4] = {0.f, 0.f, 0.f, 0.f};  // EPI_RESID: sums of squares per token of the warp
   float bv[4];
   int bi[4];
@@ -347,26 +350,29 @@ __global__ void __launch_bounds__(kBThreads, 2) bgemv_kernel(const BGemvParams p
   bool nan = false;
   for (int rl = 0; rl < p.rtb; ++rl) {
     const int r = rl * 32 + lane, row = row0 + r;
+    // EPI_RESID: the residual rows, requested with the partials (one round trip)
+    float rv[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k)
+      rv[k] = ldcg1_if(p.resid + (size_t)(warp + 8 * k) * p.out_cols + row,
+                       p.epi == EPI_RESID && warp + 8 * k < p.M && row < p.rows);
     float y[4];
     if (p.ks == 1) {
 #pragma unroll
       for (int k = 0; k < 4; ++k) y[k] = cta_sum(r, warp + 8 * k);
-    } else {  // the K-split partials, added in CTA order; two tokens' loads in flight together
+    } else {  // the K-split partials of the 4 tokens, all in flight together, added in CTA order
+      float pv[4][kBKsMax];
 #pragma unroll
-      for (int k0 = 0; k0 < 4; k0 += 2) {
-        float pv[2][KSMAX];
+      for (int k = 0; k < 4; ++k)
 #pragma unroll
-        for (int k = 0; k < 2; ++k)
+        for (int j = 0; j < kBKsMax; ++j)
+          pv[k][j] = ldcg1_if(p.part + ((size_t)j * kBM + warp + 8 * k) * rows_pad + row, j < p.ks);
 #pragma unroll
-          for (int j = 0; j < KSMAX; ++j)
-            pv[k][j] = ldcg1_if(p.part + ((size_t)j * kBM + warp + 8 * (k0 + k)) * rows_pad + row, j < p.ks);
+      for (int k = 0; k < 4; ++k) {
+        float sum = 0.f;
 #pragma unroll
-        for (int k = 0; k < 2; ++k) {
-          float sum = 0.f;
-#pragma unroll
-          for (int j = 0; j < KSMAX; ++j) sum += pv[k][j];
-          y[k0 + k] = sum;
-        }
+        for (int j = 0; j < kBKsMax; ++j) sum += pv[k][j];
+        y[k] = sum;
       }
     }
     if (p.ss_in)  // RMSNorm of the input: 1/rms per token on the result
@@ -387,7 +393,7 @@ __global__ void __launch_bounds__(kBThreads, 2) bgemv_kernel(const BGemvParams p
       }
       if (mm >= p.M || row >= p.rows) continue;
       if (p.epi == EPI_RESID) {
-        const float xn = __ldcg(p.resid + (size_t)mm * p.out_cols + row) + y[k];
+        const float xn = rv[k] + y[k];
         p.out[(size_t)mm * p.out_cols + row] = xn;
         if (p.out_hl) store_hl(p.out_hl, p.out_cols, mm, row, p.out_norm ? xn * __ldg(p.out_norm + row) : xn);
         ssq[k] += xn * xn;

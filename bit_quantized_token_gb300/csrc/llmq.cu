@@ -61,15 +61,15 @@ struct BPlan {
 BPlan plan_bgemv(const Mat& mat, int n_sm) {
   // 256 inputs per chunk (4 four-bit units or 16 bf16 units per row tile);
   // 1, 2 or 4 row tiles per CTA (8 warps = 16-row halves x unit subsets);
-  // enough CTAs to fill the GPU twice through the K splits (at most 16, the
-  // epilogue's limit)
+  // enough CTAs to fill the GPU once through the K splits (at most kBKsMax:
+  // the merging CTA keeps every split's partial of its 4 tokens in flight)
   BPlan p;
   p.m = mat;
   const int epu = mat.bf16 ? kBF16UnitCols : 64;
   p.kc = 256 / epu;
   // more row tiles per CTA only while the row blocks alone fill the GPU; else
   // one row tile per CTA and just enough K splits to fill it once (split-K
-  // costs a partial round trip and a merge)
+  // costs a partial round trip and a merge; at most kBKsMax splits)
   const int max_ks = std::max(1, (mat.G + p.kc - 1) / p.kc);
   p.rtb = 1;
   for (int r : {4, 2})  // bf16 units: at most 2 row tiles (two CTAs of double-buffered 16 KB units per SM)
@@ -78,7 +78,7 @@ BPlan plan_bgemv(const Mat& mat, int n_sm) {
       break;
     }
   p.n_blocks = mat.n_rt / p.rtb;
-  p.ks = std::min({max_ks, 16, std::max(1, (n_sm + p.n_blocks - 1) / p.n_blocks)});
+  p.ks = std::min({max_ks, kBKsMax, std::max(1, (n_sm + p.n_blocks - 1) / p.n_blocks)});
   p.smem = bgemv_stage_bytes(p.rtb, p.kc, mat.unit_bytes(), epu);
   return p;
 }
