@@ -882,7 +882,9 @@ cudaError_t enqueue_batched(llm_model* m, const BatchedIO& io) {
     } else {
       bp.mode = BA_APPEND_ATTEND;
     }
-    if ((e = launch_battn(m, bp, m->attn_P, B, pdl)) != cudaSuccess) return e;
+    // splits of LLMQ_BATTN_SPLIT_LEN positions: no cache of this model needs more than its capacity's
+    const int splits = std::min(m->attn_P, (c.max_seq + LLMQ_BATTN_SPLIT_LEN - 1) / LLMQ_BATTN_SPLIT_LEN);
+    if ((e = launch_battn(m, bp, splits, B, pdl)) != cudaSuccess) return e;
     p = bgemv_params(m, m->bwo[l], B);  // h = x + Wo o (staged for gate|up with ffn_norm[l])
     p.xl = m->d_bo_hl;
     p.epi = EPI_RESID;
