@@ -207,6 +207,7 @@ __global__ void __launch_bounds__(kBThreads, 2) bgemv_kernel(const BGemvParams p
   for (int i = 0; i < 4; ++i) qacc[i][0][0] = qacc[i][0][1] = qacc[i][1][0] = qacc[i][1][1] = 0.f;
 
   bool ok = true;
+  int n_issued = min(2, (g1 - g0 + p.kc - 1) / p.kc), ci_fail = 0;  // weight chunks requested (thread 0)
   for (int ga = g0, ci = 0; ga < g1 && ok; ga += p.kc, ++ci) {
     const int nk = min(p.kc, g1 - ga);
     const uint8_t* wb = wbuf + (ci & 1) * wchunk;
@@ -215,6 +216,7 @@ __global__ void __launch_bounds__(kBThreads, 2) bgemv_kernel(const BGemvParams p
     cp_async_commit();
     cp_async_wait_group<1>();  // this chunk's inputs
     ok = __syncthreads_and(mbar_wait(&s_bar[ci & 1], (ci >> 1) & 1, p.status));  // uniform across the CTA
+    ci_fail = ci;
     if (ok) {
       for (int u = usub; u < nk; u += wp) {
         float d[8][4];
@@ -286,10 +288,15 @@ __global__ void __launch_bounds__(kBThreads, 2) bgemv_kernel(const BGemvParams p
       }
     }
     __syncthreads();  // the buffers are restaged by the next chunks
-    if (tid == 0 && ok && ga + 2 * p.kc < g1) stage_weights(ga + 2 * p.kc);  // into this chunk's buffer
+    if (tid == 0 && ok && ga + 2 * p.kc < g1) {
+      stage_weights(ga + 2 * p.kc);  // into this chunk's buffer
+      ++n_issued;
+    }
   }
   if (!ok) {  // every wait is bounded; the status word carries the timeout
     cp_async_wait_all();
+    if (tid == 0)  // the weight copies still in flight land (bounded waits) before the CTA leaves
+      for (int c = ci_fail; c < n_issued; ++c) mbar_wait(&s_bar[c & 1], (c >> 1) & 1, p.status);
     return;
   }
 
@@ -519,12 +526,16 @@ __global__ void __launch_bounds__(kHThreads, 1) bhead_kernel(const BGemvParams p
     if (lane == 0) {
       const uint64_t pol = policy_evict_first();
       int ci = 0;
-      for (int gi = 0; gi < n_groups; ++gi) {
+      bool live = true;
+      for (int gi = 0; gi < n_groups && live; ++gi) {
         const int rt0 = rt_a + gi * kHWarps, nrt = min(kHWarps, rt_b - rt0);
-        for (int u0 = 0; u0 < p.G; u0 += kHUC, ++ci) {
+        for (int u0 = 0; u0 < p.G && live; u0 += kHUC, ++ci) {
           const int slot = ci % kHSlots;
           if (ci >= kHSlots) {
-            if (!mbar_wait_spin(&s_empty[slot], ((ci / kHSlots) - 1) & 1, p.status)) return;
+            if (!mbar_wait_spin(&s_empty[slot], ((ci / kHSlots) - 1) & 1, p.status)) {
+              live = false;
+              break;
+            }
             asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // the consumers' reads of the slot
           }
           mbar_expect_tx(&s_full[slot], (uint32_t)(nrt * kHUC * kHUnitBytes));
@@ -536,6 +547,9 @@ __global__ void __launch_bounds__(kHThreads, 1) bhead_kernel(const BGemvParams p
           }
         }
       }
+      // before leaving, every copy this warp issued has landed (at once on the normal path, where the
+      // consumers waited for them; bounded after a timeout): the last chunk of each slot
+      for (int c = max(0, ci - kHSlots); c < ci; ++c) mbar_wait(&s_full[c % kHSlots], (c / kHSlots) & 1, p.status);
     }
     return;
   }
