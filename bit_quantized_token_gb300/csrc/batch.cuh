@@ -807,7 +807,9 @@ struct BAttnParams {
 #ifndef LLMQ_BATTN_SPLIT_LEN
 // Cached positions per split (at most 24 splits per (sequence, kv head)).
 // Measured on the 32-sequence workload, bf16 cache: 128 -> 9408, 256 -> 10005,
-// 512 -> 10826, 768 -> 10176, 1024 -> 10735 tok/s
+// 512 -> 10826, 768 -> 10176, 1024 -> 10735 tok/s; again with the bf16 MMAs
+// and the one-round-trip GEMV merge, ms per step: 384 -> 2.68, 512 -> 2.56,
+// 768 -> 2.76
 #define LLMQ_BATTN_SPLIT_LEN 512
 #endif
 constexpr int kBAttnThreads = 256;
