@@ -516,6 +516,14 @@ def test_batched_tied_head_ragged_vocabulary():
     _batched_vs_oracle(cfg, [70, 130, 5], 3, synth.make_first_tokens(cfg, 3), hidden=True)
 
 
+def test_batched_tied_head_wider_than_the_resident_input():
+    # a tied bf16 head of dim 2048: its staged 32-token input (2 x 32 x 2056
+    # bf16) does not fit in one CTA's shared memory beside the ring, so the
+    # LM head runs as the split-K GEMV with the greedy epilogue instead
+    cfg = synth.workload(2, n_layers=1, vocab=4096, dim=2048)
+    _batched_vs_oracle(cfg, [40, 300, 7], 3, synth.make_first_tokens(cfg, 3), hidden=True)
+
+
 def test_batched_tiny_int8_kv_matches_oracle():
     # the grouped int8 cache (LLM_KV_Q8) against the oracle's int8 caches
     cfg = synth.workload(0)
